@@ -1,0 +1,414 @@
+"""KDA forward prefill throughput on GB300.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+One step = one kda_fwd call (the whole hot path: prologue, intra-chunk UT/WY,
+chunk-sequential state pass, state load/store) over the long-prefill workload
+B=1, T=8192, H=64, K=V=128 with bf16 initial/final state.  Inputs are seeded
+synthetic data resident in HBM; out/final_state are preallocated.  The working
+set (~676 MB) is larger than L2 (129 MB) and a 256 MB L2-flush write runs
+between timed steps (outside the timed kernel).  Each step is timed with CUDA
+events on the launching stream; rank 0 prints one JSON line.
+
+--impl reference times the fp64 CPU oracle (the baseline, on the host cores) on
+a bounded sample of the same workload.
+
+Under torchrun (N > 1) every rank processes its own copy of the workload with a
+different seed (weak scaling, no data-path collective); the timed region is
+bracketed by barriers and the max over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KDA fwd prefill tokens/s on 1 GB300 (T=8192,H=64,K=V=128) + % of roofline"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+# Algorithmic work per (token, head): q,k,v,g,out bf16 (5 x 256 B) + beta (2 B);
+# FLOPs of the chunked form with C=64, K=V=128 (A, M, W, U~, M U dense; W S, Q S, K^T U).
+BYTES_PER_TOKEN_HEAD = 5 * 128 * 2 + 2
+FLOPS_PER_TOKEN_HEAD = 2 * 64 * (3 * 128 + 2 * 128) + 2 * 3 * 128 * 128
+KERNEL_SOURCES = ("gated_delta_rule_52_gb300/csrc",)
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# --------------------------------------------------------------------------- helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def shard_seed(base_seed: int, rank: int) -> int:
+    """Each rank draws an independent problem of the same shape."""
+    return base_seed + 1000 * rank
+
+
+def aggregate(tokens_per_rank: int, world: int, times_ms):
+    """Whole-job throughput from the per-rank timed-region durations (ms): the
+    slowest rank bounds the job."""
+    t = max(times_ms)
+    return world * tokens_per_rank / (t / 1e3), t
+
+
+def algorithmic_bytes(d) -> int:
+    th = d["B"] * d["T"] * d["H"]
+    sb = {"fp32": 4, "bf16": 2, None: 0}[d["state_dtype"]]
+    n_state = (1 if d["initial_state"] is not None else 0) + (1 if d["state_dtype"] else 0)
+    return th * BYTES_PER_TOKEN_HEAD + d["N"] * d["H"] * 128 * 128 * sb * n_state
+
+
+def algorithmic_flops(d) -> int:
+    return d["B"] * d["T"] * d["H"] * FLOPS_PER_TOKEN_HEAD
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        base = os.path.join(ROOT, rel)
+        for name in sorted(os.listdir(base)):
+            if name.endswith((".cu", ".cuh", ".h")):
+                with open(os.path.join(base, name), "rb") as f:
+                    h.update(name.encode())
+                    h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j.get("bf16_tflops", FALLBACK_BF16_TFLOPS)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def stored_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel sources (else None)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            j = json.load(f)
+        e = j.get(workload)
+        if e and e.get("source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        rows = [r for r in csv.reader(io.StringIO(self.tmp.read())) if len(r) >= 9]
+        self.tmp.close()
+        os.unlink(self.tmp.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for i, nm in enumerate(names):
+                if r[5 + i].strip() == "Active":
+                    reasons.add(nm)
+        loaded = [s for s in sm if mx and s >= 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------- oracle
+def oracle_sample(d, pairs_per_call: int, tokens: int, nthreads: int):
+    """Runs the fp64 oracle on the first `tokens` tokens of `pairs_per_call`
+    (sequence, head) pairs of the workload; returns (seconds, token-heads)."""
+    import oracle
+    T = min(tokens, d["T"])
+    H = d["H"]
+    pairs = [(0, h % H) for h in range(pairs_per_call)]
+    sub = {key: d[key][:, :T].contiguous() for key in ("q", "k", "v", "g", "beta")}
+    t0 = time.perf_counter()
+    oracle.kda_fwd(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], d["scale"], d["A_log"],
+                   d["dt_bias"], d["lower_bound"], initial_state=d["initial_state"],
+                   want_final=True, pairs=pairs, nthreads=nthreads)
+    return time.perf_counter() - t0, len(pairs) * T
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(d, budget_s: float = 12.0):
+    """The oracle, as it stands, timed on the host cores on a bounded sample of the
+    workload: `cores` full-length (sequence, head) pairs, grown until ~budget_s."""
+    import oracle
+    cores = cpu_cores()
+    nthreads = min(cores, oracle.max_threads()) or cores
+    pairs = nthreads
+    secs, th = oracle_sample(d, pairs, d["T"], nthreads)
+    if secs < budget_s / 4:
+        reps = max(1, min(8, int(budget_s / max(secs, 1e-3))))
+        pairs = min(d["H"], nthreads * reps)
+        if pairs > nthreads:
+            secs, th = oracle_sample(d, pairs, d["T"], nthreads)
+    value = (th / d["H"]) / secs
+    return {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+            "sample": f"{pairs} of {d['N'] * d['H']} (sequence, head) pairs x {d['T']} tokens, "
+                      f"fp64, {secs:.1f} s wall; tokens/s = token-heads / H / s"}
+
+
+# --------------------------------------------------------------------------- arms
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from gated_delta_rule_52_gb300 import workloads as W
+    import oracle
+    oracle.build()
+    w = W.get(args.workload)
+    d = W.make_inputs(w)
+    cores = cpu_cores()
+    nthreads = min(cores, oracle.max_threads()) or cores
+    # size one step so that warmup + steps fit in ~150 s
+    per_step = max(0.05, 150.0 / max(1, args.steps + args.warmup))
+    secs, _ = oracle_sample(d, nthreads, 128, nthreads)
+    tokens = int(max(16, min(d["T"], 128 * per_step / max(secs, 1e-4))))
+    for _ in range(args.warmup):
+        oracle_sample(d, nthreads, tokens, nthreads)
+    tot_s, tot_th = 0.0, 0
+    for _ in range(args.steps):
+        s, th = oracle_sample(d, nthreads, tokens, nthreads)
+        tot_s += s
+        tot_th += th
+    value = (tot_th / d["H"]) / tot_s
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / max(1, args.steps),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "B": d["B"], "T": d["T"], "H": d["H"], "K": 128,
+                       "V": 128, "state": d["state_dtype"]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+                             "sample": f"per step {nthreads} (sequence, head) pairs x {tokens} "
+                                       f"tokens, fp64"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from gated_delta_rule_52_gb300 import build as kbuild
+    from gated_delta_rule_52_gb300 import kda
+    from gated_delta_rule_52_gb300 import workloads as W
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or ws == 1:
+        kbuild.build_library()
+    if ws > 1:
+        dist.barrier()
+    kda.lib()
+
+    w = W.get(args.workload)
+    w = W.get(args.workload, seed=shard_seed(w.seed, rank))
+    d_cpu = W.make_inputs(w)
+    e = {key: (val.to(dev) if torch.is_tensor(val) else val) for key, val in d_cpu.items()}
+    B, T, H, N = d_cpu["B"], d_cpu["T"], d_cpu["H"], d_cpu["N"]
+    out = torch.empty((B, T, H, 128), dtype=torch.bfloat16, device=dev)
+    fin = None
+    if d_cpu["state_dtype"]:
+        sdt = torch.bfloat16 if d_cpu["state_dtype"] == "bf16" else torch.float32
+        fin = torch.empty((N, H, 128, 128), dtype=sdt, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda.kda_fwd(e["q"], e["k"], e["v"], e["g"], e["beta"], e["scale"], out, e["A_log"],
+                    e["dt_bias"], e["lower_bound"], initial_state=e["initial_state"],
+                    final_state=fin, cu_seqlens=e["cu_seqlens"], stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if kda.get_device_status(stream) != kda.KDA_OK:
+        raise RuntimeError("device reported an error during warm-up")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if ws > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    if kda.get_device_status(stream) != kda.KDA_OK:
+        raise RuntimeError("device reported an error during the timed region")
+    per_step = [s.elapsed_time(t) for s, t in zip(starts, ends)]
+    kernel_ms = sum(per_step)
+    times = [kernel_ms]
+    if ws > 1:
+        tt = torch.tensor([kernel_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        times = [float(tt.item())]
+    tokens_per_rank = B * T * args.steps
+    value, tmax = aggregate(tokens_per_rank, ws, times)
+    ms_per_step = tmax / args.steps
+    avg_launch_ms = kernel_ms / args.steps
+
+    # end to end: pinned host inputs -> device, kda_fwd, result -> pinned host
+    e2e = None
+    if rank == 0:
+        names = ["q", "k", "v", "g", "beta", "A_log", "dt_bias", "initial_state"]
+        host = {nm: d_cpu[nm].pin_memory() for nm in names if d_cpu[nm] is not None}
+        dev_in = {nm: torch.empty_like(host[nm], device=dev) for nm in host}
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h_fin = torch.empty(fin.shape, dtype=fin.dtype).pin_memory() if fin is not None else None
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = h_out.numel() * h_out.element_size() + (
+            h_fin.numel() * h_fin.element_size() if h_fin is not None else 0)
+
+        def e2e_step():
+            for nm, t in host.items():
+                dev_in[nm].copy_(t, non_blocking=True)
+            kda.kda_fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"],
+                        e["scale"], out, dev_in["A_log"], dev_in["dt_bias"], e["lower_bound"],
+                        initial_state=dev_in.get("initial_state"), final_state=fin,
+                        cu_seqlens=e["cu_seqlens"], stream=stream)
+            h_out.copy_(out, non_blocking=True)
+            if h_fin is not None:
+                h_fin.copy_(fin, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(3, min(args.steps, 20))
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = s0.elapsed_time(s1) / n_e2e
+        e2e = {"value": B * T / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e}
+
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return 0
+
+    hbm, tflops, src = measured_peaks()
+    abytes = algorithmic_bytes(d_cpu)
+    achieved = abytes / (avg_launch_ms / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "traffic": stored_traffic(w.name),
+            "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
+            else f"{src} {hbm} GB/s",
+            "kernel": "kda_fwd (one launch per step)",
+            "algorithmic_bytes_per_launch": abytes,
+            "algorithmic_flops_per_launch": algorithmic_flops(d_cpu),
+            "tensor_frac": algorithmic_flops(d_cpu) / (avg_launch_ms / 1e3) / (tflops * 1e12)}
+    cpu = cpu_baseline(d_cpu) if ws == 1 else None
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": B, "T": T, "H": H, "K": 128, "V": 128,
+                       "state": d_cpu["state_dtype"], "lower_bound": d_cpu["lower_bound"],
+                       "l2": "inputs (676 MB) larger than L2 and a 256 MB flush write between "
+                             "timed steps", "timing": "CUDA events around each kda_fwd call"},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+            "gpu_launches": args.steps * 1,
+            "wall_s_timed_region": wall}
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="prefill_8k")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,117 @@
+// Host side of the C ABI declared in include/kda.h: argument validation, the
+// device error word, and dispatch to the kernels.
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/kda.h"
+#include "kda_internal.h"
+
+namespace {
+
+// Set by kernels whose bounded waits give up; read and cleared by
+// kda_get_device_status().  One word per device (module-scope __device__).
+__device__ int g_kda_error = 0;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Validates the arguments of kda_fwd and fills `p`.  Touches no device state.
+kda_status validate(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                    float scale, void *out, const float *A_log, const float *dt_bias,
+                    float lower_bound, const void *initial_state, void *final_state,
+                    int state_dtype, const int64_t *cu_seqlens, int64_t num_seqs, int64_t B,
+                    int64_t T, int64_t H, int64_t K, int64_t V, kda::Params &p) {
+    if (K != kda::kHeadDim || V != kda::kHeadDim) return KDA_ERR_UNSUPPORTED;
+    if (B < 0 || T < 0 || H < 0) return KDA_ERR_SHAPE;
+    // Token tensors may be NULL only when they hold no element (B*T*H == 0).
+    const bool has_tokens = B > 0 && T > 0 && H > 0;
+    if (has_tokens && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_NULL;
+    if (H > 0 && (!A_log || !dt_bias)) return KDA_ERR_NULL;
+    if (cu_seqlens) {
+        if (B != 1 || num_seqs < 1) return KDA_ERR_SHAPE;
+    }
+    const int64_t N = cu_seqlens ? num_seqs : B;
+    if (H == 0 && N > 0 && T > 0) return KDA_ERR_SHAPE;
+    if (initial_state || final_state) {
+        if (state_dtype != KDA_STATE_BF16 && state_dtype != KDA_STATE_FP32) return KDA_ERR_DTYPE;
+    } else if (state_dtype != KDA_STATE_NONE && state_dtype != KDA_STATE_BF16 &&
+               state_dtype != KDA_STATE_FP32) {
+        return KDA_ERR_DTYPE;
+    }
+    if (!(lower_bound >= -5.0f && lower_bound <= 0.0f)) return KDA_ERR_VALUE;
+    if (!std::isfinite(scale)) return KDA_ERR_VALUE;
+    const void *ptrs[] = {q, k, v, g, beta, out, A_log, dt_bias, initial_state, final_state};
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return KDA_ERR_ALIGN;
+
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.k = static_cast<const __nv_bfloat16 *>(k);
+    p.v = static_cast<const __nv_bfloat16 *>(v);
+    p.g = static_cast<const __nv_bfloat16 *>(g);
+    p.beta = static_cast<const __nv_bfloat16 *>(beta);
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.A_log = A_log;
+    p.dt_bias = dt_bias;
+    p.scale = scale;
+    p.lower_bound = lower_bound;
+    p.init = initial_state;
+    p.fin = final_state;
+    p.state_type = state_dtype;
+    p.cu_seqlens = cu_seqlens;
+    p.n_seqs = N;
+    p.B = B;
+    p.T = T;
+    p.H = H;
+    p.err = nullptr;
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_fwd(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                   float scale, void *out, const float *A_log, const float *dt_bias,
+                   float lower_bound, const void *initial_state, void *final_state,
+                   int state_dtype, const int64_t *cu_seqlens, int64_t num_seqs, int64_t B,
+                   int64_t T, int64_t H, int64_t K, int64_t V, void *stream) {
+    kda::Params p;
+    kda_status st = validate(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound,
+                             initial_state, final_state, state_dtype, cu_seqlens, num_seqs, B, T,
+                             H, K, V, p);
+    if (st != KDA_OK) return st;
+    if (p.n_seqs == 0 || p.H == 0) return KDA_OK;
+    int *err = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void **>(&err), g_kda_error) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    p.err = err;
+    cudaError_t e = kda::launch_simt(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+const char *kda_status_string(int status) {
+    switch (status) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_NULL: return "KDA_ERR_NULL: a required pointer is NULL";
+        case KDA_ERR_DTYPE: return "KDA_ERR_DTYPE: bad state dtype";
+        case KDA_ERR_SHAPE: return "KDA_ERR_SHAPE: inconsistent sizes";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: only K = V = 128 is supported";
+        case KDA_ERR_ALIGN: return "KDA_ERR_ALIGN: tensor pointer not 16-byte aligned";
+        case KDA_ERR_VALUE: return "KDA_ERR_VALUE: lower_bound outside [-5, 0] or non-finite scale";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA call or launch failed";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded device wait expired";
+        default: return "KDA: unknown status";
+    }
+}
+
+kda_status kda_get_device_status(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KDA_ERR_CUDA;
+    int h = 0;
+    if (cudaMemcpyFromSymbol(&h, g_kda_error, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_kda_error, &zero, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    return h == 0 ? KDA_OK : static_cast<kda_status>(h);
+}
+
+int kda_version(void) { return 100; }
+
+}  // extern "C"

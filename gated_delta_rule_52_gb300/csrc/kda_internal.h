@@ -1,0 +1,50 @@
+// Internal launch parameters shared by the host entry points and the kernels of
+// libkda.so.  Not part of the public ABI (that is include/kda.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace kda {
+
+constexpr int kHeadDim = 128;   // K = V = 128, the only supported head size
+constexpr int kChunk = 64;      // tokens per chunk of the UT/WY form
+
+enum StateType : int { kStateNone = 0, kStateBF16 = 1, kStateFP32 = 2 };
+
+// Problem description after host-side validation.  Tensor layouts are those of
+// the FlashKDA README "Kernel API" table: q,k,g [B,T,H,128], v,out [B,T,H,128],
+// beta [B,T,H], A_log [H], dt_bias [H,128], states [N,H,V,K].
+struct Params {
+    const __nv_bfloat16 *q, *k, *v, *g, *beta;
+    __nv_bfloat16 *out;
+    const float *A_log, *dt_bias;
+    float scale, lower_bound;
+    const void *init;   // nullptr = zero state
+    void *fin;          // nullptr = not written
+    int state_type;
+    const int64_t *cu_seqlens;   // nullptr = fixed-length batch
+    int64_t n_seqs;     // N: sequences (B without cu_seqlens)
+    int64_t B, T, H;
+    int *err;           // device error word (bounded waits that give up set it)
+};
+
+// Token range of sequence n: packed batch row `b`, first token `t0`, `len` tokens.
+__device__ __forceinline__ void seq_range(const Params &p, int64_t n, int64_t &b, int64_t &t0,
+                                          int64_t &len) {
+    if (p.cu_seqlens) {
+        b = 0;
+        t0 = p.cu_seqlens[n];
+        len = p.cu_seqlens[n + 1] - t0;
+    } else {
+        b = n;
+        t0 = 0;
+        len = p.T;
+    }
+}
+
+// Launchers (each returns the cudaError_t of its launch).
+cudaError_t launch_simt(const Params &p, cudaStream_t stream);
+
+}  // namespace kda

@@ -1,0 +1,159 @@
+"""ctypes binding of libkda.so (C ABI in include/kda.h).
+
+Argument marshalling only: torch tensors are turned into device pointers and
+sizes, the state tensors' dtype into the ABI's state-dtype code.  Every step of
+the computation runs in the library's CUDA kernels; if the library is missing
+or fails to load this module raises, it never falls back to anything else.
+
+The Python signature mirrors flash_kda.fwd from the FlashKDA README "Kernel
+API" section: ``kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias,
+lower_bound, initial_state=None, final_state=None, cu_seqlens=None)``; it
+returns nothing and writes ``out`` (and ``final_state``) in place.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkda.so")
+
+KDA_OK = 0
+KDA_ERR_NULL = 1
+KDA_ERR_DTYPE = 2
+KDA_ERR_SHAPE = 3
+KDA_ERR_UNSUPPORTED = 4
+KDA_ERR_ALIGN = 5
+KDA_ERR_VALUE = 6
+KDA_ERR_CUDA = 7
+KDA_ERR_TIMEOUT = 8
+
+KDA_STATE_NONE = 0
+KDA_STATE_BF16 = 1
+KDA_STATE_FP32 = 2
+
+# Every symbol include/kda.h declares.
+EXPORTED = ("kda_fwd", "kda_status_string", "kda_get_device_status", "kda_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KDAError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Open libkda.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                   "`python -m gated_delta_rule_52_gb300.build`")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, f, i64, ci = ctypes.c_void_p, ctypes.c_float, ctypes.c_int64, ctypes.c_int
+            L.kda_fwd.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp, f, vp, vp, ci, vp, i64,
+                                  i64, i64, i64, i64, i64, vp]
+            L.kda_fwd.restype = ci
+            L.kda_status_string.argtypes = [ci]
+            L.kda_status_string.restype = ctypes.c_char_p
+            L.kda_get_device_status.argtypes = [vp]
+            L.kda_get_device_status.restype = ci
+            L.kda_version.argtypes = []
+            L.kda_version.restype = ci
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().kda_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_tensor(name, t, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def state_dtype_code(initial_state, final_state) -> int:
+    dts = {t.dtype for t in (initial_state, final_state) if t is not None}
+    if not dts:
+        return KDA_STATE_NONE
+    if len(dts) != 1:
+        raise ValueError("initial_state and final_state must have the same dtype")
+    dt = dts.pop()
+    if dt == torch.bfloat16:
+        return KDA_STATE_BF16
+    if dt == torch.float32:
+        return KDA_STATE_FP32
+    raise ValueError(f"state dtype must be bf16 or fp32, got {dt}")
+
+
+def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=None,
+            final_state=None, cu_seqlens=None, stream=None) -> None:
+    """KDA forward through libkda.so.  Writes ``out`` [B,T,H,V] (and ``final_state``)
+    in place, asynchronously on ``stream`` (default: the current torch stream)."""
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, H, K]")
+    B, T, H, K = q.shape
+    V = v.shape[-1] if v.dim() == 4 else -1
+    _check_tensor("q", q, torch.bfloat16)
+    _check_tensor("k", k, torch.bfloat16, (B, T, H, K))
+    _check_tensor("g", g, torch.bfloat16, (B, T, H, K))
+    _check_tensor("v", v, torch.bfloat16, (B, T, H, V))
+    _check_tensor("beta", beta, torch.bfloat16, (B, T, H))
+    _check_tensor("out", out, torch.bfloat16, (B, T, H, V))
+    _check_tensor("A_log", A_log, torch.float32, (H,))
+    _check_tensor("dt_bias", dt_bias, torch.float32, (H, K))
+    num_seqs = 0
+    if cu_seqlens is not None:
+        _check_tensor("cu_seqlens", cu_seqlens, torch.int64)
+        if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+            raise ValueError("cu_seqlens must be 1-D with at least 2 entries")
+        num_seqs = cu_seqlens.numel() - 1
+    N = num_seqs if cu_seqlens is not None else B
+    code = state_dtype_code(initial_state, final_state)
+    for name, s in (("initial_state", initial_state), ("final_state", final_state)):
+        if s is not None:
+            _check_tensor(name, s, s.dtype, (N, H, V, K))
+    st = lib().kda_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out),
+                       _ptr(A_log), _ptr(dt_bias), float(lower_bound), _ptr(initial_state),
+                       _ptr(final_state), code, _ptr(cu_seqlens), num_seqs, B, T, H, K, V,
+                       _stream_handle(stream))
+    if st != KDA_OK:
+        raise KDAError(st, status_string(st))
+
+
+def get_device_status(stream=None) -> int:
+    """Synchronise ``stream`` and return (and clear) the device error word."""
+    return int(lib().kda_get_device_status(_stream_handle(stream)))
+
+
+def raw_call(*args):
+    """Direct call of the C entry point with already-marshalled arguments (tests of
+    the validation path use this with host-side fake pointers; nothing is launched
+    when validation fails)."""
+    return int(lib().kda_fwd(*args))

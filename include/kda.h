@@ -1,0 +1,116 @@
+/*
+ * kda.h — C ABI of the GB300 (sm_103a) Kimi Delta Attention forward library
+ * (libkda.so).
+ *
+ * The operation is the one the FlashKDA README documents under "Kernel API"
+ * (flash_kda.fwd and its parameter table): the forward pass of KDA, the
+ * channel-wise gated delta rule (agents-report.net "FlashKDA" article,
+ * background section).  Per (sequence, head), with S a K x V state:
+ *
+ *   q_hat, k_hat = L2-normalised q, k        beta_t = sigmoid(beta_logit_t)
+ *   gk_t[c]      = lower_bound * sigmoid(exp(A_log[h]) * (g_t[c] + dt_bias[h][c]))
+ *   S_t          = (I - beta_t k_t k_t^T) Diag(exp(gk_t)) S_{t-1} + beta_t k_t v_t^T
+ *   out_t        = scale * S_t^T q_t
+ *
+ * The pages name the gate inputs (A_log "log-gate parameter", dt_bias "gate
+ * bias", lower_bound "gate lower bound, -5.0 to 0") but print no formula; the
+ * gate above is this library's reading.  The L2 norm uses eps = 1e-6 inside the
+ * square root.
+ *
+ * Everything here is plain C: device pointers, host scalars, a stream handle.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes.  Argument errors are detected on the host before any work is
+ * enqueued; nothing is launched and no output is touched when one is returned. */
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_NULL = 1,        /* a required pointer is NULL (token tensors may be NULL
+                                only when B*T*H == 0; A_log, dt_bias when H == 0)       */
+    KDA_ERR_DTYPE = 2,       /* state pointer given with state_dtype KDA_STATE_NONE,
+                                or an unknown state_dtype code                          */
+    KDA_ERR_SHAPE = 3,       /* negative size, H == 0 with work to do, B != 1 with
+                                cu_seqlens, num_seqs < 1 with cu_seqlens                */
+    KDA_ERR_UNSUPPORTED = 4, /* K != 128 or V != 128 (the only head size supported)    */
+    KDA_ERR_ALIGN = 5,       /* a tensor pointer is not 16-byte aligned                 */
+    KDA_ERR_VALUE = 6,       /* lower_bound outside [-5, 0] or non-finite scale         */
+    KDA_ERR_CUDA = 7,        /* a CUDA runtime call or kernel launch failed             */
+    KDA_ERR_TIMEOUT = 8      /* a bounded on-device wait expired (kda_get_device_status) */
+} kda_status;
+
+/* Element type of initial_state / final_state (both, when both are given). */
+typedef enum {
+    KDA_STATE_NONE = 0,
+    KDA_STATE_BF16 = 1,
+    KDA_STATE_FP32 = 2
+} kda_state_dtype;
+
+/*
+ * kda_fwd — KDA forward pass, written in place into `out` (and `final_state`).
+ * Follows the FlashKDA README "Kernel API" table (flash_kda.fwd) and the 2kiu.com
+ * article on its `out` parameter (section 一, "what is the out parameter": the
+ * caller allocates `out`, the call returns nothing and writes it in place).
+ *
+ * Arguments (all tensors contiguous, row-major, on the current CUDA device):
+ *   q, k, g        bf16 [B, T, H, K]   query, key, gate before activation
+ *   v              bf16 [B, T, H, V]   value
+ *   beta           bf16 [B, T, H]      beta logits (sigmoid applied inside)
+ *   scale          host float          output scale
+ *   out            bf16 [B, T, H, V]   output, fully overwritten (never read)
+ *   A_log          fp32 [H]            log-gate parameter
+ *   dt_bias        fp32 [H, K]         gate bias
+ *   lower_bound    host float in [-5, 0]
+ *   initial_state  [N, H, V, K] or NULL (NULL = zero state); state[n][h][v][c]
+ *                  holds S[c][v] (V before K)
+ *   final_state    [N, H, V, K] or NULL (NULL = not written)
+ *   state_dtype    kda_state_dtype of both states; KDA_STATE_NONE only when both
+ *                  state pointers are NULL
+ *   cu_seqlens     device int64 [num_seqs + 1] or NULL.  With it, B must be 1,
+ *                  sequence n is tokens [cu_seqlens[n], cu_seqlens[n+1]) of the
+ *                  packed T, and N = num_seqs.  Without it, each batch row is a
+ *                  sequence and N = B.  Its contents are not validated on the host
+ *                  (that would need a device sync): they must start at 0, be
+ *                  non-decreasing and end at T.
+ *   B, T, H, K, V  sizes; K = V = 128 is required
+ *   stream         cudaStream_t to enqueue on (NULL = legacy default stream)
+ *
+ * Ownership: the caller owns every buffer.  The call allocates no device memory
+ * and keeps no pointer after it returns.  It is asynchronous: it returns once the
+ * work is enqueued, without synchronising.  q/k/v/g/beta/out/A_log/dt_bias/states
+ * must be 16-byte aligned.  `out` must not alias an input.
+ *
+ * Returns KDA_OK, or an argument error (nothing enqueued), or KDA_ERR_CUDA if
+ * the launch failed.
+ */
+kda_status kda_fwd(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                   float scale, void *out, const float *A_log, const float *dt_bias,
+                   float lower_bound, const void *initial_state, void *final_state,
+                   int state_dtype, const int64_t *cu_seqlens, int64_t num_seqs, int64_t B,
+                   int64_t T, int64_t H, int64_t K, int64_t V, void *stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *kda_status_string(int status);
+
+/*
+ * kda_get_device_status — synchronises `stream`, then reads and clears the
+ * device-side error word that kernels set when a bounded wait gives up
+ * (KDA_ERR_TIMEOUT).  Returns KDA_OK when no kernel reported a problem, or
+ * KDA_ERR_CUDA if the synchronisation itself failed.
+ */
+kda_status kda_get_device_status(void *stream);
+
+/* Library ABI version (major * 100 + minor). */
+int kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,175 @@
+"""GPU parity: libkda (through the C ABI) against the fp64 oracle on the same
+seeded inputs.  Reduced sizes compare every element and still span several
+64-token chunks and ragged tails; the full workload sizes compare sampled
+(sequence, head) pairs, which the oracle computes one by one."""
+import numpy as np
+import pytest
+import torch
+
+from gated_delta_rule_52_gb300 import kda
+from gated_delta_rule_52_gb300 import workloads as W
+from tests import parity_util as pu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from gated_delta_rule_52_gb300 import build
+    build.build_library()
+    kda.lib()
+
+
+REDUCED = {
+    "tiny": W.get("tiny"),
+    "batch_state": W.get("batch_state", T=200, H=4),
+    "prefill_8k": W.get("prefill_8k", T=1000, H=4),
+    "varlen_uniform": W.get("varlen_uniform", T=8 * 130, H=4),
+    "varlen_ragged": W.get("varlen_ragged", H=4, seqlens=(1, 17, 63, 64, 65, 0, 129, 300, 2, 191)),
+}
+
+
+@pytest.mark.parametrize("name", list(REDUCED))
+def test_reduced_all_elements(name):
+    d = W.make_inputs(REDUCED[name])
+    out, fin = pu.run_gpu(d)
+    ref_out, ref_fin = pu.run_oracle(d)
+    res = pu.check(d, out, fin, ref_out, ref_fin, label=name)
+    print(name, res)
+
+
+def _sample_pairs(d, count, seed):
+    N, H = d["N"], d["H"]
+    r = np.random.default_rng(seed)
+    pairs = {(int(r.integers(N)), int(r.integers(H))) for _ in range(count)}
+    pairs.add((N - 1, H - 1))
+    if d["seqlens"] is not None:   # always include the longest sequence
+        pairs.add((int(np.argmax(d["seqlens"])), 0))
+    return sorted(pairs)
+
+
+@pytest.mark.parametrize("name,count", [("batch_state", 6), ("prefill_8k", 4),
+                                        ("varlen_uniform", 6), ("varlen_ragged", 5)])
+def test_full_size_sampled_pairs(name, count):
+    d = W.make_inputs(W.get(name))
+    out, fin = pu.run_gpu(d)
+    pairs = _sample_pairs(d, count, seed=len(name))
+    ref_out, ref_fin = pu.run_oracle(d, pairs=pairs)
+    res = pu.check(d, out, fin, ref_out, ref_fin, pairs=pairs, label=name)
+    print(name, pairs, res)
+    # every output element was written (out was NaN-filled before the call)
+    assert torch.isfinite(out.float()).all()
+    if fin is not None:
+        assert torch.isfinite(fin.float()).all()
+
+
+def test_chained_calls_match_single_call():
+    # Two T=1024 calls chained through final_state -> initial_state equal one T=2048 call.
+    d = W.make_inputs(W.get("batch_state"))
+    out, fin = pu.run_gpu(d)
+    T1 = 1024
+    d1 = dict(d, T=T1, q=d["q"][:, :T1], k=d["k"][:, :T1], v=d["v"][:, :T1], g=d["g"][:, :T1],
+              beta=d["beta"][:, :T1])
+    d1 = {kk: (vv.contiguous() if torch.is_tensor(vv) else vv) for kk, vv in d1.items()}
+    o1, f1 = pu.run_gpu(d1)
+    d2 = dict(d, T=d["T"] - T1, q=d["q"][:, T1:], k=d["k"][:, T1:], v=d["v"][:, T1:],
+              g=d["g"][:, T1:], beta=d["beta"][:, T1:], initial_state=f1)
+    d2 = {kk: (vv.contiguous() if torch.is_tensor(vv) else vv) for kk, vv in d2.items()}
+    o2, f2 = pu.run_gpu(d2)
+    chained = torch.cat([o1, o2], 1).float().numpy()
+    mx, rl = pu.errors(chained, out.float().numpy())
+    assert mx <= pu.OUT_MAX_ABS and rl <= pu.OUT_REL_L2, (mx, rl)
+    _, srl = pu.errors(f2.numpy(), fin.numpy())
+    assert srl <= pu.STATE_REL_L2["fp32"], srl
+    # and the chained result against the oracle on sampled pairs
+    pairs = [(0, 0), (1, 5), (3, 15)]
+    ref_out, ref_fin = pu.run_oracle(d, pairs=pairs)
+    pu.check(d, torch.cat([o1, o2], 1), f2, ref_out, ref_fin, pairs=pairs, label="chained")
+
+
+def test_zero_length_tokens_pass_state_through():
+    d = W.make_inputs(W.get("batch_state", B=2, T=0, H=3))
+    out, fin = pu.run_gpu(d)
+    assert out.numel() == 0
+    torch.testing.assert_close(fin, d["initial_state"], rtol=0, atol=0)
+
+
+def test_state_variants():
+    base = W.get("batch_state", B=2, T=130, H=2)
+    for sd, init in (("fp32", "none"), ("bf16", "normal"), ("bf16", "none")):
+        d = W.make_inputs(W.get("batch_state", B=2, T=130, H=2, state_dtype=sd, initial_state=init))
+        out, fin = pu.run_gpu(d)
+        ref_out, ref_fin = pu.run_oracle(d)
+        pu.check(d, out, fin, ref_out, ref_fin, label=f"{sd}/{init}")
+    # initial state given, final state not requested
+    d = W.make_inputs(base)
+    out, _ = pu.run_gpu(d, want_final=False)
+    ref_out, _ = pu.run_oracle(d, want_final=False)
+    pu.check(d, out, None, ref_out, None, label="no-final")
+    # no state at all
+    d = W.make_inputs(W.get("tiny", state_dtype=None))
+    out, fin = pu.run_gpu(d)
+    assert fin is None
+    ref_out, _ = pu.run_oracle(d, want_final=False)
+    pu.check(d, out, None, ref_out, None, label="stateless")
+
+
+@pytest.mark.parametrize("lb", [0.0, -0.5, -5.0])
+def test_lower_bound_extremes(lb):
+    # lb = 0: no decay (pure delta rule); lb = -5 with large gates: decay saturates.
+    d = W.make_inputs(W.get("varlen_ragged", H=2, seqlens=(70, 129, 5), lower_bound=lb))
+    out, fin = pu.run_gpu(d)
+    ref_out, ref_fin = pu.run_oracle(d)
+    pu.check(d, out, fin, ref_out, ref_fin, label=f"lb={lb}")
+
+
+def test_out_guard_region_untouched():
+    # Varlen tails must not write outside [0, T): surround `out` with guard rows.
+    d = W.make_inputs(W.get("varlen_ragged", H=3, seqlens=(65, 1, 130, 63)))
+    e = pu.to_device(d)
+    T, H = d["T"], d["H"]
+    buf = torch.full((T + 128, H, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    out = buf[64:64 + T].view(1, T, H, 128)
+    fin = torch.empty((d["N"], H, 128, 128), dtype=torch.float32, device="cuda")
+    kda.kda_fwd(e["q"], e["k"], e["v"], e["g"], e["beta"], d["scale"], out, e["A_log"],
+                e["dt_bias"], d["lower_bound"], initial_state=e["initial_state"], final_state=fin,
+                cu_seqlens=e["cu_seqlens"])
+    torch.cuda.synchronize()
+    assert (buf[:64] == 7.0).all() and (buf[64 + T:] == 7.0).all()
+    ref_out, ref_fin = pu.run_oracle(d)
+    pu.check(d, out.cpu(), fin.cpu(), ref_out, ref_fin, label="guard")
+
+
+def test_deterministic():
+    d = W.make_inputs(W.get("prefill_8k", T=700, H=3))
+    a, fa = pu.run_gpu(d)
+    b, fb = pu.run_gpu(d)
+    assert torch.equal(a, b) and torch.equal(fa, fb)
+
+
+def test_runs_on_a_side_stream():
+    d = W.make_inputs(W.get("tiny"))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out, fin = pu.run_gpu(d, stream=s)
+    ref_out, ref_fin = pu.run_oracle(d)
+    pu.check(d, out, fin, ref_out, ref_fin, label="stream")
+
+
+def test_binding_rejects_bad_tensors():
+    d = pu.to_device(W.make_inputs(W.get("tiny")))
+    out = torch.empty_like(d["v"])
+    args = [d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], out, d["A_log"], d["dt_bias"],
+            d["lower_bound"]]
+    bad = list(args); bad[0] = d["q"].float()
+    with pytest.raises(ValueError):
+        kda.kda_fwd(*bad)
+    bad = list(args); bad[2] = d["v"][:, :, :, :64]
+    with pytest.raises(ValueError):
+        kda.kda_fwd(*bad)
+    with pytest.raises(kda.KDAError) as ei:
+        kda.kda_fwd(*args[:9], -7.0)
+    assert ei.value.status == kda.KDA_ERR_VALUE
+    with pytest.raises(ValueError):
+        kda.kda_fwd(*args, initial_state=torch.zeros(1, 2, 128, 128, device="cuda"),
+                    final_state=torch.zeros(1, 2, 128, 128, device="cuda", dtype=torch.bfloat16))
