@@ -69,6 +69,18 @@ def aggregate(tokens_per_rank: int, world: int, times_ms):
     return world * tokens_per_rank / (t / 1e3), t
 
 
+def max_over_ranks(ms: float, device=None) -> float:
+    """Max of a per-rank duration over all ranks (identity without a process group).
+    Works with gloo (CPU tensors) and nccl (device tensors)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def algorithmic_bytes(d) -> int:
     th = d["B"] * d["T"] * d["H"]
     sb = {"fp32": 4, "bf16": 2, None: 0}[d["state_dtype"]]
@@ -315,11 +327,7 @@ def run_ours(args):
         raise RuntimeError("device reported an error during the timed region")
     per_step = [s.elapsed_time(t) for s, t in zip(starts, ends)]
     kernel_ms = sum(per_step)
-    times = [kernel_ms]
-    if ws > 1:
-        tt = torch.tensor([kernel_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        times = [float(tt.item())]
+    times = [max_over_ranks(kernel_ms, dev)]
     tokens_per_rank = B * T * args.steps
     value, tmax = aggregate(tokens_per_rank, ws, times)
     ms_per_step = tmax / args.steps

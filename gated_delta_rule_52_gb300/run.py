@@ -1,0 +1,69 @@
+"""Runs kda_fwd on a seeded synthetic workload (for profiling and quick checks).
+
+  python -m gated_delta_rule_52_gb300.run [--workload prefill_8k] [--T 2048] [--H 64]
+                                          [--iters 3] [--check]
+
+Builds libkda.so if needed, draws the workload's inputs on the GPU, calls
+kda_fwd `iters` times and prints the CUDA-event time of the last call.  With
+--check it also compares a few (sequence, head) pairs with the fp64 oracle (a
+test-only dependency).
+"""
+import argparse
+import os
+import sys
+
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from gated_delta_rule_52_gb300 import build, kda  # noqa: E402
+from gated_delta_rule_52_gb300 import workloads as W  # noqa: E402
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="prefill_8k")
+    ap.add_argument("--T", type=int, default=None)
+    ap.add_argument("--H", type=int, default=None)
+    ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--check", action="store_true")
+    a = ap.parse_args(argv)
+    over = {}
+    if a.T is not None:
+        over["T"] = a.T
+    if a.H is not None:
+        over["H"] = a.H
+    build.build_library()
+    d = W.make_inputs(W.get(a.workload, **over))
+    e = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in d.items()}
+    out = torch.empty((d["B"], d["T"], d["H"], 128), dtype=torch.bfloat16, device="cuda")
+    fin = None
+    if d["state_dtype"]:
+        fin = torch.empty((d["N"], d["H"], 128, 128), device="cuda",
+                          dtype=torch.bfloat16 if d["state_dtype"] == "bf16" else torch.float32)
+    s, t = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(a.iters):
+        s.record()
+        kda.kda_fwd(e["q"], e["k"], e["v"], e["g"], e["beta"], e["scale"], out, e["A_log"],
+                    e["dt_bias"], e["lower_bound"], initial_state=e["initial_state"],
+                    final_state=fin, cu_seqlens=e["cu_seqlens"])
+        t.record()
+    torch.cuda.synchronize()
+    st = kda.get_device_status()
+    print(f"{a.workload} B={d['B']} T={d['T']} H={d['H']}: {s.elapsed_time(t):.3f} ms "
+          f"(last call), device status {st}")
+    if st != kda.KDA_OK:
+        return 1
+    if a.check:
+        sys.path.insert(0, ROOT)
+        from tests import parity_util as pu
+        pairs = [(0, 0), (d["N"] - 1, d["H"] - 1)]
+        ro, rf = pu.run_oracle(d, pairs=pairs)
+        print(pu.check(d, out.cpu(), fin.cpu() if fin is not None else None, ro, rf, pairs=pairs))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

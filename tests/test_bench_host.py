@@ -1,0 +1,79 @@
+"""Host-side logic of bench.py without a GPU: the roofline byte/FLOP model, the
+weak-scaling shard seeds and aggregation, and the cross-rank max reduction over
+world_size-2 gloo process groups."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+from gated_delta_rule_52_gb300 import workloads as W
+
+
+def test_roofline_model_prefill():
+    d = W.make_inputs(W.get("prefill_8k", T=64, H=2))   # small draw, then scale the sizes
+    d = dict(d, T=8192, H=64, N=1)
+    # 524,288 token-heads x 1,282 B + 64 heads x bf16 state in and out
+    assert bench.algorithmic_bytes(d) == 524288 * 1282 + 64 * 128 * 128 * 2 * 2 == 676331520
+    assert bench.algorithmic_flops(d) == 524288 * 180224
+
+
+def test_roofline_model_state_variants():
+    base = dict(B=1, T=64, H=2, N=1)
+    d = dict(base, state_dtype=None, initial_state=None)
+    assert bench.algorithmic_bytes(d) == 128 * 1282
+    d = dict(base, state_dtype="fp32", initial_state=None)        # final only
+    assert bench.algorithmic_bytes(d) == 128 * 1282 + 2 * 128 * 128 * 4
+    d = dict(base, state_dtype="fp32", initial_state=object())    # in and out
+    assert bench.algorithmic_bytes(d) == 128 * 1282 + 2 * 2 * 128 * 128 * 4
+
+
+def test_shard_seeds_distinct_and_aggregate():
+    seeds = {bench.shard_seed(2, r) for r in range(8)}
+    assert len(seeds) == 8
+    value, t = bench.aggregate(8192, 4, [10.0, 12.5, 11.0, 9.0])
+    assert t == 12.5 and value == pytest.approx(4 * 8192 / 0.0125)
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _rank_main(rank, world, port, ms_list, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        m = bench.max_over_ranks(ms_list[rank])
+        value, t = bench.aggregate(1000, world, [m])
+        out[rank] = (m, value)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
+    port = _free_port()
+    ms = [3.0, 7.5]
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, ms, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    for r in range(2):
+        m, value = out[r]
+        assert m == 7.5
+        assert value == pytest.approx(2 * 1000 / 0.0075)
+
+
+def test_max_over_ranks_without_group_is_identity():
+    assert bench.max_over_ranks(4.25) == 4.25

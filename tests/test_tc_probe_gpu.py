@@ -1,0 +1,63 @@
+"""tcgen05 building blocks on the GPU: single MMAs through the shared-memory
+descriptor encodings (K-major and MN-major 128B-swizzled tiles, M = 128, the N
+and K extents the KDA kernel uses) against torch.matmul, plus a TMEM store/load
+round trip."""
+import ctypes
+
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def probe():
+    from gated_delta_rule_52_gb300 import build
+    L = ctypes.CDLL(build.build_probe())
+    L.kda_probe_mma.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 5 + [ctypes.c_void_p] * 2
+    L.kda_probe_mma.restype = ctypes.c_int
+    return L
+
+
+CASES = [(N, K, a, b, f) for (N, K) in [(64, 64), (64, 128), (128, 128), (160, 128), (192, 64),
+                                        (256, 64)]
+         for a in (0, 1) for b in (0, 1) for f in (0, 1) if not (b and N % 64)]
+
+
+@pytest.mark.parametrize("N,K,a_mn,b_mn,fp16", CASES)
+def test_mma_layouts(probe, N, K, a_mn, b_mn, fp16):
+    g = torch.Generator(device="cpu").manual_seed(N * 1000 + K * 10 + 2 * a_mn + b_mn)
+    A = torch.randn(128, K, generator=g).to(torch.bfloat16).cuda()
+    B = torch.randn(K, N, generator=g).to(torch.bfloat16).cuda()
+    D = torch.full((128, N), float("nan"), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = probe.kda_probe_mma(A.data_ptr(), B.data_ptr(), D.data_ptr(), N, K, a_mn, b_mn, fp16,
+                             st.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert st.item() == 0, f"probe status {st.item()}"
+    # bf16 inputs convert exactly to fp16 at these magnitudes, so both kinds match
+    ref = A.float() @ B.float()
+    torch.testing.assert_close(D, ref, rtol=1e-4, atol=1e-4)
+
+
+@pytest.mark.parametrize("T,H,h,t0,c0", [(256, 4, 1, 0, 0), (256, 4, 3, 37, 64), (100, 2, 0, 70, 0),
+                                         (300, 64, 63, 256, 64)])
+def test_tma_3d_swizzled_load(probe, T, H, h, t0, c0):
+    probe.kda_probe_tma.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                    ctypes.c_void_p]
+    probe.kda_probe_tma.restype = ctypes.c_int
+    g = torch.Generator(device="cpu").manual_seed(T + H + h + t0 + c0)
+    src = torch.randn(T, H, 128, generator=g).to(torch.bfloat16).cuda()
+    out = torch.full((64, 64), float("nan"), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = probe.kda_probe_tma(src.data_ptr(), T, H, h, t0, c0, out.data_ptr(), st.data_ptr(),
+                             torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, rc
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    ref = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
+    n = max(0, min(64, T - t0))
+    ref[:n] = src[t0:t0 + n, h, c0:c0 + 64]
+    assert torch.equal(out, ref)
