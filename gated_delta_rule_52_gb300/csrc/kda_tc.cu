@@ -50,7 +50,7 @@ constexpr int VS = 64;                 // V columns per CTA
 constexpr int NSLICE = kHeadDim / VS;
 constexpr int NT = 256;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr uint32_t kWaitLimit = 1u << 20;
+constexpr uint64_t kWaitLimit = 2000000000ull;  // 2 s per wait, then KDA_ERR_TIMEOUT
 
 // Tensor-memory columns (512 allocated; lanes = rows of each MMA's D).
 constexpr uint32_t COL_S = 0;      // S[c][v]           64 cols

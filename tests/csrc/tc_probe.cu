@@ -72,7 +72,7 @@ probe_kernel(const __nv_bfloat16 *A, const __nv_bfloat16 *B, float *D, int N, in
         }
         mma_commit(&bar);
     }
-    if (!mbar_wait(&bar, 0, 1u << 22)) {
+    if (!mbar_wait(&bar, 0, 2000000000ull)) {
         if (lane == 0) atomicExch(status, 1);
     }
     tc_fence_after();
@@ -137,7 +137,7 @@ __global__ void tma_probe_kernel(const __grid_constant__ CUtensorMap tmap, int h
         mbar_arrive_expect_tx(&bar, 64 * 64 * 2);
         tma_load_3d(tile, &tmap, &bar, c0, h, t0);
     }
-    if (!mbar_wait(&bar, 0, 1u << 22)) {
+    if (!mbar_wait(&bar, 0, 2000000000ull)) {
         if (threadIdx.x == 0) atomicExch(status, 1);
         return;
     }
