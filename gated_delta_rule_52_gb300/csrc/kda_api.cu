@@ -84,7 +84,7 @@ kda_status kda_fwd(const void *q, const void *k, const void *v, const void *g, c
     if (cudaGetSymbolAddress(reinterpret_cast<void **>(&err), g_kda_error) != cudaSuccess)
         return KDA_ERR_CUDA;
     p.err = err;
-    cudaError_t e = kda::launch_tc(p, static_cast<cudaStream_t>(stream));
+    cudaError_t e = kda::launch_cluster(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
