@@ -51,7 +51,7 @@ constexpr int NP = 256;            // front prologue group: warps 0-7
 constexpr int NS = 128;            // front solver group: warps 8-11
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kWait = 2000000000ull;   // 2 s per wait
-constexpr int LDA = 65;
+constexpr int LDA = 68;             // fp32 row stride of A and T (16-byte aligned rows)
 constexpr uint32_t kChunkBytes = 16384 * 3 + 512 + 8192 * 2;   // front -> chain per chunk
 
 // ---- front shared memory
@@ -60,9 +60,9 @@ constexpr uint32_t F_SLOT = 49152;
 constexpr uint32_t F_AMA = 98304;      // [Kp; Qp]: 2 x [128][64] bf16
 constexpr uint32_t F_AMB = 131072;     // Kn variants: 2 x [160][64] bf16
 constexpr uint32_t F_MST = 172032;     // M staging fp16 [64 t][64 i]
-constexpr uint32_t F_AMAT = 180224;    // A fp32 [64][65]; T' staging (fp16) after the inverse
-constexpr uint32_t F_TF = 196864;      // T fp32 [64][65]
-constexpr uint32_t F_ZS = 213504;      // inverse scratch fp32 [3][16][16]
+constexpr uint32_t F_AMAT = 180224;    // A fp32 [64][68]; T' staging (fp16) after the inverse
+constexpr uint32_t F_TF = 197632;      // T fp32 [64][68]
+constexpr uint32_t F_ZS = 215040;      // inverse scratch fp32 [3][16][16]
 // ---- chain shared memory
 constexpr uint32_t C_B2 = 0;           // K_hat*Gamma 2 x [64 i][64 c] | V 2 x [64 t][64 v] (MN-major)
 constexpr uint32_t C_G3A = 32768;      // [-W; Q_hat*Gamma]: 2 x [128][64] (K-major)
@@ -70,7 +70,7 @@ constexpr uint32_t C_KB = 65536;       // 2 slots x Kbar 2 x [64 i][64 c] (MN-ma
 constexpr uint32_t C_TZM = 98304;      // T' | Z | M0 | Z | M1, each [64][64] (K-major)
 constexpr uint32_t C_SB = 139264;      // S fp16 2 x [128 c][64 v] (MN-major)
 constexpr uint32_t C_UT = 172032;      // U fp16 2 x [64 i][64 v] (MN-major)
-constexpr uint32_t SMALL = 216576;     // common offset in both CTAs (remote addresses)
+constexpr uint32_t SMALL = 218112;     // common offset in both CTAs (remote addresses)
 
 struct Small {
     float rq[2][C], rk[2][C], beta[2][C];   // front, per slot
@@ -86,6 +86,56 @@ constexpr uint32_t SMEM_BYTES = SMALL + sizeof(Small) + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 __device__ __forceinline__ int variant_off(int bt) { return 8 * bt * (bt + 1); }
+
+// G1's A-operand rows hold the 16-token blocks in the order 0, 3, 1, 2, so that
+// each 32-lane TMEM quarter of the result needs 80 of the 160 variant columns
+// (blocks 0 and 3: variants 0 and 3; blocks 1 and 2: variants 1 and 2).
+__device__ __forceinline__ int row_block_of(int blk) { return (0x1320 >> (4 * blk)) & 0xF; }
+__device__ __forceinline__ int block_of_row_block(int rb) { return (0x2130 >> (4 * rb)) & 0xF; }
+
+// One off-diagonal level of the blocked inverse T = (I + A)^-1 (16x16 blocks):
+// for every block pair (bt, ba) with bt - ba = D,
+//   Z = sum_{ba <= m < bt} A[bt][m] T[m][ba],   T[bt][ba] = -T[bt][bt] Z.
+// Each task computes four adjacent columns of one row (float4 accumulators).
+template <int D>
+__device__ __forceinline__ void inverse_level(const float *Amat, float *Tf, float *Zs, int stid,
+                                              int nthreads, uint32_t bar_id) {
+    constexpr int NTASK = (4 - D) * 64;
+    for (int task = stid; task < NTASK; task += nthreads) {
+        const int ba = task >> 6, r = (task >> 2) & 15, jg = task & 3, bt = ba + D;
+        const float *arow = Amat + (16 * bt + r) * LDA + 16 * ba;
+        const float *tcol = Tf + (16 * ba) * LDA + 16 * ba + 4 * jg;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < 16 * D; ++q) {
+            const float a = arow[q];
+            const float4 tv = *reinterpret_cast<const float4 *>(tcol + q * LDA);
+            acc.x = fmaf(a, tv.x, acc.x);
+            acc.y = fmaf(a, tv.y, acc.y);
+            acc.z = fmaf(a, tv.z, acc.z);
+            acc.w = fmaf(a, tv.w, acc.w);
+        }
+        *reinterpret_cast<float4 *>(Zs + ba * 256 + r * 16 + 4 * jg) = acc;
+    }
+    named_bar(bar_id, nthreads);
+    for (int task = stid; task < NTASK; task += nthreads) {
+        const int ba = task >> 6, r = (task >> 2) & 15, jg = task & 3, bt = ba + D;
+        const float *trow = Tf + (16 * bt + r) * LDA + 16 * bt;   // T[bt][bt] row (zero above r)
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const float a = trow[q];
+            const float4 z = *reinterpret_cast<const float4 *>(Zs + ba * 256 + q * 16 + 4 * jg);
+            acc.x = fmaf(a, z.x, acc.x);
+            acc.y = fmaf(a, z.y, acc.y);
+            acc.z = fmaf(a, z.z, acc.z);
+            acc.w = fmaf(a, z.w, acc.w);
+        }
+        *reinterpret_cast<float4 *>(Tf + (16 * bt + r) * LDA + 16 * ba + 4 * jg) =
+            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+    }
+    named_bar(bar_id, nthreads);
+}
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool fp16) {
     return fp16 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
@@ -139,6 +189,7 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
         const float a2 = -__expf(p.A_log[h]) * kLog2e;
         const float lb2 = p.lower_bound * kLog2e;
         const int blk = warp >> 1;                   // 16-token block
+        const int arow0 = 16 * row_block_of(blk);    // its rows in G1's A operand
         const int c = (warp & 1) * 64 + 2 * lane;    // channel pair (c, c+1)
         const int kb = c >> 6, cc = c & 63;
         const float b0 = a2 * p.dt_bias[h * DK + c], b1 = a2 * p.dt_bias[h * DK + c + 1];
@@ -156,35 +207,48 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
             named_bar(1, NP);
             if (sm.abort_p) break;
 
-            // norms and beta
-            for (int t = warp; t < C; t += NP / 32) {
-                const int kbb = lane >> 4, col = (lane * 4) & 63;
-                const uint32_t off = kbb * 8192 + sw128_off(t, col);
-                const uint2 qv = *reinterpret_cast<const uint2 *>(smem + rq_off + off);
-                const uint2 kv = *reinterpret_cast<const uint2 *>(smem + rk_off + off);
-                float sq = bf16lo(qv.x) * bf16lo(qv.x) + bf16hi(qv.x) * bf16hi(qv.x) +
-                           bf16lo(qv.y) * bf16lo(qv.y) + bf16hi(qv.y) * bf16hi(qv.y);
-                float sk = bf16lo(kv.x) * bf16lo(kv.x) + bf16hi(kv.x) * bf16hi(kv.x) +
-                           bf16lo(kv.y) * bf16lo(kv.y) + bf16hi(kv.y) * bf16hi(kv.y);
+            // beta logits: global loads issued first, consumed after the norms
+            float bl0 = 0.f, bl1 = 0.f;
+            if (warp == 0) {
+                if (lane < L) bl0 = __bfloat162float(p.beta[(row0 + lane) * p.H + h]);
+                if (lane + 32 < L) bl1 = __bfloat162float(p.beta[(row0 + lane + 32) * p.H + h]);
+            }
+            // norms: each warp 8 rows, two at a time
+#pragma unroll 2
+            for (int t2 = 0; t2 < C / 16; ++t2) {
+                float sq[2], sk[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int t = warp + (NP / 32) * (2 * t2 + u);
+                    const int kbb = lane >> 4, col = (lane * 4) & 63;
+                    const uint32_t off = kbb * 8192 + sw128_off(t, col);
+                    const uint2 qv = *reinterpret_cast<const uint2 *>(smem + rq_off + off);
+                    const uint2 kv = *reinterpret_cast<const uint2 *>(smem + rk_off + off);
+                    sq[u] = bf16lo(qv.x) * bf16lo(qv.x) + bf16hi(qv.x) * bf16hi(qv.x) +
+                            bf16lo(qv.y) * bf16lo(qv.y) + bf16hi(qv.y) * bf16hi(qv.y);
+                    sk[u] = bf16lo(kv.x) * bf16lo(kv.x) + bf16hi(kv.x) * bf16hi(kv.x) +
+                            bf16lo(kv.y) * bf16lo(kv.y) + bf16hi(kv.y) * bf16hi(kv.y);
+                }
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) {
-                    sq += __shfl_xor_sync(0xffffffffu, sq, o);
-                    sk += __shfl_xor_sync(0xffffffffu, sk, o);
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        sq[u] += __shfl_xor_sync(0xffffffffu, sq[u], o);
+                        sk[u] += __shfl_xor_sync(0xffffffffu, sk[u], o);
+                    }
                 }
                 if (lane == 0) {
-                    sm.rq[s][t] = t < L ? rsqrtf(sq + 1e-6f) : 0.f;
-                    sm.rk[s][t] = t < L ? rsqrtf(sk + 1e-6f) : 0.f;
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int t = warp + (NP / 32) * (2 * t2 + u);
+                        sm.rq[s][t] = t < L ? rsqrtf(sq[u] + 1e-6f) : 0.f;
+                        sm.rk[s][t] = t < L ? rsqrtf(sk[u] + 1e-6f) : 0.f;
+                    }
                 }
             }
             if (warp == 0) {
-                for (int t = lane; t < C; t += 32) {
-                    float bt = 0.f;
-                    if (t < L) {
-                        const float bl = __bfloat162float(p.beta[(row0 + t) * p.H + h]);
-                        bt = 1.f / (1.f + exp2f(-bl * kLog2e));
-                    }
-                    sm.beta[s][t] = bt;
-                }
+                sm.beta[s][lane] = lane < L ? 1.f / (1.f + exp2f(-bl0 * kLog2e)) : 0.f;
+                sm.beta[s][lane + 32] = lane + 32 < L ? 1.f / (1.f + exp2f(-bl1 * kLog2e)) : 0.f;
             }
 
             // gate and block-local cumulative decay (log2 units)
@@ -252,10 +316,10 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                 const float kp0 = k0 * e10, kp1 = k1 * e11;
                 const float qp0 = q0 * e10, qp1 = q1 * e11;
                 const float kn0 = k0 * e20, kn1 = k1 * e21;
-                *reinterpret_cast<uint32_t *>(smem + F_AMA + kb * 16384 + sw128_off(t, cc)) =
+                *reinterpret_cast<uint32_t *>(smem + F_AMA + kb * 16384 + sw128_off(arow0 + r, cc)) =
                     pack_bf16(kp0, kp1);
-                *reinterpret_cast<uint32_t *>(smem + F_AMA + kb * 16384 + sw128_off(64 + t, cc)) =
-                    pack_bf16(qp0, qp1);
+                *reinterpret_cast<uint32_t *>(smem + F_AMA + kb * 16384 +
+                                              sw128_off(64 + arow0 + r, cc)) = pack_bf16(qp0, qp1);
 #pragma unroll
                 for (int bt = 0; bt < 4; ++bt) {
                     if (bt >= blk) {
@@ -334,9 +398,9 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
             // A (fp32, beta_t/|k_t| x 1/|k_i|, strictly lower) and M (fp16, 1/|q_t| x 1/|k_i|)
             {
                 const bool is_m = sw >= 2;
-                const int t = (sw & 1) * 32 + lane;
-                const int bt = t >> 4;
-                const int jlo = (sw & 1) ? 3 : 0, jhi = (sw & 1) ? 10 : 3;
+                const int lr = (sw & 1) * 32 + lane;            // row within the A or M half
+                const int bt = block_of_row_block(lr >> 4);
+                const int t = 16 * bt + (lr & 15);
                 const float rowf = is_m ? sm.rq[s][t] : sm.beta[s][t] * sm.rk[s][t];
                 for (int i = 16 * (bt + 1); i < 64; i += 16) {
                     if (is_m) {
@@ -347,10 +411,9 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                         for (int e = 0; e < 16; ++e) Amat[t * LDA + i + e] = 0.f;
                     }
                 }
-                for (int jj = jlo; jj < jhi; ++jj) {
-                    float r[16];
-                    tmem_ld16(tmem_addr(tmem, sw * 32, 256 * s + 16 * jj), r);
-                    tmem_ld_wait();
+                // this quarter's five 16-column chunks: {0, 6..9} or {1..5}
+                auto chunk_of = [&](int k) { return (sw & 1) ? 1 + k : (k == 0 ? 0 : 5 + k); };
+                auto emit = [&](int jj, float (&r)[16]) {
                     const int vo = variant_off(bt);
                     if (16 * jj >= vo && 16 * jj < vo + 16 * (bt + 1)) {
                         const int ib = 16 * jj - vo;
@@ -366,7 +429,20 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                                     (ib + e < t) ? rowf * sm.rk[s][ib + e] * r[e] : 0.f;
                         }
                     }
-                }
+                };
+                float r0[16], r1[16], r2[16];
+                tmem_ld16(tmem_addr(tmem, sw * 32, 256 * s + 16 * chunk_of(0)), r0);
+                tmem_ld16(tmem_addr(tmem, sw * 32, 256 * s + 16 * chunk_of(1)), r1);
+                tmem_ld16(tmem_addr(tmem, sw * 32, 256 * s + 16 * chunk_of(2)), r2);
+                tmem_ld_wait();
+                emit(chunk_of(0), r0);
+                emit(chunk_of(1), r1);
+                emit(chunk_of(2), r2);
+                tmem_ld16(tmem_addr(tmem, sw * 32, 256 * s + 16 * chunk_of(3)), r0);
+                tmem_ld16(tmem_addr(tmem, sw * 32, 256 * s + 16 * chunk_of(4)), r1);
+                tmem_ld_wait();
+                emit(chunk_of(3), r0);
+                emit(chunk_of(4), r1);
             }
             tc_fence_before();
             named_bar(2, NS);
@@ -390,25 +466,9 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                 for (int r = 0; r < 16; ++r) Tf[(16 * bb + r) * LDA + 16 * bb + j] = x[r];
             }
             named_bar(2, NS);
-            for (int d = 1; d < 4; ++d) {
-                const int cnt = (4 - d) * 256;
-                for (int e = stid; e < cnt; e += NS) {
-                    const int ba = e >> 8, r = (e >> 4) & 15, j = e & 15, bt = ba + d;
-                    float acc = 0.f;
-                    for (int q = 16 * ba; q < 16 * bt; ++q)
-                        acc = fmaf(Amat[(16 * bt + r) * LDA + q], Tf[q * LDA + 16 * ba + j], acc);
-                    Zs[e] = acc;
-                }
-                named_bar(2, NS);
-                for (int e = stid; e < cnt; e += NS) {
-                    const int ba = e >> 8, r = (e >> 4) & 15, j = e & 15, bt = ba + d;
-                    float acc = 0.f;
-                    for (int q = 0; q <= r; ++q)
-                        acc = fmaf(Tf[(16 * bt + r) * LDA + 16 * bt + q], Zs[(ba << 8) + q * 16 + j], acc);
-                    Tf[(16 * bt + r) * LDA + 16 * ba + j] = -acc;
-                }
-                named_bar(2, NS);
-            }
+            inverse_level<1>(Amat, Tf, Zs, stid, NS, 2);
+            inverse_level<2>(Amat, Tf, Zs, stid, NS, 2);
+            inverse_level<3>(Amat, Tf, Zs, stid, NS, 2);
             // T' = T Diag(beta), fp16, into the staging tile (over the dead A)
             {
                 const int t = stid >> 1, i0 = (stid & 1) * 32;
@@ -492,6 +552,21 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
             }
         }
     };
+    // D_S columns of this warp (lane quarter, column half) times g, written back
+    auto scale_s = [&](float g) {
+        float r[4][16];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+            tmem_ld16(tmem_addr(D_S, quarter * 32, 64 * half + 16 * jj), r[jj]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) r[jj][e] *= g;
+            tmem_st16(tmem_addr(D_S, quarter * 32, 64 * half + 16 * jj), r[jj]);
+        }
+        tmem_st_wait();
+    };
     auto issue_g2w = [&]() {
         const uint32_t id = idesc_fp16(128, 128, false, true);
         for (int ks = 0; ks < C / 16; ++ks)
@@ -546,8 +621,11 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
         }
         if (lead_wait(ok)) nchunks = 0;
         if (nchunks > 0) {
+            tc_fence_after();
+            if (warp < 8) scale_s(sm.gamC_c[0][quarter * 32 + lane]);
             convert_v();
             fence_proxy_async_smem();
+            tc_fence_before();
             __syncthreads();
             if (tid == 0) {
                 tc_fence_after();
@@ -592,26 +670,17 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
             mbar_arrive_remote(front_bar(&sm.single_free));
             if (m + 1 < nchunks) issue_v(m + 1);
         }
-        if (warp < 8) {
-            const int c = quarter * 32 + lane;
-            const float g = sm.gamC_c[s][c];
-            for (int jj = 0; jj < 4; ++jj) {
-                float r[16];
-                const uint32_t a = tmem_addr(D_S, quarter * 32, 64 * half + 16 * jj);
-                tmem_ld16(a, r);
+        if (warp == 8 || warp == 9) {
+            const int t = (warp - 8) * 32 + lane;
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+                float r[4][16];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    tmem_ld16(tmem_addr(D_U, (warp & 3) * 32, 64 * hb + 16 * jj), r[jj]);
                 tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) r[e] *= g;
-                tmem_st16(a, r);
-            }
-            tmem_st_wait();
-        } else if (warp == 8 || warp == 9) {
-            const int t = (warp - 8) * 32 + lane;
-            for (int jj = 0; jj < 8; ++jj) {
-                float r[16];
-                tmem_ld16(tmem_addr(D_U, (warp & 3) * 32, 16 * jj), r);
-                tmem_ld_wait();
-                st_pack16<true>(sbase + C_UT + (jj >> 2) * 8192, t, (16 * jj) & 63, r);
+                for (int jj = 0; jj < 4; ++jj) st_pack16<true>(sbase + C_UT + hb * 8192, t, 16 * jj, r[jj]);
             }
         }
         fence_proxy_async_smem();
@@ -650,28 +719,47 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
         if (lead_wait(ok)) break;
         tc_fence_after();
 
-        // (d) O -> out; S -> fp16 operand; next chunk's -W and V
+        // (d) S -> fp16 operand, S *= Gamma_C of the next chunk; O -> out; next -W and V
         if (warp < 8) {
             const int c = quarter * 32 + lane;
-            for (int jj = 0; jj < 4; ++jj) {
-                float r[16];
-                tmem_ld16(tmem_addr(D_S, quarter * 32, 64 * half + 16 * jj), r);
-                tmem_ld_wait();
-                st_pack16<true>(sbase + C_SB + half * 16384, c, 16 * jj, r);
+            float r[4][16];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+                tmem_ld16(tmem_addr(D_S, quarter * 32, 64 * half + 16 * jj), r[jj]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) st_pack16<true>(sbase + C_SB + half * 16384, c, 16 * jj, r[jj]);
+            if (m + 1 < nchunks) {
+                const float g = sm.gamC_c[s ^ 1][c];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) r[jj][e] *= g;
+                    tmem_st16(tmem_addr(D_S, quarter * 32, 64 * half + 16 * jj), r[jj]);
+                }
+                tmem_st_wait();
             }
         } else if (warp == 10 || warp == 11) {
             const int t = (warp - 10) * 32 + lane;
             const float sc = p.scale;
-            for (int jj = 0; jj < 8; ++jj) {
-                float r[16];
-                tmem_ld16(tmem_addr(D_U, (warp & 3) * 32, 16 * jj), r);
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+                float r[4][16];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    tmem_ld16(tmem_addr(D_U, (warp & 3) * 32, 64 * hb + 16 * jj), r[jj]);
                 tmem_ld_wait();
                 if (t < L) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((row0 + t) * p.H + h) * DK + 16 * jj);
-                    dst[0] = make_uint4(pack_bf16(sc * r[0], sc * r[1]), pack_bf16(sc * r[2], sc * r[3]),
-                                        pack_bf16(sc * r[4], sc * r[5]), pack_bf16(sc * r[6], sc * r[7]));
-                    dst[1] = make_uint4(pack_bf16(sc * r[8], sc * r[9]), pack_bf16(sc * r[10], sc * r[11]),
-                                        pack_bf16(sc * r[12], sc * r[13]), pack_bf16(sc * r[14], sc * r[15]));
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((row0 + t) * p.H + h) * DK +
+                                                               64 * hb + 16 * jj);
+                        const float *x = r[jj];
+                        dst[0] = make_uint4(pack_bf16(sc * x[0], sc * x[1]), pack_bf16(sc * x[2], sc * x[3]),
+                                            pack_bf16(sc * x[4], sc * x[5]), pack_bf16(sc * x[6], sc * x[7]));
+                        dst[1] = make_uint4(pack_bf16(sc * x[8], sc * x[9]), pack_bf16(sc * x[10], sc * x[11]),
+                                            pack_bf16(sc * x[12], sc * x[13]), pack_bf16(sc * x[14], sc * x[15]));
+                    }
                 }
             }
         }
