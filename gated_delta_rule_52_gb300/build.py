@@ -19,6 +19,7 @@ OUT = os.path.join(PKG, "libkda.so")
 OBJ = os.path.join(PKG, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
+         "-ftz=true", "-prec-div=false", "-prec-sqrt=false",
          "--expt-relaxed-constexpr", "-cudart", "shared"]
 
 

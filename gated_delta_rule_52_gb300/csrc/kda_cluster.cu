@@ -93,6 +93,86 @@ __device__ __forceinline__ int variant_off(int bt) { return 8 * bt * (bt + 1); }
 __device__ __forceinline__ int row_block_of(int blk) { return (0x1320 >> (4 * blk)) & 0xF; }
 __device__ __forceinline__ int block_of_row_block(int rb) { return (0x2130 >> (4 * rb)) & 0xF; }
 
+// 16x16 = 16xK * Kx16 block product on the tensor cores (mma.sync, tf32 with a
+// hi/lo split of both operands: hi*hi + hi*lo + lo*hi, ~fp32 accuracy).
+// A(r, k) = a[r * lda + k], B(k, c) = b[k * ldb + c]; acc holds two 16x8 tiles.
+template <int K>
+__device__ __forceinline__ void block_mma_16x16(const float *a, int lda, const float *b, int ldb,
+                                                int lane, float (&acc)[2][4]) {
+    const int g = lane >> 2, q = lane & 3;
+    float av[K / 8][4], bv[K / 8][2][2];
+#pragma unroll
+    for (int kk = 0; kk < K / 8; ++kk) {   // all operand loads first
+        av[kk][0] = a[g * lda + 8 * kk + q];
+        av[kk][1] = a[(g + 8) * lda + 8 * kk + q];
+        av[kk][2] = a[g * lda + 8 * kk + q + 4];
+        av[kk][3] = a[(g + 8) * lda + 8 * kk + q + 4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            bv[kk][nt][0] = b[(8 * kk + q) * ldb + 8 * nt + g];
+            bv[kk][nt][1] = b[(8 * kk + q + 4) * ldb + 8 * nt + g];
+        }
+    }
+    float corr[2][4] = {};   // hi*lo + lo*hi terms, a separate dependency chain
+#pragma unroll
+    for (int kk = 0; kk < K / 8; ++kk) {
+        uint32_t ah[4], al[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            ah[i] = to_tf32(av[kk][i]);
+            al[i] = to_tf32(av[kk][i] - __uint_as_float(ah[i]));
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            uint32_t bh[2], bl[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                bh[i] = to_tf32(bv[kk][nt][i]);
+                bl[i] = to_tf32(bv[kk][nt][i] - __uint_as_float(bh[i]));
+            }
+            mma_tf32_16x8x8(acc[nt], ah, bh);
+            mma_tf32_16x8x8(corr[nt], al, bh);
+            mma_tf32_16x8x8(corr[nt], ah, bl);
+        }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nt][i] += corr[nt][i];
+}
+
+// Off-diagonal levels of the blocked inverse on one warp per block pair (bt, ba),
+// bt - ba = D: Z = sum_{ba <= m < bt} A[bt][m] T[m][ba], T[bt][ba] = -T[bt][bt] Z.
+template <int D>
+__device__ __forceinline__ void inverse_level_mma(const float *Amat, float *Tf, float *Zs, int wq,
+                                                  int lane) {
+    if (wq < 4 - D) {
+        const int ba = wq, bt = ba + D, g = lane >> 2, q = lane & 3;
+        float z[2][4] = {};
+        block_mma_16x16<16 * D>(Amat + (16 * bt) * LDA + 16 * ba, LDA, Tf + (16 * ba) * LDA + 16 * ba,
+                                LDA, lane, z);
+        float *zt = Zs + wq * 256;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            zt[g * 16 + 8 * nt + 2 * q] = z[nt][0];
+            zt[g * 16 + 8 * nt + 2 * q + 1] = z[nt][1];
+            zt[(g + 8) * 16 + 8 * nt + 2 * q] = z[nt][2];
+            zt[(g + 8) * 16 + 8 * nt + 2 * q + 1] = z[nt][3];
+        }
+        __syncwarp();
+        float t2[2][4] = {};
+        block_mma_16x16<16>(Tf + (16 * bt) * LDA + 16 * bt, LDA, zt, 16, lane, t2);
+        float *dst = Tf + (16 * bt) * LDA + 16 * ba;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            dst[g * LDA + 8 * nt + 2 * q] = -t2[nt][0];
+            dst[g * LDA + 8 * nt + 2 * q + 1] = -t2[nt][1];
+            dst[(g + 8) * LDA + 8 * nt + 2 * q] = -t2[nt][2];
+            dst[(g + 8) * LDA + 8 * nt + 2 * q + 1] = -t2[nt][3];
+        }
+    }
+}
+
 // One off-diagonal level of the blocked inverse T = (I + A)^-1 (16x16 blocks):
 // for every block pair (bt, ba) with bt - ba = D,
 //   Z = sum_{ba <= m < bt} A[bt][m] T[m][ba],   T[bt][ba] = -T[bt][bt] Z.
@@ -213,34 +293,40 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                 if (lane < L) bl0 = __bfloat162float(p.beta[(row0 + lane) * p.H + h]);
                 if (lane + 32 < L) bl1 = __bfloat162float(p.beta[(row0 + lane + 32) * p.H + h]);
             }
-            // norms: each warp 8 rows, two at a time
-#pragma unroll 2
-            for (int t2 = 0; t2 < C / 16; ++t2) {
-                float sq[2], sk[2];
+            // norms: half-warps take one row each (8 channels per lane, 16-byte loads)
+            {
+                const int hw = lane >> 4, l16 = lane & 15;
+                const int kbb = l16 >> 3, col = (l16 & 7) * 8;
+                float sq[4], sk[4];
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int t = warp + (NP / 32) * (2 * t2 + u);
-                    const int kbb = lane >> 4, col = (lane * 4) & 63;
+                for (int u = 0; u < 4; ++u) {
+                    const int t = warp + (NP / 32) * (2 * u + hw);
                     const uint32_t off = kbb * 8192 + sw128_off(t, col);
-                    const uint2 qv = *reinterpret_cast<const uint2 *>(smem + rq_off + off);
-                    const uint2 kv = *reinterpret_cast<const uint2 *>(smem + rk_off + off);
-                    sq[u] = bf16lo(qv.x) * bf16lo(qv.x) + bf16hi(qv.x) * bf16hi(qv.x) +
-                            bf16lo(qv.y) * bf16lo(qv.y) + bf16hi(qv.y) * bf16hi(qv.y);
-                    sk[u] = bf16lo(kv.x) * bf16lo(kv.x) + bf16hi(kv.x) * bf16hi(kv.x) +
-                            bf16lo(kv.y) * bf16lo(kv.y) + bf16hi(kv.y) * bf16hi(kv.y);
+                    const uint4 qv = *reinterpret_cast<const uint4 *>(smem + rq_off + off);
+                    const uint4 kv = *reinterpret_cast<const uint4 *>(smem + rk_off + off);
+                    const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w}, kw[4] = {kv.x, kv.y, kv.z, kv.w};
+                    float a = 0.f, b = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        a = fmaf(bf16lo(qw[i]), bf16lo(qw[i]), a);
+                        a = fmaf(bf16hi(qw[i]), bf16hi(qw[i]), a);
+                        b = fmaf(bf16lo(kw[i]), bf16lo(kw[i]), b);
+                        b = fmaf(bf16hi(kw[i]), bf16hi(kw[i]), b);
+                    }
+                    sq[u] = a;
+                    sk[u] = b;
                 }
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
+                for (int o = 8; o > 0; o >>= 1)
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
+                    for (int u = 0; u < 4; ++u) {
                         sq[u] += __shfl_xor_sync(0xffffffffu, sq[u], o);
                         sk[u] += __shfl_xor_sync(0xffffffffu, sk[u], o);
                     }
-                }
-                if (lane == 0) {
+                if (l16 == 0) {
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int t = warp + (NP / 32) * (2 * t2 + u);
+                    for (int u = 0; u < 4; ++u) {
+                        const int t = warp + (NP / 32) * (2 * u + hw);
                         sm.rq[s][t] = t < L ? rsqrtf(sq[u] + 1e-6f) : 0.f;
                         sm.rk[s][t] = t < L ? rsqrtf(sk[u] + 1e-6f) : 0.f;
                     }
@@ -407,8 +493,9 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                         sts128(sbase + F_MST + sw128_off(t, i), 0, 0, 0, 0);
                         sts128(sbase + F_MST + sw128_off(t, i + 8), 0, 0, 0, 0);
                     } else {
+                        float4 *dst = reinterpret_cast<float4 *>(Amat + t * LDA + i);
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) Amat[t * LDA + i + e] = 0.f;
+                        for (int e4 = 0; e4 < 4; ++e4) dst[e4] = make_float4(0.f, 0.f, 0.f, 0.f);
                     }
                 }
                 // this quarter's five 16-column chunks: {0, 6..9} or {1..5}
@@ -417,16 +504,23 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                     const int vo = variant_off(bt);
                     if (16 * jj >= vo && 16 * jj < vo + 16 * (bt + 1)) {
                         const int ib = 16 * jj - vo;
-                        if (is_m) {
+                        const float4 *rk4 = reinterpret_cast<const float4 *>(&sm.rk[s][ib]);
+                        float cf[16];
 #pragma unroll
-                            for (int e = 0; e < 16; ++e)
-                                r[e] = (ib + e <= t) ? rowf * sm.rk[s][ib + e] * r[e] : 0.f;
+                        for (int e4 = 0; e4 < 4; ++e4) {
+                            const float4 x = rk4[e4];
+                            cf[4 * e4] = x.x; cf[4 * e4 + 1] = x.y; cf[4 * e4 + 2] = x.z; cf[4 * e4 + 3] = x.w;
+                        }
+                        const int lim = is_m ? t - ib : t - ib - 1;   // last column kept
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) r[e] = (e <= lim) ? rowf * cf[e] * r[e] : 0.f;
+                        if (is_m) {
                             st_pack16<true>(sbase + F_MST, t, ib, r);
                         } else {
+                            float4 *dst = reinterpret_cast<float4 *>(Amat + t * LDA + ib);
 #pragma unroll
-                            for (int e = 0; e < 16; ++e)
-                                Amat[t * LDA + ib + e] =
-                                    (ib + e < t) ? rowf * sm.rk[s][ib + e] * r[e] : 0.f;
+                            for (int e4 = 0; e4 < 4; ++e4)
+                                dst[e4] = make_float4(r[4 * e4], r[4 * e4 + 1], r[4 * e4 + 2], r[4 * e4 + 3]);
                         }
                     }
                 };
@@ -466,9 +560,12 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                 for (int r = 0; r < 16; ++r) Tf[(16 * bb + r) * LDA + 16 * bb + j] = x[r];
             }
             named_bar(2, NS);
-            inverse_level<1>(Amat, Tf, Zs, stid, NS, 2);
-            inverse_level<2>(Amat, Tf, Zs, stid, NS, 2);
-            inverse_level<3>(Amat, Tf, Zs, stid, NS, 2);
+            inverse_level_mma<1>(Amat, Tf, Zs, sw, lane);
+            named_bar(2, NS);
+            inverse_level_mma<2>(Amat, Tf, Zs, sw, lane);
+            named_bar(2, NS);
+            inverse_level_mma<3>(Amat, Tf, Zs, sw, lane);
+            named_bar(2, NS);
             // T' = T Diag(beta), fp16, into the staging tile (over the dead A)
             {
                 const int t = stid >> 1, i0 = (stid & 1) * 32;
