@@ -14,8 +14,10 @@
 //     warps 0-7  prologue of chunk m: gate, norms, block-local decay, the
 //                operands of G1 and the chain's K_hat*Gamma, Q_hat*Gamma, Kbar;
 //                issues G1 = [Kp; Qp] x Kn^T into a double-buffered TMEM slot;
-//     warps 8-11 solver of chunk m-1: A and M out of TMEM, the blocked fp32
+//     warps 8-11 solver of chunk m-1: A and M out of TMEM, the blocked
 //                inverse, T' (fp16);
+//     warp 12    control: issues G1, ships the prologue's tiles, prefetches
+//                the next raw tiles, so the prologue never waits on the chain;
 //     both groups ship their tiles into the chain CTA's shared memory with bulk
 //     shared->shared copies that complete as transaction bytes on the chain's
 //     per-slot mbarrier.
@@ -46,7 +48,7 @@ using namespace sm103;
 
 constexpr int C = kChunk;
 constexpr int DK = kHeadDim;
-constexpr int NT = 384;            // 12 warps in both CTAs
+constexpr int NT = 416;            // 13 warps in both CTAs
 constexpr int NP = 256;            // front prologue group: warps 0-7
 constexpr int NS = 128;            // front solver group: warps 8-11
 constexpr float kLog2e = 1.4426950408889634f;
@@ -93,8 +95,8 @@ __device__ __forceinline__ int variant_off(int bt) { return 8 * bt * (bt + 1); }
 __device__ __forceinline__ int row_block_of(int blk) { return (0x1320 >> (4 * blk)) & 0xF; }
 __device__ __forceinline__ int block_of_row_block(int rb) { return (0x2130 >> (4 * rb)) & 0xF; }
 
-// 16x16 = 16xK * Kx16 block product on the tensor cores (mma.sync, tf32 with a
-// hi/lo split of both operands: hi*hi + hi*lo + lo*hi, ~fp32 accuracy).
+// 16x16 = 16xK * Kx16 block product on the tensor cores (mma.sync, tf32 operands
+// rounded to nearest, fp32 accumulation).
 // A(r, k) = a[r * lda + k], B(k, c) = b[k * ldb + c]; acc holds two 16x8 tiles.
 template <int K>
 __device__ __forceinline__ void block_mma_16x16(const float *a, int lda, const float *b, int ldb,
@@ -113,32 +115,19 @@ __device__ __forceinline__ void block_mma_16x16(const float *a, int lda, const f
             bv[kk][nt][1] = b[(8 * kk + q + 4) * ldb + 8 * nt + g];
         }
     }
-    float corr[2][4] = {};   // hi*lo + lo*hi terms, a separate dependency chain
 #pragma unroll
     for (int kk = 0; kk < K / 8; ++kk) {
-        uint32_t ah[4], al[4];
+        uint32_t ah[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            ah[i] = to_tf32(av[kk][i]);
-            al[i] = to_tf32(av[kk][i] - __uint_as_float(ah[i]));
-        }
+        for (int i = 0; i < 4; ++i) ah[i] = to_tf32(av[kk][i]);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            uint32_t bh[2], bl[2];
+            uint32_t bh[2];
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                bh[i] = to_tf32(bv[kk][nt][i]);
-                bl[i] = to_tf32(bv[kk][nt][i] - __uint_as_float(bh[i]));
-            }
+            for (int i = 0; i < 2; ++i) bh[i] = to_tf32(bv[kk][nt][i]);
             mma_tf32_16x8x8(acc[nt], ah, bh);
-            mma_tf32_16x8x8(corr[nt], al, bh);
-            mma_tf32_16x8x8(corr[nt], ah, bl);
         }
     }
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[nt][i] += corr[nt][i];
 }
 
 // Off-diagonal levels of the blocked inverse on one warp per block pair (bt, ba),
@@ -262,10 +251,6 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
 
     if (tid < NP) {
         // ------------------------------------------------ prologue group
-        if (tid == 0) {
-            if (nchunks > 0) issue_raw(0);
-            if (nchunks > 1) issue_raw(1);
-        }
         const float a2 = -__expf(p.A_log[h]) * kLog2e;
         const float lb2 = p.lower_bound * kLog2e;
         const int blk = warp >> 1;                   // 16-token block
@@ -425,10 +410,18 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
             fence_proxy_async_smem();
             named_bar(1, NP);
 
-            if (tid == 0) {
-                mbar_arrive(&sm.pdone[s]);   // publishes rq/rk/beta of this chunk to the solver
-                bool ok = true;
-                if (m >= 2) ok = mbar_wait(&sm.am_free[s], ((m - 2) >> 1) & 1, kWait);
+            if (tid == 0) mbar_arrive(&sm.pdone[s]);   // operands and rq/rk/beta of chunk m ready
+        }
+    } else if (warp == 12) {
+        // ------------------------------------------------ control warp (lane 0)
+        if (lane == 0) {
+            if (nchunks > 0) issue_raw(0);
+            if (nchunks > 1) issue_raw(1);
+            for (int m = 0; m < nchunks; ++m) {
+                const int s = m & 1;
+                const uint32_t rq_off = F_RAW + s * F_SLOT, rk_off = rq_off + 16384, rg_off = rq_off + 32768;
+                bool ok = mbar_wait(&sm.pdone[s], (m >> 1) & 1, kWait);
+                if (ok && m >= 2) ok = mbar_wait(&sm.am_free[s], ((m - 2) >> 1) & 1, kWait);
                 if (ok) {
                     tc_fence_after();
                     const uint32_t id = idesc_bf16(128, 160, false, false);
@@ -456,11 +449,16 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                 }
                 bulk_commit();
                 bulk_wait_read0();
-                if (ok && m + 2 < nchunks) issue_raw(m + 2);
-                if (!ok) { set_err(p); sm.abort_p = 1; sm.abort_s = 1; }
+                if (!ok) {
+                    set_err(p);
+                    sm.abort_p = 1;
+                    sm.abort_s = 1;
+                    break;
+                }
+                if (m + 2 < nchunks) issue_raw(m + 2);
             }
+            bulk_wait0();
         }
-        if (tid == 0) bulk_wait0();
     } else {
         // ------------------------------------------------ solver group
         const int stid = tid - NP, sw = warp - 8;          // sw = TMEM lane quarter

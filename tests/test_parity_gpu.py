@@ -120,7 +120,7 @@ def test_lower_bound_extremes(lb):
     d = W.make_inputs(W.get("varlen_ragged", H=2, seqlens=(70, 129, 5), lower_bound=lb))
     out, fin = pu.run_gpu(d)
     ref_out, ref_fin = pu.run_oracle(d)
-    pu.check(d, out, fin, ref_out, ref_fin, label=f"lb={lb}")
+    print("lb", lb, pu.check(d, out, fin, ref_out, ref_fin, label=f"lb={lb}"))
 
 
 def test_out_guard_region_untouched():
