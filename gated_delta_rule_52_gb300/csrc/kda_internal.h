@@ -45,8 +45,6 @@ __device__ __forceinline__ void seq_range(const Params &p, int64_t n, int64_t &b
 }
 
 // Launchers (each returns the cudaError_t of its launch).
-cudaError_t launch_simt(const Params &p, cudaStream_t stream);
-cudaError_t launch_tc(const Params &p, cudaStream_t stream);
 cudaError_t launch_cluster(const Params &p, cudaStream_t stream);
 
 }  // namespace kda
