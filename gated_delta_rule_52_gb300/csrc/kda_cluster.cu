@@ -55,6 +55,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kWait = 2000000000ull;   // 2 s per wait
 constexpr int LDA = 68;             // fp32 row stride of A and T (16-byte aligned rows)
 constexpr uint32_t kChunkBytes = 16384 * 3 + 512 + 8192 * 2;   // front -> chain per chunk
+constexpr int kOrderMax = 256;     // varlen batches up to this many sequences run longest first
 
 // ---- front shared memory
 constexpr uint32_t F_RAW = 0;          // 2 slots x {q, k, g}: 16 KB each, 2 x [64 t][64 c]
@@ -895,7 +896,30 @@ kda_cluster_kernel(const __grid_constant__ TmaMaps maps, Params p) {
     Small &sm = *reinterpret_cast<Small *>(smem + SMALL);
     const uint32_t rank = cluster_ctarank();
     const int64_t unit = cluster_id_x();
-    const int64_t h = unit % p.H, n = unit / p.H;
+    const int64_t h = unit % p.H;
+    int64_t n = unit / p.H;
+    // Varlen: clusters take sequences longest first, so the longest recurrences
+    // start in the first wave.  Every CTA ranks the lengths itself (no host sync,
+    // no workspace); batches with more than kOrderMax sequences keep their order.
+    if (p.cu_seqlens && p.n_seqs > 1 && p.n_seqs <= kOrderMax) {
+        int64_t *lens = reinterpret_cast<int64_t *>(smem);   // scratch before any TMA
+        int *sel = reinterpret_cast<int *>(smem + 8 * kOrderMax);
+        for (int i = threadIdx.x; i < p.n_seqs; i += NT) lens[i] = p.cu_seqlens[i + 1] - p.cu_seqlens[i];
+        if (threadIdx.x == 0) *sel = (int)n;
+        __syncthreads();
+        for (int i = threadIdx.x; i < p.n_seqs; i += NT) {
+            const int64_t li = lens[i];
+            int64_t r = 0;
+            for (int j = 0; j < p.n_seqs; ++j) {
+                const int64_t lj = lens[j];
+                r += (lj > li) || (lj == li && j < i);
+            }
+            if (r == n) *sel = i;
+        }
+        __syncthreads();
+        n = *sel;
+        __syncthreads();
+    }
     int64_t b, t0, len;
     seq_range(p, n, b, t0, len);
     const int64_t row_base = b * p.T + t0;

@@ -173,3 +173,15 @@ def test_binding_rejects_bad_tensors():
     with pytest.raises(ValueError):
         kda.kda_fwd(*args, initial_state=torch.zeros(1, 2, 128, 128, device="cuda"),
                     final_state=torch.zeros(1, 2, 128, 128, device="cuda", dtype=torch.bfloat16))
+
+
+def test_many_short_sequences_longest_first_order():
+    # More clusters than SMs, zero-length and single-token sequences mixed in:
+    # every sequence must land on exactly one cluster whatever the order.
+    r = np.random.default_rng(7)
+    lens = [int(x) for x in r.integers(0, 90, 300)]
+    lens[0], lens[5], lens[-1] = 0, 1, 200
+    d = W.make_inputs(W.get("varlen_ragged", H=1, seqlens=tuple(lens)))
+    out, fin = pu.run_gpu(d)
+    ref_out, ref_fin = pu.run_oracle(d)
+    print("many-seqs", pu.check(d, out, fin, ref_out, ref_fin, label="many-seqs"))
