@@ -382,7 +382,7 @@ def run_ours(args):
             "frac": achieved / hbm, "traffic": stored_traffic(w.name),
             "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
             else f"{src} {hbm} GB/s",
-            "kernel": "kda_fwd (one launch per step)",
+            "kernel": "kda_cluster_kernel (kda_fwd: one launch per step)",
             "algorithmic_bytes_per_launch": abytes,
             "algorithmic_flops_per_launch": algorithmic_flops(d_cpu),
             "tensor_frac": algorithmic_flops(d_cpu) / (avg_launch_ms / 1e3) / (tflops * 1e12)}
