@@ -56,6 +56,7 @@ constexpr uint64_t kWait = 2000000000ull;   // 2 s per wait
 constexpr int LDA = 68;             // fp32 row stride of A and T (16-byte aligned rows)
 constexpr uint32_t kChunkBytes = 16384 * 3 + 512 + 8192 * 2;   // front -> chain per chunk
 constexpr int kOrderMax = 256;     // varlen batches up to this many sequences run longest first
+constexpr int kFacRows = 14;       // rows of the per-chunk decay-factor table (fac_base)
 
 // ---- front shared memory
 constexpr uint32_t F_RAW = 0;          // 2 slots x {q, k, g}: 16 KB each, 2 x [64 t][64 c]
@@ -65,7 +66,6 @@ constexpr uint32_t F_AMB = 131072;     // Kn variants: 2 x [160][64] bf16
 constexpr uint32_t F_MST = 172032;     // M staging fp16 [64 t][64 i]
 constexpr uint32_t F_AMAT = 180224;    // A fp32 [64][68]; T' staging (fp16) after the inverse
 constexpr uint32_t F_TF = 197632;      // T fp32 [64][68]
-constexpr uint32_t F_ZS = 215040;      // inverse scratch fp32 [3][16][16]
 // ---- chain shared memory
 constexpr uint32_t C_B2 = 0;           // K_hat*Gamma 2 x [64 i][64 c] | V 2 x [64 t][64 v] (MN-major)
 constexpr uint32_t C_G3A = 32768;      // [-W; Q_hat*Gamma]: 2 x [128][64] (K-major)
@@ -78,6 +78,7 @@ constexpr uint32_t SMALL = 218112;     // common offset in both CTAs (remote add
 struct Small {
     float rq[2][C], rk[2][C], beta[2][C];   // front, per slot
     float btot[4][DK];                       // front
+    float fac[kFacRows][DK];                 // front: decay factors, see fac_base
     float gamC_f[2][DK];                     // front: exp(G_C) per slot (copy source)
     float gamC_c[2][DK];                     // chain: copy destination
     uint64_t raw_full[2], g1_done[2], am_free[2], s_done[2], slot_free[2], single_free, pdone[2];
@@ -90,122 +91,33 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 __device__ __forceinline__ int variant_off(int bt) { return 8 * bt * (bt + 1); }
 
-// G1's A-operand rows hold the 16-token blocks in the order 0, 3, 1, 2, so that
-// each 32-lane TMEM quarter of the result needs 80 of the 160 variant columns
-// (blocks 0 and 3: variants 0 and 3; blocks 1 and 2: variants 1 and 2).
-__device__ __forceinline__ int row_block_of(int blk) { return (0x1320 >> (4 * blk)) & 0xF; }
-__device__ __forceinline__ int block_of_row_block(int rb) { return (0x2130 >> (4 * rb)) & 0xF; }
-
-// 16x16 = 16xK * Kx16 block product on the tensor cores (mma.sync, tf32 operands
-// rounded to nearest, fp32 accumulation).
-// A(r, k) = a[r * lda + k], B(k, c) = b[k * ldb + c]; acc holds two 16x8 tiles.
-template <int K>
-__device__ __forceinline__ void block_mma_16x16(const float *a, int lda, const float *b, int ldb,
-                                                int lane, float (&acc)[2][4]) {
+// acc (16 x 8) += A (16 x 8) * B (8 x 8) on the tensor cores (mma.sync, tf32
+// operands rounded to nearest, fp32 accumulation); A(r, k) = a[r * lda + k],
+// B(k, n) = b[k * ldb + n].
+__device__ __forceinline__ void mma_16x8x8(const float *a, int lda, const float *b, int ldb, int lane,
+                                           float (&acc)[4]) {
     const int g = lane >> 2, q = lane & 3;
-    float av[K / 8][4], bv[K / 8][2][2];
-#pragma unroll
-    for (int kk = 0; kk < K / 8; ++kk) {   // all operand loads first
-        av[kk][0] = a[g * lda + 8 * kk + q];
-        av[kk][1] = a[(g + 8) * lda + 8 * kk + q];
-        av[kk][2] = a[g * lda + 8 * kk + q + 4];
-        av[kk][3] = a[(g + 8) * lda + 8 * kk + q + 4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            bv[kk][nt][0] = b[(8 * kk + q) * ldb + 8 * nt + g];
-            bv[kk][nt][1] = b[(8 * kk + q + 4) * ldb + 8 * nt + g];
-        }
-    }
-#pragma unroll
-    for (int kk = 0; kk < K / 8; ++kk) {
-        uint32_t ah[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) ah[i] = to_tf32(av[kk][i]);
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            uint32_t bh[2];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) bh[i] = to_tf32(bv[kk][nt][i]);
-            mma_tf32_16x8x8(acc[nt], ah, bh);
-        }
-    }
+    const uint32_t ah[4] = {to_tf32(a[g * lda + q]), to_tf32(a[(g + 8) * lda + q]),
+                            to_tf32(a[g * lda + q + 4]), to_tf32(a[(g + 8) * lda + q + 4])};
+    const uint32_t bh[2] = {to_tf32(b[q * ldb + g]), to_tf32(b[(q + 4) * ldb + g])};
+    mma_tf32_16x8x8(acc, ah, bh);
 }
 
-// Off-diagonal levels of the blocked inverse on one warp per block pair (bt, ba),
-// bt - ba = D: Z = sum_{ba <= m < bt} A[bt][m] T[m][ba], T[bt][ba] = -T[bt][bt] Z.
-template <int D>
-__device__ __forceinline__ void inverse_level_mma(const float *Amat, float *Tf, float *Zs, int wq,
-                                                  int lane) {
-    if (wq < 4 - D) {
-        const int ba = wq, bt = ba + D, g = lane >> 2, q = lane & 3;
-        float z[2][4] = {};
-        block_mma_16x16<16 * D>(Amat + (16 * bt) * LDA + 16 * ba, LDA, Tf + (16 * ba) * LDA + 16 * ba,
-                                LDA, lane, z);
-        float *zt = Zs + wq * 256;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            zt[g * 16 + 8 * nt + 2 * q] = z[nt][0];
-            zt[g * 16 + 8 * nt + 2 * q + 1] = z[nt][1];
-            zt[(g + 8) * 16 + 8 * nt + 2 * q] = z[nt][2];
-            zt[(g + 8) * 16 + 8 * nt + 2 * q + 1] = z[nt][3];
-        }
-        __syncwarp();
-        float t2[2][4] = {};
-        block_mma_16x16<16>(Tf + (16 * bt) * LDA + 16 * bt, LDA, zt, 16, lane, t2);
-        float *dst = Tf + (16 * bt) * LDA + 16 * ba;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            dst[g * LDA + 8 * nt + 2 * q] = -t2[nt][0];
-            dst[g * LDA + 8 * nt + 2 * q + 1] = -t2[nt][1];
-            dst[(g + 8) * LDA + 8 * nt + 2 * q] = -t2[nt][2];
-            dst[(g + 8) * LDA + 8 * nt + 2 * q + 1] = -t2[nt][3];
-        }
-    }
+// Stores a 16 x 8 accumulator tile (times `sign`) at d (row stride ldd).
+__device__ __forceinline__ void store_16x8(float *d, int ldd, int lane, const float (&acc)[4],
+                                           float sign) {
+    const int g = lane >> 2, q = lane & 3;
+    d[g * ldd + 2 * q] = sign * acc[0];
+    d[g * ldd + 2 * q + 1] = sign * acc[1];
+    d[(g + 8) * ldd + 2 * q] = sign * acc[2];
+    d[(g + 8) * ldd + 2 * q + 1] = sign * acc[3];
 }
 
-// One off-diagonal level of the blocked inverse T = (I + A)^-1 (16x16 blocks):
-// for every block pair (bt, ba) with bt - ba = D,
-//   Z = sum_{ba <= m < bt} A[bt][m] T[m][ba],   T[bt][ba] = -T[bt][bt] Z.
-// Each task computes four adjacent columns of one row (float4 accumulators).
-template <int D>
-__device__ __forceinline__ void inverse_level(const float *Amat, float *Tf, float *Zs, int stid,
-                                              int nthreads, uint32_t bar_id) {
-    constexpr int NTASK = (4 - D) * 64;
-    for (int task = stid; task < NTASK; task += nthreads) {
-        const int ba = task >> 6, r = (task >> 2) & 15, jg = task & 3, bt = ba + D;
-        const float *arow = Amat + (16 * bt + r) * LDA + 16 * ba;
-        const float *tcol = Tf + (16 * ba) * LDA + 16 * ba + 4 * jg;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int q = 0; q < 16 * D; ++q) {
-            const float a = arow[q];
-            const float4 tv = *reinterpret_cast<const float4 *>(tcol + q * LDA);
-            acc.x = fmaf(a, tv.x, acc.x);
-            acc.y = fmaf(a, tv.y, acc.y);
-            acc.z = fmaf(a, tv.z, acc.z);
-            acc.w = fmaf(a, tv.w, acc.w);
-        }
-        *reinterpret_cast<float4 *>(Zs + ba * 256 + r * 16 + 4 * jg) = acc;
-    }
-    named_bar(bar_id, nthreads);
-    for (int task = stid; task < NTASK; task += nthreads) {
-        const int ba = task >> 6, r = (task >> 2) & 15, jg = task & 3, bt = ba + D;
-        const float *trow = Tf + (16 * bt + r) * LDA + 16 * bt;   // T[bt][bt] row (zero above r)
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-            const float a = trow[q];
-            const float4 z = *reinterpret_cast<const float4 *>(Zs + ba * 256 + q * 16 + 4 * jg);
-            acc.x = fmaf(a, z.x, acc.x);
-            acc.y = fmaf(a, z.y, acc.y);
-            acc.z = fmaf(a, z.z, acc.z);
-            acc.w = fmaf(a, z.w, acc.w);
-        }
-        *reinterpret_cast<float4 *>(Tf + (16 * bt + r) * LDA + 16 * ba + 4 * jg) =
-            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-    }
-    named_bar(bar_id, nthreads);
-}
+// Rows of the decay-factor table of one chunk (per 16-token block b and channel):
+// fac_base(b) + 0: 2^Gs[b], + 1: 2^(G_C - Gs[b]), + 1 + (bt - b): 2^(Gs[bt] - Gs[b])
+// for bt > b, with Gs[b] the cumulative log2 decay before block b and G_C the
+// chunk total.
+__device__ __forceinline__ int fac_base(int b) { return b * (11 - b) / 2; }
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool fp16) {
     return fp16 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
@@ -252,18 +164,32 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
 
     if (tid < NP) {
         // ------------------------------------------------ prologue group
+        // Thread layout for the gate and the operands: warp = (16-token block, 64-channel
+        // half), lane = (4-token quarter of the block, 8-channel group); every access to
+        // the tiles is one 16-byte vector (8 channels of one token).
         const float a2 = -__expf(p.A_log[h]) * kLog2e;
         const float lb2 = p.lower_bound * kLog2e;
-        const int blk = warp >> 1;                   // 16-token block
-        const int arow0 = 16 * row_block_of(blk);    // its rows in G1's A operand
-        const int c = (warp & 1) * 64 + 2 * lane;    // channel pair (c, c+1)
-        const int kb = c >> 6, cc = c & 63;
-        const float b0 = a2 * p.dt_bias[h * DK + c], b1 = a2 * p.dt_bias[h * DK + c + 1];
+        const int blk = warp >> 1, kh = warp & 1;
+        const int cg = lane & 7, qr = lane >> 3;
+        const int c0 = 64 * kh + 8 * cg;             // first of this thread's 8 channels
+        const uint32_t kho = kh * 8192;              // the half inside a raw tile
+        float bias[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) bias[e] = a2 * p.dt_bias[h * DK + c0 + e];
+        // beta logits are loaded one chunk ahead (warp 0, two tokens per lane)
+        auto load_beta = [&](int mm, float &x0, float &x1) {
+            const int64_t cs = (int64_t)mm * C;
+            const int Lm = (int)((len - cs) < C ? (len - cs) : C);
+            const int64_t r0 = row_base + cs;
+            x0 = lane < Lm ? __bfloat162float(p.beta[(r0 + lane) * p.H + h]) : 0.f;
+            x1 = lane + 32 < Lm ? __bfloat162float(p.beta[(r0 + lane + 32) * p.H + h]) : 0.f;
+        };
+        float bl0 = 0.f, bl1 = 0.f;
+        if (warp == 0 && nchunks > 0) load_beta(0, bl0, bl1);
         for (int m = 0; m < nchunks; ++m) {
             const int s = m & 1;
             const int64_t cs = (int64_t)m * C;
             const int L = (int)((len - cs) < C ? (len - cs) : C);
-            const int64_t row0 = row_base + cs;
             const uint32_t rq_off = F_RAW + s * F_SLOT, rk_off = rq_off + 16384, rg_off = rq_off + 32768;
             if (tid == 0) {
                 bool ok = mbar_wait(&sm.raw_full[s], (m >> 1) & 1, kWait);
@@ -272,13 +198,9 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
             }
             named_bar(1, NP);
             if (sm.abort_p) break;
+            float nb0 = 0.f, nb1 = 0.f;
+            if (warp == 0 && m + 1 < nchunks) load_beta(m + 1, nb0, nb1);
 
-            // beta logits: global loads issued first, consumed after the norms
-            float bl0 = 0.f, bl1 = 0.f;
-            if (warp == 0) {
-                if (lane < L) bl0 = __bfloat162float(p.beta[(row0 + lane) * p.H + h]);
-                if (lane + 32 < L) bl1 = __bfloat162float(p.beta[(row0 + lane + 32) * p.H + h]);
-            }
             // norms: half-warps take one row each (8 channels per lane, 16-byte loads)
             {
                 const int hw = lane >> 4, l16 = lane & 15;
@@ -321,48 +243,73 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
             if (warp == 0) {
                 sm.beta[s][lane] = lane < L ? 1.f / (1.f + exp2f(-bl0 * kLog2e)) : 0.f;
                 sm.beta[s][lane + 32] = lane + 32 < L ? 1.f / (1.f + exp2f(-bl1 * kLog2e)) : 0.f;
+                bl0 = nb0;
+                bl1 = nb1;
             }
 
-            // gate and block-local cumulative decay (log2 units)
-            float H0[16], H1[16];
+            // gate (log2 units) and its block-local inclusive cumulative sum H
+            float H[4][8];
             {
-                float acc0 = 0.f, acc1 = 0.f;
+                float acc[8];
 #pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    const int t = blk * 16 + r;
-                    const uint32_t gv =
-                        *reinterpret_cast<const uint32_t *>(smem + rg_off + kb * 8192 + sw128_off(t, cc));
+                for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int t = 16 * blk + 4 * qr + j;
+                    const uint4 gv = *reinterpret_cast<const uint4 *>(smem + rg_off + kho + sw128_off(t, 8 * cg));
                     if (t < L) {
-                        acc0 += lb2 * __fdividef(1.f, 1.f + exp2f(fmaf(bf16lo(gv), a2, b0)));
-                        acc1 += lb2 * __fdividef(1.f, 1.f + exp2f(fmaf(bf16hi(gv), a2, b1)));
+                        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            acc[2 * i] += lb2 * __fdividef(1.f, 1.f + exp2f(fmaf(bf16lo(gw[i]), a2, bias[2 * i])));
+                            acc[2 * i + 1] +=
+                                lb2 * __fdividef(1.f, 1.f + exp2f(fmaf(bf16hi(gw[i]), a2, bias[2 * i + 1])));
+                        }
                     }
-                    H0[r] = acc0;
-                    H1[r] = acc1;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) H[j][e] = acc[e];
                 }
-                sm.btot[blk][c] = acc0;
-                sm.btot[blk][c + 1] = acc1;
+                // add the totals of the earlier quarters (lanes 8 and 16 apart share channels)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    float v = acc[e];
+                    float u = __shfl_up_sync(0xffffffffu, v, 8);
+                    if (qr >= 1) v += u;
+                    u = __shfl_up_sync(0xffffffffu, v, 16);
+                    if (qr >= 2) v += u;
+                    float ex = __shfl_up_sync(0xffffffffu, v, 8);
+                    ex = qr >= 1 ? ex : 0.f;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) H[j][e] += ex;
+                    acc[e] = v;
+                }
+                if (qr == 3) {
+                    float4 *bt4 = reinterpret_cast<float4 *>(&sm.btot[blk][c0]);
+                    bt4[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                    bt4[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+                }
             }
             named_bar(1, NP);
 
-            float Gs0[4], Gs1[4], s0 = 0.f, s1 = 0.f;
+            // decay factors per (block, channel): thread = channel, two blocks each
+            {
+                const int c = tid & (DK - 1), bh = tid >> 7;
+                float Gs[4], tot = 0.f;
 #pragma unroll
-            for (int bb = 0; bb < 4; ++bb) {
-                Gs0[bb] = s0;
-                Gs1[bb] = s1;
-                s0 += sm.btot[bb][c];
-                s1 += sm.btot[bb][c + 1];
-            }
-            if (blk == 0) {
-                sm.gamC_f[s][c] = exp2f(s0);
-                sm.gamC_f[s][c + 1] = exp2f(s1);
-            }
-            const float Fs0 = exp2f(Gs0[blk]), Fs1 = exp2f(Gs1[blk]);
-            const float FC0 = exp2f(s0 - Gs0[blk]), FC1 = exp2f(s1 - Gs1[blk]);
-            float D0[4], D1[4];
+                for (int bb = 0; bb < 4; ++bb) {
+                    Gs[bb] = tot;
+                    tot += sm.btot[bb][c];
+                }
+                if (bh == 0) sm.gamC_f[s][c] = exp2f(tot);
 #pragma unroll
-            for (int bt = 0; bt < 4; ++bt) {
-                D0[bt] = bt > blk ? exp2f(Gs0[bt] - Gs0[blk]) : 1.f;
-                D1[bt] = bt > blk ? exp2f(Gs1[bt] - Gs1[blk]) : 1.f;
+                for (int b = 0; b < 4; ++b) {
+                    if ((b >> 1) != bh) continue;
+                    float *f = &sm.fac[fac_base(b)][c];
+                    f[0] = exp2f(Gs[b]);
+                    f[DK] = exp2f(tot - Gs[b]);
+#pragma unroll
+                    for (int bt = b + 1; bt < 4; ++bt) f[(1 + bt - b) * DK] = exp2f(Gs[bt] - Gs[b]);
+                }
             }
             // [Kp; Qp] and Kn are free once G1 of the previous chunk completed
             if (tid == 0 && m >= 1) {
@@ -374,39 +321,75 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
             named_bar(1, NP);
             if (sm.abort_p) break;
 
+            // Operands.  G1 (bf16, raw q/k times block-local decay): Kp = k 2^H and
+            // Qp = q 2^H at rows 32 blk + r and 32 blk + 16 + r of [Kp; Qp]; key
+            // variants Kn(bt) = k 2^(Gs[bt] - Gs[blk] - H) at row variant_off(bt) + t for
+            // bt >= blk.  Chain (fp16, in place of the raw tiles): Q_hat*Gamma,
+            // K_hat*Gamma and Kbar = k_hat 2^(G_C - G).
+            {
+                const int fb = fac_base(blk);
+                const float4 *fs4 = reinterpret_cast<const float4 *>(&sm.fac[fb][c0]);
+                const float4 *fc4 = reinterpret_cast<const float4 *>(&sm.fac[fb + 1][c0]);
+                const float4 fsa = fs4[0], fsb = fs4[1], fca = fc4[0], fcb = fc4[1];
+                const float Fs[8] = {fsa.x, fsa.y, fsa.z, fsa.w, fsb.x, fsb.y, fsb.z, fsb.w};
+                const float FC[8] = {fca.x, fca.y, fca.z, fca.w, fcb.x, fcb.y, fcb.z, fcb.w};
+                const uint32_t ama = sbase + F_AMA + kh * 16384, amb = sbase + F_AMB + kh * 20480;
+#pragma unroll 1
+                for (int j = 0; j < 4; ++j) {
+                    const int r = 4 * qr + j, t = 16 * blk + r;
+                    const uint32_t off = kho + sw128_off(t, 8 * cg);
+                    uint4 qv = *reinterpret_cast<const uint4 *>(smem + rq_off + off);
+                    uint4 kv = *reinterpret_cast<const uint4 *>(smem + rk_off + off);
+                    if (t >= L) qv = kv = make_uint4(0u, 0u, 0u, 0u);
+                    const float rq = sm.rq[s][t], rk = sm.rk[s][t];
+                    const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w}, kw[4] = {kv.x, kv.y, kv.z, kv.w};
+                    float kp[8], qp[8];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                const int t = blk * 16 + r;
-                const uint32_t off = kb * 8192 + sw128_off(t, cc);
-                const uint32_t qv = *reinterpret_cast<const uint32_t *>(smem + rq_off + off);
-                const uint32_t kv = *reinterpret_cast<const uint32_t *>(smem + rk_off + off);
-                const float rq = sm.rq[s][t], rk = sm.rk[s][t];
-                const float q0 = t < L ? bf16lo(qv) : 0.f, q1 = t < L ? bf16hi(qv) : 0.f;
-                const float k0 = t < L ? bf16lo(kv) : 0.f, k1 = t < L ? bf16hi(kv) : 0.f;
-                const float e10 = exp2f(H0[r]), e11 = exp2f(H1[r]);
-                const float e20 = exp2f(-H0[r]), e21 = exp2f(-H1[r]);
-                const float kp0 = k0 * e10, kp1 = k1 * e11;
-                const float qp0 = q0 * e10, qp1 = q1 * e11;
-                const float kn0 = k0 * e20, kn1 = k1 * e21;
-                *reinterpret_cast<uint32_t *>(smem + F_AMA + kb * 16384 + sw128_off(arow0 + r, cc)) =
-                    pack_bf16(kp0, kp1);
-                *reinterpret_cast<uint32_t *>(smem + F_AMA + kb * 16384 +
-                                              sw128_off(64 + arow0 + r, cc)) = pack_bf16(qp0, qp1);
-#pragma unroll
-                for (int bt = 0; bt < 4; ++bt) {
-                    if (bt >= blk) {
-                        const int row = variant_off(bt) + t;
-                        *reinterpret_cast<uint32_t *>(smem + F_AMB + kb * 20480 + sw128_off(row, cc)) =
-                            pack_bf16(kn0 * D0[bt], kn1 * D1[bt]);
+                    for (int i = 0; i < 4; ++i) {
+                        const float e1a = exp2f(H[0][2 * i]), e1b = exp2f(H[0][2 * i + 1]);
+                        kp[2 * i] = bf16lo(kw[i]) * e1a;
+                        kp[2 * i + 1] = bf16hi(kw[i]) * e1b;
+                        qp[2 * i] = bf16lo(qw[i]) * e1a;
+                        qp[2 * i + 1] = bf16hi(qw[i]) * e1b;
                     }
+                    sts128(ama + sw128_off(32 * blk + r, 8 * cg), pack_bf16(kp[0], kp[1]), pack_bf16(kp[2], kp[3]),
+                           pack_bf16(kp[4], kp[5]), pack_bf16(kp[6], kp[7]));
+                    sts128(ama + sw128_off(32 * blk + 16 + r, 8 * cg), pack_bf16(qp[0], qp[1]),
+                           pack_bf16(qp[2], qp[3]), pack_bf16(qp[4], qp[5]), pack_bf16(qp[6], qp[7]));
+                    uint32_t w[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        w[i] = pack_f16(qp[2 * i] * (Fs[2 * i] * rq), qp[2 * i + 1] * (Fs[2 * i + 1] * rq));
+                    sts128(sbase + rq_off + off, w[0], w[1], w[2], w[3]);               // Q_hat*Gamma
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        w[i] = pack_f16(kp[2 * i] * (Fs[2 * i] * rk), kp[2 * i + 1] * (Fs[2 * i + 1] * rk));
+                    sts128(sbase + rk_off + off, w[0], w[1], w[2], w[3]);               // K_hat*Gamma
+                    float kn[8];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        kn[2 * i] = bf16lo(kw[i]) * exp2f(-H[0][2 * i]);
+                        kn[2 * i + 1] = bf16hi(kw[i]) * exp2f(-H[0][2 * i + 1]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        w[i] = pack_f16(kn[2 * i] * (FC[2 * i] * rk), kn[2 * i + 1] * (FC[2 * i + 1] * rk));
+                    sts128(sbase + rg_off + off, w[0], w[1], w[2], w[3]);               // Kbar
+                    sts128(amb + sw128_off(variant_off(blk) + t, 8 * cg), pack_bf16(kn[0], kn[1]),
+                           pack_bf16(kn[2], kn[3]), pack_bf16(kn[4], kn[5]), pack_bf16(kn[6], kn[7]));
+#pragma unroll 1
+                    for (int bt = blk + 1; bt < 4; ++bt) {
+                        const float4 *d4 = reinterpret_cast<const float4 *>(&sm.fac[fb + 1 + bt - blk][c0]);
+                        const float4 da = d4[0], db = d4[1];
+                        sts128(amb + sw128_off(variant_off(bt) + t, 8 * cg), pack_bf16(kn[0] * da.x, kn[1] * da.y),
+                               pack_bf16(kn[2] * da.z, kn[3] * da.w), pack_bf16(kn[4] * db.x, kn[5] * db.y),
+                               pack_bf16(kn[6] * db.z, kn[7] * db.w));
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < 3; ++jj)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) H[jj][e] = H[jj + 1][e];
                 }
-                // chain operands, in place of the raw tiles (same layouts)
-                *reinterpret_cast<uint32_t *>(smem + rq_off + off) =
-                    pack_f16(qp0 * (Fs0 * rq), qp1 * (Fs1 * rq));        // Q_hat*Gamma
-                *reinterpret_cast<uint32_t *>(smem + rk_off + off) =
-                    pack_f16(kp0 * (Fs0 * rk), kp1 * (Fs1 * rk));        // K_hat*Gamma
-                *reinterpret_cast<uint32_t *>(smem + rg_off + off) =
-                    pack_f16(kn0 * (FC0 * rk), kn1 * (FC1 * rk));        // Kbar
             }
             fence_proxy_async_smem();
             named_bar(1, NP);
@@ -462,10 +445,15 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
         }
     } else {
         // ------------------------------------------------ solver group
-        const int stid = tid - NP, sw = warp - 8;          // sw = TMEM lane quarter
+        // Warp sw reads TMEM lane quarter sw of G1 = rows of token block sw: lanes 0-15
+        // are A rows (Kp), lanes 16-31 M rows (Qp); it needs the sw + 1 chunks of 16
+        // columns of variant sw.
+        const int stid = tid - NP, sw = warp - 8;
         float *Amat = reinterpret_cast<float *>(smem + F_AMAT);
         float *Tf = reinterpret_cast<float *>(smem + F_TF);
-        float *Zs = reinterpret_cast<float *>(smem + F_ZS);
+        // the M staging tile above the diagonal blocks stays zero for the whole run
+        for (int k16 = stid; k16 < 512; k16 += NS) sts128(sbase + F_MST + k16 * 16, 0u, 0u, 0u, 0u);
+        named_bar(2, NS);
         for (int m = 0; m < nchunks; ++m) {
             const int s = m & 1;
             if (stid == 0) {
@@ -480,101 +468,114 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
             if (sm.abort_s) break;
             tc_fence_after();
 
-            // A (fp32, beta_t/|k_t| x 1/|k_i|, strictly lower) and M (fp16, 1/|q_t| x 1/|k_i|)
+            // A (fp32, beta_t/|k_t| x 1/|k_i|; only i < t is used later) and
+            // M (fp16, 1/|q_t| x 1/|k_i|, zero for i > t)
             {
-                const bool is_m = sw >= 2;
-                const int lr = (sw & 1) * 32 + lane;            // row within the A or M half
-                const int bt = block_of_row_block(lr >> 4);
-                const int t = 16 * bt + (lr & 15);
+                const bool is_m = lane >= 16;
+                const int t = 16 * sw + (lane & 15);
                 const float rowf = is_m ? sm.rq[s][t] : sm.beta[s][t] * sm.rk[s][t];
-                for (int i = 16 * (bt + 1); i < 64; i += 16) {
-                    if (is_m) {
-                        sts128(sbase + F_MST + sw128_off(t, i), 0, 0, 0, 0);
-                        sts128(sbase + F_MST + sw128_off(t, i + 8), 0, 0, 0, 0);
-                    } else {
-                        float4 *dst = reinterpret_cast<float4 *>(Amat + t * LDA + i);
+                const uint32_t col0 = 256 * s + variant_off(sw);
+#pragma unroll 1
+                for (int kk = 0; kk <= sw; ++kk) {
+                    float r[16];
+                    tmem_ld16(tmem_addr(tmem, 32 * sw, col0 + 16 * kk), r);
+                    tmem_ld_wait();
+                    const float4 *rk4 = reinterpret_cast<const float4 *>(&sm.rk[s][16 * kk]);
 #pragma unroll
-                        for (int e4 = 0; e4 < 4; ++e4) dst[e4] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int e4 = 0; e4 < 4; ++e4) {
+                        const float4 x = rk4[e4];
+                        r[4 * e4] *= rowf * x.x;
+                        r[4 * e4 + 1] *= rowf * x.y;
+                        r[4 * e4 + 2] *= rowf * x.z;
+                        r[4 * e4 + 3] *= rowf * x.w;
+                    }
+                    if (is_m) {
+                        if (kk == sw) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) r[e] = e <= (lane & 15) ? r[e] : 0.f;
+                        }
+                        st_pack16<true>(sbase + F_MST, t, 16 * kk, r);
+                    } else {
+                        float4 *dst = reinterpret_cast<float4 *>(Amat + t * LDA + 16 * kk);
+#pragma unroll
+                        for (int e4 = 0; e4 < 4; ++e4)
+                            dst[e4] = make_float4(r[4 * e4], r[4 * e4 + 1], r[4 * e4 + 2], r[4 * e4 + 3]);
                     }
                 }
-                // this quarter's five 16-column chunks: {0, 6..9} or {1..5}
-                auto chunk_of = [&](int k) { return (sw & 1) ? 1 + k : (k == 0 ? 0 : 5 + k); };
-                auto emit = [&](int jj, float (&r)[16]) {
-                    const int vo = variant_off(bt);
-                    if (16 * jj >= vo && 16 * jj < vo + 16 * (bt + 1)) {
-                        const int ib = 16 * jj - vo;
-                        const float4 *rk4 = reinterpret_cast<const float4 *>(&sm.rk[s][ib]);
-                        float cf[16];
-#pragma unroll
-                        for (int e4 = 0; e4 < 4; ++e4) {
-                            const float4 x = rk4[e4];
-                            cf[4 * e4] = x.x; cf[4 * e4 + 1] = x.y; cf[4 * e4 + 2] = x.z; cf[4 * e4 + 3] = x.w;
-                        }
-                        const int lim = is_m ? t - ib : t - ib - 1;   // last column kept
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) r[e] = (e <= lim) ? rowf * cf[e] * r[e] : 0.f;
-                        if (is_m) {
-                            st_pack16<true>(sbase + F_MST, t, ib, r);
-                        } else {
-                            float4 *dst = reinterpret_cast<float4 *>(Amat + t * LDA + ib);
-#pragma unroll
-                            for (int e4 = 0; e4 < 4; ++e4)
-                                dst[e4] = make_float4(r[4 * e4], r[4 * e4 + 1], r[4 * e4 + 2], r[4 * e4 + 3]);
-                        }
-                    }
-                };
-                float r0[16], r1[16], r2[16];
-                tmem_ld16(tmem_addr(tmem, sw * 32, 256 * s + 16 * chunk_of(0)), r0);
-                tmem_ld16(tmem_addr(tmem, sw * 32, 256 * s + 16 * chunk_of(1)), r1);
-                tmem_ld16(tmem_addr(tmem, sw * 32, 256 * s + 16 * chunk_of(2)), r2);
-                tmem_ld_wait();
-                emit(chunk_of(0), r0);
-                emit(chunk_of(1), r1);
-                emit(chunk_of(2), r2);
-                tmem_ld16(tmem_addr(tmem, sw * 32, 256 * s + 16 * chunk_of(3)), r0);
-                tmem_ld16(tmem_addr(tmem, sw * 32, 256 * s + 16 * chunk_of(4)), r1);
-                tmem_ld_wait();
-                emit(chunk_of(3), r0);
-                emit(chunk_of(4), r1);
             }
             tc_fence_before();
             named_bar(2, NS);
             if (stid == 0) mbar_arrive(&sm.am_free[s]);
 
-            // T = (I + A)^-1: 16x16 diagonal blocks, then off-diagonal block levels
+            // T = (I + A)^-1 in 16x16 blocks.  Diagonal blocks: forward substitution,
+            // thread = (block, column j), updating all later rows after each solved row.
             if (stid < 64) {
                 const int bb = stid >> 4, j = stid & 15;
-                float x[16];
+                const float *Ab = Amat + (16 * bb) * LDA + 16 * bb;
+                float acc[16], x[16];
 #pragma unroll
-                for (int r = 0; r < 16; ++r) x[r] = (r == j) ? 1.f : 0.f;
+                for (int r = 0; r < 16; ++r) acc[r] = 0.f;
 #pragma unroll
-                for (int r = 1; r < 16; ++r) {
-                    float acc = 0.f;
+                for (int q = 0; q < 16; ++q) {
+                    x[q] = q == j ? 1.f : (q < j ? 0.f : -acc[q]);
 #pragma unroll
-                    for (int q = 0; q < r; ++q)
-                        acc = fmaf(Amat[(16 * bb + r) * LDA + 16 * bb + q], x[q], acc);
-                    if (r > j) x[r] = -acc;
+                    for (int r = q + 1; r < 16; ++r) acc[r] = fmaf(Ab[r * LDA + q], x[q], acc[r]);
                 }
 #pragma unroll
                 for (int r = 0; r < 16; ++r) Tf[(16 * bb + r) * LDA + 16 * bb + j] = x[r];
             }
             named_bar(2, NS);
-            inverse_level_mma<1>(Amat, Tf, Zs, sw, lane);
+            // B[bt][m] = T[bt][bt] A[bt][m] for m < bt, in place of A's blocks (warp bt)
+            if (sw >= 1) {
+                const float *Tb = Tf + (16 * sw) * LDA + 16 * sw;
+                float *Ab = Amat + (16 * sw) * LDA;
+#pragma unroll 1
+                for (int nt = 0; nt < 2 * sw; ++nt) {
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma_16x8x8(Tb, LDA, Ab + 8 * nt, LDA, lane, acc);
+                    mma_16x8x8(Tb + 8, LDA, Ab + 8 * LDA + 8 * nt, LDA, lane, acc);
+                    __syncwarp();
+                    store_16x8(Ab + 8 * nt, LDA, lane, acc, 1.f);
+                }
+            }
             named_bar(2, NS);
-            inverse_level_mma<2>(Amat, Tf, Zs, sw, lane);
-            named_bar(2, NS);
-            inverse_level_mma<3>(Amat, Tf, Zs, sw, lane);
+            // Off-diagonal blocks of column block ba (warp ba), top to bottom:
+            // T[bt][ba] = -sum_{ba <= m < bt} B[bt][m] T[m][ba]
+            if (sw <= 2) {
+                const int ba = sw;
+#pragma unroll 1
+                for (int bt = ba + 1; bt < 4; ++bt) {
+                    float acc[2][4] = {};
+                    const float *Bp = Amat + (16 * bt) * LDA + 16 * ba;
+                    const float *Tp = Tf + (16 * ba) * LDA + 16 * ba;
+#pragma unroll 1
+                    for (int kk = 0; kk < 2 * (bt - ba); ++kk) {
+                        mma_16x8x8(Bp + 8 * kk, LDA, Tp + 8 * kk * LDA, LDA, lane, acc[0]);
+                        mma_16x8x8(Bp + 8 * kk, LDA, Tp + 8 * kk * LDA + 8, LDA, lane, acc[1]);
+                    }
+                    float *dst = Tf + (16 * bt) * LDA + 16 * ba;
+                    store_16x8(dst, LDA, lane, acc[0], -1.f);
+                    store_16x8(dst + 8, LDA, lane, acc[1], -1.f);
+                    __syncwarp();
+                }
+            }
             named_bar(2, NS);
             // T' = T Diag(beta), fp16, into the staging tile (over the dead A)
             {
                 const int t = stid >> 1, i0 = (stid & 1) * 32;
+                const float4 *b4 = reinterpret_cast<const float4 *>(&sm.beta[s][i0]);
+                const float4 *t4 = reinterpret_cast<const float4 *>(Tf + t * LDA + i0);
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     float r[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int i = i0 + 16 * hh + e;
-                        r[e] = (i <= t) ? Tf[t * LDA + i] * sm.beta[s][i] : 0.f;
+                    for (int e4 = 0; e4 < 4; ++e4) {
+                        const float4 tv = t4[4 * hh + e4], bv = b4[4 * hh + e4];
+                        const int i = i0 + 16 * hh + 4 * e4;
+                        r[4 * e4] = i <= t ? tv.x * bv.x : 0.f;
+                        r[4 * e4 + 1] = i + 1 <= t ? tv.y * bv.y : 0.f;
+                        r[4 * e4 + 2] = i + 2 <= t ? tv.z * bv.z : 0.f;
+                        r[4 * e4 + 3] = i + 3 <= t ? tv.w * bv.w : 0.f;
                     }
                     st_pack16<true>(sbase + F_AMAT, t, i0 + 16 * hh, r);
                 }
