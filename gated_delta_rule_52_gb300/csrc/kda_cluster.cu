@@ -91,16 +91,19 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 __device__ __forceinline__ int variant_off(int bt) { return 8 * bt * (bt + 1); }
 
-// acc (16 x 8) += A (16 x 8) * B (8 x 8) on the tensor cores (mma.sync, tf32
-// operands rounded to nearest, fp32 accumulation); A(r, k) = a[r * lda + k],
-// B(k, n) = b[k * ldb + n].
-__device__ __forceinline__ void mma_16x8x8(const float *a, int lda, const float *b, int ldb, int lane,
-                                           float (&acc)[4]) {
+// mma.sync operand fragments (g = lane / 4, q = lane % 4) of a row-major fp32
+// tile in shared memory, rounded to tf32: A (16 x 8) at a, B (8 x 8) at b.
+__device__ __forceinline__ void frag_a(const float *a, int lda, int lane, uint32_t (&f)[4]) {
     const int g = lane >> 2, q = lane & 3;
-    const uint32_t ah[4] = {to_tf32(a[g * lda + q]), to_tf32(a[(g + 8) * lda + q]),
-                            to_tf32(a[g * lda + q + 4]), to_tf32(a[(g + 8) * lda + q + 4])};
-    const uint32_t bh[2] = {to_tf32(b[q * ldb + g]), to_tf32(b[(q + 4) * ldb + g])};
-    mma_tf32_16x8x8(acc, ah, bh);
+    f[0] = to_tf32(a[g * lda + q]);
+    f[1] = to_tf32(a[(g + 8) * lda + q]);
+    f[2] = to_tf32(a[g * lda + q + 4]);
+    f[3] = to_tf32(a[(g + 8) * lda + q + 4]);
+}
+__device__ __forceinline__ void frag_b(const float *b, int ldb, int lane, uint32_t (&f)[2]) {
+    const int g = lane >> 2, q = lane & 3;
+    f[0] = to_tf32(b[q * ldb + g]);
+    f[1] = to_tf32(b[(q + 4) * ldb + g]);
 }
 
 // Stores a 16 x 8 accumulator tile (times `sign`) at d (row stride ldd).
@@ -173,9 +176,10 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
         const int cg = lane & 7, qr = lane >> 3;
         const int c0 = 64 * kh + 8 * cg;             // first of this thread's 8 channels
         const uint32_t kho = kh * 8192;              // the half inside a raw tile
-        float bias[8];
+        float2 bias[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) bias[e] = a2 * p.dt_bias[h * DK + c0 + e];
+        for (int i = 0; i < 4; ++i)
+            bias[i] = make_float2(a2 * p.dt_bias[h * DK + c0 + 2 * i], a2 * p.dt_bias[h * DK + c0 + 2 * i + 1]);
         // beta logits are loaded one chunk ahead (warp 0, two tokens per lane)
         auto load_beta = [&](int mm, float &x0, float &x1) {
             const int64_t cs = (int64_t)mm * C;
@@ -247,12 +251,14 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                 bl1 = nb1;
             }
 
-            // gate (log2 units) and its block-local inclusive cumulative sum H
-            float H[4][8];
+            // gate (log2 units) and its block-local inclusive cumulative sum H (channel pairs)
+            float2 H[4][4];
             {
-                float acc[8];
+                const float2 a2v = make_float2(a2, a2), lb2v = make_float2(lb2, lb2);
+                const float2 one = make_float2(1.f, 1.f);
+                float2 acc[4];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+                for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int t = 16 * blk + 4 * qr + j;
@@ -261,32 +267,32 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                         const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            acc[2 * i] += lb2 * __fdividef(1.f, 1.f + exp2f(fmaf(bf16lo(gw[i]), a2, bias[2 * i])));
-                            acc[2 * i + 1] +=
-                                lb2 * __fdividef(1.f, 1.f + exp2f(fmaf(bf16hi(gw[i]), a2, bias[2 * i + 1])));
+                            const float2 z = fma2(bf16x2_to_f2(gw[i]), a2v, bias[i]);
+                            const float2 d = add2(make_float2(exp2f(z.x), exp2f(z.y)), one);
+                            acc[i] = fma2(lb2v, make_float2(__fdividef(1.f, d.x), __fdividef(1.f, d.y)), acc[i]);
                         }
                     }
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) H[j][e] = acc[e];
+                    for (int i = 0; i < 4; ++i) H[j][i] = acc[i];
                 }
                 // add the totals of the earlier quarters (lanes 8 and 16 apart share channels)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    float v = acc[e];
-                    float u = __shfl_up_sync(0xffffffffu, v, 8);
-                    if (qr >= 1) v += u;
-                    u = __shfl_up_sync(0xffffffffu, v, 16);
-                    if (qr >= 2) v += u;
-                    float ex = __shfl_up_sync(0xffffffffu, v, 8);
-                    ex = qr >= 1 ? ex : 0.f;
+                for (int i = 0; i < 4; ++i) {
+                    float2 v = acc[i];
+                    float2 u = make_float2(__shfl_up_sync(0xffffffffu, v.x, 8), __shfl_up_sync(0xffffffffu, v.y, 8));
+                    if (qr >= 1) v = add2(v, u);
+                    u = make_float2(__shfl_up_sync(0xffffffffu, v.x, 16), __shfl_up_sync(0xffffffffu, v.y, 16));
+                    if (qr >= 2) v = add2(v, u);
+                    float2 ex = make_float2(__shfl_up_sync(0xffffffffu, v.x, 8), __shfl_up_sync(0xffffffffu, v.y, 8));
+                    if (qr == 0) ex = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) H[j][e] += ex;
-                    acc[e] = v;
+                    for (int j = 0; j < 4; ++j) H[j][i] = add2(H[j][i], ex);
+                    acc[i] = v;
                 }
                 if (qr == 3) {
                     float4 *bt4 = reinterpret_cast<float4 *>(&sm.btot[blk][c0]);
-                    bt4[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                    bt4[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+                    bt4[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+                    bt4[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
                 }
             }
             named_bar(1, NP);
@@ -331,8 +337,10 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                 const float4 *fs4 = reinterpret_cast<const float4 *>(&sm.fac[fb][c0]);
                 const float4 *fc4 = reinterpret_cast<const float4 *>(&sm.fac[fb + 1][c0]);
                 const float4 fsa = fs4[0], fsb = fs4[1], fca = fc4[0], fcb = fc4[1];
-                const float Fs[8] = {fsa.x, fsa.y, fsa.z, fsa.w, fsb.x, fsb.y, fsb.z, fsb.w};
-                const float FC[8] = {fca.x, fca.y, fca.z, fca.w, fcb.x, fcb.y, fcb.z, fcb.w};
+                const float2 Fs[4] = {make_float2(fsa.x, fsa.y), make_float2(fsa.z, fsa.w), make_float2(fsb.x, fsb.y),
+                                      make_float2(fsb.z, fsb.w)};
+                const float2 FC[4] = {make_float2(fca.x, fca.y), make_float2(fca.z, fca.w), make_float2(fcb.x, fcb.y),
+                                      make_float2(fcb.z, fcb.w)};
                 const uint32_t ama = sbase + F_AMA + kh * 16384, amb = sbase + F_AMB + kh * 20480;
 #pragma unroll 1
                 for (int j = 0; j < 4; ++j) {
@@ -342,53 +350,46 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                     uint4 kv = *reinterpret_cast<const uint4 *>(smem + rk_off + off);
                     if (t >= L) qv = kv = make_uint4(0u, 0u, 0u, 0u);
                     const float rq = sm.rq[s][t], rk = sm.rk[s][t];
+                    const float2 rq2 = make_float2(rq, rq), rk2 = make_float2(rk, rk);
                     const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w}, kw[4] = {kv.x, kv.y, kv.z, kv.w};
-                    float kp[8], qp[8];
+                    uint32_t wkp[4], wqp[4], wq[4], wk[4], wb[4], wn[4];
+                    float2 kn[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const float e1a = exp2f(H[0][2 * i]), e1b = exp2f(H[0][2 * i + 1]);
-                        kp[2 * i] = bf16lo(kw[i]) * e1a;
-                        kp[2 * i + 1] = bf16hi(kw[i]) * e1b;
-                        qp[2 * i] = bf16lo(qw[i]) * e1a;
-                        qp[2 * i + 1] = bf16hi(qw[i]) * e1b;
+                        const float2 k2 = bf16x2_to_f2(kw[i]), q2 = bf16x2_to_f2(qw[i]);
+                        const float2 e1 = make_float2(exp2f(H[0][i].x), exp2f(H[0][i].y));
+                        const float2 e2 = make_float2(exp2f(-H[0][i].x), exp2f(-H[0][i].y));
+                        const float2 kp = mul2(k2, e1), qp = mul2(q2, e1);
+                        kn[i] = mul2(k2, e2);
+                        wkp[i] = pack_bf16(kp.x, kp.y);
+                        wqp[i] = pack_bf16(qp.x, qp.y);
+                        wn[i] = pack_bf16(kn[i].x, kn[i].y);
+                        const float2 xq = mul2(qp, mul2(Fs[i], rq2));     // Q_hat*Gamma
+                        const float2 xk = mul2(kp, mul2(Fs[i], rk2));     // K_hat*Gamma
+                        const float2 xb = mul2(kn[i], mul2(FC[i], rk2));  // Kbar
+                        wq[i] = pack_f16(xq.x, xq.y);
+                        wk[i] = pack_f16(xk.x, xk.y);
+                        wb[i] = pack_f16(xb.x, xb.y);
                     }
-                    sts128(ama + sw128_off(32 * blk + r, 8 * cg), pack_bf16(kp[0], kp[1]), pack_bf16(kp[2], kp[3]),
-                           pack_bf16(kp[4], kp[5]), pack_bf16(kp[6], kp[7]));
-                    sts128(ama + sw128_off(32 * blk + 16 + r, 8 * cg), pack_bf16(qp[0], qp[1]),
-                           pack_bf16(qp[2], qp[3]), pack_bf16(qp[4], qp[5]), pack_bf16(qp[6], qp[7]));
-                    uint32_t w[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        w[i] = pack_f16(qp[2 * i] * (Fs[2 * i] * rq), qp[2 * i + 1] * (Fs[2 * i + 1] * rq));
-                    sts128(sbase + rq_off + off, w[0], w[1], w[2], w[3]);               // Q_hat*Gamma
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        w[i] = pack_f16(kp[2 * i] * (Fs[2 * i] * rk), kp[2 * i + 1] * (Fs[2 * i + 1] * rk));
-                    sts128(sbase + rk_off + off, w[0], w[1], w[2], w[3]);               // K_hat*Gamma
-                    float kn[8];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        kn[2 * i] = bf16lo(kw[i]) * exp2f(-H[0][2 * i]);
-                        kn[2 * i + 1] = bf16hi(kw[i]) * exp2f(-H[0][2 * i + 1]);
-                    }
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        w[i] = pack_f16(kn[2 * i] * (FC[2 * i] * rk), kn[2 * i + 1] * (FC[2 * i + 1] * rk));
-                    sts128(sbase + rg_off + off, w[0], w[1], w[2], w[3]);               // Kbar
-                    sts128(amb + sw128_off(variant_off(blk) + t, 8 * cg), pack_bf16(kn[0], kn[1]),
-                           pack_bf16(kn[2], kn[3]), pack_bf16(kn[4], kn[5]), pack_bf16(kn[6], kn[7]));
+                    sts128(ama + sw128_off(32 * blk + r, 8 * cg), wkp[0], wkp[1], wkp[2], wkp[3]);
+                    sts128(ama + sw128_off(32 * blk + 16 + r, 8 * cg), wqp[0], wqp[1], wqp[2], wqp[3]);
+                    sts128(amb + sw128_off(variant_off(blk) + t, 8 * cg), wn[0], wn[1], wn[2], wn[3]);
+                    sts128(sbase + rq_off + off, wq[0], wq[1], wq[2], wq[3]);
+                    sts128(sbase + rk_off + off, wk[0], wk[1], wk[2], wk[3]);
+                    sts128(sbase + rg_off + off, wb[0], wb[1], wb[2], wb[3]);
 #pragma unroll 1
                     for (int bt = blk + 1; bt < 4; ++bt) {
                         const float4 *d4 = reinterpret_cast<const float4 *>(&sm.fac[fb + 1 + bt - blk][c0]);
                         const float4 da = d4[0], db = d4[1];
-                        sts128(amb + sw128_off(variant_off(bt) + t, 8 * cg), pack_bf16(kn[0] * da.x, kn[1] * da.y),
-                               pack_bf16(kn[2] * da.z, kn[3] * da.w), pack_bf16(kn[4] * db.x, kn[5] * db.y),
-                               pack_bf16(kn[6] * db.z, kn[7] * db.w));
+                        const float2 v0 = mul2(kn[0], make_float2(da.x, da.y)), v1 = mul2(kn[1], make_float2(da.z, da.w));
+                        const float2 v2 = mul2(kn[2], make_float2(db.x, db.y)), v3 = mul2(kn[3], make_float2(db.z, db.w));
+                        sts128(amb + sw128_off(variant_off(bt) + t, 8 * cg), pack_bf16(v0.x, v0.y), pack_bf16(v1.x, v1.y),
+                               pack_bf16(v2.x, v2.y), pack_bf16(v3.x, v3.y));
                     }
 #pragma unroll
                     for (int jj = 0; jj < 3; ++jj)
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) H[jj][e] = H[jj + 1][e];
+                        for (int i = 0; i < 4; ++i) H[jj][i] = H[jj + 1][i];
                 }
             }
             fence_proxy_async_smem();
@@ -469,37 +470,42 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
             tc_fence_after();
 
             // A (fp32, beta_t/|k_t| x 1/|k_i|; only i < t is used later) and
-            // M (fp16, 1/|q_t| x 1/|k_i|, zero for i > t)
+            // M (fp16, 1/|q_t| x 1/|k_i|, zero for i > t); all column loads in flight at once
             {
                 const bool is_m = lane >= 16;
                 const int t = 16 * sw + (lane & 15);
                 const float rowf = is_m ? sm.rq[s][t] : sm.beta[s][t] * sm.rk[s][t];
                 const uint32_t col0 = 256 * s + variant_off(sw);
-#pragma unroll 1
-                for (int kk = 0; kk <= sw; ++kk) {
-                    float r[16];
-                    tmem_ld16(tmem_addr(tmem, 32 * sw, col0 + 16 * kk), r);
-                    tmem_ld_wait();
+                float r[4][16];
+                tmem_ld16(tmem_addr(tmem, 32 * sw, col0), r[0]);
+                if (sw >= 1) tmem_ld16(tmem_addr(tmem, 32 * sw, col0 + 16), r[1]);
+                if (sw >= 2) tmem_ld16(tmem_addr(tmem, 32 * sw, col0 + 32), r[2]);
+                if (sw >= 3) tmem_ld16(tmem_addr(tmem, 32 * sw, col0 + 48), r[3]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    if (kk > sw) break;
                     const float4 *rk4 = reinterpret_cast<const float4 *>(&sm.rk[s][16 * kk]);
 #pragma unroll
                     for (int e4 = 0; e4 < 4; ++e4) {
                         const float4 x = rk4[e4];
-                        r[4 * e4] *= rowf * x.x;
-                        r[4 * e4 + 1] *= rowf * x.y;
-                        r[4 * e4 + 2] *= rowf * x.z;
-                        r[4 * e4 + 3] *= rowf * x.w;
+                        r[kk][4 * e4] *= rowf * x.x;
+                        r[kk][4 * e4 + 1] *= rowf * x.y;
+                        r[kk][4 * e4 + 2] *= rowf * x.z;
+                        r[kk][4 * e4 + 3] *= rowf * x.w;
                     }
                     if (is_m) {
                         if (kk == sw) {
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) r[e] = e <= (lane & 15) ? r[e] : 0.f;
+                            for (int e = 0; e < 16; ++e) r[kk][e] = e <= (lane & 15) ? r[kk][e] : 0.f;
                         }
-                        st_pack16<true>(sbase + F_MST, t, 16 * kk, r);
+                        st_pack16<true>(sbase + F_MST, t, 16 * kk, r[kk]);
                     } else {
                         float4 *dst = reinterpret_cast<float4 *>(Amat + t * LDA + 16 * kk);
 #pragma unroll
                         for (int e4 = 0; e4 < 4; ++e4)
-                            dst[e4] = make_float4(r[4 * e4], r[4 * e4 + 1], r[4 * e4 + 2], r[4 * e4 + 3]);
+                            dst[e4] = make_float4(r[kk][4 * e4], r[kk][4 * e4 + 1], r[kk][4 * e4 + 2],
+                                                  r[kk][4 * e4 + 3]);
                     }
                 }
             }
@@ -525,37 +531,74 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                 for (int r = 0; r < 16; ++r) Tf[(16 * bb + r) * LDA + 16 * bb + j] = x[r];
             }
             named_bar(2, NS);
-            // B[bt][m] = T[bt][bt] A[bt][m] for m < bt, in place of A's blocks (warp bt)
-            if (sw >= 1) {
-                const float *Tb = Tf + (16 * sw) * LDA + 16 * sw;
-                float *Ab = Amat + (16 * sw) * LDA;
-#pragma unroll 1
-                for (int nt = 0; nt < 2 * sw; ++nt) {
-                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                    mma_16x8x8(Tb, LDA, Ab + 8 * nt, LDA, lane, acc);
-                    mma_16x8x8(Tb + 8, LDA, Ab + 8 * LDA + 8 * nt, LDA, lane, acc);
-                    __syncwarp();
-                    store_16x8(Ab + 8 * nt, LDA, lane, acc, 1.f);
+            // B[bt][m] = T[bt][bt] A[bt][m] for m < bt, in place of A's blocks: twelve
+            // 16x8 tiles (bt, nt), three per warp, all operands loaded before the MMAs
+            {
+                uint32_t fa[3][2][4], fb[3][2][2];
+#pragma unroll
+                for (int u = 0; u < 3; ++u) {
+                    const int idx = sw + 4 * u;
+                    const int bt = idx < 2 ? 1 : (idx < 6 ? 2 : 3);
+                    const int nt = idx - (bt == 1 ? 0 : (bt == 2 ? 2 : 6));
+                    const float *Tb = Tf + (16 * bt) * LDA + 16 * bt;
+                    const float *Ab = Amat + (16 * bt) * LDA + 8 * nt;
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks) {
+                        frag_a(Tb + 8 * ks, LDA, lane, fa[u][ks]);
+                        frag_b(Ab + 8 * ks * LDA, LDA, lane, fb[u][ks]);
+                    }
+                }
+                float acc[3][4];
+#pragma unroll
+                for (int u = 0; u < 3; ++u) {
+                    acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.f;
+                    mma_tf32_16x8x8(acc[u], fa[u][0], fb[u][0]);
+                    mma_tf32_16x8x8(acc[u], fa[u][1], fb[u][1]);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int u = 0; u < 3; ++u) {
+                    const int idx = sw + 4 * u;
+                    const int bt = idx < 2 ? 1 : (idx < 6 ? 2 : 3);
+                    const int nt = idx - (bt == 1 ? 0 : (bt == 2 ? 2 : 6));
+                    store_16x8(Amat + (16 * bt) * LDA + 8 * nt, LDA, lane, acc[u], 1.f);
                 }
             }
             named_bar(2, NS);
-            // Off-diagonal blocks of column block ba (warp ba), top to bottom:
-            // T[bt][ba] = -sum_{ba <= m < bt} B[bt][m] T[m][ba]
+            // Off-diagonal blocks of column block ba (warp ba), right-looking: once
+            // T[m][ba] is final, B[bt][m] T[m][ba] is added to the sum of every bt > m,
+            // and T[m+1][ba] = -(its completed sum).
             if (sw <= 2) {
                 const int ba = sw;
-#pragma unroll 1
-                for (int bt = ba + 1; bt < 4; ++bt) {
-                    float acc[2][4] = {};
-                    const float *Bp = Amat + (16 * bt) * LDA + 16 * ba;
-                    const float *Tp = Tf + (16 * ba) * LDA + 16 * ba;
-#pragma unroll 1
-                    for (int kk = 0; kk < 2 * (bt - ba); ++kk) {
-                        mma_16x8x8(Bp + 8 * kk, LDA, Tp + 8 * kk * LDA, LDA, lane, acc[0]);
-                        mma_16x8x8(Bp + 8 * kk, LDA, Tp + 8 * kk * LDA + 8, LDA, lane, acc[1]);
+                float P[3][2][4];   // [bt - 1][n tile]
+#pragma unroll
+                for (int i = 0; i < 3; ++i)
+#pragma unroll
+                    for (int n = 0; n < 2; ++n) P[i][n][0] = P[i][n][1] = P[i][n][2] = P[i][n][3] = 0.f;
+#pragma unroll
+                for (int m = 0; m < 3; ++m) {
+                    if (m < ba) continue;
+                    uint32_t tb[2][2][2];
+                    const float *Tm = Tf + (16 * m) * LDA + 16 * ba;
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+                        for (int n = 0; n < 2; ++n) frag_b(Tm + 8 * ks * LDA + 8 * n, LDA, lane, tb[ks][n]);
+#pragma unroll
+                    for (int bt = m + 1; bt < 4; ++bt) {
+                        uint32_t fa[2][4];
+                        const float *Bp = Amat + (16 * bt) * LDA + 16 * m;
+                        frag_a(Bp, LDA, lane, fa[0]);
+                        frag_a(Bp + 8, LDA, lane, fa[1]);
+#pragma unroll
+                        for (int n = 0; n < 2; ++n) {
+                            mma_tf32_16x8x8(P[bt - 1][n], fa[0], tb[0][n]);
+                            mma_tf32_16x8x8(P[bt - 1][n], fa[1], tb[1][n]);
+                        }
                     }
-                    float *dst = Tf + (16 * bt) * LDA + 16 * ba;
-                    store_16x8(dst, LDA, lane, acc[0], -1.f);
-                    store_16x8(dst + 8, LDA, lane, acc[1], -1.f);
+                    float *dst = Tf + (16 * (m + 1)) * LDA + 16 * ba;
+                    store_16x8(dst, LDA, lane, P[m][0], -1.f);
+                    store_16x8(dst + 8, LDA, lane, P[m][1], -1.f);
                     __syncwarp();
                 }
             }
