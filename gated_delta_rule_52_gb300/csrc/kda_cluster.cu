@@ -935,8 +935,9 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT, 1)
 kda_cluster_kernel(const __grid_constant__ TmaMaps maps, Params p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte alignment (128B-swizzled tiles) by pointer arithmetic on the shared
+    // array itself, so that every access through `smem` stays a shared-memory access
+    unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     Small &sm = *reinterpret_cast<Small *>(smem + SMALL);
     const uint32_t rank = cluster_ctarank();
     const int64_t unit = cluster_id_x();
