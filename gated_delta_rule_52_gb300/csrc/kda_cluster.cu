@@ -678,17 +678,24 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
             *ptr = x;
         }
     };
-    // -W (D_W lanes 0..63) -> rows 0..63 of the G3 A operand; warps 8, 9
+    // -W (D_W lanes 0..63) -> rows 0..63 of the G3 A operand: warps 8 and 12 take
+    // the two column halves of lane quarter 0, warp 9 both halves of quarter 1
     auto read_w = [&]() {
-        if (warp == 8 || warp == 9) {
-            const int t = (warp - 8) * 32 + lane;
-            for (int jj = 0; jj < 8; ++jj) {
-                float r[16];
-                tmem_ld16(tmem_addr(D_W, (warp & 3) * 32, 16 * jj), r);
+        if (warp == 8 || warp == 9 || warp == 12) {
+            const int t = quarter * 32 + lane;
+            const int cb0 = warp == 12 ? 1 : 0, cb1 = warp == 8 ? 0 : 1;
+#pragma unroll 1
+            for (int cb = cb0; cb <= cb1; ++cb) {
+                float r[4][16];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) tmem_ld16(tmem_addr(D_W, quarter * 32, 64 * cb + 16 * jj), r[jj]);
                 tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) r[e] = -r[e];
-                st_pack16<true>(sbase + C_G3A + (jj >> 2) * 16384, t, (16 * jj) & 63, r);
+                for (int jj = 0; jj < 4; ++jj) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) r[jj][e] = -r[jj][e];
+                    st_pack16<true>(sbase + C_G3A + cb * 16384, t, 16 * jj, r[jj]);
+                }
             }
         }
     };
@@ -810,18 +817,14 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
             mbar_arrive_remote(front_bar(&sm.single_free));
             if (m + 1 < nchunks) issue_v(m + 1);
         }
-        if (warp == 8 || warp == 9) {
-            const int t = (warp - 8) * 32 + lane;
+        if (warp < 8 && quarter < 2) {   // warps 0, 1, 4, 5: lane quarter 0/1, column half
+            const int t = quarter * 32 + lane;
+            float r[4][16];
 #pragma unroll
-            for (int hb = 0; hb < 2; ++hb) {
-                float r[4][16];
+            for (int jj = 0; jj < 4; ++jj) tmem_ld16(tmem_addr(D_U, quarter * 32, 64 * half + 16 * jj), r[jj]);
+            tmem_ld_wait();
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj)
-                    tmem_ld16(tmem_addr(D_U, (warp & 3) * 32, 64 * hb + 16 * jj), r[jj]);
-                tmem_ld_wait();
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) st_pack16<true>(sbase + C_UT + hb * 8192, t, 16 * jj, r[jj]);
-            }
+            for (int jj = 0; jj < 4; ++jj) st_pack16<true>(sbase + C_UT + half * 8192, t, 16 * jj, r[jj]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
