@@ -51,6 +51,12 @@ constexpr int DK = kHeadDim;
 constexpr int NT = 416;            // 13 warps in both CTAs
 constexpr int NP = 256;            // front prologue group: warps 0-7
 constexpr int NS = 128;            // front solver group: warps 8-11
+// Threads that wait on mbarriers for their group (and publish through a named
+// barrier): warp 1 for the prologue, warp 10 for the solver, so that the waiting
+// threads of the front sit on different schedulers (warp 12, the control warp,
+// shares its scheduler with neither).
+constexpr int kProLead = 32;       // thread index
+constexpr int kSolLead = 64;       // index within the solver group
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kWait = 2000000000ull;   // 2 s per wait
 constexpr int LDA = 68;             // fp32 row stride of A and T (16-byte aligned rows)
@@ -195,7 +201,7 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
             const int64_t cs = (int64_t)m * C;
             const int L = (int)((len - cs) < C ? (len - cs) : C);
             const uint32_t rq_off = F_RAW + s * F_SLOT, rk_off = rq_off + 16384, rg_off = rq_off + 32768;
-            if (tid == 0) {
+            if (tid == kProLead) {
                 bool ok = mbar_wait(&sm.raw_full[s], (m >> 1) & 1, kWait);
                 if (ok && m >= 2) ok = mbar_wait(&sm.s_done[s], ((m - 2) >> 1) & 1, kWait);
                 if (!ok) { set_err(p); sm.abort_p = 1; }
@@ -395,7 +401,7 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
             fence_proxy_async_smem();
             named_bar(1, NP);
 
-            if (tid == 0) mbar_arrive(&sm.pdone[s]);   // operands and rq/rk/beta of chunk m ready
+            if (tid == kProLead) mbar_arrive(&sm.pdone[s]);   // operands and rq/rk/beta of chunk m ready
         }
     } else if (warp == 12) {
         // ------------------------------------------------ control warp (lane 0)
@@ -457,7 +463,7 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
         named_bar(2, NS);
         for (int m = 0; m < nchunks; ++m) {
             const int s = m & 1;
-            if (stid == 0) {
+            if (stid == kSolLead) {
                 bulk_wait_read0();   // previous T'/M staging shipped
                 if (!mbar_wait(&sm.pdone[s], (m >> 1) & 1, kWait) ||
                     !mbar_wait(&sm.g1_done[s], (m >> 1) & 1, kWait)) {
@@ -511,7 +517,7 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
             }
             tc_fence_before();
             named_bar(2, NS);
-            if (stid == 0) mbar_arrive(&sm.am_free[s]);
+            if (stid == kSolLead) mbar_arrive(&sm.am_free[s]);
 
             // T = (I + A)^-1 in 16x16 blocks.  Diagonal blocks: forward substitution,
             // thread = (block, column j), updating all later rows after each solved row.
@@ -625,7 +631,7 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
             }
             fence_proxy_async_smem();
             named_bar(2, NS);
-            if (stid == 0) {
+            if (stid == kSolLead) {
                 mbar_arrive(&sm.s_done[s]);
                 bool ok = true;
                 const uint32_t full = chain_bar(&sm.full[s]);
@@ -637,7 +643,7 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                 if (!ok) { set_err(p); sm.abort_s = 1; sm.abort_p = 1; }
             }
         }
-        if (stid == 0) bulk_wait0();
+        if (stid == kSolLead) bulk_wait0();
     }
 }
 
