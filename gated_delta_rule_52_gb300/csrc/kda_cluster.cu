@@ -11,13 +11,15 @@
 // Work split.  Only the last two lines are sequential across chunks; everything
 // before them depends on the chunk's own inputs.  So:
 //   CTA rank 0 ("front") runs the chunk-parallel part one chunk ahead:
-//     warps 0-7  prologue of chunk m: gate, norms, block-local decay, the
-//                operands of G1 and the chain's K_hat*Gamma, Q_hat*Gamma, Kbar;
-//                issues G1 = [Kp; Qp] x Kn^T into a double-buffered TMEM slot;
+//     warps 0-7  prologue of chunk m: gate, block-local decay, the operands
+//                of G1 = [Kp; Qp] x Kn^T and the chain's K_hat*Gamma,
+//                Q_hat*Gamma, Kbar;
+//     warps 13-15 beside the gate: row norms of q and k, beta;
 //     warps 8-11 solver of chunk m-1: A and M out of TMEM, the blocked
 //                inverse, T' (fp16);
-//     warp 12    control: issues G1, ships the prologue's tiles, prefetches
-//                the next raw tiles, so the prologue never waits on the chain;
+//     warp 12    control: issues G1 into a double-buffered TMEM slot, ships
+//                the prologue's tiles, prefetches the next raw tiles, so the
+//                prologue never waits on the chain;
 //     both groups ship their tiles into the chain CTA's shared memory with bulk
 //     shared->shared copies that complete as transaction bytes on the chain's
 //     per-slot mbarrier.
@@ -26,7 +28,8 @@
 //     U readout, S decay
 //     G4 = Kbar^T U -> S,  G5 = [0; M] x U -> O
 //     O and S readout; W for the next chunk (G2w = [T'; 0] x K_hat*Gamma) is
-//     computed and read out beside this, off the sequential path.
+//     computed and read out beside this, off the sequential path (16 warps:
+//     S by warps 0-7, -W by 8/9/12/13, O by 10/11/14/15, one column half each).
 // Flow control: the chain arrives remotely on the front's "slot free" barriers
 // (per-slot tiles K_bar, M, Gamma_C) and "single free" barrier (single-buffered
 // tiles T', K_hat*Gamma, Q_hat*Gamma); the front waits on them before shipping.
@@ -48,9 +51,11 @@ using namespace sm103;
 
 constexpr int C = kChunk;
 constexpr int DK = kHeadDim;
-constexpr int NT = 416;            // 13 warps in both CTAs
+constexpr int NT = 512;            // 16 warps in both CTAs
 constexpr int NP = 256;            // front prologue group: warps 0-7
 constexpr int NS = 128;            // front solver group: warps 8-11
+constexpr int NH = 96;             // front helper group (norms, beta): warps 13-15
+constexpr int kHelp0 = 416;        // first helper thread
 // Threads that wait on mbarriers for their group (and publish through a named
 // barrier): warp 1 for the prologue, warp 10 for the solver, so that the waiting
 // threads of the front sit on different schedulers (warp 12, the control warp,
@@ -91,6 +96,7 @@ struct Small {
     uint64_t full[2], v_full, mma_bar, w_bar;
     uint32_t tmem_base;
     int abort_p, abort_s, abort_c;
+    int dec_p, dec_s;   // a group's abort decision, written by its lead thread only, before a barrier
 };
 constexpr uint32_t SMEM_BYTES = SMALL + sizeof(Small) + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -186,16 +192,6 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
 #pragma unroll
         for (int i = 0; i < 4; ++i)
             bias[i] = make_float2(a2 * p.dt_bias[h * DK + c0 + 2 * i], a2 * p.dt_bias[h * DK + c0 + 2 * i + 1]);
-        // beta logits are loaded one chunk ahead (warp 0, two tokens per lane)
-        auto load_beta = [&](int mm, float &x0, float &x1) {
-            const int64_t cs = (int64_t)mm * C;
-            const int Lm = (int)((len - cs) < C ? (len - cs) : C);
-            const int64_t r0 = row_base + cs;
-            x0 = lane < Lm ? __bfloat162float(p.beta[(r0 + lane) * p.H + h]) : 0.f;
-            x1 = lane + 32 < Lm ? __bfloat162float(p.beta[(r0 + lane + 32) * p.H + h]) : 0.f;
-        };
-        float bl0 = 0.f, bl1 = 0.f;
-        if (warp == 0 && nchunks > 0) load_beta(0, bl0, bl1);
         for (int m = 0; m < nchunks; ++m) {
             const int s = m & 1;
             const int64_t cs = (int64_t)m * C;
@@ -205,57 +201,10 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                 bool ok = mbar_wait(&sm.raw_full[s], (m >> 1) & 1, kWait);
                 if (ok && m >= 2) ok = mbar_wait(&sm.s_done[s], ((m - 2) >> 1) & 1, kWait);
                 if (!ok) { set_err(p); sm.abort_p = 1; }
+                sm.dec_p = sm.abort_p;
             }
-            named_bar(1, NP);
-            if (sm.abort_p) break;
-            float nb0 = 0.f, nb1 = 0.f;
-            if (warp == 0 && m + 1 < nchunks) load_beta(m + 1, nb0, nb1);
-
-            // norms: half-warps take one row each (8 channels per lane, 16-byte loads)
-            {
-                const int hw = lane >> 4, l16 = lane & 15;
-                const int kbb = l16 >> 3, col = (l16 & 7) * 8;
-                float sq[4], sk[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int t = warp + (NP / 32) * (2 * u + hw);
-                    const uint32_t off = kbb * 8192 + sw128_off(t, col);
-                    const uint4 qv = *reinterpret_cast<const uint4 *>(smem + rq_off + off);
-                    const uint4 kv = *reinterpret_cast<const uint4 *>(smem + rk_off + off);
-                    const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w}, kw[4] = {kv.x, kv.y, kv.z, kv.w};
-                    float a = 0.f, b = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        a = fmaf(bf16lo(qw[i]), bf16lo(qw[i]), a);
-                        a = fmaf(bf16hi(qw[i]), bf16hi(qw[i]), a);
-                        b = fmaf(bf16lo(kw[i]), bf16lo(kw[i]), b);
-                        b = fmaf(bf16hi(kw[i]), bf16hi(kw[i]), b);
-                    }
-                    sq[u] = a;
-                    sk[u] = b;
-                }
-#pragma unroll
-                for (int o = 8; o > 0; o >>= 1)
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        sq[u] += __shfl_xor_sync(0xffffffffu, sq[u], o);
-                        sk[u] += __shfl_xor_sync(0xffffffffu, sk[u], o);
-                    }
-                if (l16 == 0) {
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int t = warp + (NP / 32) * (2 * u + hw);
-                        sm.rq[s][t] = t < L ? rsqrtf(sq[u] + 1e-6f) : 0.f;
-                        sm.rk[s][t] = t < L ? rsqrtf(sk[u] + 1e-6f) : 0.f;
-                    }
-                }
-            }
-            if (warp == 0) {
-                sm.beta[s][lane] = lane < L ? 1.f / (1.f + exp2f(-bl0 * kLog2e)) : 0.f;
-                sm.beta[s][lane + 32] = lane + 32 < L ? 1.f / (1.f + exp2f(-bl1 * kLog2e)) : 0.f;
-                bl0 = nb0;
-                bl1 = nb1;
-            }
+            named_bar(1, NP + NH);   // with the helpers: raw tiles of chunk m are in
+            if (sm.dec_p) break;
 
             // gate (log2 units) and its block-local inclusive cumulative sum H (channel pairs)
             float2 H[4][4];
@@ -301,7 +250,7 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                     bt4[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
                 }
             }
-            named_bar(1, NP);
+            named_bar(1, NP + NH);   // gate totals, and the helpers' norms and beta
 
             // decay factors per (block, channel): thread = channel, two blocks each
             {
@@ -324,14 +273,18 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                 }
             }
             // [Kp; Qp] and Kn are free once G1 of the previous chunk completed
-            if (tid == 0 && m >= 1) {
-                if (!mbar_wait(&sm.g1_done[(m - 1) & 1], ((m - 1) >> 1) & 1, kWait)) {
+            if (tid == kProLead) {
+                if (m >= 1 && !mbar_wait(&sm.g1_done[(m - 1) & 1], ((m - 1) >> 1) & 1, kWait)) {
                     set_err(p);
                     sm.abort_p = 1;
                 }
+                sm.dec_p = sm.abort_p;
             }
-            named_bar(1, NP);
-            if (sm.abort_p) break;
+            named_bar(3, NP);
+            if (sm.dec_p) {
+                named_bar(1, NP + NH);   // the helpers read the decision at their next barrier
+                break;
+            }
 
             // Operands.  G1 (bf16, raw q/k times block-local decay): Kp = k 2^H and
             // Qp = q 2^H at rows 32 blk + r and 32 blk + 16 + r of [Kp; Qp]; key
@@ -399,9 +352,55 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                 }
             }
             fence_proxy_async_smem();
-            named_bar(1, NP);
+            named_bar(3, NP);
 
             if (tid == kProLead) mbar_arrive(&sm.pdone[s]);   // operands and rq/rk/beta of chunk m ready
+        }
+    } else if (tid >= kHelp0) {
+        // ------------------------------------------------ helper group
+        // Row norms (one thread per row of q or k) and beta, beside the prologue's gate;
+        // published to the prologue by the barrier that ends its gate step.
+        const int htid = tid - kHelp0;
+        auto load_logit = [&](int mm) {
+            const int64_t cs = (int64_t)mm * C;
+            const int Lm = (int)((len - cs) < C ? (len - cs) : C);
+            return htid < Lm ? __bfloat162float(p.beta[(row_base + cs + htid) * p.H + h]) : 0.f;
+        };
+        float nb = 0.f;   // logit of token htid, loaded one chunk ahead
+        if (htid < C && nchunks > 0) nb = load_logit(0);
+        for (int m = 0; m < nchunks; ++m) {
+            const int s = m & 1;
+            const int64_t cs = (int64_t)m * C;
+            const int L = (int)((len - cs) < C ? (len - cs) : C);
+            const uint32_t rq_off = F_RAW + s * F_SLOT, rk_off = rq_off + 16384;
+            named_bar(1, NP + NH);
+            if (sm.dec_p) break;
+            const float bl = nb;
+            if (htid < C && m + 1 < nchunks) nb = load_logit(m + 1);
+            for (int i = htid; i < 2 * C; i += NH) {
+                const int t = i >> 1;
+                const uint32_t base = (i & 1) ? rk_off : rq_off;
+                float2 acc[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) acc[u] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int c16 = 0; c16 < 16; ++c16) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(
+                        smem + base + (c16 >> 3) * 8192 + sw128_off(t, (c16 & 7) * 8));
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float2 x = bf16x2_to_f2(w[u]);
+                        acc[u] = fma2(x, x, acc[u]);
+                    }
+                }
+                const float2 s01 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+                const float r = t < L ? rsqrtf(s01.x + s01.y + 1e-6f) : 0.f;
+                if (i & 1) sm.rk[s][t] = r;
+                else sm.rq[s][t] = r;
+            }
+            if (htid < C) sm.beta[s][htid] = htid < L ? 1.f / (1.f + exp2f(-bl * kLog2e)) : 0.f;
+            named_bar(1, NP + NH);
         }
     } else if (warp == 12) {
         // ------------------------------------------------ control warp (lane 0)
@@ -470,9 +469,10 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                     set_err(p);
                     sm.abort_s = 1;
                 }
+                sm.dec_s = sm.abort_s;
             }
             named_bar(2, NS);
-            if (sm.abort_s) break;
+            if (sm.dec_s) break;
             tc_fence_after();
 
             // A (fp32, beta_t/|k_t| x 1/|k_i|; only i < t is used later) and
@@ -653,7 +653,7 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
                                           int64_t row_base, int64_t len, int nchunks) {
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, half = (warp >> 2) & 1;   // warps 0-7: (lane quarter, column half)
+    const int quarter = warp & 3, half = (warp >> 2) & 1;   // TMEM lane quarter; column half
     const uint32_t D_S = tmem, D_W = tmem + 128, D_U = tmem + 256;
     const uint32_t front_small = mapa_shared(smem_u32(&sm), 0);
     auto front_bar = [&](uint64_t *local_bar) {
@@ -684,14 +684,13 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
             *ptr = x;
         }
     };
-    // -W (D_W lanes 0..63) -> rows 0..63 of the G3 A operand: warps 8 and 12 take
-    // the two column halves of lane quarter 0, warp 9 both halves of quarter 1
+    // -W (D_W lanes 0..63) -> rows 0..63 of the G3 A operand: warps 8, 9, 12, 13
+    // (lane quarter 0/1, one column half each)
     auto read_w = [&]() {
-        if (warp == 8 || warp == 9 || warp == 12) {
+        if (warp == 8 || warp == 9 || warp == 12 || warp == 13) {
             const int t = quarter * 32 + lane;
-            const int cb0 = warp == 12 ? 1 : 0, cb1 = warp == 8 ? 0 : 1;
-#pragma unroll 1
-            for (int cb = cb0; cb <= cb1; ++cb) {
+            {
+                const int cb = half;
                 float r[4][16];
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) tmem_ld16(tmem_addr(D_W, quarter * 32, 64 * cb + 16 * jj), r[jj]);
@@ -888,11 +887,12 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
                 }
                 tmem_st_wait();
             }
-        } else if (warp == 10 || warp == 11) {
-            const int t = (warp - 10) * 32 + lane;
+        } else if (warp == 10 || warp == 11 || warp == 14 || warp == 15) {
+            // O rows (D_U lanes 64..127): lane quarter 2/3, one column half each
+            const int t = (quarter - 2) * 32 + lane;
             const float sc = p.scale;
-#pragma unroll
-            for (int hb = 0; hb < 2; ++hb) {
+            {
+                const int hb = half;
                 float r[4][16];
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj)
@@ -994,6 +994,7 @@ kda_cluster_kernel(const __grid_constant__ TmaMaps maps, Params p) {
         mbar_init(&sm.mma_bar, 1);
         mbar_init(&sm.w_bar, 1);
         sm.abort_p = sm.abort_s = sm.abort_c = 0;
+        sm.dec_p = sm.dec_s = 0;
         fence_mbar_init();
     }
     if (threadIdx.x < 32) {
