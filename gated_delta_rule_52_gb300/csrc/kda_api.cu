@@ -2,9 +2,13 @@
 // device error word, and dispatch to the kernels.
 #include <cmath>
 #include <cstdint>
+#include <mutex>
+#include <vector>
 
 #include "../../include/kda.h"
 #include "kda_internal.h"
+
+static_assert(KDA_WORKSPACE_BYTES_PER_UNIT == kda::kWsBytesPerUnit, "workspace size in kda.h");
 
 namespace {
 
@@ -62,7 +66,41 @@ kda_status validate(const void *q, const void *k, const void *v, const void *g, 
     p.T = T;
     p.H = H;
     p.err = nullptr;
+    p.ws = nullptr;
     return KDA_OK;
+}
+
+// Memory pool for kda_fwd's workspaces, one per device, created on first use and
+// kept for the life of the process.  Its release threshold keeps freed blocks
+// mapped, so the stream-ordered allocation of a call after the first is cheap;
+// the device's default pool is left untouched.
+cudaMemPool_t workspace_pool(int device) {
+    static std::mutex mu;
+    static std::vector<cudaMemPool_t> pools;
+    std::lock_guard<std::mutex> lock(mu);
+    if ((int)pools.size() <= device) pools.resize(device + 1, nullptr);
+    if (!pools[device]) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = device;
+        cudaMemPool_t pool = nullptr;
+        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
+        uint64_t keep = UINT64_MAX;
+        cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        pools[device] = pool;
+    }
+    return pools[device];
+}
+
+kda_status launch(kda::Params &p, void *stream) {
+    int *err = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void **>(&err), g_kda_error) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    p.err = err;
+    return kda::launch_cluster(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KDA_OK
+                                                                                    : KDA_ERR_CUDA;
 }
 
 }  // namespace
@@ -80,12 +118,39 @@ kda_status kda_fwd(const void *q, const void *k, const void *v, const void *g, c
                              H, K, V, p);
     if (st != KDA_OK) return st;
     if (p.n_seqs == 0 || p.H == 0) return KDA_OK;
-    int *err = nullptr;
-    if (cudaGetSymbolAddress(reinterpret_cast<void **>(&err), g_kda_error) != cudaSuccess)
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return KDA_ERR_CUDA;
+    cudaMemPool_t pool = workspace_pool(device);
+    if (!pool) return KDA_ERR_CUDA;
+    void *ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, (size_t)(p.n_seqs * p.H) * kda::kWsBytesPerUnit, pool, cs) !=
+        cudaSuccess)
         return KDA_ERR_CUDA;
-    p.err = err;
-    cudaError_t e = kda::launch_cluster(p, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    p.ws = static_cast<unsigned char *>(ws);
+    st = launch(p, stream);
+    if (cudaFreeAsync(ws, cs) != cudaSuccess) st = KDA_ERR_CUDA;
+    return st;
+}
+
+kda_status kda_fwd_ws(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                      float scale, void *out, const float *A_log, const float *dt_bias,
+                      float lower_bound, const void *initial_state, void *final_state,
+                      int state_dtype, const int64_t *cu_seqlens, int64_t num_seqs, int64_t B,
+                      int64_t T, int64_t H, int64_t K, int64_t V, void *workspace,
+                      size_t workspace_bytes, void *stream) {
+    kda::Params p;
+    kda_status st = validate(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound,
+                             initial_state, final_state, state_dtype, cu_seqlens, num_seqs, B, T,
+                             H, K, V, p);
+    if (st != KDA_OK) return st;
+    const int64_t units = p.n_seqs * p.H;
+    if (units > 0 && !workspace) return KDA_ERR_NULL;
+    if (workspace && !aligned16(workspace)) return KDA_ERR_ALIGN;
+    if ((uint64_t)workspace_bytes < (uint64_t)units * kda::kWsBytesPerUnit) return KDA_ERR_VALUE;
+    if (units == 0) return KDA_OK;
+    p.ws = static_cast<unsigned char *>(workspace);
+    return launch(p, stream);
 }
 
 const char *kda_status_string(int status) {
@@ -96,7 +161,7 @@ const char *kda_status_string(int status) {
         case KDA_ERR_SHAPE: return "KDA_ERR_SHAPE: inconsistent sizes";
         case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: only K = V = 128 is supported";
         case KDA_ERR_ALIGN: return "KDA_ERR_ALIGN: tensor pointer not 16-byte aligned";
-        case KDA_ERR_VALUE: return "KDA_ERR_VALUE: lower_bound outside [-5, 0] or non-finite scale";
+        case KDA_ERR_VALUE: return "KDA_ERR_VALUE: lower_bound outside [-5, 0], non-finite scale or workspace too small";
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA call or launch failed";
         case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded device wait expired";
         default: return "KDA: unknown status";
@@ -112,6 +177,6 @@ kda_status kda_get_device_status(void *stream) {
     return h == 0 ? KDA_OK : static_cast<kda_status>(h);
 }
 
-int kda_version(void) { return 100; }
+int kda_version(void) { return 101; }
 
 }  // extern "C"

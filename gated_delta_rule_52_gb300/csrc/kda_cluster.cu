@@ -66,6 +66,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kWait = 2000000000ull;   // 2 s per wait
 constexpr int LDA = 68;             // fp32 row stride of A and T (16-byte aligned rows)
 constexpr uint32_t kChunkBytes = 16384 * 3 + 512 + 8192 * 2;   // front -> chain per chunk
+constexpr uint32_t WS_KB = 0, WS_QG = 16384, WS_KG = 32768, WS_GC = 49152;   // workspace slot layout
 constexpr int kOrderMax = 256;     // varlen batches up to this many sequences run longest first
 constexpr int kFacRows = 14;       // rows of the per-chunk decay-factor table (fac_base)
 
@@ -94,6 +95,7 @@ struct Small {
     float gamC_c[2][DK];                     // chain: copy destination
     uint64_t raw_full[2], g1_done[2], am_free[2], s_done[2], slot_free[2], single_free, pdone[2];
     uint64_t full[2], v_full, mma_bar, w_bar;
+    uint64_t gready[2], gfree[2];   // workspace slot written (chain side) / loaded (front side)
     uint32_t tmem_base;
     int abort_p, abort_s, abort_c;
     int dec_p, dec_s;   // a group's abort decision, written by its lead thread only, before a barrier
@@ -155,8 +157,9 @@ __device__ __forceinline__ void set_err(const Params &p) {
 
 // ============================================================== front CTA
 __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, unsigned char *smem,
-                                          Small &sm, uint32_t tmem, int64_t h, int64_t row_base,
-                                          int64_t len, int nchunks) {
+                                          Small &sm, uint32_t tmem, int64_t unit, int64_t h,
+                                          int64_t row_base, int64_t len, int nchunks) {
+    unsigned char *wsu = p.ws + unit * kWsBytesPerUnit;   // this cluster's workspace
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t chain_small = mapa_shared(smem_u32(&sm), 1);
@@ -424,21 +427,21 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                     }
                     mma_commit(&sm.g1_done[s]);
                 }
-                if (ok && m >= 2) ok = mbar_wait_cluster(&sm.slot_free[s], ((m - 2) >> 1) & 1, kWait);
-                const uint32_t full = chain_bar(&sm.full[s]);
+                // Kbar, Q_hat*Gamma, K_hat*Gamma and exp(G_C) of chunk m go to workspace
+                // slot s (L2) once the chain has loaded chunk m - 2 from it; the chain
+                // pulls them with bulk loads.  (Shared-to-shared copies between the two
+                // SMs move ~14 bytes per cycle; the slot round trip through L2 frees the
+                // raw tiles sooner.)
+                if (ok && m >= 2) ok = mbar_wait_cluster(&sm.gfree[s], ((m - 2) >> 1) & 1, kWait);
+                unsigned char *slot = wsu + s * kWsSlot;
                 if (ok) {
-                    bulk_copy_to_peer(chain_addr(C_KB + s * 16384), sbase + rg_off, 16384, full);
-                    bulk_copy_to_peer(chain_small + (smem_u32(&sm.gamC_c[s][0]) - smem_u32(&sm)),
-                                      smem_u32(&sm.gamC_f[s][0]), 512, full);
-                }
-                if (ok && m >= 1) ok = mbar_wait_cluster(&sm.single_free, (m - 1) & 1, kWait);
-                if (ok) {
-                    bulk_copy_to_peer(chain_addr(C_G3A + 8192), sbase + rq_off, 8192, full);
-                    bulk_copy_to_peer(chain_addr(C_G3A + 16384 + 8192), sbase + rq_off + 8192, 8192, full);
-                    bulk_copy_to_peer(chain_addr(C_B2), sbase + rk_off, 16384, full);
+                    bulk_store(slot + WS_KB, smem + rg_off, 16384);
+                    bulk_store(slot + WS_QG, smem + rq_off, 16384);
+                    bulk_store(slot + WS_KG, smem + rk_off, 16384);
+                    bulk_store(slot + WS_GC, &sm.gamC_f[s][0], 512);
                 }
                 bulk_commit();
-                bulk_wait_read0();
+                bulk_wait_read0();   // raw tiles and exp(G_C) of slot s may be overwritten
                 if (!ok) {
                     set_err(p);
                     sm.abort_p = 1;
@@ -446,6 +449,9 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                     break;
                 }
                 if (m + 2 < nchunks) issue_raw(m + 2);
+                bulk_wait0();        // the stores are complete in global memory
+                fence_proxy_async_global();
+                mbar_arrive_remote(chain_bar(&sm.gready[s]));
             }
             bulk_wait0();
         }
@@ -649,8 +655,9 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
 
 // ============================================================== chain CTA
 __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, unsigned char *smem,
-                                          Small &sm, uint32_t tmem, int64_t n, int64_t h,
+                                          Small &sm, uint32_t tmem, int64_t unit, int64_t n, int64_t h,
                                           int64_t row_base, int64_t len, int nchunks) {
+    const unsigned char *wsu = p.ws + unit * kWsBytesPerUnit;   // this cluster's workspace
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = (warp >> 2) & 1;   // TMEM lane quarter; column half
@@ -666,6 +673,21 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
         mbar_arrive_expect_tx(&sm.v_full, 16384);
         tma_load_3d(smem + C_B2 + 16384, &maps.v, &sm.v_full, 0, (int)h, row);
         tma_load_3d(smem + C_B2 + 16384 + 8192, &maps.v, &sm.v_full, 64, (int)h, row);
+    };
+    // Thread 0: the workspace tiles of chunk j into their operand buffers (on full[j & 1]),
+    // once the front has written them; returns false if that wait gave up.
+    auto load_chunk = [&](int j) -> bool {
+        const int sj = j & 1;
+        if (!mbar_wait_cluster(&sm.gready[sj], (j >> 1) & 1, kWait)) return false;
+        fence_proxy_async_global();
+        const unsigned char *slot = wsu + sj * kWsSlot;
+        const uint32_t fb = smem_u32(&sm.full[sj]);
+        bulk_load(sbase + C_KB + sj * 16384, slot + WS_KB, 16384, fb);
+        bulk_load(sbase + C_G3A + 8192, slot + WS_QG, 8192, fb);
+        bulk_load(sbase + C_G3A + 16384 + 8192, slot + WS_QG + 8192, 8192, fb);
+        bulk_load(sbase + C_B2, slot + WS_KG, 16384, fb);
+        bulk_load(smem_u32(&sm.gamC_c[sj][0]), slot + WS_GC, 512, fb);
+        return true;
     };
     // waits done by thread 0 and published to the CTA; returns true to abort
     auto lead_wait = [&](bool ok) -> bool {
@@ -769,7 +791,8 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
     if (nchunks > 0) {
         bool ok = true;
         if (tid == 0) {
-            ok = mbar_wait(&sm.full[0], 0, kWait) && mbar_wait(&sm.v_full, 0, kWait);
+            ok = load_chunk(0) && mbar_wait(&sm.full[0], 0, kWait) && mbar_wait(&sm.v_full, 0, kWait);
+            if (ok) mbar_arrive_remote(front_bar(&sm.gfree[0]));
         }
         if (lead_wait(ok)) nchunks = 0;
         if (nchunks > 0) {
@@ -820,7 +843,10 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
         // (b) U -> fp16 operand; S *= Gamma_C; release T', K_hat*Gamma, Q_hat*Gamma, V
         if (tid == 0) {
             mbar_arrive_remote(front_bar(&sm.single_free));
-            if (m + 1 < nchunks) issue_v(m + 1);
+            if (m + 1 < nchunks) {
+                issue_v(m + 1);
+                if (!load_chunk(m + 1)) set_err(p);   // the full wait of step (c) then gives up too
+            }
         }
         if (warp < 8 && quarter < 2) {   // warps 0, 1, 4, 5: lane quarter 0/1, column half
             const int t = quarter * 32 + lane;
@@ -850,6 +876,7 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
             if (m + 1 < nchunks) {
                 ok = mbar_wait(&sm.full[s ^ 1], ((m + 1) >> 1) & 1, kWait);
                 if (ok) {
+                    mbar_arrive_remote(front_bar(&sm.gfree[s ^ 1]));
                     tc_fence_after();
                     issue_g2w();
                 }
@@ -990,6 +1017,10 @@ kda_cluster_kernel(const __grid_constant__ TmaMaps maps, Params p) {
             mbar_init(&sm.pdone[i], 1);
         }
         mbar_init(&sm.single_free, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.gready[i], 1);
+            mbar_init(&sm.gfree[i], 1);
+        }
         mbar_init(&sm.v_full, 1);
         mbar_init(&sm.mma_bar, 1);
         mbar_init(&sm.w_bar, 1);
@@ -1007,9 +1038,9 @@ kda_cluster_kernel(const __grid_constant__ TmaMaps maps, Params p) {
     const uint32_t tmem = sm.tmem_base;
 
     if (rank == 0)
-        run_front(maps, p, smem, sm, tmem, h, row_base, len, nchunks);
+        run_front(maps, p, smem, sm, tmem, unit, h, row_base, len, nchunks);
     else
-        run_chain(maps, p, smem, sm, tmem, n, h, row_base, len, nchunks);
+        run_chain(maps, p, smem, sm, tmem, unit, n, h, row_base, len, nchunks);
 
     tc_fence_before();
     __syncthreads();

@@ -10,6 +10,10 @@ namespace kda {
 
 constexpr int kHeadDim = 128;   // K = V = 128, the only supported head size
 constexpr int kChunk = 64;      // tokens per chunk of the UT/WY form
+// Workspace per (sequence, head): two slots of the chain operands of one chunk
+// (Kbar, Q_hat*Gamma, K_hat*Gamma as fp16 tiles, 16 KB each, and exp(G_C), 512 B).
+constexpr int64_t kWsSlot = 3 * 16384 + 512;
+constexpr int64_t kWsBytesPerUnit = 2 * kWsSlot;
 
 enum StateType : int { kStateNone = 0, kStateBF16 = 1, kStateFP32 = 2 };
 
@@ -28,6 +32,7 @@ struct Params {
     int64_t n_seqs;     // N: sequences (B without cu_seqlens)
     int64_t B, T, H;
     int *err;           // device error word (bounded waits that give up set it)
+    unsigned char *ws;  // workspace: kWsBytesPerUnit bytes per (sequence, head), 16-byte aligned
 };
 
 // Token range of sequence n: packed batch row `b`, first token `t0`, `len` tokens.

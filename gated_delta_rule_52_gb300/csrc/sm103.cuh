@@ -162,6 +162,21 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, uint64_
         : "memory");
 }
 
+// Bulk copy global -> this CTA's shared memory, completing on `bar` (tx bytes);
+// both addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst_cta, const void *src, uint32_t bytes,
+                                          uint32_t bar_cta) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst_cta),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar_cta)
+                 : "memory");
+}
+// Orders this thread's generic-proxy and async-proxy (bulk copy, TMA) accesses to
+// global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Bulk copy shared -> global (both 16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(

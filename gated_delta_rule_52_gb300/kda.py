@@ -36,7 +36,10 @@ KDA_STATE_BF16 = 1
 KDA_STATE_FP32 = 2
 
 # Every symbol include/kda.h declares.
-EXPORTED = ("kda_fwd", "kda_status_string", "kda_get_device_status", "kda_version")
+EXPORTED = ("kda_fwd", "kda_fwd_ws", "kda_status_string", "kda_get_device_status", "kda_version")
+
+# Workspace bytes per (sequence, head) of kda_fwd_ws (KDA_WORKSPACE_BYTES_PER_UNIT).
+WORKSPACE_BYTES_PER_UNIT = 99328
 
 _lock = threading.Lock()
 _lib = None
@@ -61,6 +64,9 @@ def lib() -> ctypes.CDLL:
             L.kda_fwd.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp, f, vp, vp, ci, vp, i64,
                                   i64, i64, i64, i64, i64, vp]
             L.kda_fwd.restype = ci
+            L.kda_fwd_ws.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp, f, vp, vp, ci, vp, i64,
+                                     i64, i64, i64, i64, i64, vp, ctypes.c_size_t, vp]
+            L.kda_fwd_ws.restype = ci
             L.kda_status_string.argtypes = [ci]
             L.kda_status_string.restype = ctypes.c_char_p
             L.kda_get_device_status.argtypes = [vp]
@@ -112,10 +118,17 @@ def state_dtype_code(initial_state, final_state) -> int:
     raise ValueError(f"state dtype must be bf16 or fp32, got {dt}")
 
 
+def workspace_bytes(num_seqs: int, H: int) -> int:
+    """Size of the workspace kda_fwd_ws needs for N sequences of H heads."""
+    return int(num_seqs) * int(H) * WORKSPACE_BYTES_PER_UNIT
+
+
 def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=None,
-            final_state=None, cu_seqlens=None, stream=None) -> None:
+            final_state=None, cu_seqlens=None, stream=None, workspace=None) -> None:
     """KDA forward through libkda.so.  Writes ``out`` [B,T,H,V] (and ``final_state``)
-    in place, asynchronously on ``stream`` (default: the current torch stream)."""
+    in place, asynchronously on ``stream`` (default: the current torch stream).
+    With ``workspace`` (a CUDA uint8 tensor of at least ``workspace_bytes(N, H)``
+    bytes) the call goes to kda_fwd_ws and allocates nothing."""
     if q.dim() != 4:
         raise ValueError("q must be [B, T, H, K]")
     B, T, H, K = q.shape
@@ -139,10 +152,14 @@ def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_s
     for name, s in (("initial_state", initial_state), ("final_state", final_state)):
         if s is not None:
             _check_tensor(name, s, s.dtype, (N, H, V, K))
-    st = lib().kda_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out),
-                       _ptr(A_log), _ptr(dt_bias), float(lower_bound), _ptr(initial_state),
-                       _ptr(final_state), code, _ptr(cu_seqlens), num_seqs, B, T, H, K, V,
-                       _stream_handle(stream))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out), _ptr(A_log),
+            _ptr(dt_bias), float(lower_bound), _ptr(initial_state), _ptr(final_state), code,
+            _ptr(cu_seqlens), num_seqs, B, T, H, K, V)
+    if workspace is None:
+        st = lib().kda_fwd(*args, _stream_handle(stream))
+    else:
+        _check_tensor("workspace", workspace, torch.uint8)
+        st = lib().kda_fwd_ws(*args, _ptr(workspace), workspace.numel(), _stream_handle(stream))
     if st != KDA_OK:
         raise KDAError(st, status_string(st))
 
@@ -157,3 +174,8 @@ def raw_call(*args):
     the validation path use this with host-side fake pointers; nothing is launched
     when validation fails)."""
     return int(lib().kda_fwd(*args))
+
+
+def raw_call_ws(*args):
+    """Direct call of kda_fwd_ws with already-marshalled arguments (validation tests)."""
+    return int(lib().kda_fwd_ws(*args))

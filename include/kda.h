@@ -22,6 +22,7 @@
 #ifndef KDA_H_
 #define KDA_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -40,7 +41,8 @@ typedef enum {
                                 cu_seqlens, num_seqs < 1 with cu_seqlens                */
     KDA_ERR_UNSUPPORTED = 4, /* K != 128 or V != 128 (the only head size supported)    */
     KDA_ERR_ALIGN = 5,       /* a tensor pointer is not 16-byte aligned                 */
-    KDA_ERR_VALUE = 6,       /* lower_bound outside [-5, 0] or non-finite scale         */
+    KDA_ERR_VALUE = 6,       /* lower_bound outside [-5, 0], non-finite scale, or (for
+                                kda_fwd_ws) a workspace smaller than required          */
     KDA_ERR_CUDA = 7,        /* a CUDA runtime call or kernel launch failed             */
     KDA_ERR_TIMEOUT = 8      /* a bounded on-device wait expired (kda_get_device_status) */
 } kda_status;
@@ -81,19 +83,50 @@ typedef enum {
  *   B, T, H, K, V  sizes; K = V = 128 is required
  *   stream         cudaStream_t to enqueue on (NULL = legacy default stream)
  *
- * Ownership: the caller owns every buffer.  The call allocates no device memory
- * and keeps no pointer after it returns.  It is asynchronous: it returns once the
- * work is enqueued, without synchronising.  q/k/v/g/beta/out/A_log/dt_bias/states
- * must be 16-byte aligned.  `out` must not alias an input.
+ * Ownership: the caller owns every buffer and the call keeps no pointer after it
+ * returns.  The only memory the call allocates is its workspace
+ * (KDA_WORKSPACE_BYTES_PER_UNIT bytes per (sequence, head), holding the
+ * per-chunk operands that move between the two CTAs of a cluster through L2),
+ * taken stream-ordered on `stream` from a memory pool that libkda.so creates
+ * once per device and keeps mapped, and released on `stream` after the kernel.
+ * kda_fwd_ws is the same call with a caller-provided workspace.  It is
+ * asynchronous: it returns once the work is enqueued, without synchronising.
+ * q/k/v/g/beta/out/A_log/dt_bias/states must be 16-byte aligned.  `out` must not
+ * alias an input.
  *
  * Returns KDA_OK, or an argument error (nothing enqueued), or KDA_ERR_CUDA if
- * the launch failed.
+ * the workspace allocation or the launch failed.
  */
 kda_status kda_fwd(const void *q, const void *k, const void *v, const void *g, const void *beta,
                    float scale, void *out, const float *A_log, const float *dt_bias,
                    float lower_bound, const void *initial_state, void *final_state,
                    int state_dtype, const int64_t *cu_seqlens, int64_t num_seqs, int64_t B,
                    int64_t T, int64_t H, int64_t K, int64_t V, void *stream);
+
+/* Workspace bytes per (sequence, head): N * H * KDA_WORKSPACE_BYTES_PER_UNIT in
+ * total (N = num_seqs with cu_seqlens, else B). */
+#define KDA_WORKSPACE_BYTES_PER_UNIT 99328
+
+/*
+ * kda_fwd_ws — kda_fwd without any allocation: the caller passes the workspace.
+ * Same arguments and semantics as kda_fwd, plus
+ *   workspace        device buffer of at least N * H * KDA_WORKSPACE_BYTES_PER_UNIT
+ *                    bytes, 16-byte aligned; owned by the caller, read and written
+ *                    by the kernel of this call only (its contents on entry do not
+ *                    matter and are undefined on exit).  It must not be used by
+ *                    another call that can run concurrently (another stream)
+ *                    until this call's work on `stream` has completed.  May be
+ *                    NULL when the call has no work (N * H == 0).
+ *   workspace_bytes  its size in bytes
+ * Additional argument errors: KDA_ERR_NULL (NULL workspace with work to do),
+ * KDA_ERR_VALUE (workspace_bytes too small), KDA_ERR_ALIGN (misaligned workspace).
+ */
+kda_status kda_fwd_ws(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                      float scale, void *out, const float *A_log, const float *dt_bias,
+                      float lower_bound, const void *initial_state, void *final_state,
+                      int state_dtype, const int64_t *cu_seqlens, int64_t num_seqs, int64_t B,
+                      int64_t T, int64_t H, int64_t K, int64_t V, void *workspace,
+                      size_t workspace_bytes, void *stream);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *kda_status_string(int status);

@@ -127,3 +127,35 @@ def test_binding_rejects_cpu_tensors():
     with pytest.raises(ValueError):
         kda.kda_fwd(x, x, x, x, torch.zeros(1, 4, 2, dtype=torch.bfloat16), 0.1, x,
                     torch.zeros(2), torch.zeros(2, 128), -5.0)
+
+
+def call_ws(ws=P[10], ws_bytes=1 << 30, **over):
+    a = dict(q=P[0], k=P[1], v=P[2], g=P[3], beta=P[4], scale=0.088, out=P[5], A_log=P[6],
+             dt_bias=P[7], lb=-5.0, init=None, fin=None, sdt=0, cu=None, nseq=0,
+             B=1, T=64, H=2, K=128, V=128, stream=None)
+    a.update(over)
+    return kda.raw_call_ws(a["q"], a["k"], a["v"], a["g"], a["beta"], ctypes.c_float(a["scale"]),
+                           a["out"], a["A_log"], a["dt_bias"], ctypes.c_float(a["lb"]), a["init"],
+                           a["fin"], a["sdt"], a["cu"], a["nseq"], a["B"], a["T"], a["H"], a["K"],
+                           a["V"], ws, ctypes.c_size_t(ws_bytes), a["stream"])
+
+
+def test_workspace_size_constant_matches_header():
+    src = open(os.path.join(ROOT, "include", "kda.h")).read()
+    m = re.search(r"#define KDA_WORKSPACE_BYTES_PER_UNIT (\d+)", src)
+    assert m and int(m.group(1)) == kda.WORKSPACE_BYTES_PER_UNIT
+    assert kda.workspace_bytes(3, 4) == 12 * kda.WORKSPACE_BYTES_PER_UNIT
+
+
+def test_ws_entry_point_validates_workspace(L):
+    need = 1 * 2 * kda.WORKSPACE_BYTES_PER_UNIT
+    # every case below still fails validation, so nothing is launched on the fake pointers
+    assert call_ws(ws=None, ws_bytes=need) == kda.KDA_ERR_NULL
+    assert call_ws(ws=ctypes.c_void_p(0x10008), ws_bytes=need) == kda.KDA_ERR_ALIGN
+    assert call_ws(ws_bytes=need - 16) == kda.KDA_ERR_VALUE
+    # the ordinary argument checks come first
+    assert call_ws(K=64) == kda.KDA_ERR_UNSUPPORTED
+    assert call_ws(lb=1.0) == kda.KDA_ERR_VALUE
+    # no work: a NULL workspace of size 0 is accepted without touching the device
+    assert call_ws(ws=None, ws_bytes=0, q=None, k=None, v=None, g=None, beta=None, out=None,
+                   B=0) == kda.KDA_OK

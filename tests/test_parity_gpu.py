@@ -185,3 +185,24 @@ def test_many_short_sequences_longest_first_order():
     out, fin = pu.run_gpu(d)
     ref_out, ref_fin = pu.run_oracle(d)
     print("many-seqs", pu.check(d, out, fin, ref_out, ref_fin, label="many-seqs"))
+
+
+def test_caller_workspace_entry_point():
+    # kda_fwd_ws with a caller buffer full of garbage gives kda_fwd's result bit for bit
+    d = W.make_inputs(W.get("varlen_ragged", H=3, seqlens=(65, 1, 130, 63, 200)))
+    e = pu.to_device(d)
+    ref_out, ref_fin = pu.run_gpu(d)
+    out = torch.empty_like(ref_out, device="cuda")
+    fin = torch.empty_like(ref_fin, device="cuda")
+    ws = torch.full((kda.workspace_bytes(d["N"], d["H"]),), 0xFF, dtype=torch.uint8, device="cuda")
+    kda.kda_fwd(e["q"], e["k"], e["v"], e["g"], e["beta"], d["scale"], out, e["A_log"],
+                e["dt_bias"], d["lower_bound"], initial_state=e["initial_state"], final_state=fin,
+                cu_seqlens=e["cu_seqlens"], workspace=ws)
+    torch.cuda.synchronize()
+    assert kda.get_device_status() == kda.KDA_OK
+    assert torch.equal(out.cpu(), ref_out) and torch.equal(fin.cpu(), ref_fin)
+    with pytest.raises(kda.KDAError) as ei:
+        kda.kda_fwd(e["q"], e["k"], e["v"], e["g"], e["beta"], d["scale"], out, e["A_log"],
+                    e["dt_bias"], d["lower_bound"], initial_state=e["initial_state"],
+                    final_state=fin, cu_seqlens=e["cu_seqlens"], workspace=ws[:-16])
+    assert ei.value.status == kda.KDA_ERR_VALUE
