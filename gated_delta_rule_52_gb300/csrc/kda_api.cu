@@ -99,8 +99,9 @@ kda_status launch(kda::Params &p, void *stream) {
     if (cudaGetSymbolAddress(reinterpret_cast<void **>(&err), g_kda_error) != cudaSuccess)
         return KDA_ERR_CUDA;
     p.err = err;
-    return kda::launch_cluster(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KDA_OK
-                                                                                    : KDA_ERR_CUDA;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = p.T <= kda::kDecodeMaxT ? kda::launch_decode(p, cs) : kda::launch_cluster(p, cs);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 }  // namespace
@@ -118,6 +119,7 @@ kda_status kda_fwd(const void *q, const void *k, const void *v, const void *g, c
                              H, K, V, p);
     if (st != KDA_OK) return st;
     if (p.n_seqs == 0 || p.H == 0) return KDA_OK;
+    if (p.T <= kda::kDecodeMaxT) return launch(p, stream);   // the short-step kernel needs no workspace
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess) return KDA_ERR_CUDA;

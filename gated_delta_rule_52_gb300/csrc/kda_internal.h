@@ -49,7 +49,12 @@ __device__ __forceinline__ void seq_range(const Params &p, int64_t n, int64_t &b
     }
 }
 
+// Calls with at most this many token rows (T of the packed batch) run the
+// token-recurrence kernel (decode and short steps) instead of the chunked one.
+constexpr int64_t kDecodeMaxT = 16;
+
 // Launchers (each returns the cudaError_t of its launch).
-cudaError_t launch_cluster(const Params &p, cudaStream_t stream);
+cudaError_t launch_cluster(const Params &p, cudaStream_t stream);   // chunked, needs p.ws
+cudaError_t launch_decode(const Params &p, cudaStream_t stream);    // token recurrence
 
 }  // namespace kda

@@ -80,6 +80,14 @@ WORKLOADS = {
         ragged_total=(117965, 144179),
         description="32 log-uniform lengths in [17,16384] (~131K tokens) H=32; fp32 state; "
                     "zeros/N(0,0.02) alternating initial state; g~N(0,2); beta~N(2,1)"),
+    # Short steps (the token-recurrence kernel): one decode token for 64 sequences with
+    # their fp32 recurrent states, and a 16-token step.
+    "decode": Workload(
+        name="decode", B=64, T=1, H=64, seed=5, state_dtype="fp32", initial_state="normal",
+        description="B=64 T=1 H=64 (one decode token per sequence); fp32 state N(0,0.02)"),
+    "decode_16": Workload(
+        name="decode_16", B=64, T=16, H=64, seed=6, state_dtype="bf16", initial_state="normal",
+        description="B=64 T=16 H=64 (16-token step); bf16 state N(0,0.02)"),
 }
 
 # The throughput workload timed by bench.py.

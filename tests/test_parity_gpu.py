@@ -206,3 +206,48 @@ def test_caller_workspace_entry_point():
                     e["dt_bias"], d["lower_bound"], initial_state=e["initial_state"],
                     final_state=fin, cu_seqlens=e["cu_seqlens"], workspace=ws[:-16])
     assert ei.value.status == kda.KDA_ERR_VALUE
+
+
+# ---- short steps (T <= 16 token rows): the token-recurrence kernel
+
+@pytest.mark.parametrize("T,sd,init", [(1, "fp32", "normal"), (3, "bf16", "normal"),
+                                       (16, "fp32", "none"), (16, "bf16", "normal"), (5, None, "none")])
+def test_short_step_all_elements(T, sd, init):
+    d = W.make_inputs(W.get("decode", B=5, T=T, H=3, state_dtype=sd, initial_state=init))
+    out, fin = pu.run_gpu(d, want_final=sd is not None)
+    ref_out, ref_fin = pu.run_oracle(d, want_final=sd is not None)
+    print("short", T, sd, init, pu.check(d, out, fin, ref_out, ref_fin, label=f"short T={T}"))
+
+
+def test_short_step_varlen_with_empty_sequences():
+    d = W.make_inputs(W.get("varlen_ragged", H=2, seqlens=(1, 0, 5, 10, 0)))
+    assert d["T"] <= 16
+    out, fin = pu.run_gpu(d)
+    ref_out, ref_fin = pu.run_oracle(d)
+    pu.check(d, out, fin, ref_out, ref_fin, label="short varlen")
+    # zero-length sequences pass their state through unchanged
+    for n in (1, 4):
+        torch.testing.assert_close(fin[n], d["initial_state"][n].to(fin.dtype), rtol=0, atol=0)
+
+
+@pytest.mark.parametrize("name", ["decode", "decode_16"])
+def test_short_step_full_size_sampled(name):
+    d = W.make_inputs(W.get(name))
+    out, fin = pu.run_gpu(d)
+    pairs = _sample_pairs(d, 8, seed=7)
+    ref_out, ref_fin = pu.run_oracle(d, pairs=pairs)
+    print(name, pu.check(d, out, fin, ref_out, ref_fin, pairs=pairs, label=name))
+    assert torch.isfinite(out.float()).all() and torch.isfinite(fin.float()).all()
+
+
+def test_short_and_chunked_paths_agree_at_the_threshold():
+    # T = 16 runs the token recurrence, T = 17 the chunked kernel; their first 16
+    # outputs and (chained) states must agree within the parity tolerances.
+    d17 = W.make_inputs(W.get("decode", B=3, T=17, H=2))
+    d16 = dict(d17, T=16, q=d17["q"][:, :16], k=d17["k"][:, :16], v=d17["v"][:, :16],
+               g=d17["g"][:, :16], beta=d17["beta"][:, :16])
+    d16 = {kk: (vv.contiguous() if torch.is_tensor(vv) else vv) for kk, vv in d16.items()}
+    o17, _ = pu.run_gpu(d17)
+    o16, _ = pu.run_gpu(d16)
+    mx, rl = pu.errors(o16.float().numpy(), o17[:, :16].float().numpy())
+    assert mx <= pu.OUT_MAX_ABS and rl <= pu.OUT_REL_L2, (mx, rl)
