@@ -19,9 +19,12 @@
 #include <cuda_bf16.h>
 
 #include "kda_internal.h"
+#include "sm103.cuh"
 
 namespace kda {
 namespace {
+
+using namespace sm103;
 
 constexpr int DK = kHeadDim;
 constexpr int VS = 32;                // state columns per CTA
@@ -30,10 +33,23 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float bf(const __nv_bfloat16 *p, int64_t i) { return __bfloat162float(p[i]); }
 
-__global__ void __launch_bounds__(NTD) kda_decode_kernel(Params p) {
-    __shared__ float alpha[DK], kn[DK], qn[DK];
+// 16-byte asynchronous copy global -> shared (both 16-byte aligned)
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src)
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(NTD, 6) kda_decode_kernel(Params p) {
+    __shared__ __align__(16) float alpha[DK], kn[DK], qn[DK];
     __shared__ float red[2][4][VS];
     __shared__ float nrm[2][4];
+    __shared__ __align__(16) float tile[VS * DK];   // state slice staging (16 KB)
+    // the call's token inputs (at most kDecodeMaxT tokens), copied in once
+    __shared__ __align__(16) __nv_bfloat16 tin[3][kDecodeMaxT][DK];   // q, k, g
+    __shared__ __align__(16) __nv_bfloat16 tv[kDecodeMaxT][VS];       // v, this slice
+    __shared__ float tb[kDecodeMaxT];                                 // beta logits
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t unit = blockIdx.x / (DK / VS);
     const int vs = blockIdx.x % (DK / VS);
@@ -45,47 +61,71 @@ __global__ void __launch_bounds__(NTD) kda_decode_kernel(Params p) {
     const int v = vs * VS + lane;       // this thread's state column
     const int c0 = warp * 32;           // its 32 rows of K
     const size_t state_base = (size_t)(n * p.H + h) * DK * DK;
-    float s[32];
-    if (p.init) {
-        if (p.state_type == kStateBF16) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(
-                reinterpret_cast<const __nv_bfloat16 *>(p.init) + state_base + (size_t)v * DK + c0);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint4 w = src[i];
-                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    s[8 * i + 2 * j] = __uint_as_float(ws[j] << 16);
-                    s[8 * i + 2 * j + 1] = __uint_as_float(ws[j] & 0xFFFF0000u);
-                }
-            }
-        } else {
-            const float4 *src = reinterpret_cast<const float4 *>(
-                reinterpret_cast<const float *>(p.init) + state_base + (size_t)v * DK + c0);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 w = src[i];
-                s[4 * i] = w.x; s[4 * i + 1] = w.y; s[4 * i + 2] = w.z; s[4 * i + 3] = w.w;
-            }
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[i] = 0.f;
+    // Token inputs of the whole call (at most kDecodeMaxT tokens) into shared memory
+    // with 16-byte asynchronous copies, issued before the state load so the two
+    // latencies overlap; the token loop then reads only shared memory.
+    for (int i = tid; i < (int)len * 48; i += NTD) {
+        const int t = i / 48, j = i % 48, x = j >> 4, ch = j & 15;
+        const __nv_bfloat16 *src = (x == 0 ? p.q : (x == 1 ? p.k : p.g)) + ((row_base + t) * p.H + h) * DK + 8 * ch;
+        cp_async16(&tin[x][t][8 * ch], src);
     }
+    for (int i = tid; i < (int)len * 4; i += NTD) {
+        const int t = i >> 2, ch = i & 3;
+        cp_async16(&tv[t][8 * ch], p.v + ((row_base + t) * p.H + h) * DK + vs * VS + 8 * ch);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    if (tid < len) tb[tid] = bf(p.beta, (row_base + tid) * p.H + h);
 
     // gate constants of this head for channel c = tid (log2 units)
     const float a2 = -__expf(p.A_log[h]) * kLog2e;
     const float b2 = a2 * p.dt_bias[h * DK + tid];
     const float lb2 = p.lower_bound * kLog2e;
 
+    // The state slice (32 rows v of 128 fp32, 16 KB contiguous) moves between HBM and
+    // the registers through a shared tile: global accesses are whole 512-byte rows per
+    // warp instruction, and 16-byte chunk q of row v sits at chunk q ^ (v & 7) of the
+    // tile row, so both the row-wise copies and the per-thread 32-value reads are
+    // free of bank conflicts.
+    float s[32];
+    const size_t slice = state_base + (size_t)(vs * VS) * DK;   // first element of the slice
+    auto tile_chunk = [&](int row, int q) -> float4 * {
+        return reinterpret_cast<float4 *>(&tile[row * DK + 4 * (q ^ (row & 7))]);
+    };
+    if (p.init) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const int row = warp * 8 + r;   // this warp's rows, lane = 16-byte chunk
+            float4 x;
+            if (p.state_type == kStateBF16) {
+                const uint2 w = reinterpret_cast<const uint2 *>(
+                    reinterpret_cast<const __nv_bfloat16 *>(p.init) + slice + (size_t)row * DK)[lane];
+                x = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                                __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+            } else {
+                x = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(p.init) + slice +
+                                                     (size_t)row * DK)[lane];
+            }
+            *tile_chunk(row, lane) = x;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 x = *tile_chunk(lane, (c0 >> 2) + j);
+            s[4 * j] = x.x; s[4 * j + 1] = x.y; s[4 * j + 2] = x.z; s[4 * j + 3] = x.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[i] = 0.f;
+    }
+
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
     for (int64_t t = 0; t < len; ++t) {
         const int64_t row = row_base + t;
         const int64_t tok = (row * p.H + h) * DK;
-        // activations of this token, one channel per thread
-        const float qc = bf(p.q, tok + tid), kc = bf(p.k, tok + tid), gc = bf(p.g, tok + tid);
-        const float beta = 1.f / (1.f + exp2f(-bf(p.beta, row * p.H + h) * kLog2e));
-        const float vv = bf(p.v, tok + v);
+        const float qc = __bfloat162float(tin[0][t][tid]), kc = __bfloat162float(tin[1][t][tid]);
+        const float gc = __bfloat162float(tin[2][t][tid]), vv = __bfloat162float(tv[t][lane]);
+        const float beta = 1.f / (1.f + exp2f(-tb[t] * kLog2e));
         float sq = qc * qc, sk = kc * kc;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -105,22 +145,35 @@ __global__ void __launch_bounds__(NTD) kda_decode_kernel(Params p) {
         qn[tid] = qc * rq;
         __syncthreads();
 
-        // decay, then the column sum S^T k_hat over this thread's 32 rows
-        float ks = 0.f;
+        // decay, then the column sum S^T k_hat over this thread's 32 rows (pairs of
+        // rows per instruction, 16-byte shared loads)
+        float2 ks2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            s[i] *= alpha[c0 + i];
-            ks = fmaf(kn[c0 + i], s[i], ks);
+        for (int i = 0; i < 32; i += 4) {
+            const float4 a4 = *reinterpret_cast<const float4 *>(&alpha[c0 + i]);
+            const float4 k4 = *reinterpret_cast<const float4 *>(&kn[c0 + i]);
+            float2 x0 = mul2(make_float2(s[i], s[i + 1]), make_float2(a4.x, a4.y));
+            float2 x1 = mul2(make_float2(s[i + 2], s[i + 3]), make_float2(a4.z, a4.w));
+            ks2 = fma2(make_float2(k4.x, k4.y), x0, ks2);
+            ks2 = fma2(make_float2(k4.z, k4.w), x1, ks2);
+            s[i] = x0.x; s[i + 1] = x0.y; s[i + 2] = x1.x; s[i + 3] = x1.y;
         }
-        red[0][warp][lane] = ks;
+        red[0][warp][lane] = ks2.x + ks2.y;
         __syncthreads();
         const float u = beta * (vv - (red[0][0][lane] + red[0][1][lane] + red[0][2][lane] + red[0][3][lane]));
-        float os = 0.f;
+        const float2 u2 = make_float2(u, u);
+        float2 os2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            s[i] = fmaf(kn[c0 + i], u, s[i]);
-            os = fmaf(qn[c0 + i], s[i], os);
+        for (int i = 0; i < 32; i += 4) {
+            const float4 k4 = *reinterpret_cast<const float4 *>(&kn[c0 + i]);
+            const float4 q4 = *reinterpret_cast<const float4 *>(&qn[c0 + i]);
+            const float2 x0 = fma2(make_float2(k4.x, k4.y), u2, make_float2(s[i], s[i + 1]));
+            const float2 x1 = fma2(make_float2(k4.z, k4.w), u2, make_float2(s[i + 2], s[i + 3]));
+            os2 = fma2(make_float2(q4.x, q4.y), x0, os2);
+            os2 = fma2(make_float2(q4.z, q4.w), x1, os2);
+            s[i] = x0.x; s[i + 1] = x0.y; s[i + 2] = x1.x; s[i + 3] = x1.y;
         }
+        const float os = os2.x + os2.y;
         red[1][warp][lane] = os;
         __syncthreads();
         if (warp == 0)
@@ -129,24 +182,22 @@ __global__ void __launch_bounds__(NTD) kda_decode_kernel(Params p) {
     }
 
     if (p.fin) {
-        if (p.state_type == kStateBF16) {
-            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.fin) + state_base +
-                                                   (size_t)v * DK + c0);
+        __syncthreads();   // the tile may still hold the initial state being read
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                uint32_t w[4];
+        for (int j = 0; j < 8; ++j)
+            *tile_chunk(lane, (c0 >> 2) + j) = make_float4(s[4 * j], s[4 * j + 1], s[4 * j + 2], s[4 * j + 3]);
+        __syncthreads();
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const __nv_bfloat162 pr = __floats2bfloat162_rn(s[8 * i + 2 * j], s[8 * i + 2 * j + 1]);
-                    w[j] = *reinterpret_cast<const uint32_t *>(&pr);
-                }
-                dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int r = 0; r < 8; ++r) {
+            const int row = warp * 8 + r;
+            const float4 x = *tile_chunk(row, lane);
+            if (p.state_type == kStateBF16) {
+                const __nv_bfloat162 a = __floats2bfloat162_rn(x.x, x.y), b = __floats2bfloat162_rn(x.z, x.w);
+                reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.fin) + slice + (size_t)row * DK)[lane] =
+                    make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));
+            } else {
+                reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.fin) + slice + (size_t)row * DK)[lane] = x;
             }
-        } else {
-            float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.fin) + state_base +
-                                                     (size_t)v * DK + c0);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) dst[i] = make_float4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]);
         }
     }
 }
