@@ -41,15 +41,26 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
                  : "memory");
 }
 
+// Dynamic shared memory for a call of T token rows (T <= kDecodeMaxT):
+//   tile   fp32 [32][128]  state slice staging; then the normalised k and q of every
+//                          token ([T][128] each) while the tokens run
+//   tin    bf16 [3][T][128] q, k, g of every token
+//   tv     bf16 [T][32]     v, this slice
+//   alf    fp32 [T][128]    decay factors
+//   tb     fp32 [16]        beta logits, then beta
+__host__ __device__ constexpr int decode_smem_bytes(int T) { return VS * DK * 4 + T * (3 * DK * 2 + VS * 2 + DK * 4) + 16 * 4; }
+
 __global__ void __launch_bounds__(NTD, 6) kda_decode_kernel(Params p) {
-    __shared__ __align__(16) float alpha[DK], kn[DK], qn[DK];
+    extern __shared__ __align__(16) unsigned char dsm[];
     __shared__ float red[2][4][VS];
-    __shared__ float nrm[2][4];
-    __shared__ __align__(16) float tile[VS * DK];   // state slice staging (16 KB)
-    // the call's token inputs (at most kDecodeMaxT tokens), copied in once
-    __shared__ __align__(16) __nv_bfloat16 tin[3][kDecodeMaxT][DK];   // q, k, g
-    __shared__ __align__(16) __nv_bfloat16 tv[kDecodeMaxT][VS];       // v, this slice
-    __shared__ float tb[kDecodeMaxT];                                 // beta logits
+    __shared__ float rnq[kDecodeMaxT], rnk[kDecodeMaxT];
+    const int Tm = (int)p.T;
+    float *tile = reinterpret_cast<float *>(dsm);
+    __nv_bfloat16 *tin = reinterpret_cast<__nv_bfloat16 *>(dsm + VS * DK * 4);   // [3][Tm][DK]
+    __nv_bfloat16 *tv = tin + 3 * Tm * DK;                                       // [Tm][VS]
+    float *alf = reinterpret_cast<float *>(tv + Tm * VS);                        // [Tm][DK]
+    float *tb = alf + Tm * DK;                                                   // [16]
+    float *knt = tile, *qnt = tile + Tm * DK;                                    // [Tm][DK] each
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t unit = blockIdx.x / (DK / VS);
     const int vs = blockIdx.x % (DK / VS);
@@ -67,11 +78,11 @@ __global__ void __launch_bounds__(NTD, 6) kda_decode_kernel(Params p) {
     for (int i = tid; i < (int)len * 48; i += NTD) {
         const int t = i / 48, j = i % 48, x = j >> 4, ch = j & 15;
         const __nv_bfloat16 *src = (x == 0 ? p.q : (x == 1 ? p.k : p.g)) + ((row_base + t) * p.H + h) * DK + 8 * ch;
-        cp_async16(&tin[x][t][8 * ch], src);
+        cp_async16(&tin[(x * Tm + t) * DK + 8 * ch], src);
     }
     for (int i = tid; i < (int)len * 4; i += NTD) {
         const int t = i >> 2, ch = i & 3;
-        cp_async16(&tv[t][8 * ch], p.v + ((row_base + t) * p.H + h) * DK + vs * VS + 8 * ch);
+        cp_async16(&tv[t * VS + 8 * ch], p.v + ((row_base + t) * p.H + h) * DK + vs * VS + 8 * ch);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
     if (tid < len) tb[tid] = bf(p.beta, (row_base + tid) * p.H + h);
@@ -120,60 +131,79 @@ __global__ void __launch_bounds__(NTD, 6) kda_decode_kernel(Params p) {
 
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
-    for (int64_t t = 0; t < len; ++t) {
-        const int64_t row = row_base + t;
-        const int64_t tok = (row * p.H + h) * DK;
-        const float qc = __bfloat162float(tin[0][t][tid]), kc = __bfloat162float(tin[1][t][tid]);
-        const float gc = __bfloat162float(tin[2][t][tid]), vv = __bfloat162float(tv[t][lane]);
-        const float beta = 1.f / (1.f + exp2f(-tb[t] * kLog2e));
-        float sq = qc * qc, sk = kc * kc;
+    // Activations of every token of the call, once: decay factors (thread = channel),
+    // L2 norms (warp = token), then the normalised k and q over the dead state tile.
+    for (int t = 0; t < (int)len; ++t) {
+        const float gc = __bfloat162float(tin[(2 * Tm + t) * DK + tid]);
+        alf[t * DK + tid] = exp2f(lb2 * __fdividef(1.f, 1.f + exp2f(fmaf(gc, a2, b2))));
+    }
+    for (int t = warp; t < (int)len; t += 4) {
+        const uint2 qw = *reinterpret_cast<const uint2 *>(&tin[t * DK + 4 * lane]);
+        const uint2 kw = *reinterpret_cast<const uint2 *>(&tin[(Tm + t) * DK + 4 * lane]);
+        float sq = 0.f, sk = 0.f;
+        const uint32_t qa[2] = {qw.x, qw.y}, ka[2] = {kw.x, kw.y};
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float q0 = __uint_as_float(qa[i] << 16), q1 = __uint_as_float(qa[i] & 0xFFFF0000u);
+            const float k0 = __uint_as_float(ka[i] << 16), k1 = __uint_as_float(ka[i] & 0xFFFF0000u);
+            sq = fmaf(q0, q0, fmaf(q1, q1, sq));
+            sk = fmaf(k0, k0, fmaf(k1, k1, sk));
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             sq += __shfl_xor_sync(0xffffffffu, sq, o);
             sk += __shfl_xor_sync(0xffffffffu, sk, o);
         }
         if (lane == 0) {
-            nrm[0][warp] = sq;
-            nrm[1][warp] = sk;
+            rnq[t] = rsqrtf(sq + 1e-6f);
+            rnk[t] = rsqrtf(sk + 1e-6f);
         }
-        const float gk2 = lb2 * __fdividef(1.f, 1.f + exp2f(fmaf(gc, a2, b2)));
-        alpha[tid] = exp2f(gk2);
-        __syncthreads();
-        const float rq = rsqrtf(nrm[0][0] + nrm[0][1] + nrm[0][2] + nrm[0][3] + 1e-6f);
-        const float rk = rsqrtf(nrm[1][0] + nrm[1][1] + nrm[1][2] + nrm[1][3] + 1e-6f);
-        kn[tid] = kc * rk;
-        qn[tid] = qc * rq;
-        __syncthreads();
+    }
+    __syncthreads();   // norms ready; every thread is done with the initial-state tile
+    for (int t = 0; t < (int)len; ++t) {
+        knt[t * DK + tid] = __bfloat162float(tin[(Tm + t) * DK + tid]) * rnk[t];
+        qnt[t * DK + tid] = __bfloat162float(tin[t * DK + tid]) * rnq[t];
+    }
+    if (tid < len) tb[tid] = 1.f / (1.f + exp2f(-tb[tid] * kLog2e));
+    __syncthreads();
+
+    for (int64_t t = 0; t < len; ++t) {
+        const int64_t row = row_base + t;
+        const int64_t tok = (row * p.H + h) * DK;
+        const float *alpha = alf + t * DK, *kn = knt + t * DK, *qn = qnt + t * DK;
+        const float vv = __bfloat162float(tv[t * VS + lane]), beta = tb[t];
 
         // decay, then the column sum S^T k_hat over this thread's 32 rows (pairs of
         // rows per instruction, 16-byte shared loads)
-        float2 ks2 = make_float2(0.f, 0.f);
+        float2 ks2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};   // two chains
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
             const float4 a4 = *reinterpret_cast<const float4 *>(&alpha[c0 + i]);
             const float4 k4 = *reinterpret_cast<const float4 *>(&kn[c0 + i]);
             float2 x0 = mul2(make_float2(s[i], s[i + 1]), make_float2(a4.x, a4.y));
             float2 x1 = mul2(make_float2(s[i + 2], s[i + 3]), make_float2(a4.z, a4.w));
-            ks2 = fma2(make_float2(k4.x, k4.y), x0, ks2);
-            ks2 = fma2(make_float2(k4.z, k4.w), x1, ks2);
+            ks2[0] = fma2(make_float2(k4.x, k4.y), x0, ks2[0]);
+            ks2[1] = fma2(make_float2(k4.z, k4.w), x1, ks2[1]);
             s[i] = x0.x; s[i + 1] = x0.y; s[i + 2] = x1.x; s[i + 3] = x1.y;
         }
-        red[0][warp][lane] = ks2.x + ks2.y;
+        const float2 ksum = add2(ks2[0], ks2[1]);
+        red[0][warp][lane] = ksum.x + ksum.y;
         __syncthreads();
         const float u = beta * (vv - (red[0][0][lane] + red[0][1][lane] + red[0][2][lane] + red[0][3][lane]));
         const float2 u2 = make_float2(u, u);
-        float2 os2 = make_float2(0.f, 0.f);
+        float2 os2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
             const float4 k4 = *reinterpret_cast<const float4 *>(&kn[c0 + i]);
             const float4 q4 = *reinterpret_cast<const float4 *>(&qn[c0 + i]);
             const float2 x0 = fma2(make_float2(k4.x, k4.y), u2, make_float2(s[i], s[i + 1]));
             const float2 x1 = fma2(make_float2(k4.z, k4.w), u2, make_float2(s[i + 2], s[i + 3]));
-            os2 = fma2(make_float2(q4.x, q4.y), x0, os2);
-            os2 = fma2(make_float2(q4.z, q4.w), x1, os2);
+            os2[0] = fma2(make_float2(q4.x, q4.y), x0, os2[0]);
+            os2[1] = fma2(make_float2(q4.z, q4.w), x1, os2[1]);
             s[i] = x0.x; s[i + 1] = x0.y; s[i + 2] = x1.x; s[i + 3] = x1.y;
         }
-        const float os = os2.x + os2.y;
+        const float2 osum = add2(os2[0], os2[1]);
+        const float os = osum.x + osum.y;
         red[1][warp][lane] = os;
         __syncthreads();
         if (warp == 0)
@@ -207,7 +237,7 @@ __global__ void __launch_bounds__(NTD, 6) kda_decode_kernel(Params p) {
 cudaError_t launch_decode(const Params &p, cudaStream_t stream) {
     const int64_t units = p.n_seqs * p.H;
     if (units == 0) return cudaSuccess;
-    kda_decode_kernel<<<(unsigned)(units * (DK / VS)), NTD, 0, stream>>>(p);
+    kda_decode_kernel<<<(unsigned)(units * (DK / VS)), NTD, decode_smem_bytes((int)p.T), stream>>>(p);
     return cudaGetLastError();
 }
 
