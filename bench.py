@@ -45,7 +45,14 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # FLOPs of the chunked form with C=64, K=V=128 (A, M, W, U~, M U dense; W S, Q S, K^T U).
 BYTES_PER_TOKEN_HEAD = 5 * 128 * 2 + 2
 FLOPS_PER_TOKEN_HEAD = 2 * 64 * (3 * 128 + 2 * 128) + 2 * 3 * 128 * 128
-KERNEL_SOURCES = ("gated_delta_rule_52_gb300/csrc",)
+# Source files each kernel is built from (a stored ncu traffic figure is valid only
+# while these are unchanged).
+KERNEL_SOURCES = {
+    "cluster": ("kda_cluster.cu", "sm103.cuh", "kda_internal.h"),
+    "decode": ("kda_decode.cu", "sm103.cuh", "kda_internal.h"),
+}
+CSRC = os.path.join("gated_delta_rule_52_gb300", "csrc")
+DECODE_MAX_T = 16   # calls with at most this many token rows run the decode kernel
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -92,15 +99,17 @@ def algorithmic_flops(d) -> int:
     return d["B"] * d["T"] * d["H"] * FLOPS_PER_TOKEN_HEAD
 
 
-def kernel_source_hash() -> str:
+def kernel_of(w) -> str:
+    """The kernel libkda runs for a workload (decided by its packed token count)."""
+    return "decode" if w.T <= DECODE_MAX_T else "cluster"
+
+
+def kernel_source_hash(kernel: str = "cluster") -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
-        base = os.path.join(ROOT, rel)
-        for name in sorted(os.listdir(base)):
-            if name.endswith((".cu", ".cuh", ".h")):
-                with open(os.path.join(base, name), "rb") as f:
-                    h.update(name.encode())
-                    h.update(f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, CSRC, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -114,14 +123,14 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def stored_traffic(workload: str):
+def stored_traffic(workload: str, kernel: str = "cluster"):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current kernel sources (else None)."""
+    current sources of the kernel (else None)."""
     try:
         with open(TRAFFIC_FILE) as f:
             j = json.load(f)
         e = j.get(workload)
-        if e and e.get("source_hash") == kernel_source_hash():
+        if e and e.get("source_hash") == kernel_source_hash(kernel):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -379,10 +388,10 @@ def run_ours(args):
     abytes = algorithmic_bytes(d_cpu)
     achieved = abytes / (avg_launch_ms / 1e3) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-            "frac": achieved / hbm, "traffic": stored_traffic(w.name),
+            "frac": achieved / hbm, "traffic": stored_traffic(w.name, kernel_of(w)),
             "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
             else f"{src} {hbm} GB/s",
-            "kernel": "kda_cluster_kernel (kda_fwd: one launch per step)",
+            "kernel": ("kda_decode_kernel" if kernel_of(w) == "decode" else "kda_cluster_kernel") + " (kda_fwd: one launch per step)",
             "algorithmic_bytes_per_launch": abytes,
             "algorithmic_flops_per_launch": algorithmic_flops(d_cpu),
             "tensor_frac": algorithmic_flops(d_cpu) / (avg_launch_ms / 1e3) / (tflops * 1e12)}
