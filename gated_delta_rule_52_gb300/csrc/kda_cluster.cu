@@ -17,24 +17,27 @@
 //     warps 13-15 beside the gate: row norms of q and k, beta;
 //     warps 8-11 solver of chunk m-1: A and M out of TMEM, the blocked
 //                inverse, T' (fp16);
-//     warp 12    control: issues G1 into a double-buffered TMEM slot, ships
-//                the prologue's tiles, prefetches the next raw tiles, so the
-//                prologue never waits on the chain;
-//     both groups ship their tiles into the chain CTA's shared memory with bulk
+//     warp 12    control: issues G1 into a double-buffered TMEM slot, writes the
+//                prologue's chain tiles (Kbar, Q_hat*Gamma, K_hat*Gamma,
+//                exp(G_C)) to a workspace slot in global memory (L2) with bulk
+//                stores and signals the chain, and reloads the raw tile slot two
+//                chunks ahead once the stores have read it;
+//     the solver ships T' and M into the chain CTA's shared memory with bulk
 //     shared->shared copies that complete as transaction bytes on the chain's
 //     per-slot mbarrier.
 //   CTA rank 1 ("chain") owns the whole state (V = 128) in tensor memory:
 //     G2u = [T'; 0] x V and G3 = [-W; Q_hat*Gamma] x S  -> U | Q Gamma S
-//     U readout, S decay
+//     U readout, S decay; bulk loads of the next chunk's workspace tiles
 //     G4 = Kbar^T U -> S,  G5 = [0; M] x U -> O
 //     O and S readout; W for the next chunk (G2w = [T'; 0] x K_hat*Gamma) is
 //     computed and read out beside this, off the sequential path (16 warps:
 //     S by warps 0-7, -W by 8/9/12/13, O by 10/11/14/15, one column half each).
-// Flow control: the chain arrives remotely on the front's "slot free" barriers
-// (per-slot tiles K_bar, M, Gamma_C) and "single free" barrier (single-buffered
-// tiles T', K_hat*Gamma, Q_hat*Gamma); the front waits on them before shipping.
+// Flow control: the chain arrives remotely on the front's "slot free" (M),
+// "single free" (T') and "workspace free" barriers, the front on the chain's
+// "workspace ready" barrier; each side waits before writing into the other's
+// buffers.
 //
-// Precision and exponent handling are those of the single-CTA path: G1 on bf16
+// Precision and exponent handling: G1 on bf16
 // operands of the raw q/k scaled by 16-token-block-local decay factors, the
 // other GEMMs on fp16 operands, fp32 accumulators, fp32 state.  Every wait is
 // bounded (2 s); a timeout sets the device error word and both CTAs unwind.
