@@ -22,9 +22,9 @@
 //                exp(G_C)) to a workspace slot in global memory (L2) with bulk
 //                stores and signals the chain, and reloads the raw tile slot two
 //                chunks ahead once the stores have read it;
-//     the solver ships T' and M into the chain CTA's shared memory with bulk
-//     shared->shared copies that complete as transaction bytes on the chain's
-//     per-slot mbarrier.
+//     the solver ships T' and M into a double-buffered slot of the chain CTA's
+//     shared memory with bulk shared->shared copies that complete as
+//     transaction bytes on the chain's per-slot mbarrier.
 //   CTA rank 1 ("chain") owns the whole state (V = 128) in tensor memory:
 //     G2u = [T'; 0] x V and G3 = [-W; Q_hat*Gamma] x S  -> U | Q Gamma S
 //     U readout, S decay; bulk loads of the next chunk's workspace tiles
@@ -32,8 +32,8 @@
 //     O and S readout; W for the next chunk (G2w = [T'; 0] x K_hat*Gamma) is
 //     computed and read out beside this, off the sequential path (16 warps:
 //     S by warps 0-7, -W by 8/9/12/13, O by 10/11/14/15, one column half each).
-// Flow control: the chain arrives remotely on the front's "slot free" (M),
-// "single free" (T') and "workspace free" barriers, the front on the chain's
+// Flow control: the chain arrives remotely on the front's "slot free" (T' and M
+// of a slot) and "workspace free" barriers, the front on the chain's
 // "workspace ready" barrier; each side waits before writing into the other's
 // buffers.
 //
@@ -85,9 +85,10 @@ constexpr uint32_t F_TF = 197632;      // T fp32 [64][68]
 constexpr uint32_t C_B2 = 0;           // K_hat*Gamma 2 x [64 i][64 c] | V 2 x [64 t][64 v] (MN-major)
 constexpr uint32_t C_G3A = 32768;      // [-W; Q_hat*Gamma]: 2 x [128][64] (K-major)
 constexpr uint32_t C_KB = 65536;       // 2 slots x Kbar 2 x [64 i][64 c] (MN-major)
-constexpr uint32_t C_TZM = 98304;      // T' | Z | M0 | Z | M1, each [64][64] (K-major)
+constexpr uint32_t C_TZM = 98304;      // T'0 | Z | M0 | Z | M1, each [64][64] (K-major)
 constexpr uint32_t C_SB = 139264;      // S fp16 2 x [128 c][64 v] (MN-major)
 constexpr uint32_t C_UT = 172032;      // U fp16 2 x [64 i][64 v] (MN-major)
+constexpr uint32_t C_T1 = 188416;      // T'1 | Z, each [64][64] (K-major)
 constexpr uint32_t SMALL = 218112;     // common offset in both CTAs (remote addresses)
 
 struct Small {
@@ -96,7 +97,7 @@ struct Small {
     float fac[kFacRows][DK];                 // front: decay factors, see fac_base
     float gamC_f[2][DK];                     // front: exp(G_C) per slot (copy source)
     float gamC_c[2][DK];                     // chain: copy destination
-    uint64_t raw_full[2], g1_done[2], am_free[2], s_done[2], slot_free[2], single_free, pdone[2];
+    uint64_t raw_full[2], g1_done[2], am_free[2], s_done[2], slot_free[2], pdone[2];
     uint64_t full[2], v_full, mma_bar, w_bar;
     uint64_t gready[2], gfree[2];   // workspace slot written (chain side) / loaded (front side)
     uint32_t tmem_base;
@@ -109,18 +110,21 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 __device__ __forceinline__ int variant_off(int bt) { return 8 * bt * (bt + 1); }
 
 // mma.sync operand fragments (g = lane / 4, q = lane % 4) of a row-major fp32
-// tile in shared memory, rounded to tf32: A (16 x 8) at a, B (8 x 8) at b.
+// tile in shared memory: A (16 x 8) at a, B (8 x 8) at b.  The fp32 bit patterns
+// go to the tf32 MMA as they are (it uses the leading 19 bits, i.e. truncates);
+// an explicit round-to-nearest conversion cost 3.5% of the prefill time and moved
+// the parity figures by at most a few percent of their size.
 __device__ __forceinline__ void frag_a(const float *a, int lda, int lane, uint32_t (&f)[4]) {
     const int g = lane >> 2, q = lane & 3;
-    f[0] = to_tf32(a[g * lda + q]);
-    f[1] = to_tf32(a[(g + 8) * lda + q]);
-    f[2] = to_tf32(a[g * lda + q + 4]);
-    f[3] = to_tf32(a[(g + 8) * lda + q + 4]);
+    f[0] = __float_as_uint(a[g * lda + q]);
+    f[1] = __float_as_uint(a[(g + 8) * lda + q]);
+    f[2] = __float_as_uint(a[g * lda + q + 4]);
+    f[3] = __float_as_uint(a[(g + 8) * lda + q + 4]);
 }
 __device__ __forceinline__ void frag_b(const float *b, int ldb, int lane, uint32_t (&f)[2]) {
     const int g = lane >> 2, q = lane & 3;
-    f[0] = to_tf32(b[q * ldb + g]);
-    f[1] = to_tf32(b[(q + 4) * ldb + g]);
+    f[0] = __float_as_uint(b[q * ldb + g]);
+    f[1] = __float_as_uint(b[(q + 4) * ldb + g]);
 }
 
 // Stores a 16 x 8 accumulator tile (times `sign`) at d (row stride ldd).
@@ -468,6 +472,9 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
         float *Tf = reinterpret_cast<float *>(smem + F_TF);
         // the M staging tile above the diagonal blocks stays zero for the whole run
         for (int k16 = stid; k16 < 512; k16 += NS) sts128(sbase + F_MST + k16 * 16, 0u, 0u, 0u, 0u);
+        // T above its diagonal blocks is never written: zero once, so T' needs no mask
+        for (int k4 = stid; k4 < 64 * LDA / 4; k4 += NS)
+            reinterpret_cast<float4 *>(Tf)[k4] = make_float4(0.f, 0.f, 0.f, 0.f);
         named_bar(2, NS);
         for (int m = 0; m < nchunks; ++m) {
             const int s = m & 1;
@@ -504,10 +511,12 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
 #pragma unroll
                     for (int e4 = 0; e4 < 4; ++e4) {
                         const float4 x = rk4[e4];
-                        r[kk][4 * e4] *= rowf * x.x;
-                        r[kk][4 * e4 + 1] *= rowf * x.y;
-                        r[kk][4 * e4 + 2] *= rowf * x.z;
-                        r[kk][4 * e4 + 3] *= rowf * x.w;
+                        const float2 f0 = mul2(make_float2(rowf, rowf), make_float2(x.x, x.y));
+                        const float2 f1 = mul2(make_float2(rowf, rowf), make_float2(x.z, x.w));
+                        const float2 y0 = mul2(f0, make_float2(r[kk][4 * e4], r[kk][4 * e4 + 1]));
+                        const float2 y1 = mul2(f1, make_float2(r[kk][4 * e4 + 2], r[kk][4 * e4 + 3]));
+                        r[kk][4 * e4] = y0.x; r[kk][4 * e4 + 1] = y0.y;
+                        r[kk][4 * e4 + 2] = y1.x; r[kk][4 * e4 + 3] = y1.y;
                     }
                     if (is_m) {
                         if (kk == sw) {
@@ -629,11 +638,10 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
 #pragma unroll
                     for (int e4 = 0; e4 < 4; ++e4) {
                         const float4 tv = t4[4 * hh + e4], bv = b4[4 * hh + e4];
-                        const int i = i0 + 16 * hh + 4 * e4;
-                        r[4 * e4] = i <= t ? tv.x * bv.x : 0.f;
-                        r[4 * e4 + 1] = i + 1 <= t ? tv.y * bv.y : 0.f;
-                        r[4 * e4 + 2] = i + 2 <= t ? tv.z * bv.z : 0.f;
-                        r[4 * e4 + 3] = i + 3 <= t ? tv.w * bv.w : 0.f;
+                        r[4 * e4] = tv.x * bv.x;
+                        r[4 * e4 + 1] = tv.y * bv.y;
+                        r[4 * e4 + 2] = tv.z * bv.z;
+                        r[4 * e4 + 3] = tv.w * bv.w;
                     }
                     st_pack16<true>(sbase + F_AMAT, t, i0 + 16 * hh, r);
                 }
@@ -645,9 +653,10 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                 bool ok = true;
                 const uint32_t full = chain_bar(&sm.full[s]);
                 if (m >= 2) ok = mbar_wait_cluster(&sm.slot_free[s], ((m - 2) >> 1) & 1, kWait);
-                if (ok) bulk_copy_to_peer(chain_addr(C_TZM + 16384 + s * 16384), sbase + F_MST, 8192, full);
-                if (ok && m >= 1) ok = mbar_wait_cluster(&sm.single_free, (m - 1) & 1, kWait);
-                if (ok) bulk_copy_to_peer(chain_addr(C_TZM), sbase + F_AMAT, 8192, full);
+                if (ok) {
+                    bulk_copy_to_peer(chain_addr(s ? C_T1 : C_TZM), sbase + F_AMAT, 8192, full);
+                    bulk_copy_to_peer(chain_addr(C_TZM + 16384 + s * 16384), sbase + F_MST, 8192, full);
+                }
                 bulk_commit();
                 if (!ok) { set_err(p); sm.abort_s = 1; sm.abort_p = 1; }
             }
@@ -744,10 +753,10 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
         }
         tmem_st_wait();
     };
-    auto issue_g2w = [&]() {
+    auto issue_g2w = [&](int j) {   // W of chunk j (its T' slot)
         const uint32_t id = idesc_fp16(128, 128, false, true);
         for (int ks = 0; ks < C / 16; ++ks)
-            mma_bf16(D_W, sdesc_sw128(sbase + C_TZM + ks * 32, 16, 1024),
+            mma_bf16(D_W, sdesc_sw128(sbase + ((j & 1) ? C_T1 : C_TZM) + ks * 32, 16, 1024),
                      sdesc_sw128(sbase + C_B2 + ks * 2048, 8192, 1024), id, ks > 0);
         mma_commit(&sm.w_bar);
     };
@@ -756,6 +765,7 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
     for (int k16 = tid; k16 < 512; k16 += NT) {
         sts128(sbase + C_TZM + 8192 + k16 * 16, 0, 0, 0, 0);
         sts128(sbase + C_TZM + 24576 + k16 * 16, 0, 0, 0, 0);
+        sts128(sbase + C_T1 + 8192 + k16 * 16, 0, 0, 0, 0);
     }
     // initial state -> D_S (fp32) and S fp16 operand copy; warps 0-7
     if (warp < 8) {
@@ -807,7 +817,7 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
             __syncthreads();
             if (tid == 0) {
                 tc_fence_after();
-                issue_g2w();
+                issue_g2w(0);
                 ok = mbar_wait(&sm.w_bar, 0, kWait);
             }
             if (lead_wait(ok)) nchunks = 0;
@@ -831,7 +841,7 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
             tc_fence_after();
             const uint32_t idv = idesc_fp16(128, 128, false, true);
             for (int ks = 0; ks < C / 16; ++ks)
-                mma_bf16(D_U, sdesc_sw128(sbase + C_TZM + ks * 32, 16, 1024),
+                mma_bf16(D_U, sdesc_sw128(sbase + (s ? C_T1 : C_TZM) + ks * 32, 16, 1024),
                          sdesc_sw128(sbase + C_B2 + 16384 + ks * 2048, 8192, 1024), idv, ks > 0);
             for (int ks = 0; ks < DK / 16; ++ks)
                 mma_bf16(D_U, sdesc_sw128(sbase + C_G3A + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
@@ -845,7 +855,6 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
 
         // (b) U -> fp16 operand; S *= Gamma_C; release T', K_hat*Gamma, Q_hat*Gamma, V
         if (tid == 0) {
-            mbar_arrive_remote(front_bar(&sm.single_free));
             if (m + 1 < nchunks) {
                 issue_v(m + 1);
                 if (!load_chunk(m + 1)) set_err(p);   // the full wait of step (c) then gives up too
@@ -881,7 +890,7 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
                 if (ok) {
                     mbar_arrive_remote(front_bar(&sm.gfree[s ^ 1]));
                     tc_fence_after();
-                    issue_g2w();
+                    issue_g2w(m + 1);
                 }
             }
             ok = ok && mbar_wait(&sm.mma_bar, ph_mma, kWait);
@@ -1019,7 +1028,6 @@ kda_cluster_kernel(const __grid_constant__ TmaMaps maps, Params p) {
             mbar_init(&sm.full[i], 1);
             mbar_init(&sm.pdone[i], 1);
         }
-        mbar_init(&sm.single_free, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.gready[i], 1);
             mbar_init(&sm.gfree[i], 1);

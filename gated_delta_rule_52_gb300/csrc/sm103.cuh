@@ -323,13 +323,6 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
     return r;
 }
 
-// fp32 -> tf32 (round to nearest, ties away), as the 32-bit register mma.sync reads.
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-
 // D += A * B on a 16x8x8 tile with tf32 inputs and fp32 accumulation (warp-wide).
 // Fragments (g = lane / 4, q = lane % 4): a = A[g][q], A[g+8][q], A[g][q+4],
 // A[g+8][q+4]; b = B[q][g], B[q+4][g]; d = D[g][2q], D[g][2q+1], D[g+8][2q],

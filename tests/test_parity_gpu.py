@@ -251,3 +251,39 @@ def test_short_and_chunked_paths_agree_at_the_threshold():
     o16, _ = pu.run_gpu(d16)
     mx, rl = pu.errors(o16.float().numpy(), o17[:, :16].float().numpy())
     assert mx <= pu.OUT_MAX_ABS and rl <= pu.OUT_REL_L2, (mx, rl)
+
+
+# ---- seeded random configurations: shapes, lengths (empty, short, chunk-crossing),
+# state types, gate lower bounds and input spreads drawn per case; both kernels
+
+def _random_case(i):
+    r = np.random.default_rng(9000 + i)
+    H = int(r.integers(1, 6))
+    sd = [None, "fp32", "bf16"][int(r.integers(3))]
+    init = ["none", "normal", "alternate"][int(r.integers(3))]
+    common = dict(H=H, seed=9000 + i, state_dtype=sd, initial_state=init,
+                  lower_bound=float(r.uniform(-5.0, 0.0)),
+                  g_std=float(r.choice([0.5, 1.0, 2.0, 3.0])),
+                  beta_mean=float(r.choice([-2.0, 0.0, 2.0])),
+                  state_std=float(r.choice([0.02, 0.3])))
+    short = i % 3 == 0
+    if i % 2 == 0:
+        T = int(r.integers(1, 17)) if short else int(r.integers(17, 400))
+        return W.Workload(name=f"rand{i}", B=int(r.integers(1, 4)), T=T, **common)
+    n = int(r.integers(1, 7))
+    if short:
+        lens = [int(x) for x in r.integers(0, 4, size=n)]
+    else:
+        lens = [int(r.choice([0, int(r.integers(1, 17)), int(r.integers(17, 300))])) for _ in range(n)]
+    return W.Workload(name=f"rand{i}", B=1, T=0, varlen="ragged", n_seqs=n,
+                      seqlens=tuple(lens), **common)
+
+
+@pytest.mark.parametrize("i", range(18))
+def test_random_configurations(i):
+    w = _random_case(i)
+    d = W.make_inputs(w)
+    want = w.state_dtype is not None
+    out, fin = pu.run_gpu(d, want_final=want)
+    ref_out, ref_fin = pu.run_oracle(d, want_final=want)
+    print(w, pu.check(d, out, fin, ref_out, ref_fin, label=w.name))
