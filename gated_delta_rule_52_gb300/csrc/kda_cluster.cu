@@ -311,7 +311,7 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                 const float2 FC[4] = {make_float2(fca.x, fca.y), make_float2(fca.z, fca.w), make_float2(fcb.x, fcb.y),
                                       make_float2(fcb.z, fcb.w)};
                 const uint32_t ama = sbase + F_AMA + kh * 16384, amb = sbase + F_AMB + kh * 20480;
-#pragma unroll 1
+#pragma unroll 2
                 for (int j = 0; j < 4; ++j) {
                     const int r = 4 * qr + j, t = 16 * blk + r;
                     const uint32_t off = kho + sw128_off(t, 8 * cg);
@@ -638,10 +638,9 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
 #pragma unroll
                     for (int e4 = 0; e4 < 4; ++e4) {
                         const float4 tv = t4[4 * hh + e4], bv = b4[4 * hh + e4];
-                        r[4 * e4] = tv.x * bv.x;
-                        r[4 * e4 + 1] = tv.y * bv.y;
-                        r[4 * e4 + 2] = tv.z * bv.z;
-                        r[4 * e4 + 3] = tv.w * bv.w;
+                        const float2 y0 = mul2(make_float2(tv.x, tv.y), make_float2(bv.x, bv.y));
+                        const float2 y1 = mul2(make_float2(tv.z, tv.w), make_float2(bv.z, bv.w));
+                        r[4 * e4] = y0.x; r[4 * e4 + 1] = y0.y; r[4 * e4 + 2] = y1.x; r[4 * e4 + 3] = y1.y;
                     }
                     st_pack16<true>(sbase + F_AMAT, t, i0 + 16 * hh, r);
                 }
