@@ -50,9 +50,11 @@ FLOPS_PER_TOKEN_HEAD = 2 * 64 * (3 * 128 + 2 * 128) + 2 * 3 * 128 * 128
 KERNEL_SOURCES = {
     "cluster": ("kda_cluster.cu", "sm103.cuh", "kda_internal.h"),
     "decode": ("kda_decode.cu", "sm103.cuh", "kda_internal.h"),
+    "short": ("kda_short.cu", "sm103.cuh", "kda_internal.h"),
 }
+KERNEL_NAMES = {"cluster": "kda_cluster_kernel", "decode": "kda_decode_kernel", "short": "kda_short_kernel"}
 CSRC = os.path.join("gated_delta_rule_52_gb300", "csrc")
-DECODE_MAX_T = 16   # calls with at most this many token rows run the decode kernel
+DECODE_MAX_T = 16   # calls with at most this many token rows run a single-chunk kernel
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -99,9 +101,9 @@ def algorithmic_flops(d) -> int:
     return d["B"] * d["T"] * d["H"] * FLOPS_PER_TOKEN_HEAD
 
 
-def kernel_of(w) -> str:
-    """The kernel libkda runs for a workload (decided by its packed token count)."""
-    return "decode" if w.T <= DECODE_MAX_T else "cluster"
+def kernel_of(T: int) -> str:
+    """The kernel libkda runs for a call of T packed token rows."""
+    return "decode" if T == 1 else ("short" if T <= DECODE_MAX_T else "cluster")
 
 
 def kernel_source_hash(kernel: str = "cluster") -> str:
@@ -420,10 +422,10 @@ def run_ours(args):
     abytes = algorithmic_bytes(d_cpu)
     achieved = abytes / (avg_launch_ms / 1e3) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-            "frac": achieved / hbm, "traffic": stored_traffic(w.name, kernel_of(w)),
+            "frac": achieved / hbm, "traffic": stored_traffic(w.name, kernel_of(d_cpu["T"])),
             "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
             else f"{src} {hbm} GB/s",
-            "kernel": ("kda_decode_kernel" if kernel_of(w) == "decode" else "kda_cluster_kernel") + " (kda_fwd: one launch per step)",
+            "kernel": KERNEL_NAMES[kernel_of(d_cpu["T"])] + " (kda_fwd: one launch per step)",
             "algorithmic_bytes_per_launch": abytes,
             "algorithmic_flops_per_launch": algorithmic_flops(d_cpu),
             "tensor_frac": algorithmic_flops(d_cpu) / (avg_launch_ms / 1e3) / (tflops * 1e12)}

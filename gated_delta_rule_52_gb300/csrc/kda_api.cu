@@ -100,7 +100,9 @@ kda_status launch(kda::Params &p, void *stream) {
         return KDA_ERR_CUDA;
     p.err = err;
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = p.T <= kda::kDecodeMaxT ? kda::launch_decode(p, cs) : kda::launch_cluster(p, cs);
+    const cudaError_t e = p.T == 1 ? kda::launch_decode(p, cs)
+                          : p.T <= kda::kDecodeMaxT ? kda::launch_short(p, cs)
+                                                    : kda::launch_cluster(p, cs);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

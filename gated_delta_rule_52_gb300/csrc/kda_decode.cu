@@ -1,6 +1,6 @@
-// KDA forward for calls with few tokens per sequence (decode and short
-// multi-token steps): the token recurrence applied directly, one token at a
-// time, with the state held in registers.
+// KDA forward for decode (kda_fwd runs it for calls of one token row; it handles
+// up to 16): the token recurrence applied directly, one token at a time, with
+// the state held in registers.
 //
 // Per (sequence, head), with S the K x V state (FlashKDA README "Kernel API"
 // semantics; the same activations as the chunked kernel):
@@ -10,11 +10,14 @@
 // each state column needs only its own dot products.
 //
 // Work split: one CTA per (sequence, head, 32-column slice of V); 128 threads,
-// thread = (state column v of the slice, 32-row group of K), so each thread keeps
-// 32 fp32 state values in registers.  Per token the CTA computes the normalised
-// q, k and the decay factors once (one channel per thread) into shared memory,
-// then every thread updates its 32 values; the two column sums over K (S^T k and
-// S^T q) combine the four row groups through shared memory.  The state crosses
+// thread = (quad of state columns, 8-row group of K), so each thread keeps 4 x 8
+// fp32 state values in registers and reads only its own 8 rows of the per-token
+// vectors (the decay factors, k_hat and q_hat, computed once per token into shared
+// memory, one channel per thread).  The column sums over K (S^T k and S^T q)
+// combine the 16 row groups by two shuffles inside each warp and through shared
+// memory across the four warps.  (The first version gave each thread one column
+// and 32 rows: every lane then read the same 32 rows of all three vectors per
+// token, and the shared-memory load path was the bound.)  The state crosses
 // HBM once in and once out per call, which bounds the kernel for short steps.
 #include <cuda_bf16.h>
 
@@ -52,7 +55,7 @@ __host__ __device__ constexpr int decode_smem_bytes(int T) { return VS * DK * 4 
 
 __global__ void __launch_bounds__(NTD, 6) kda_decode_kernel(Params p) {
     extern __shared__ __align__(16) unsigned char dsm[];
-    __shared__ float red[2][4][VS];
+    __shared__ __align__(16) float red[2][4][VS];   // per-warp column sums: [0] S^T k, [1] S^T q
     __shared__ float rnq[kDecodeMaxT], rnk[kDecodeMaxT];
     const int Tm = (int)p.T;
     float *tile = reinterpret_cast<float *>(dsm);
@@ -69,8 +72,8 @@ __global__ void __launch_bounds__(NTD, 6) kda_decode_kernel(Params p) {
     seq_range(p, n, b, t0, len);
     const int64_t row_base = b * p.T + t0;
 
-    const int v = vs * VS + lane;       // this thread's state column
-    const int c0 = warp * 32;           // its 32 rows of K
+    const int cq = lane & 7;            // columns 4 cq .. 4 cq + 3 of the slice
+    const int rg = warp * 4 + (lane >> 3);   // rows 8 rg .. 8 rg + 7 of K
     const size_t state_base = (size_t)(n * p.H + h) * DK * DK;
     // Token inputs of the whole call (at most kDecodeMaxT tokens) into shared memory
     // with 16-byte asynchronous copies, issued before the state load so the two
@@ -94,13 +97,14 @@ __global__ void __launch_bounds__(NTD, 6) kda_decode_kernel(Params p) {
 
     // The state slice (32 rows v of 128 fp32, 16 KB contiguous) moves between HBM and
     // the registers through a shared tile: global accesses are whole 512-byte rows per
-    // warp instruction, and 16-byte chunk q of row v sits at chunk q ^ (v & 7) of the
-    // tile row, so both the row-wise copies and the per-thread 32-value reads are
-    // free of bank conflicts.
+    // warp instruction, and 16-byte chunk q of row v sits at chunk q ^ ((v / 4) & 7) of
+    // the tile row, so both the row-wise copies and the per-thread reads (eight lanes
+    // of a quarter-warp read eight rows 4 apart) are free of bank conflicts.
+    // s[8 i + e] = S[row 8 rg + e][column 4 cq + i].
     float s[32];
     const size_t slice = state_base + (size_t)(vs * VS) * DK;   // first element of the slice
     auto tile_chunk = [&](int row, int q) -> float4 * {
-        return reinterpret_cast<float4 *>(&tile[row * DK + 4 * (q ^ (row & 7))]);
+        return reinterpret_cast<float4 *>(&tile[row * DK + 4 * (q ^ ((row >> 2) & 7))]);
     };
     if (p.init) {
 #pragma unroll
@@ -120,9 +124,13 @@ __global__ void __launch_bounds__(NTD, 6) kda_decode_kernel(Params p) {
         }
         __syncthreads();
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float4 x = *tile_chunk(lane, (c0 >> 2) + j);
-            s[4 * j] = x.x; s[4 * j + 1] = x.y; s[4 * j + 2] = x.z; s[4 * j + 3] = x.w;
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int hq = 0; hq < 2; ++hq) {
+                const float4 x = *tile_chunk(4 * cq + i, 2 * rg + hq);
+                s[8 * i + 4 * hq] = x.x; s[8 * i + 4 * hq + 1] = x.y;
+                s[8 * i + 4 * hq + 2] = x.z; s[8 * i + 4 * hq + 3] = x.w;
+            }
         }
     } else {
 #pragma unroll
@@ -168,54 +176,97 @@ __global__ void __launch_bounds__(NTD, 6) kda_decode_kernel(Params p) {
     __syncthreads();
 
     for (int64_t t = 0; t < len; ++t) {
-        const int64_t row = row_base + t;
-        const int64_t tok = (row * p.H + h) * DK;
-        const float *alpha = alf + t * DK, *kn = knt + t * DK, *qn = qnt + t * DK;
-        const float vv = __bfloat162float(tv[t * VS + lane]), beta = tb[t];
+        const int64_t tok = ((row_base + t) * p.H + h) * DK;
+        const float4 *alpha4 = reinterpret_cast<const float4 *>(alf + t * DK) + 2 * rg;
+        const float4 *kn4 = reinterpret_cast<const float4 *>(knt + t * DK) + 2 * rg;
+        const float4 *qn4 = reinterpret_cast<const float4 *>(qnt + t * DK) + 2 * rg;
+        const float4 a0 = alpha4[0], a1 = alpha4[1], k0 = kn4[0], k1 = kn4[1];
+        const float2 al[4] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w), make_float2(a1.x, a1.y),
+                              make_float2(a1.z, a1.w)};
+        const float2 kk[4] = {make_float2(k0.x, k0.y), make_float2(k0.z, k0.w), make_float2(k1.x, k1.y),
+                              make_float2(k1.z, k1.w)};
 
-        // decay, then the column sum S^T k_hat over this thread's 32 rows (pairs of
-        // rows per instruction, 16-byte shared loads)
-        float2 ks2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};   // two chains
+        // decay, then this thread's part of S^T k_hat for its four columns
+        float ks[4];
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-            const float4 a4 = *reinterpret_cast<const float4 *>(&alpha[c0 + i]);
-            const float4 k4 = *reinterpret_cast<const float4 *>(&kn[c0 + i]);
-            float2 x0 = mul2(make_float2(s[i], s[i + 1]), make_float2(a4.x, a4.y));
-            float2 x1 = mul2(make_float2(s[i + 2], s[i + 3]), make_float2(a4.z, a4.w));
-            ks2[0] = fma2(make_float2(k4.x, k4.y), x0, ks2[0]);
-            ks2[1] = fma2(make_float2(k4.z, k4.w), x1, ks2[1]);
-            s[i] = x0.x; s[i + 1] = x0.y; s[i + 2] = x1.x; s[i + 3] = x1.y;
-        }
-        const float2 ksum = add2(ks2[0], ks2[1]);
-        red[0][warp][lane] = ksum.x + ksum.y;
-        __syncthreads();
-        const float u = beta * (vv - (red[0][0][lane] + red[0][1][lane] + red[0][2][lane] + red[0][3][lane]));
-        const float2 u2 = make_float2(u, u);
-        float2 os2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        for (int i = 0; i < 4; ++i) {
+            float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-            const float4 k4 = *reinterpret_cast<const float4 *>(&kn[c0 + i]);
-            const float4 q4 = *reinterpret_cast<const float4 *>(&qn[c0 + i]);
-            const float2 x0 = fma2(make_float2(k4.x, k4.y), u2, make_float2(s[i], s[i + 1]));
-            const float2 x1 = fma2(make_float2(k4.z, k4.w), u2, make_float2(s[i + 2], s[i + 3]));
-            os2[0] = fma2(make_float2(q4.x, q4.y), x0, os2[0]);
-            os2[1] = fma2(make_float2(q4.z, q4.w), x1, os2[1]);
-            s[i] = x0.x; s[i + 1] = x0.y; s[i + 2] = x1.x; s[i + 3] = x1.y;
+            for (int e = 0; e < 4; ++e) {
+                const float2 x = mul2(make_float2(s[8 * i + 2 * e], s[8 * i + 2 * e + 1]), al[e]);
+                acc = fma2(kk[e], x, acc);
+                s[8 * i + 2 * e] = x.x; s[8 * i + 2 * e + 1] = x.y;
+            }
+            ks[i] = acc.x + acc.y;
         }
-        const float2 osum = add2(os2[0], os2[1]);
-        const float os = osum.x + osum.y;
-        red[1][warp][lane] = os;
+        // the warp's four row groups (lanes 8 and 16 apart), then the four warps
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            ks[i] += __shfl_xor_sync(0xffffffffu, ks[i], 8);
+            ks[i] += __shfl_xor_sync(0xffffffffu, ks[i], 16);
+        }
+        if (lane < 8) *reinterpret_cast<float4 *>(&red[0][warp][4 * cq]) = make_float4(ks[0], ks[1], ks[2], ks[3]);
         __syncthreads();
-        if (warp == 0)
-            p.out[tok + v] = __float2bfloat16(
-                p.scale * (red[1][0][lane] + red[1][1][lane] + red[1][2][lane] + red[1][3][lane]));
+        float u[4];
+        {
+            const float4 r0 = *reinterpret_cast<const float4 *>(&red[0][0][4 * cq]);
+            const float4 r1 = *reinterpret_cast<const float4 *>(&red[0][1][4 * cq]);
+            const float4 r2 = *reinterpret_cast<const float4 *>(&red[0][2][4 * cq]);
+            const float4 r3 = *reinterpret_cast<const float4 *>(&red[0][3][4 * cq]);
+            const uint2 vw = *reinterpret_cast<const uint2 *>(&tv[t * VS + 4 * cq]);
+            const float beta = tb[t];
+            u[0] = beta * (__uint_as_float(vw.x << 16) - (r0.x + r1.x + r2.x + r3.x));
+            u[1] = beta * (__uint_as_float(vw.x & 0xFFFF0000u) - (r0.y + r1.y + r2.y + r3.y));
+            u[2] = beta * (__uint_as_float(vw.y << 16) - (r0.z + r1.z + r2.z + r3.z));
+            u[3] = beta * (__uint_as_float(vw.y & 0xFFFF0000u) - (r0.w + r1.w + r2.w + r3.w));
+        }
+        // rank-1 update and this thread's part of S^T q_hat
+        const float4 q0 = qn4[0], q1 = qn4[1];
+        const float2 qq[4] = {make_float2(q0.x, q0.y), make_float2(q0.z, q0.w), make_float2(q1.x, q1.y),
+                              make_float2(q1.z, q1.w)};
+        float os[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 u2 = make_float2(u[i], u[i]);
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 x = fma2(kk[e], u2, make_float2(s[8 * i + 2 * e], s[8 * i + 2 * e + 1]));
+                acc = fma2(qq[e], x, acc);
+                s[8 * i + 2 * e] = x.x; s[8 * i + 2 * e + 1] = x.y;
+            }
+            os[i] = acc.x + acc.y;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            os[i] += __shfl_xor_sync(0xffffffffu, os[i], 8);
+            os[i] += __shfl_xor_sync(0xffffffffu, os[i], 16);
+        }
+        if (lane < 8) *reinterpret_cast<float4 *>(&red[1][warp][4 * cq]) = make_float4(os[0], os[1], os[2], os[3]);
+        __syncthreads();
+        if (warp == 0 && lane < 8) {
+            const float4 r0 = *reinterpret_cast<const float4 *>(&red[1][0][4 * cq]);
+            const float4 r1 = *reinterpret_cast<const float4 *>(&red[1][1][4 * cq]);
+            const float4 r2 = *reinterpret_cast<const float4 *>(&red[1][2][4 * cq]);
+            const float4 r3 = *reinterpret_cast<const float4 *>(&red[1][3][4 * cq]);
+            const float sc = p.scale;
+            const __nv_bfloat162 o01 = __floats2bfloat162_rn(sc * (r0.x + r1.x + r2.x + r3.x),
+                                                             sc * (r0.y + r1.y + r2.y + r3.y));
+            const __nv_bfloat162 o23 = __floats2bfloat162_rn(sc * (r0.z + r1.z + r2.z + r3.z),
+                                                             sc * (r0.w + r1.w + r2.w + r3.w));
+            *reinterpret_cast<uint2 *>(p.out + tok + vs * VS + 4 * cq) =
+                make_uint2(*reinterpret_cast<const uint32_t *>(&o01), *reinterpret_cast<const uint32_t *>(&o23));
+        }
     }
 
     if (p.fin) {
         __syncthreads();   // the tile may still hold the initial state being read
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            *tile_chunk(lane, (c0 >> 2) + j) = make_float4(s[4 * j], s[4 * j + 1], s[4 * j + 2], s[4 * j + 3]);
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int hq = 0; hq < 2; ++hq)
+                *tile_chunk(4 * cq + i, 2 * rg + hq) = make_float4(s[8 * i + 4 * hq], s[8 * i + 4 * hq + 1],
+                                                                   s[8 * i + 4 * hq + 2], s[8 * i + 4 * hq + 3]);
         __syncthreads();
 #pragma unroll
         for (int r = 0; r < 8; ++r) {

@@ -49,12 +49,14 @@ __device__ __forceinline__ void seq_range(const Params &p, int64_t n, int64_t &b
     }
 }
 
-// Calls with at most this many token rows (T of the packed batch) run the
-// token-recurrence kernel (decode and short steps) instead of the chunked one.
+// Calls with at most this many token rows (T of the packed batch) run a
+// single-chunk kernel instead of the chunked cluster kernel: the token recurrence
+// for one row (decode), one 16-row chunk on warp-level tensor-core MMAs otherwise.
 constexpr int64_t kDecodeMaxT = 16;
 
 // Launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_cluster(const Params &p, cudaStream_t stream);   // chunked, needs p.ws
-cudaError_t launch_decode(const Params &p, cudaStream_t stream);    // token recurrence
+cudaError_t launch_decode(const Params &p, cudaStream_t stream);    // token recurrence, T = 1
+cudaError_t launch_short(const Params &p, cudaStream_t stream);     // one chunk, 2 <= T <= 16
 
 }  // namespace kda
