@@ -20,8 +20,9 @@
 // the norms and beta,
 // A and M from one bf16 MMA each (raw q/k times 2^G against k times 2^-G, the
 // norms applied in fp32 afterwards, as in the chunked kernel), and the 16 x 16
-// inverse by forward substitution.  CTAs are persistent (two per SM) and prefetch
-// the next unit's state and token rows into L2.  The row norms of k are folded into U
+// inverse by forward substitution.  CTAs are persistent (two per SM): a unit's
+// token rows are copied in while the previous unit finishes, and its state is
+// prefetched into L2 at the same time.  The row norms of k are folded into U
 // (U' = Diag(1/|k|) U) and out of M and Kbar, so every fp16 tile is the raw input
 // times decay factors in [0, 1].
 #include <cuda_bf16.h>
@@ -115,8 +116,31 @@ __global__ void __launch_bounds__(NTS, 2) kda_short_kernel(Params p) {
     const int64_t units = p.n_seqs * p.H;
     const size_t selt = p.state_type == kStateBF16 ? 2 : 4;
 
-    // Persistent CTAs: unit after unit, each one prefetching the next one's state and
-    // token rows into L2 before it starts.
+    // Token rows of unit u into the q, k, g, v tiles (16-byte asynchronous copies for
+    // rows t < L, zeros for the rest), committed as one cp.async group.
+    auto load_inputs = [&](int64_t u) {
+        const int64_t uh = u % p.H, un = u / p.H;
+        int64_t ub, ut0, ulen;
+        seq_range(p, un, ub, ut0, ulen);
+        for (int i = tid; i < 4 * LT * 16; i += NTS) {
+            const int x = i >> 8, t = (i >> 4) & 15, ch = i & 15;
+            __nv_bfloat16 *dst = (x == 0 ? &sm.q[t][8 * ch] : x == 1 ? &sm.k[t][8 * ch]
+                                  : x == 2 ? &sm.g[t][8 * ch] : &sm.v[t][8 * ch]);
+            if (t < ulen) {
+                const __nv_bfloat16 *src = (x == 0 ? p.q : x == 1 ? p.k : x == 2 ? p.g : p.v) +
+                                           ((ub * p.T + ut0 + t) * p.H + uh) * DK + 8 * ch;
+                cp_async16(dst, src);
+            } else {
+                *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+
+    // Persistent CTAs, unit after unit.  The next unit's token rows are copied in as
+    // soon as the current one's are dead (after its second barrier), and its state is
+    // prefetched into L2 at the same point.
+    if (blockIdx.x < units) load_inputs(blockIdx.x);
     for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
         const int64_t h = unit % p.H, n = unit / p.H;
         int64_t b, t0, len64;
@@ -124,38 +148,6 @@ __global__ void __launch_bounds__(NTS, 2) kda_short_kernel(Params p) {
         const int L = (int)len64;   // <= 16 (the packed batch has at most 16 token rows)
         const int64_t row_base = b * p.T + t0;
         const size_t state_base = (size_t)(n * p.H + h) * DK * DK;
-        {
-            const int64_t nu = unit + gridDim.x;
-            if (nu < units) {
-                const int64_t nh = nu % p.H, nn = nu / p.H;
-                int64_t nb, nt0, nlen;
-                seq_range(p, nn, nb, nt0, nlen);
-                if (tid == LT * 4 && p.init)
-                    prefetch_l2(static_cast<const unsigned char *>(p.init) + (size_t)(nn * p.H + nh) * DK * DK * selt,
-                                (uint32_t)(DK * DK * selt));
-                if (tid < LT * 4 && (tid & 15) < nlen) {
-                    const int x = tid >> 4;
-                    const __nv_bfloat16 *src = x == 0 ? p.q : x == 1 ? p.k : x == 2 ? p.g : p.v;
-                    prefetch_l2(src + ((nb * p.T + nt0 + (tid & 15)) * p.H + nh) * DK, DK * 2);
-                }
-            }
-        }
-        __syncthreads();   // the previous unit's tiles have been read
-
-        // ---- inputs: q, k, g, v rows t < L by 16-byte asynchronous copies, zero rows >= L
-        for (int i = tid; i < 4 * LT * 16; i += NTS) {
-            const int x = i >> 8, t = (i >> 4) & 15, ch = i & 15;
-            __nv_bfloat16 *dst = (x == 0 ? &sm.q[t][8 * ch] : x == 1 ? &sm.k[t][8 * ch]
-                                  : x == 2 ? &sm.g[t][8 * ch] : &sm.v[t][8 * ch]);
-            if (t < L) {
-                const __nv_bfloat16 *src = (x == 0 ? p.q : x == 1 ? p.k : x == 2 ? p.g : p.v) +
-                                           ((row_base + t) * p.H + h) * DK + 8 * ch;
-                cp_async16(dst, src);
-            } else {
-                *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
 
         // ---- this warp's state rows as MMA accumulators: z[2i + r][e] (rows v0) and
         // z[2i + r][2 + e] (rows v0 + 8) hold channel 16 i + 4 qq + 2 r + e
@@ -212,13 +204,14 @@ __global__ void __launch_bounds__(NTS, 2) kda_short_kernel(Params p) {
                                              __shfl_xor_sync(0xffffffffu, run.y, 1));
             const float2 GL = add2(run, other);
             const float2 off = hf ? other : make_float2(0.f, 0.f);
+            const float2 eL = make_float2(exp2f(GL.x), exp2f(GL.y));
 #pragma unroll
             for (int tt = 0; tt < 8; ++tt) {
                 const int t = 8 * hf + tt;
                 const float2 G = add2(Gs[tt], off);
                 const float2 e = make_float2(exp2f(G.x), exp2f(G.y));
                 const float2 ei = make_float2(exp2f(-G.x), exp2f(-G.y));
-                const float2 ec = make_float2(exp2f(GL.x - G.x), exp2f(GL.y - G.y));
+                const float2 ec = mul2(eL, ei);   // 2^(G_L - G) <= 1
                 const float2 kx = bf16x2_to_f2(*reinterpret_cast<const uint32_t *>(&sm.k[t][c0]));
                 const float2 qx = bf16x2_to_f2(*reinterpret_cast<const uint32_t *>(&sm.q[t][c0]));
                 const float2 ke = mul2(kx, e), qe = mul2(qx, e), ki = mul2(kx, ei), kc = mul2(kx, ec);
@@ -229,7 +222,7 @@ __global__ void __launch_bounds__(NTS, 2) kda_short_kernel(Params p) {
                 *reinterpret_cast<uint32_t *>(&sm.y[LT + t][col]) = h2_bits(qe.x, qe.y);
                 *reinterpret_cast<uint32_t *>(&sm.kc[t][col]) = h2_bits(kc.x, kc.y);
             }
-            if (hf == 0) *reinterpret_cast<float2 *>(&sm.gam[col]) = make_float2(exp2f(GL.x), exp2f(GL.y));
+            if (hf == 0) *reinterpret_cast<float2 *>(&sm.gam[col]) = eL;
         } else {
             // ---- row norms of q and k (warps 4-7, four tokens each) and beta
             const int w4 = warp - 4;
@@ -297,8 +290,8 @@ __global__ void __launch_bounds__(NTS, 2) kda_short_kernel(Params p) {
                 __syncwarp();
                 // T = (I + A)^-1 by forward substitution, lane = column j (right-looking:
                 // once x[r] is final it is added into every later row), then T' = T Diag(beta)
-                if (lane < LT) {
-                    const int j = lane;
+                {
+                    const int j = lane & (LT - 1);   // lanes 16-31 repeat the columns, without stores
                     float acc[LT], x[LT];
 #pragma unroll
                     for (int r = 0; r < LT; ++r) acc[r] = 0.f;
@@ -309,8 +302,10 @@ __global__ void __launch_bounds__(NTS, 2) kda_short_kernel(Params p) {
                         for (int r2 = r + 1; r2 < LT; ++r2) acc[r2] = fmaf(sm.a[r2][r], x[r], acc[r2]);
                     }
                     const float bj = sm.beta[j];
+                    if (lane < LT) {
 #pragma unroll
-                    for (int r = 0; r < LT; ++r) sm.tp[r][j] = __float2half_rn(x[r] * bj);
+                        for (int r = 0; r < LT; ++r) sm.tp[r][j] = __float2half_rn(x[r] * bj);
+                    }
                 }
             }
         }
@@ -344,6 +339,13 @@ __global__ void __launch_bounds__(NTS, 2) kda_short_kernel(Params p) {
             x[1][nt][0] *= rq0; x[1][nt][1] *= rq0; x[1][nt][2] *= rq1; x[1][nt][3] *= rq1;
         }
         __syncthreads();   // T', M' (warps 0, 1) and every warp's R are in shared memory
+        if (unit + gridDim.x < units) {   // q, k, g, v are dead: the next unit's rows go in
+            const int64_t nu = unit + gridDim.x;
+            load_inputs(nu);
+            if (tid == 0 && p.init)
+                prefetch_l2(static_cast<const unsigned char *>(p.init) + (size_t)nu * DK * DK * selt,
+                            (uint32_t)(DK * DK * selt));
+        }
 
         // ---- U = T' R, U' = Diag(1/|k|) U (fp16)
         {
