@@ -94,13 +94,16 @@ cudaMemPool_t workspace_pool(int device) {
     return pools[device];
 }
 
-kda_status launch(kda::Params &p, void *stream) {
+// tsplit > 0: the sequence-parallel path with that many segments per sequence (p.ws is
+// then its scratch, tsplit_scratch_bytes long).
+kda_status launch(kda::Params &p, void *stream, int64_t tsplit = 0) {
     int *err = nullptr;
     if (cudaGetSymbolAddress(reinterpret_cast<void **>(&err), g_kda_error) != cudaSuccess)
         return KDA_ERR_CUDA;
     p.err = err;
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = p.T == 1 ? kda::launch_decode(p, cs)
+    const cudaError_t e = tsplit > 0 ? kda::launch_tsplit(p, tsplit, p.ws, cs)
+                          : p.T == 1 ? kda::launch_decode(p, cs)
                           : p.T <= kda::kDecodeMaxT ? kda::launch_short(p, cs)
                                                     : kda::launch_cluster(p, cs);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
@@ -127,12 +130,16 @@ kda_status kda_fwd(const void *q, const void *k, const void *v, const void *g, c
     if (cudaGetDevice(&device) != cudaSuccess) return KDA_ERR_CUDA;
     cudaMemPool_t pool = workspace_pool(device);
     if (!pool) return KDA_ERR_CUDA;
+    // Few (sequence, head) units on a long fixed-length call: the sequence-parallel path
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return KDA_ERR_CUDA;
+    const int64_t tsplit = kda::tsplit_segments(p, sms);
+    const size_t bytes = tsplit > 0 ? kda::tsplit_scratch_bytes(p.n_seqs, p.H, tsplit)
+                                    : (size_t)(p.n_seqs * p.H) * kda::kWsBytesPerUnit;
     void *ws = nullptr;
-    if (cudaMallocFromPoolAsync(&ws, (size_t)(p.n_seqs * p.H) * kda::kWsBytesPerUnit, pool, cs) !=
-        cudaSuccess)
-        return KDA_ERR_CUDA;
+    if (cudaMallocFromPoolAsync(&ws, bytes, pool, cs) != cudaSuccess) return KDA_ERR_CUDA;
     p.ws = static_cast<unsigned char *>(ws);
-    st = launch(p, stream);
+    st = launch(p, stream, tsplit);
     if (cudaFreeAsync(ws, cs) != cudaSuccess) st = KDA_ERR_CUDA;
     return st;
 }

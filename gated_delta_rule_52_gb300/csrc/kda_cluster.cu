@@ -680,6 +680,10 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
     const size_t state_base = (size_t)(n * p.H + h) * DK * DK;
 
     auto issue_v = [&](int chunk) {
+        if (!p.v) {   // values taken as zero (the tile stays zero): only the phase completes
+            mbar_arrive(&sm.v_full);
+            return;
+        }
         const int row = (int)(row_base + (int64_t)chunk * C);
         mbar_arrive_expect_tx(&sm.v_full, 16384);
         tma_load_3d(smem + C_B2 + 16384, &maps.v, &sm.v_full, 0, (int)h, row);
@@ -766,6 +770,8 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
         sts128(sbase + C_TZM + 24576 + k16 * 16, 0, 0, 0, 0);
         sts128(sbase + C_T1 + 8192 + k16 * 16, 0, 0, 0, 0);
     }
+    if (!p.v)
+        for (int k16 = tid; k16 < 1024; k16 += NT) sts128(sbase + C_B2 + 16384 + k16 * 16, 0, 0, 0, 0);
     // initial state -> D_S (fp32) and S fp16 operand copy; warps 0-7
     if (warp < 8) {
         const int c = quarter * 32 + lane;
@@ -936,7 +942,7 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
                 for (int jj = 0; jj < 4; ++jj)
                     tmem_ld16(tmem_addr(D_U, (warp & 3) * 32, 64 * hb + 16 * jj), r[jj]);
                 tmem_ld_wait();
-                if (t < L) {
+                if (t < L && p.out) {
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
                         uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((row0 + t) * p.H + h) * DK +

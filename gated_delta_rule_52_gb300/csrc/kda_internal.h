@@ -21,8 +21,8 @@ enum StateType : int { kStateNone = 0, kStateBF16 = 1, kStateFP32 = 2 };
 // the FlashKDA README "Kernel API" table: q,k,g [B,T,H,128], v,out [B,T,H,128],
 // beta [B,T,H], A_log [H], dt_bias [H,128], states [N,H,V,K].
 struct Params {
-    const __nv_bfloat16 *q, *k, *v, *g, *beta;
-    __nv_bfloat16 *out;
+    const __nv_bfloat16 *q, *k, *v, *g, *beta;   // v may be null inside the library: values of zero
+    __nv_bfloat16 *out;                            // null inside the library: outputs not written
     const float *A_log, *dt_bias;
     float scale, lower_bound;
     const void *init;   // nullptr = zero state
@@ -58,5 +58,13 @@ constexpr int64_t kDecodeMaxT = 16;
 cudaError_t launch_cluster(const Params &p, cudaStream_t stream);   // chunked, needs p.ws
 cudaError_t launch_decode(const Params &p, cudaStream_t stream);    // token recurrence, T = 1
 cudaError_t launch_short(const Params &p, cudaStream_t stream);     // one chunk, 2 <= T <= 16
+
+// Sequence-parallel prefill (fixed-length calls with few (sequence, head) units): each
+// sequence cut into P segments of at least kTsplitMinSeg tokens, P in [4, kTsplitMaxSeg].
+constexpr int64_t kTsplitMinSeg = 2048;
+constexpr int64_t kTsplitMaxSeg = 32;
+int64_t tsplit_segments(const Params &p, int sms);   // P, or 0: run the plain path
+size_t tsplit_scratch_bytes(int64_t N, int64_t H, int64_t P);
+cudaError_t launch_tsplit(const Params &p, int64_t P, unsigned char *scratch, cudaStream_t stream);
 
 }  // namespace kda

@@ -1,0 +1,213 @@
+// Sequence-parallel (T-split) prefill for calls with few (sequence, head) units.
+//
+// The chunk map of the KDA recurrence is affine in the entering state:
+//   S_out = P S_in + R,  P = prod over the chunks of (Diag(Gamma_C) - Kbar^T W),
+// with R the state reached from S_in = 0 (the chunk equations of the tensor-core
+// path: U = T'V - W S_in, S_out = Diag(Gamma_C) S_in + Kbar^T U).  So a sequence
+// cut into segments runs as:
+//   1. every segment from S = 0 (segment 0 from the call's initial state): R_s;
+//   2. every segment with v = 0 from S = I: the transition P_s (the same kernel, the
+//      identity as the initial state and zero values);
+//   3. a scan over the segments: S_in(0) = S_0, S_in(s) = P_{s-1} S_in(s-1) + R_{s-1};
+//   4. every segment from S_in(s), writing the outputs (and, for the last segment,
+//      the final state).
+// Steps 1, 2 and 4 are the chunked cluster kernel over the segments as independent
+// packed sequences (segment boundaries as cu_seqlens); 1 and 2 write no outputs.
+// With P segments per sequence each of those launches has P times the parallelism
+// of the plain call, at three times its work.
+#include <cuda_bf16.h>
+
+#include "kda_internal.h"
+#include "sm103.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int DK = kHeadDim;
+constexpr int64_t kState = (int64_t)DK * DK;             // elements of one state
+constexpr int64_t kStateBytes = kState * 4;               // fp32 segment states
+
+// cu_seqlens of the segments over the flattened [B*T] token rows: segment i = b P + s
+// covers rows b T + s Ls .. min(b T + (s + 1) Ls, (b + 1) T); entry N P is N T.
+__global__ void seg_bounds_kernel(int64_t *cu, int64_t N, int64_t P, int64_t T, int64_t Ls) {
+    const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (i > N * P) return;
+    const int64_t b = i / P, s = i % P;
+    cu[i] = b * T + (s * Ls < T ? s * Ls : T);
+}
+
+// Initial states of steps 1 and 2: r0[b P + s, h] = the call's initial state for s = 0
+// (zero if none), zero otherwise; id[b P + s, h] = I.  Grid (segment states, 16):
+// block y covers rows 8 y .. 8 y + 7 of one state, four channels per thread.
+__global__ void seg_init_kernel(float *r0, float *id, const void *init, int state_type, int64_t P,
+                                int64_t H) {
+    const int64_t idx = blockIdx.x, h = idx % H, seg = idx / H, b = seg / P, s = seg % P;
+    const int i = (int)blockIdx.y * 1024 + 4 * threadIdx.x;   // 256 threads x 4 = 8 rows
+    const int row = i / DK, col = i % DK;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (s == 0 && init) {
+        const int64_t off = (b * H + h) * kState + i;
+        if (state_type == kStateBF16) {
+            const uint2 w = *reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(init) + off);
+            x = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                            __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+        } else {
+            x = *reinterpret_cast<const float4 *>(static_cast<const float *>(init) + off);
+        }
+    }
+    *reinterpret_cast<float4 *>(r0 + idx * kState + i) = x;
+    *reinterpret_cast<float4 *>(id + idx * kState + i) =
+        make_float4(row == col, row == col + 1, row == col + 2, row == col + 3);
+}
+
+// The scan of step 3 for one (sequence, head): sin[s] = sin[s-1] x Pst[s-1] + R[s-1] in
+// the stored (transposed) layout, sin[0] given.  fp32 on paired FMAs; 512 threads,
+// thread (tv, tk) = rows 4 tv .. 4 tv + 3 and columns 2 tk + 32 c + (0, 1) (c = 0..3)
+// of the product.  The previous state sits in shared memory with rows padded to 129
+// floats (reads are broadcasts), the transition unpadded (reads are 32 consecutive
+// float pairs of a warp).
+constexpr int kZs = DK + 1;
+constexpr int kScanThreads = 512;
+__global__ void __launch_bounds__(kScanThreads) seg_scan_kernel(float *sin, const float *R, const float *Pst,
+                                                                int64_t P, int64_t H) {
+    extern __shared__ __align__(16) float scan_sm[];
+    float *pm = scan_sm;                 // [j][k]: stored transition of the previous segment
+    float *zs = scan_sm + kState;        // [v][j]: entering state of the previous segment
+    const int64_t b = blockIdx.x / H, h = blockIdx.x % H;
+    const int tid = threadIdx.x, tv = tid >> 4, tk = tid & 15;
+    auto slot = [&](int64_t s) { return ((b * P + s) * H + h) * kState; };
+    const float *z0 = sin + slot(0);
+    for (int i = tid; i < kState; i += kScanThreads) zs[(i / DK) * kZs + i % DK] = z0[i];
+    for (int64_t s = 1; s < P; ++s) {
+        const float *ps = Pst + slot(s - 1);
+        for (int i = tid * 4; i < kState; i += 4 * kScanThreads)
+            *reinterpret_cast<float4 *>(pm + i) = *reinterpret_cast<const float4 *>(ps + i);
+        __syncthreads();
+        float2 acc[4][4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[a][c] = make_float2(0.f, 0.f);
+#pragma unroll 4
+        for (int j = 0; j < DK; ++j) {
+            float2 zv[4], pv[4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const float z = zs[(4 * tv + a) * kZs + j];
+                zv[a] = make_float2(z, z);
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) pv[c] = *reinterpret_cast<const float2 *>(pm + j * DK + 2 * tk + 32 * c);
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[a][c] = sm103::fma2(zv[a], pv[c], acc[a][c]);
+        }
+        __syncthreads();   // every thread is done with zs and pm
+        const float *rs = R + slot(s - 1);
+        float *out = sin + slot(s);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const int v = 4 * tv + a;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int k = 2 * tk + 32 * c;
+                const float2 r2 = *reinterpret_cast<const float2 *>(rs + v * DK + k);
+                const float2 x = sm103::add2(acc[a][c], r2);
+                *reinterpret_cast<float2 *>(out + v * DK + k) = x;
+                zs[v * kZs + k] = x.x;
+                zs[v * kZs + k + 1] = x.y;
+            }
+        }
+    }
+}
+
+// Step 4's final states -> the call's final state: fin[b, h] = fin3[b P + P - 1, h].
+// Grid (sequence states, 16), four channels per thread.
+__global__ void seg_final_kernel(void *fin, int state_type, const float *fin3, int64_t P, int64_t H) {
+    const int64_t b = blockIdx.x / H, h = blockIdx.x % H;
+    const int i = (int)blockIdx.y * 1024 + 4 * threadIdx.x;
+    const float4 x = *reinterpret_cast<const float4 *>(fin3 + ((b * P + P - 1) * H + h) * kState + i);
+    const int64_t dst = (b * H + h) * kState + i;
+    if (state_type == kStateBF16)
+        *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(fin) + dst) =
+            make_uint2(sm103::pack_bf16(x.x, x.y), sm103::pack_bf16(x.z, x.w));
+    else
+        *reinterpret_cast<float4 *>(static_cast<float *>(fin) + dst) = x;
+}
+
+int64_t seg_len(int64_t T, int64_t P) {
+    const int64_t per = (T + P - 1) / P;
+    return (per + kChunk - 1) / kChunk * kChunk;
+}
+
+}  // namespace
+
+int64_t tsplit_segments(const Params &p, int sms) {
+    if (p.cu_seqlens || p.B <= 0 || p.T < kTsplitMinSeg * 4) return 0;
+    const int64_t units = p.n_seqs * p.H, slots = sms / 2;   // clusters in flight
+    if (units <= 0) return 0;
+    int64_t P = slots / units;
+    if (P > p.T / kTsplitMinSeg) P = p.T / kTsplitMinSeg;
+    if (P > kTsplitMaxSeg) P = kTsplitMaxSeg;
+    return P >= 4 ? P : 0;
+}
+
+size_t tsplit_scratch_bytes(int64_t N, int64_t H, int64_t P) {
+    const size_t cu = ((size_t)(N * P + 1) * 8 + 255) / 256 * 256;
+    return cu + 4 * (size_t)(N * P * H) * kStateBytes + (size_t)(N * P * H) * kWsBytesPerUnit;
+}
+
+cudaError_t launch_tsplit(const Params &p, int64_t P, unsigned char *scratch, cudaStream_t stream) {
+    const int64_t N = p.n_seqs, H = p.H, T = p.T, Ls = seg_len(T, P), S = N * P;
+    const size_t cu_bytes = ((size_t)(S + 1) * 8 + 255) / 256 * 256, sb = (size_t)(S * H) * kStateBytes;
+    int64_t *cu = reinterpret_cast<int64_t *>(scratch);
+    float *sin = reinterpret_cast<float *>(scratch + cu_bytes);            // also step 1's initial states
+    float *fin3 = reinterpret_cast<float *>(scratch + cu_bytes + sb);      // also step 2's identities
+    float *R = reinterpret_cast<float *>(scratch + cu_bytes + 2 * sb);
+    float *Pst = reinterpret_cast<float *>(scratch + cu_bytes + 3 * sb);
+    unsigned char *ws = scratch + cu_bytes + 4 * sb;
+
+    seg_bounds_kernel<<<(unsigned)((S + 1 + 255) / 256), 256, 0, stream>>>(cu, N, P, T, Ls);
+    seg_init_kernel<<<dim3((unsigned)(S * H), 16), 256, 0, stream>>>(sin, fin3, p.init, p.state_type, P, H);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    Params q = p;   // the segments as packed sequences over the flattened rows
+    q.cu_seqlens = cu;
+    q.n_seqs = S;
+    q.B = 1;
+    q.T = N * T;
+    q.state_type = kStateFP32;
+    q.ws = ws;
+    // 1. R_s from S = 0 (segment 0 from the call's initial state); no outputs
+    q.init = sin;
+    q.fin = R;
+    q.out = nullptr;
+    if ((e = launch_cluster(q, stream)) != cudaSuccess) return e;
+    // 2. the transitions P_s: zero values from S = I; no outputs
+    q.v = nullptr;
+    q.init = fin3;
+    q.fin = Pst;
+    if ((e = launch_cluster(q, stream)) != cudaSuccess) return e;
+    // 3. the scan
+    const int scan_smem = (int)((kState + (int64_t)DK * kZs) * 4);
+    if ((e = cudaFuncSetAttribute(seg_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, scan_smem)) !=
+        cudaSuccess)
+        return e;
+    seg_scan_kernel<<<(unsigned)(N * H), kScanThreads, scan_smem, stream>>>(sin, R, Pst, P, H);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // 4. every segment from its entering state, with outputs
+    q.v = p.v;
+    q.init = sin;
+    q.fin = fin3;
+    q.out = p.out;
+    if ((e = launch_cluster(q, stream)) != cudaSuccess) return e;
+    if (p.fin) {
+        seg_final_kernel<<<dim3((unsigned)(N * H), 16), 256, 0, stream>>>(p.fin, p.state_type, fin3, P, H);
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
+}  // namespace kda

@@ -88,6 +88,11 @@ WORKLOADS = {
     "decode_16": Workload(
         name="decode_16", B=64, T=16, H=64, seed=6, state_dtype="bf16", initial_state="normal",
         description="B=64 T=16 H=64 (16-token step); bf16 state N(0,0.02)"),
+    # A long prefill with few heads (e.g. 8 heads on one GPU of a tensor-parallel group):
+    # 8 (sequence, head) units, the sequence-parallel path.
+    "prefill_64k_h8": Workload(
+        name="prefill_64k_h8", B=1, T=65536, H=8, seed=7, state_dtype="bf16", initial_state="normal",
+        description="B=1 T=65536 H=8; bf16 initial/final state N(0,0.02)"),
 }
 
 # The throughput workload timed by bench.py.

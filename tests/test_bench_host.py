@@ -91,3 +91,14 @@ def test_kernel_of_follows_the_packed_token_count():
     assert bench.kernel_of(d["T"]) == "cluster"   # the ragged workload's T is the packed total
     for k in bench.KERNEL_SOURCES:
         assert len(bench.kernel_source_hash(k)) == 16 and k in bench.KERNEL_NAMES
+
+
+def test_tsplit_rule_mirror():
+    # the few-units rule of kda_fwd's sequence-parallel path, as bench.py mirrors it
+    import bench
+    assert bench.tsplit_segments(1, 65536, 8, False, 152) == 9      # 76 clusters / 8 units
+    assert bench.tsplit_segments(1, 8192, 64, False, 152) == 0      # the headline: units fill the GPU
+    assert bench.tsplit_segments(1, 8192, 2, False, 152) == 4       # capped by 2048-token segments
+    assert bench.tsplit_segments(1, 65536, 1, False, 152) == 32     # capped at 32 segments
+    assert bench.tsplit_segments(1, 65536, 8, True, 152) == 0       # varlen calls never split
+    assert bench.tsplit_segments(1, 4096, 1, False, 152) == 0       # too short

@@ -287,3 +287,18 @@ def test_random_configurations(i):
     out, fin = pu.run_gpu(d, want_final=want)
     ref_out, ref_fin = pu.run_oracle(d, want_final=want)
     print(w, pu.check(d, out, fin, ref_out, ref_fin, label=w.name))
+
+
+# ---- sequence-parallel prefill: fixed-length calls with few (sequence, head) units and
+# T >= 8192 run the T-split path (segments, their affine state maps, a scan, a re-run)
+
+@pytest.mark.parametrize("B,T,H,sd,init", [(1, 8192, 2, "bf16", "normal"),
+                                           (2, 8200, 1, "fp32", "alternate"),
+                                           (1, 8192, 3, None, "none")])
+def test_sequence_parallel_prefill_all_elements(B, T, H, sd, init):
+    d = W.make_inputs(W.get("prefill_8k", B=B, T=T, H=H, seed=11 + T + H, state_dtype=sd,
+                            initial_state=init, state_std=0.3))
+    want = sd is not None
+    out, fin = pu.run_gpu(d, want_final=want)
+    ref_out, ref_fin = pu.run_oracle(d, want_final=want)
+    print("tsplit", B, T, H, sd, pu.check(d, out, fin, ref_out, ref_fin, label=f"tsplit B={B} T={T} H={H}"))
