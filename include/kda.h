@@ -89,8 +89,16 @@ typedef enum {
  * per-chunk operands that move between the two CTAs of a cluster through L2),
  * taken stream-ordered on `stream` from a memory pool that libkda.so creates
  * once per device and keeps mapped, and released on `stream` after the kernel.
- * kda_fwd_ws is the same call with a caller-provided workspace.  It is
- * asynchronous: it returns once the work is enqueued, without synchronising.
+ * Calls of at most 16 token rows need no workspace.  A fixed-length call
+ * (cu_seqlens == NULL) whose N * H (sequence, head) units would leave most of the
+ * GPU idle, with T >= 8192, runs the sequence-parallel path: each sequence is cut
+ * into P >= 4 segments of at least 2048 tokens, whose affine state maps are joined
+ * by a scan (same results within the stated tolerances, three times the work on P
+ * times the parallelism); its scratch, also from the pool, is about
+ * N * H * P * (4 * 64 KB + KDA_WORKSPACE_BYTES_PER_UNIT) bytes.
+ * kda_fwd_ws is the same call with a caller-provided workspace; it always takes
+ * the plain path.  Both are asynchronous: they return once the work is enqueued,
+ * without synchronising.
  * q/k/v/g/beta/out/A_log/dt_bias/states must be 16-byte aligned.  `out` must not
  * alias an input.
  *
