@@ -60,64 +60,53 @@ __global__ void seg_init_kernel(float *r0, float *id, const void *init, int stat
         make_float4(row == col, row == col + 1, row == col + 2, row == col + 3);
 }
 
-// The scan of step 3 for one (sequence, head): sin[s] = sin[s-1] x Pst[s-1] + R[s-1] in
-// the stored (transposed) layout, sin[0] given.  fp32 on paired FMAs; 512 threads,
-// thread (tv, tk) = rows 4 tv .. 4 tv + 3 and columns 2 tk + 32 c + (0, 1) (c = 0..3)
-// of the product.  The previous state sits in shared memory with rows padded to 129
-// floats (reads are broadcasts), the transition unpadded (reads are 32 consecutive
-// float pairs of a warp).
+// The scan of step 3: sin[s] = sin[s-1] x Pst[s-1] + R[s-1] in the stored (transposed)
+// layout, sin[0] given; fp32 on paired FMAs.  The rows of the product are independent,
+// so grid (sequence states, 8): block y carries rows 16 y .. 16 y + 15 through every
+// step, reading each transition (L2-resident) whole.  256 threads, thread (tr, tc) =
+// row 16 y + tr, columns 2 tc + 32 c + (0, 1), c = 0..3.  The block's rows sit in
+// shared memory padded to 129 floats (reads are broadcasts), the transition unpadded
+// (reads are 16 consecutive float pairs of a half-warp).
 constexpr int kZs = DK + 1;
-constexpr int kScanThreads = 512;
-__global__ void __launch_bounds__(kScanThreads) seg_scan_kernel(float *sin, const float *R, const float *Pst,
-                                                                int64_t P, int64_t H) {
+constexpr int kScanRows = 16;
+__global__ void __launch_bounds__(256) seg_scan_kernel(float *sin, const float *R, const float *Pst,
+                                                       int64_t P, int64_t H) {
     extern __shared__ __align__(16) float scan_sm[];
     float *pm = scan_sm;                 // [j][k]: stored transition of the previous segment
-    float *zs = scan_sm + kState;        // [v][j]: entering state of the previous segment
+    float *zs = scan_sm + kState;        // [tr][j]: this block's rows of the entering state
     const int64_t b = blockIdx.x / H, h = blockIdx.x % H;
-    const int tid = threadIdx.x, tv = tid >> 4, tk = tid & 15;
+    const int rb = (int)blockIdx.y * kScanRows;
+    const int tid = threadIdx.x, tr = tid >> 4, tc = tid & 15;
     auto slot = [&](int64_t s) { return ((b * P + s) * H + h) * kState; };
-    const float *z0 = sin + slot(0);
-    for (int i = tid; i < kState; i += kScanThreads) zs[(i / DK) * kZs + i % DK] = z0[i];
+    const float *z0 = sin + slot(0) + (int64_t)rb * DK;
+    for (int i = tid; i < kScanRows * DK; i += 256) zs[(i / DK) * kZs + i % DK] = z0[i];
     for (int64_t s = 1; s < P; ++s) {
         const float *ps = Pst + slot(s - 1);
-        for (int i = tid * 4; i < kState; i += 4 * kScanThreads)
+        for (int i = tid * 4; i < kState; i += 1024)
             *reinterpret_cast<float4 *>(pm + i) = *reinterpret_cast<const float4 *>(ps + i);
         __syncthreads();
-        float2 acc[4][4];
+        float2 acc[4];
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) acc[a][c] = make_float2(0.f, 0.f);
-#pragma unroll 4
+        for (int c = 0; c < 4; ++c) acc[c] = make_float2(0.f, 0.f);
+#pragma unroll 8
         for (int j = 0; j < DK; ++j) {
-            float2 zv[4], pv[4];
+            const float z = zs[tr * kZs + j];
+            const float2 z2 = make_float2(z, z);
 #pragma unroll
-            for (int a = 0; a < 4; ++a) {
-                const float z = zs[(4 * tv + a) * kZs + j];
-                zv[a] = make_float2(z, z);
-            }
-#pragma unroll
-            for (int c = 0; c < 4; ++c) pv[c] = *reinterpret_cast<const float2 *>(pm + j * DK + 2 * tk + 32 * c);
-#pragma unroll
-            for (int a = 0; a < 4; ++a)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) acc[a][c] = sm103::fma2(zv[a], pv[c], acc[a][c]);
+            for (int c = 0; c < 4; ++c)
+                acc[c] = sm103::fma2(z2, *reinterpret_cast<const float2 *>(pm + j * DK + 2 * tc + 32 * c), acc[c]);
         }
         __syncthreads();   // every thread is done with zs and pm
-        const float *rs = R + slot(s - 1);
-        float *out = sin + slot(s);
+        const int v = rb + tr;
+        const float *rs = R + slot(s - 1) + (int64_t)v * DK;
+        float *out = sin + slot(s) + (int64_t)v * DK;
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            const int v = 4 * tv + a;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int k = 2 * tk + 32 * c;
-                const float2 r2 = *reinterpret_cast<const float2 *>(rs + v * DK + k);
-                const float2 x = sm103::add2(acc[a][c], r2);
-                *reinterpret_cast<float2 *>(out + v * DK + k) = x;
-                zs[v * kZs + k] = x.x;
-                zs[v * kZs + k + 1] = x.y;
-            }
+        for (int c = 0; c < 4; ++c) {
+            const int k = 2 * tc + 32 * c;
+            const float2 x = sm103::add2(acc[c], *reinterpret_cast<const float2 *>(rs + k));
+            *reinterpret_cast<float2 *>(out + k) = x;
+            zs[tr * kZs + k] = x.x;
+            zs[tr * kZs + k + 1] = x.y;
         }
     }
 }
@@ -191,11 +180,11 @@ cudaError_t launch_tsplit(const Params &p, int64_t P, unsigned char *scratch, cu
     q.fin = Pst;
     if ((e = launch_cluster(q, stream)) != cudaSuccess) return e;
     // 3. the scan
-    const int scan_smem = (int)((kState + (int64_t)DK * kZs) * 4);
+    const int scan_smem = (int)((kState + (int64_t)kScanRows * kZs) * 4);
     if ((e = cudaFuncSetAttribute(seg_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, scan_smem)) !=
         cudaSuccess)
         return e;
-    seg_scan_kernel<<<(unsigned)(N * H), kScanThreads, scan_smem, stream>>>(sin, R, Pst, P, H);
+    seg_scan_kernel<<<dim3((unsigned)(N * H), DK / kScanRows), 256, scan_smem, stream>>>(sin, R, Pst, P, H);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // 4. every segment from its entering state, with outputs
     q.v = p.v;
