@@ -302,3 +302,31 @@ def test_sequence_parallel_prefill_all_elements(B, T, H, sd, init):
     out, fin = pu.run_gpu(d, want_final=want)
     ref_out, ref_fin = pu.run_oracle(d, want_final=want)
     print("tsplit", B, T, H, sd, pu.check(d, out, fin, ref_out, ref_fin, label=f"tsplit B={B} T={T} H={H}"))
+
+
+def test_sequence_parallel_and_plain_paths_agree():
+    # kda_fwd runs the segmented path at this size; kda_fwd_ws (caller workspace) always
+    # runs the plain one.  Both must agree within the parity tolerances.
+    d = W.make_inputs(W.get("prefill_8k", B=1, T=8192, H=2, seed=21, state_dtype="fp32"))
+    e = pu.to_device(d)
+    o_seg, f_seg = pu.run_gpu(d)
+    out = torch.empty_like(e["q"])
+    fin = torch.empty((d["N"], d["H"], 128, 128), dtype=torch.float32, device="cuda")
+    ws = torch.empty(kda.workspace_bytes(d["N"], d["H"]), dtype=torch.uint8, device="cuda")
+    kda.kda_fwd(e["q"], e["k"], e["v"], e["g"], e["beta"], d["scale"], out, e["A_log"], e["dt_bias"],
+                d["lower_bound"], initial_state=e["initial_state"], final_state=fin, workspace=ws)
+    torch.cuda.synchronize()
+    assert kda.get_device_status() == kda.KDA_OK
+    mx, rl = pu.errors(o_seg.float().numpy(), out.cpu().float().numpy())
+    assert mx <= pu.OUT_MAX_ABS and rl <= pu.OUT_REL_L2, (mx, rl)
+    _, srl = pu.errors(f_seg.numpy(), fin.cpu().numpy())
+    assert srl <= pu.STATE_REL_L2["fp32"], srl
+
+
+@pytest.mark.parametrize("init,want_final", [("none", True), ("normal", False)])
+def test_sequence_parallel_state_options(init, want_final):
+    d = W.make_inputs(W.get("prefill_8k", B=1, T=8192, H=2, seed=22, state_dtype="fp32",
+                            initial_state=init))
+    out, fin = pu.run_gpu(d, want_final=want_final)
+    ref_out, ref_fin = pu.run_oracle(d, want_final=want_final)
+    pu.check(d, out, fin, ref_out, ref_fin, label=f"tsplit init={init} final={want_final}")
