@@ -104,7 +104,7 @@ kda_status launch(kda::Params &p, void *stream, int64_t tsplit = 0) {
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const cudaError_t e = tsplit > 0 ? kda::launch_tsplit(p, tsplit, p.ws, cs)
                           : p.T == 1 ? kda::launch_decode(p, cs)
-                          : p.T <= kda::kDecodeMaxT ? kda::launch_short(p, cs)
+                          : p.T <= kda::kShortMaxT ? kda::launch_short(p, cs)
                                                     : kda::launch_cluster(p, cs);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -124,7 +124,7 @@ kda_status kda_fwd(const void *q, const void *k, const void *v, const void *g, c
                              H, K, V, p);
     if (st != KDA_OK) return st;
     if (p.n_seqs == 0 || p.H == 0) return KDA_OK;
-    if (p.T <= kda::kDecodeMaxT) return launch(p, stream);   // the short-step kernel needs no workspace
+    if (p.T <= kda::kShortMaxT) return launch(p, stream);   // the short-step kernels need no workspace
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess) return KDA_ERR_CUDA;

@@ -49,15 +49,17 @@ __device__ __forceinline__ void seq_range(const Params &p, int64_t n, int64_t &b
     }
 }
 
-// Calls with at most this many token rows (T of the packed batch) run a
-// single-chunk kernel instead of the chunked cluster kernel: the token recurrence
-// for one row (decode), one 16-row chunk on warp-level tensor-core MMAs otherwise.
+// Calls with at most kShortMaxT token rows (T of the packed batch) run a kernel with
+// no workspace instead of the chunked cluster kernel: the token recurrence for one row
+// (decode; it handles up to kDecodeMaxT rows), blocks of 16 rows on warp-level
+// tensor-core MMAs otherwise.
 constexpr int64_t kDecodeMaxT = 16;
+constexpr int64_t kShortMaxT = 64;
 
 // Launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_cluster(const Params &p, cudaStream_t stream);   // chunked, needs p.ws
 cudaError_t launch_decode(const Params &p, cudaStream_t stream);    // token recurrence, T = 1
-cudaError_t launch_short(const Params &p, cudaStream_t stream);     // one chunk, 2 <= T <= 16
+cudaError_t launch_short(const Params &p, cudaStream_t stream);     // 16-row blocks, 2 <= T <= 64
 
 // Sequence-parallel prefill (fixed-length calls with few (sequence, head) units): each
 // sequence cut into P segments of at least kTsplitMinSeg tokens, P in [4, kTsplitMaxSeg].

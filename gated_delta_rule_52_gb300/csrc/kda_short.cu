@@ -1,9 +1,10 @@
-// KDA forward for short multi-token steps (2..16 token rows per call): the
-// sequence's tokens form one chunk of the UT/WY form, evaluated with warp-level
-// tensor-core MMAs (mma.sync m16n8k16, fp32 accumulation).
+// KDA forward for short multi-token steps (2..64 token rows per call): the
+// sequence's tokens form chunks of 16 of the UT/WY form, evaluated with warp-level
+// tensor-core MMAs (mma.sync m16n8k16, fp32 accumulation), the state kept in
+// registers from one 16-token block to the next.
 //
-// Per (sequence, head), L <= 16 tokens, G the cumulative log decay from the start
-// of the step (every exponent below is <= 0 except 2^-G, which stays below 2^116
+// Per (sequence, head) and 16-token block of L <= 16 tokens, G the cumulative log
+// decay from the start of the block (every exponent below is <= 0 except 2^-G, which stays below 2^116
 // since each token's log decay is >= the lower bound of -5):
 //   A[t,i] = beta_t sum_c k_hat[t,c] k_hat[i,c] 2^(G[t,c]-G[i,c])   (i < t)
 //   M[t,i] =        sum_c q_hat[t,c] k_hat[i,c] 2^(G[t,c]-G[i,c])   (i <= t)
@@ -107,6 +108,9 @@ __device__ __forceinline__ int tau(int c) {
     return (c & ~15) | (((c >> 1) & 1) << 3) | (((c >> 2) & 3) << 1) | (c & 1);
 }
 
+// kMulti: calls of more than 16 token rows (several blocks per unit); a separate
+// instantiation keeps the single-block case free of the block loop's registers.
+template <bool kMulti>
 __global__ void __launch_bounds__(NTS, 2) kda_short_kernel(Params p) {
     extern __shared__ __align__(16) unsigned char dsm[];
     ShortSmem &sm = *reinterpret_cast<ShortSmem *>(dsm);
@@ -116,19 +120,21 @@ __global__ void __launch_bounds__(NTS, 2) kda_short_kernel(Params p) {
     const int64_t units = p.n_seqs * p.H;
     const size_t selt = p.state_type == kStateBF16 ? 2 : 4;
 
-    // Token rows of unit u into the q, k, g, v tiles (16-byte asynchronous copies for
-    // rows t < L, zeros for the rest), committed as one cp.async group.
-    auto load_inputs = [&](int64_t u) {
+    // Token rows of 16-token block sc of unit u into the q, k, g, v tiles (16-byte
+    // asynchronous copies for the rows that exist, zeros for the rest), committed as
+    // one cp.async group.
+    auto load_inputs = [&](int64_t u, int sc) {
         const int64_t uh = u % p.H, un = u / p.H;
         int64_t ub, ut0, ulen;
         seq_range(p, un, ub, ut0, ulen);
+        const int64_t first = ut0 + LT * sc, rows = ulen - LT * sc;
         for (int i = tid; i < 4 * LT * 16; i += NTS) {
             const int x = i >> 8, t = (i >> 4) & 15, ch = i & 15;
             __nv_bfloat16 *dst = (x == 0 ? &sm.q[t][8 * ch] : x == 1 ? &sm.k[t][8 * ch]
                                   : x == 2 ? &sm.g[t][8 * ch] : &sm.v[t][8 * ch]);
-            if (t < ulen) {
+            if (t < rows) {
                 const __nv_bfloat16 *src = (x == 0 ? p.q : x == 1 ? p.k : x == 2 ? p.g : p.v) +
-                                           ((ub * p.T + ut0 + t) * p.H + uh) * DK + 8 * ch;
+                                           ((ub * p.T + first + t) * p.H + uh) * DK + 8 * ch;
                 cp_async16(dst, src);
             } else {
                 *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
@@ -137,17 +143,20 @@ __global__ void __launch_bounds__(NTS, 2) kda_short_kernel(Params p) {
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
 
-    // Persistent CTAs, unit after unit.  The next unit's token rows are copied in as
-    // soon as the current one's are dead (after its second barrier), and its state is
-    // prefetched into L2 at the same point.
-    if (blockIdx.x < units) load_inputs(blockIdx.x);
+    // Persistent CTAs, unit after unit; a unit's tokens in blocks of 16, the state in
+    // the z registers from the first block to the last.  The next block's (or the next
+    // unit's first block's) token rows are copied in as soon as the current ones are
+    // dead (after the second barrier), and the next unit's state is prefetched into L2
+    // at the same point.
+    if (blockIdx.x < units) load_inputs(blockIdx.x, 0);
     for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
         const int64_t h = unit % p.H, n = unit / p.H;
         int64_t b, t0, len64;
         seq_range(p, n, b, t0, len64);
-        const int L = (int)len64;   // <= 16 (the packed batch has at most 16 token rows)
-        const int64_t row_base = b * p.T + t0;
+        const int Lseq = (int)len64;   // <= 64 (the packed batch has at most 64 token rows)
+        const int nsub = kMulti && Lseq > LT ? (Lseq + LT - 1) / LT : 1;   // a zero-length unit: one empty block
         const size_t state_base = (size_t)(n * p.H + h) * DK * DK;
+        const int64_t row_first = b * p.T + t0;
 
         // ---- this warp's state rows as MMA accumulators: z[2i + r][e] (rows v0) and
         // z[2i + r][2 + e] (rows v0 + 8) hold channel 16 i + 4 qq + 2 r + e
@@ -177,230 +186,8 @@ __global__ void __launch_bounds__(NTS, 2) kda_short_kernel(Params p) {
             for (int j = 0; j < 16; ++j) z[j][0] = z[j][1] = z[j][2] = z[j][3] = 0.f;
         }
 
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
-        __syncthreads();
-
-        if (tid < DK) {
-            // ---- gate (log2 units) and its running sum G over the step, two channels
-            // per thread, tokens 8 hf .. 8 hf + 7 (the partner lane holds the other half);
-            // then the decayed tiles at the permuted columns
-            const int c0 = 2 * (tid >> 1), hf = tid & 1, col = tau(c0);
-            const float a2 = -__expf(p.A_log[h]) * kLog2e;
-            const float2 a2v = make_float2(a2, a2);
-            const float2 b2 = make_float2(a2 * p.dt_bias[h * DK + c0], a2 * p.dt_bias[h * DK + c0 + 1]);
-            const float lb2 = p.lower_bound * kLog2e;
-            float2 run = make_float2(0.f, 0.f), Gs[8];
-#pragma unroll
-            for (int tt = 0; tt < 8; ++tt) {
-                const int t = 8 * hf + tt;
-                if (t < L) {
-                    const float2 zz = fma2(bf16x2_to_f2(*reinterpret_cast<const uint32_t *>(&sm.g[t][c0])), a2v, b2);
-                    run.x += lb2 * __fdividef(1.f, 1.f + exp2f(zz.x));
-                    run.y += lb2 * __fdividef(1.f, 1.f + exp2f(zz.y));
-                }
-                Gs[tt] = run;
-            }
-            const float2 other = make_float2(__shfl_xor_sync(0xffffffffu, run.x, 1),
-                                             __shfl_xor_sync(0xffffffffu, run.y, 1));
-            const float2 GL = add2(run, other);
-            const float2 off = hf ? other : make_float2(0.f, 0.f);
-            const float2 eL = make_float2(exp2f(GL.x), exp2f(GL.y));
-#pragma unroll
-            for (int tt = 0; tt < 8; ++tt) {
-                const int t = 8 * hf + tt;
-                const float2 G = add2(Gs[tt], off);
-                const float2 e = make_float2(exp2f(G.x), exp2f(G.y));
-                const float2 ei = make_float2(exp2f(-G.x), exp2f(-G.y));
-                const float2 ec = mul2(eL, ei);   // 2^(G_L - G) <= 1
-                const float2 kx = bf16x2_to_f2(*reinterpret_cast<const uint32_t *>(&sm.k[t][c0]));
-                const float2 qx = bf16x2_to_f2(*reinterpret_cast<const uint32_t *>(&sm.q[t][c0]));
-                const float2 ke = mul2(kx, e), qe = mul2(qx, e), ki = mul2(kx, ei), kc = mul2(kx, ec);
-                *reinterpret_cast<uint32_t *>(&sm.kp[t][col]) = pack_bf16(ke.x, ke.y);
-                *reinterpret_cast<uint32_t *>(&sm.qp[t][col]) = pack_bf16(qe.x, qe.y);
-                *reinterpret_cast<uint32_t *>(&sm.kn[t][col]) = pack_bf16(ki.x, ki.y);
-                *reinterpret_cast<uint32_t *>(&sm.y[t][col]) = h2_bits(ke.x, ke.y);
-                *reinterpret_cast<uint32_t *>(&sm.y[LT + t][col]) = h2_bits(qe.x, qe.y);
-                *reinterpret_cast<uint32_t *>(&sm.kc[t][col]) = h2_bits(kc.x, kc.y);
-            }
-            if (hf == 0) *reinterpret_cast<float2 *>(&sm.gam[col]) = eL;
-        } else {
-            // ---- row norms of q and k (warps 4-7, four tokens each) and beta
-            const int w4 = warp - 4;
-#pragma unroll
-            for (int tt = 0; tt < 4; ++tt) {
-                const int t = 4 * w4 + tt;
-                const uint2 qw = *reinterpret_cast<const uint2 *>(&sm.q[t][4 * lane]);
-                const uint2 kw = *reinterpret_cast<const uint2 *>(&sm.k[t][4 * lane]);
-                float sq = 0.f, sk = 0.f;
-                const uint32_t qa[2] = {qw.x, qw.y}, ka[2] = {kw.x, kw.y};
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const float q0 = __uint_as_float(qa[i] << 16), q1 = __uint_as_float(qa[i] & 0xFFFF0000u);
-                    const float k0 = __uint_as_float(ka[i] << 16), k1 = __uint_as_float(ka[i] & 0xFFFF0000u);
-                    sq = fmaf(q0, q0, fmaf(q1, q1, sq));
-                    sk = fmaf(k0, k0, fmaf(k1, k1, sk));
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    sq += __shfl_xor_sync(0xffffffffu, sq, o);
-                    sk += __shfl_xor_sync(0xffffffffu, sk, o);
-                }
-                if (lane == 0) {
-                    sm.rq[t] = t < L ? rsqrtf(sq + 1e-6f) : 0.f;
-                    sm.rk[t] = t < L ? rsqrtf(sk + 1e-6f) : 0.f;
-                }
-            }
-            if (tid >= NTS - LT) {
-                const int t = tid - (NTS - LT);
-                const float bl = t < L ? __bfloat162float(p.beta[(row_base + t) * p.H + h]) : 0.f;
-                sm.beta[t] = t < L ? 1.f / (1.f + exp2f(-bl * kLog2e)) : 0.f;
-            }
-        }
-        __syncthreads();
-
-        // ---- A (warp 0) and M' (warp 1): raw [k 2^G | q 2^G] x (k 2^-G)^T in bf16
-        if (warp < 2) {
-            const __nv_bfloat16 (*lhs)[RS] = warp == 0 ? sm.kp : sm.qp;
-            float d[2][4] = {};
-#pragma unroll
-            for (int s = 0; s < DK / 16; ++s) {
-                uint32_t af[4], bf[4];
-                ldsm_x4(af, &lhs[(lane & 7) + 8 * ((lane >> 3) & 1)][16 * s + 8 * (lane >> 4)]);
-                ldsm_x4(bf, &sm.kn[(lane & 7) + 8 * (lane >> 4)][16 * s + 8 * ((lane >> 3) & 1)]);
-                mma_bf16x(d[0], af, bf[0], bf[1]);
-                mma_bf16x(d[1], af, bf[2], bf[3]);
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-                for (int hr = 0; hr < 2; ++hr) {
-                    const int t = gq + 8 * hr, i0 = 8 * nt + 2 * qq;
-                    if (warp == 0) {
-                        const float f = sm.beta[t] * sm.rk[t];
-                        sm.a[t][i0] = i0 < t ? f * sm.rk[i0] * d[nt][2 * hr] : 0.f;
-                        sm.a[t][i0 + 1] = i0 + 1 < t ? f * sm.rk[i0 + 1] * d[nt][2 * hr + 1] : 0.f;
-                    } else {
-                        const float f = sm.rq[t];
-                        *reinterpret_cast<uint32_t *>(&sm.mp[t][i0]) =
-                            h2_bits(i0 <= t ? f * d[nt][2 * hr] : 0.f, i0 + 1 <= t ? f * d[nt][2 * hr + 1] : 0.f);
-                    }
-                }
-            }
-            if (warp == 0) {
-                __syncwarp();
-                // T = (I + A)^-1 by forward substitution, lane = column j (right-looking:
-                // once x[r] is final it is added into every later row), then T' = T Diag(beta)
-                {
-                    const int j = lane & (LT - 1);   // lanes 16-31 repeat the columns, without stores
-                    float acc[LT], x[LT];
-#pragma unroll
-                    for (int r = 0; r < LT; ++r) acc[r] = 0.f;
-#pragma unroll
-                    for (int r = 0; r < LT; ++r) {
-                        x[r] = r == j ? 1.f : (r < j ? 0.f : -acc[r]);
-#pragma unroll
-                        for (int r2 = r + 1; r2 < LT; ++r2) acc[r2] = fmaf(sm.a[r2][r], x[r], acc[r2]);
-                    }
-                    const float bj = sm.beta[j];
-                    if (lane < LT) {
-#pragma unroll
-                        for (int r = 0; r < LT; ++r) sm.tp[r][j] = __float2half_rn(x[r] * bj);
-                    }
-                }
-            }
-        }
-
-        // ---- X = [k 2^G; q 2^G] S^T for this warp's 16 state rows (B from the z registers)
-        float x[2][2][4] = {};   // [k rows | q rows][column half][fragment]
-#pragma unroll
-        for (int s = 0; s < DK / 16; ++s) {
-            uint32_t a0[4], a1[4];
-            ldsm_x4(a0, &sm.y[(lane & 7) + 8 * ((lane >> 3) & 1)][16 * s + 8 * (lane >> 4)]);
-            ldsm_x4(a1, &sm.y[LT + (lane & 7) + 8 * ((lane >> 3) & 1)][16 * s + 8 * (lane >> 4)]);
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const uint32_t b0 = h2_bits(z[2 * s][2 * nt], z[2 * s][2 * nt + 1]);
-                const uint32_t b1 = h2_bits(z[2 * s + 1][2 * nt], z[2 * s + 1][2 * nt + 1]);
-                mma_f16(x[0][nt], a0, b0, b1);
-                mma_f16(x[1][nt], a1, b0, b1);
-            }
-        }
-        // R = V - K_hat Gamma S^T (rows scaled by 1/|k_t|), fp16, into this warp's tile
-        const float rk0 = sm.rk[gq], rk1 = sm.rk[gq + 8], rq0 = sm.rq[gq], rq1 = sm.rq[gq + 8];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int vl = 8 * nt + 2 * qq, vg = 16 * warp + vl;
-            const float2 va = bf16x2_to_f2(*reinterpret_cast<const uint32_t *>(&sm.v[gq][vg]));
-            const float2 vb = bf16x2_to_f2(*reinterpret_cast<const uint32_t *>(&sm.v[gq + 8][vg]));
-            *reinterpret_cast<uint32_t *>(&sm.wr[warp][gq][vl]) =
-                h2_bits(va.x - rk0 * x[0][nt][0], va.y - rk0 * x[0][nt][1]);
-            *reinterpret_cast<uint32_t *>(&sm.wr[warp][gq + 8][vl]) =
-                h2_bits(vb.x - rk1 * x[0][nt][2], vb.y - rk1 * x[0][nt][3]);
-            x[1][nt][0] *= rq0; x[1][nt][1] *= rq0; x[1][nt][2] *= rq1; x[1][nt][3] *= rq1;
-        }
-        __syncthreads();   // T', M' (warps 0, 1) and every warp's R are in shared memory
-        if (unit + gridDim.x < units) {   // q, k, g, v are dead: the next unit's rows go in
-            const int64_t nu = unit + gridDim.x;
-            load_inputs(nu);
-            if (tid == 0 && p.init)
-                prefetch_l2(static_cast<const unsigned char *>(p.init) + (size_t)nu * DK * DK * selt,
-                            (uint32_t)(DK * DK * selt));
-        }
-
-        // ---- U = T' R, U' = Diag(1/|k|) U (fp16)
-        {
-            uint32_t af[4], bf[4];
-            ldsm_x4(af, &sm.tp[(lane & 7) + 8 * ((lane >> 3) & 1)][8 * (lane >> 4)]);
-            ldsm_x4_t(bf, &sm.wr[warp][(lane & 7) + 8 * ((lane >> 3) & 1)][8 * (lane >> 4)]);
-            float u[2][4] = {};
-            mma_f16(u[0], af, bf[0], bf[1]);
-            mma_f16(u[1], af, bf[2], bf[3]);
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int vl = 8 * nt + 2 * qq;
-                *reinterpret_cast<uint32_t *>(&sm.wu[warp][gq][vl]) = h2_bits(rk0 * u[nt][0], rk0 * u[nt][1]);
-                *reinterpret_cast<uint32_t *>(&sm.wu[warp][gq + 8][vl]) = h2_bits(rk1 * u[nt][2], rk1 * u[nt][3]);
-            }
-        }
-        __syncwarp();
-
-        // ---- O = scale (Q_hat Gamma S^T + M' U') -> out
-        {
-            uint32_t af[4], bf[4];
-            ldsm_x4(af, &sm.mp[(lane & 7) + 8 * ((lane >> 3) & 1)][8 * (lane >> 4)]);
-            ldsm_x4_t(bf, &sm.wu[warp][(lane & 7) + 8 * ((lane >> 3) & 1)][8 * (lane >> 4)]);
-            mma_f16(x[1][0], af, bf[0], bf[1]);
-            mma_f16(x[1][1], af, bf[2], bf[3]);
-            const float sc = p.scale;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int vg = 16 * warp + 8 * nt + 2 * qq;
-                if (gq < L)
-                    *reinterpret_cast<uint32_t *>(p.out + ((row_base + gq) * p.H + h) * DK + vg) =
-                        pack_bf16(sc * x[1][nt][0], sc * x[1][nt][1]);
-                if (gq + 8 < L)
-                    *reinterpret_cast<uint32_t *>(p.out + ((row_base + gq + 8) * p.H + h) * DK + vg) =
-                        pack_bf16(sc * x[1][nt][2], sc * x[1][nt][3]);
-            }
-        }
-
-        // ---- S^T <- S^T Diag(Gamma_L) + U'^T (k 2^(G_L - G)), fp32 in the z registers
-        if (p.fin) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float2 gm = *reinterpret_cast<const float2 *>(&sm.gam[8 * j + 2 * qq]);
-                z[j][0] *= gm.x; z[j][1] *= gm.y; z[j][2] *= gm.x; z[j][3] *= gm.y;
-            }
-            uint32_t af[4];
-            // A = U'^T (rows v, columns t): transposed 8x8 blocks of the [t][v] tile
-            ldsm_x4_t(af, &sm.wu[warp][(lane & 7) + 8 * (lane >> 4)][8 * ((lane >> 3) & 1)]);
-#pragma unroll
-            for (int j = 0; j < 16; j += 2) {
-                uint32_t bf[4];
-                ldsm_x4_t(bf, &sm.kc[(lane & 7) + 8 * ((lane >> 3) & 1)][8 * j + 8 * (lane >> 4)]);
-                mma_f16(z[j], af, bf[0], bf[1]);
-                mma_f16(z[j + 1], af, bf[2], bf[3]);
-            }
+        // the z registers -> final_state (bf16 or fp32), 16-byte pieces as they were loaded
+        auto store_state = [&]() {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int c = 16 * i + 4 * qq;
@@ -418,7 +205,240 @@ __global__ void __launch_bounds__(NTS, 2) kda_short_kernel(Params p) {
                         make_float4(z[2 * i][2], z[2 * i][3], z[2 * i + 1][2], z[2 * i + 1][3]);
                 }
             }
-        }
+        };
+        for (int sc = 0; sc < nsub; ++sc) {
+            const int L = !kMulti ? Lseq : (Lseq - LT * sc < LT ? Lseq - LT * sc : LT);   // rows of this block
+            const int64_t row_base = row_first + LT * sc;
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+            __syncthreads();
+
+            if (tid < DK) {
+                // ---- gate (log2 units) and its running sum G over the step, two channels
+                // per thread, tokens 8 hf .. 8 hf + 7 (the partner lane holds the other half);
+                // then the decayed tiles at the permuted columns
+                const int c0 = 2 * (tid >> 1), hf = tid & 1, col = tau(c0);
+                const float a2 = -__expf(p.A_log[h]) * kLog2e;
+                const float2 a2v = make_float2(a2, a2);
+                const float2 b2 = make_float2(a2 * p.dt_bias[h * DK + c0], a2 * p.dt_bias[h * DK + c0 + 1]);
+                const float lb2 = p.lower_bound * kLog2e;
+                float2 run = make_float2(0.f, 0.f), Gs[8];
+#pragma unroll
+                for (int tt = 0; tt < 8; ++tt) {
+                    const int t = 8 * hf + tt;
+                    if (t < L) {
+                        const float2 zz = fma2(bf16x2_to_f2(*reinterpret_cast<const uint32_t *>(&sm.g[t][c0])), a2v, b2);
+                        run.x += lb2 * __fdividef(1.f, 1.f + exp2f(zz.x));
+                        run.y += lb2 * __fdividef(1.f, 1.f + exp2f(zz.y));
+                    }
+                    Gs[tt] = run;
+                }
+                const float2 other = make_float2(__shfl_xor_sync(0xffffffffu, run.x, 1),
+                                                 __shfl_xor_sync(0xffffffffu, run.y, 1));
+                const float2 GL = add2(run, other);
+                const float2 off = hf ? other : make_float2(0.f, 0.f);
+                const float2 eL = make_float2(exp2f(GL.x), exp2f(GL.y));
+#pragma unroll
+                for (int tt = 0; tt < 8; ++tt) {
+                    const int t = 8 * hf + tt;
+                    const float2 G = add2(Gs[tt], off);
+                    const float2 e = make_float2(exp2f(G.x), exp2f(G.y));
+                    const float2 ei = make_float2(exp2f(-G.x), exp2f(-G.y));
+                    const float2 ec = mul2(eL, ei);   // 2^(G_L - G) <= 1
+                    const float2 kx = bf16x2_to_f2(*reinterpret_cast<const uint32_t *>(&sm.k[t][c0]));
+                    const float2 qx = bf16x2_to_f2(*reinterpret_cast<const uint32_t *>(&sm.q[t][c0]));
+                    const float2 ke = mul2(kx, e), qe = mul2(qx, e), ki = mul2(kx, ei), kc = mul2(kx, ec);
+                    *reinterpret_cast<uint32_t *>(&sm.kp[t][col]) = pack_bf16(ke.x, ke.y);
+                    *reinterpret_cast<uint32_t *>(&sm.qp[t][col]) = pack_bf16(qe.x, qe.y);
+                    *reinterpret_cast<uint32_t *>(&sm.kn[t][col]) = pack_bf16(ki.x, ki.y);
+                    *reinterpret_cast<uint32_t *>(&sm.y[t][col]) = h2_bits(ke.x, ke.y);
+                    *reinterpret_cast<uint32_t *>(&sm.y[LT + t][col]) = h2_bits(qe.x, qe.y);
+                    *reinterpret_cast<uint32_t *>(&sm.kc[t][col]) = h2_bits(kc.x, kc.y);
+                }
+                if (hf == 0) *reinterpret_cast<float2 *>(&sm.gam[col]) = eL;
+            } else {
+                // ---- row norms of q and k (warps 4-7, four tokens each) and beta
+                const int w4 = warp - 4;
+#pragma unroll
+                for (int tt = 0; tt < 4; ++tt) {
+                    const int t = 4 * w4 + tt;
+                    const uint2 qw = *reinterpret_cast<const uint2 *>(&sm.q[t][4 * lane]);
+                    const uint2 kw = *reinterpret_cast<const uint2 *>(&sm.k[t][4 * lane]);
+                    float sq = 0.f, sk = 0.f;
+                    const uint32_t qa[2] = {qw.x, qw.y}, ka[2] = {kw.x, kw.y};
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const float q0 = __uint_as_float(qa[i] << 16), q1 = __uint_as_float(qa[i] & 0xFFFF0000u);
+                        const float k0 = __uint_as_float(ka[i] << 16), k1 = __uint_as_float(ka[i] & 0xFFFF0000u);
+                        sq = fmaf(q0, q0, fmaf(q1, q1, sq));
+                        sk = fmaf(k0, k0, fmaf(k1, k1, sk));
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                        sk += __shfl_xor_sync(0xffffffffu, sk, o);
+                    }
+                    if (lane == 0) {
+                        sm.rq[t] = t < L ? rsqrtf(sq + 1e-6f) : 0.f;
+                        sm.rk[t] = t < L ? rsqrtf(sk + 1e-6f) : 0.f;
+                    }
+                }
+                if (tid >= NTS - LT) {
+                    const int t = tid - (NTS - LT);
+                    const float bl = t < L ? __bfloat162float(p.beta[(row_base + t) * p.H + h]) : 0.f;
+                    sm.beta[t] = t < L ? 1.f / (1.f + exp2f(-bl * kLog2e)) : 0.f;
+                }
+            }
+            __syncthreads();
+
+            // ---- A (warp 0) and M' (warp 1): raw [k 2^G | q 2^G] x (k 2^-G)^T in bf16
+            if (warp < 2) {
+                const __nv_bfloat16 (*lhs)[RS] = warp == 0 ? sm.kp : sm.qp;
+                float d[2][4] = {};
+#pragma unroll
+                for (int s = 0; s < DK / 16; ++s) {
+                    uint32_t af[4], bf[4];
+                    ldsm_x4(af, &lhs[(lane & 7) + 8 * ((lane >> 3) & 1)][16 * s + 8 * (lane >> 4)]);
+                    ldsm_x4(bf, &sm.kn[(lane & 7) + 8 * (lane >> 4)][16 * s + 8 * ((lane >> 3) & 1)]);
+                    mma_bf16x(d[0], af, bf[0], bf[1]);
+                    mma_bf16x(d[1], af, bf[2], bf[3]);
+                }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                    for (int hr = 0; hr < 2; ++hr) {
+                        const int t = gq + 8 * hr, i0 = 8 * nt + 2 * qq;
+                        if (warp == 0) {
+                            const float f = sm.beta[t] * sm.rk[t];
+                            sm.a[t][i0] = i0 < t ? f * sm.rk[i0] * d[nt][2 * hr] : 0.f;
+                            sm.a[t][i0 + 1] = i0 + 1 < t ? f * sm.rk[i0 + 1] * d[nt][2 * hr + 1] : 0.f;
+                        } else {
+                            const float f = sm.rq[t];
+                            *reinterpret_cast<uint32_t *>(&sm.mp[t][i0]) =
+                                h2_bits(i0 <= t ? f * d[nt][2 * hr] : 0.f, i0 + 1 <= t ? f * d[nt][2 * hr + 1] : 0.f);
+                        }
+                    }
+                }
+                if (warp == 0) {
+                    __syncwarp();
+                    // T = (I + A)^-1 by forward substitution, lane = column j (right-looking:
+                    // once x[r] is final it is added into every later row), then T' = T Diag(beta)
+                    {
+                        const int j = lane & (LT - 1);   // lanes 16-31 repeat the columns, without stores
+                        float acc[LT], x[LT];
+#pragma unroll
+                        for (int r = 0; r < LT; ++r) acc[r] = 0.f;
+#pragma unroll
+                        for (int r = 0; r < LT; ++r) {
+                            x[r] = r == j ? 1.f : (r < j ? 0.f : -acc[r]);
+#pragma unroll
+                            for (int r2 = r + 1; r2 < LT; ++r2) acc[r2] = fmaf(sm.a[r2][r], x[r], acc[r2]);
+                        }
+                        const float bj = sm.beta[j];
+                        if (lane < LT) {
+#pragma unroll
+                            for (int r = 0; r < LT; ++r) sm.tp[r][j] = __float2half_rn(x[r] * bj);
+                        }
+                    }
+                }
+            }
+
+            // ---- X = [k 2^G; q 2^G] S^T for this warp's 16 state rows (B from the z registers)
+            float x[2][2][4] = {};   // [k rows | q rows][column half][fragment]
+#pragma unroll
+            for (int s = 0; s < DK / 16; ++s) {
+                uint32_t a0[4], a1[4];
+                ldsm_x4(a0, &sm.y[(lane & 7) + 8 * ((lane >> 3) & 1)][16 * s + 8 * (lane >> 4)]);
+                ldsm_x4(a1, &sm.y[LT + (lane & 7) + 8 * ((lane >> 3) & 1)][16 * s + 8 * (lane >> 4)]);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const uint32_t b0 = h2_bits(z[2 * s][2 * nt], z[2 * s][2 * nt + 1]);
+                    const uint32_t b1 = h2_bits(z[2 * s + 1][2 * nt], z[2 * s + 1][2 * nt + 1]);
+                    mma_f16(x[0][nt], a0, b0, b1);
+                    mma_f16(x[1][nt], a1, b0, b1);
+                }
+            }
+            // R = V - K_hat Gamma S^T (rows scaled by 1/|k_t|), fp16, into this warp's tile
+            const float rk0 = sm.rk[gq], rk1 = sm.rk[gq + 8], rq0 = sm.rq[gq], rq1 = sm.rq[gq + 8];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int vl = 8 * nt + 2 * qq, vg = 16 * warp + vl;
+                const float2 va = bf16x2_to_f2(*reinterpret_cast<const uint32_t *>(&sm.v[gq][vg]));
+                const float2 vb = bf16x2_to_f2(*reinterpret_cast<const uint32_t *>(&sm.v[gq + 8][vg]));
+                *reinterpret_cast<uint32_t *>(&sm.wr[warp][gq][vl]) =
+                    h2_bits(va.x - rk0 * x[0][nt][0], va.y - rk0 * x[0][nt][1]);
+                *reinterpret_cast<uint32_t *>(&sm.wr[warp][gq + 8][vl]) =
+                    h2_bits(vb.x - rk1 * x[0][nt][2], vb.y - rk1 * x[0][nt][3]);
+                x[1][nt][0] *= rq0; x[1][nt][1] *= rq0; x[1][nt][2] *= rq1; x[1][nt][3] *= rq1;
+            }
+            __syncthreads();   // T', M' (warps 0, 1) and every warp's R are in shared memory
+            if (sc + 1 < nsub) {   // q, k, g, v are dead: the next block's rows go in
+                load_inputs(unit, sc + 1);
+            } else if (unit + gridDim.x < units) {   // or the next unit's first block
+                const int64_t nu = unit + gridDim.x;
+                load_inputs(nu, 0);
+                if (tid == 0 && p.init)
+                    prefetch_l2(static_cast<const unsigned char *>(p.init) + (size_t)nu * DK * DK * selt,
+                                (uint32_t)(DK * DK * selt));
+            }
+
+            // ---- U = T' R, U' = Diag(1/|k|) U (fp16)
+            {
+                uint32_t af[4], bf[4];
+                ldsm_x4(af, &sm.tp[(lane & 7) + 8 * ((lane >> 3) & 1)][8 * (lane >> 4)]);
+                ldsm_x4_t(bf, &sm.wr[warp][(lane & 7) + 8 * ((lane >> 3) & 1)][8 * (lane >> 4)]);
+                float u[2][4] = {};
+                mma_f16(u[0], af, bf[0], bf[1]);
+                mma_f16(u[1], af, bf[2], bf[3]);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int vl = 8 * nt + 2 * qq;
+                    *reinterpret_cast<uint32_t *>(&sm.wu[warp][gq][vl]) = h2_bits(rk0 * u[nt][0], rk0 * u[nt][1]);
+                    *reinterpret_cast<uint32_t *>(&sm.wu[warp][gq + 8][vl]) = h2_bits(rk1 * u[nt][2], rk1 * u[nt][3]);
+                }
+            }
+            __syncwarp();
+
+            // ---- O = scale (Q_hat Gamma S^T + M' U') -> out
+            {
+                uint32_t af[4], bf[4];
+                ldsm_x4(af, &sm.mp[(lane & 7) + 8 * ((lane >> 3) & 1)][8 * (lane >> 4)]);
+                ldsm_x4_t(bf, &sm.wu[warp][(lane & 7) + 8 * ((lane >> 3) & 1)][8 * (lane >> 4)]);
+                mma_f16(x[1][0], af, bf[0], bf[1]);
+                mma_f16(x[1][1], af, bf[2], bf[3]);
+                const float sc = p.scale;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int vg = 16 * warp + 8 * nt + 2 * qq;
+                    if (gq < L)
+                        *reinterpret_cast<uint32_t *>(p.out + ((row_base + gq) * p.H + h) * DK + vg) =
+                            pack_bf16(sc * x[1][nt][0], sc * x[1][nt][1]);
+                    if (gq + 8 < L)
+                        *reinterpret_cast<uint32_t *>(p.out + ((row_base + gq + 8) * p.H + h) * DK + vg) =
+                            pack_bf16(sc * x[1][nt][2], sc * x[1][nt][3]);
+                }
+            }
+
+            // ---- S^T <- S^T Diag(Gamma_L) + U'^T (k 2^(G_L - G)), fp32 in the z registers
+            if (p.fin || sc + 1 < nsub) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float2 gm = *reinterpret_cast<const float2 *>(&sm.gam[8 * j + 2 * qq]);
+                    z[j][0] *= gm.x; z[j][1] *= gm.y; z[j][2] *= gm.x; z[j][3] *= gm.y;
+                }
+                uint32_t af[4];
+                // A = U'^T (rows v, columns t): transposed 8x8 blocks of the [t][v] tile
+                ldsm_x4_t(af, &sm.wu[warp][(lane & 7) + 8 * (lane >> 4)][8 * ((lane >> 3) & 1)]);
+#pragma unroll
+                for (int j = 0; j < 16; j += 2) {
+                    uint32_t bf[4];
+                    ldsm_x4_t(bf, &sm.kc[(lane & 7) + 8 * ((lane >> 3) & 1)][8 * j + 8 * (lane >> 4)]);
+                    mma_f16(z[j], af, bf[0], bf[1]);
+                    mma_f16(z[j + 1], af, bf[2], bf[3]);
+                }
+                if (!kMulti && p.fin) store_state();
+            }
+        }   // blocks of the unit
+        if (kMulti && p.fin) store_state();
     }
 }
 
@@ -428,13 +448,18 @@ cudaError_t launch_short(const Params &p, cudaStream_t stream) {
     const int64_t units = p.n_seqs * p.H;
     if (units == 0) return cudaSuccess;
     const int bytes = (int)sizeof(ShortSmem);
-    cudaError_t e = cudaFuncSetAttribute(kda_short_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    const bool multi = p.T > LT;
+    cudaError_t e = multi ? cudaFuncSetAttribute(kda_short_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
+                          : cudaFuncSetAttribute(kda_short_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const int64_t grid = units < 2 * (int64_t)sms ? units : 2 * (int64_t)sms;   // two CTAs per SM
-    kda_short_kernel<<<(unsigned)grid, NTS, bytes, stream>>>(p);
+    if (multi)
+        kda_short_kernel<true><<<(unsigned)grid, NTS, bytes, stream>>>(p);
+    else
+        kda_short_kernel<false><<<(unsigned)grid, NTS, bytes, stream>>>(p);
     return cudaGetLastError();
 }
 

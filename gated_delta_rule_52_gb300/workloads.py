@@ -88,6 +88,11 @@ WORKLOADS = {
     "decode_16": Workload(
         name="decode_16", B=64, T=16, H=64, seed=6, state_dtype="bf16", initial_state="normal",
         description="B=64 T=16 H=64 (16-token step); bf16 state N(0,0.02)"),
+    # A 64-token step (e.g. verifying a speculative draft, or a small prefill chunk) for
+    # 64 sequences: the 16-row-block kernel, four blocks per (sequence, head).
+    "step_64": Workload(
+        name="step_64", B=64, T=64, H=64, seed=8, state_dtype="bf16", initial_state="normal",
+        description="B=64 T=64 H=64 (64-token step); bf16 state N(0,0.02)"),
     # A long prefill with few heads (e.g. 8 heads on one GPU of a tensor-parallel group):
     # 8 (sequence, head) units, the sequence-parallel path.
     "prefill_64k_h8": Workload(

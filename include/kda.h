@@ -89,7 +89,7 @@ typedef enum {
  * per-chunk operands that move between the two CTAs of a cluster through L2),
  * taken stream-ordered on `stream` from a memory pool that libkda.so creates
  * once per device and keeps mapped, and released on `stream` after the kernel.
- * Calls of at most 16 token rows need no workspace.  A fixed-length call
+ * Calls of at most 64 token rows need no workspace.  A fixed-length call
  * (cu_seqlens == NULL) whose N * H (sequence, head) units would leave most of the
  * GPU idle, with T >= 8192, runs the sequence-parallel path: each sequence is cut
  * into P >= 4 segments of at least 2048 tokens, whose affine state maps are joined

@@ -81,12 +81,12 @@ def test_max_over_ranks_without_group_is_identity():
 
 def test_kernel_of_follows_the_packed_token_count():
     # the kernel label and stored-traffic lookup follow the dispatch of kda_fwd:
-    # one row -> token recurrence, up to 16 -> single chunk, more -> cluster kernel
+    # one row -> token recurrence, up to 64 -> 16-row blocks, more -> cluster kernel
     import bench
     from gated_delta_rule_52_gb300 import workloads as W
     assert bench.kernel_of(1) == "decode"
-    assert bench.kernel_of(2) == "short" and bench.kernel_of(16) == "short"
-    assert bench.kernel_of(17) == "cluster"
+    assert bench.kernel_of(2) == "short" and bench.kernel_of(64) == "short"
+    assert bench.kernel_of(65) == "cluster"
     d = W.make_inputs(W.get("varlen_ragged", H=1, seqlens=(40, 30)))
     assert bench.kernel_of(d["T"]) == "cluster"   # the ragged workload's T is the packed total
     for k in bench.KERNEL_SOURCES:

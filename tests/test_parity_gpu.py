@@ -208,7 +208,7 @@ def test_caller_workspace_entry_point():
     assert ei.value.status == kda.KDA_ERR_VALUE
 
 
-# ---- short steps (T <= 16 token rows): the token-recurrence kernel
+# ---- short steps (T <= 64 token rows): the token recurrence (T = 1) and the 16-row-block kernel
 
 @pytest.mark.parametrize("T,sd,init", [(1, "fp32", "normal"), (3, "bf16", "normal"),
                                        (16, "fp32", "none"), (16, "bf16", "normal"), (5, None, "none")])
@@ -241,16 +241,36 @@ def test_short_step_full_size_sampled(name):
 
 
 def test_short_and_chunked_paths_agree_at_the_threshold():
-    # T = 16 runs the token recurrence, T = 17 the chunked kernel; their first 16
-    # outputs and (chained) states must agree within the parity tolerances.
-    d17 = W.make_inputs(W.get("decode", B=3, T=17, H=2))
-    d16 = dict(d17, T=16, q=d17["q"][:, :16], k=d17["k"][:, :16], v=d17["v"][:, :16],
-               g=d17["g"][:, :16], beta=d17["beta"][:, :16])
-    d16 = {kk: (vv.contiguous() if torch.is_tensor(vv) else vv) for kk, vv in d16.items()}
-    o17, _ = pu.run_gpu(d17)
-    o16, _ = pu.run_gpu(d16)
-    mx, rl = pu.errors(o16.float().numpy(), o17[:, :16].float().numpy())
+    # T = 64 runs the 16-row-block kernel, T = 65 the chunked kernel; their first 64
+    # outputs must agree within the parity tolerances.
+    d65 = W.make_inputs(W.get("decode", B=3, T=65, H=2))
+    d64 = dict(d65, T=64, q=d65["q"][:, :64], k=d65["k"][:, :64], v=d65["v"][:, :64],
+               g=d65["g"][:, :64], beta=d65["beta"][:, :64])
+    d64 = {kk: (vv.contiguous() if torch.is_tensor(vv) else vv) for kk, vv in d64.items()}
+    o65, _ = pu.run_gpu(d65)
+    o64, _ = pu.run_gpu(d64)
+    mx, rl = pu.errors(o64.float().numpy(), o65[:, :64].float().numpy())
     assert mx <= pu.OUT_MAX_ABS and rl <= pu.OUT_REL_L2, (mx, rl)
+
+
+@pytest.mark.parametrize("T,sd,init", [(17, "fp32", "normal"), (33, "bf16", "normal"),
+                                       (64, "fp32", "none"), (48, None, "none")])
+def test_multi_block_steps_all_elements(T, sd, init):
+    # 17..64 token rows: the state stays in registers across the 16-row blocks
+    d = W.make_inputs(W.get("decode", B=4, T=T, H=3, state_dtype=sd, initial_state=init, seed=30 + T))
+    out, fin = pu.run_gpu(d, want_final=sd is not None)
+    ref_out, ref_fin = pu.run_oracle(d, want_final=sd is not None)
+    print("multi-block", T, sd, init, pu.check(d, out, fin, ref_out, ref_fin, label=f"multi-block T={T}"))
+
+
+def test_multi_block_varlen_with_empty_sequences():
+    d = W.make_inputs(W.get("varlen_ragged", H=2, seqlens=(30, 0, 1, 17, 0, 16)))
+    assert 16 < d["T"] <= 64
+    out, fin = pu.run_gpu(d)
+    ref_out, ref_fin = pu.run_oracle(d)
+    pu.check(d, out, fin, ref_out, ref_fin, label="multi-block varlen")
+    for n in (1, 4):
+        torch.testing.assert_close(fin[n], d["initial_state"][n].to(fin.dtype), rtol=0, atol=0)
 
 
 # ---- seeded random configurations: shapes, lengths (empty, short, chunk-crossing),
