@@ -21,7 +21,7 @@
 // the norms and beta,
 // A and M from one bf16 MMA each (raw q/k times 2^G against k times 2^-G, the
 // norms applied in fp32 afterwards, as in the chunked kernel), and the 16 x 16
-// inverse by forward substitution.  CTAs are persistent (two per SM): a unit's
+// inverse by forward substitution (on warp 2, after its own products).  CTAs are persistent (two per SM): a unit's
 // token rows are copied in while the previous unit finishes, and its state is
 // prefetched into L2 at the same time.  The row norms of k are folded into U
 // (U' = Diag(1/|k|) U) and out of M and Kbar, so every fp16 tile is the raw input
@@ -318,30 +318,11 @@ __global__ void __launch_bounds__(NTS, 2) kda_short_kernel(Params p) {
                         }
                     }
                 }
-                if (warp == 0) {
+                if (warp == 0) {   // A is in shared memory: release warp 2 (no wait here)
                     __syncwarp();
-                    // T = (I + A)^-1 by forward substitution, lane = column j (right-looking:
-                    // once x[r] is final it is added into every later row), then T' = T Diag(beta)
-                    {
-                        const int j = lane & (LT - 1);   // lanes 16-31 repeat the columns, without stores
-                        float acc[LT], x[LT];
-#pragma unroll
-                        for (int r = 0; r < LT; ++r) acc[r] = 0.f;
-#pragma unroll
-                        for (int r = 0; r < LT; ++r) {
-                            x[r] = r == j ? 1.f : (r < j ? 0.f : -acc[r]);
-#pragma unroll
-                            for (int r2 = r + 1; r2 < LT; ++r2) acc[r2] = fmaf(sm.a[r2][r], x[r], acc[r2]);
-                        }
-                        const float bj = sm.beta[j];
-                        if (lane < LT) {
-#pragma unroll
-                            for (int r = 0; r < LT; ++r) sm.tp[r][j] = __float2half_rn(x[r] * bj);
-                        }
-                    }
+                    asm volatile("bar.arrive 1, 64;" ::: "memory");
                 }
             }
-
             // ---- X = [k 2^G; q 2^G] S^T for this warp's 16 state rows (B from the z registers)
             float x[2][2][4] = {};   // [k rows | q rows][column half][fragment]
 #pragma unroll
@@ -370,7 +351,28 @@ __global__ void __launch_bounds__(NTS, 2) kda_short_kernel(Params p) {
                     h2_bits(vb.x - rk1 * x[0][nt][2], vb.y - rk1 * x[0][nt][3]);
                 x[1][nt][0] *= rq0; x[1][nt][1] *= rq0; x[1][nt][2] *= rq1; x[1][nt][3] *= rq1;
             }
-            __syncthreads();   // T', M' (warps 0, 1) and every warp's R are in shared memory
+            if (warp == 2) {
+                // T = (I + A)^-1 by forward substitution, lane = column j (right-looking:
+                // once x[r] is final it is added into every later row), then T' = T Diag(beta).
+                // On warp 2 after its own products, once warp 0 has A in shared memory.
+                asm volatile("bar.sync 1, 64;" ::: "memory");
+                const int j = lane & (LT - 1);   // lanes 16-31 repeat the columns, without stores
+                float acc[LT], xs[LT];
+#pragma unroll
+                for (int r = 0; r < LT; ++r) acc[r] = 0.f;
+#pragma unroll
+                for (int r = 0; r < LT; ++r) {
+                    xs[r] = r == j ? 1.f : (r < j ? 0.f : -acc[r]);
+#pragma unroll
+                    for (int r2 = r + 1; r2 < LT; ++r2) acc[r2] = fmaf(sm.a[r2][r], xs[r], acc[r2]);
+                }
+                const float bj = sm.beta[j];
+                if (lane < LT) {
+#pragma unroll
+                    for (int r = 0; r < LT; ++r) sm.tp[r][j] = __float2half_rn(xs[r] * bj);
+                }
+            }
+            __syncthreads();   // T' (warp 2), M' (warp 1) and every warp's R are in shared memory
             if (sc + 1 < nsub) {   // q, k, g, v are dead: the next block's rows go in
                 load_inputs(unit, sc + 1);
             } else if (unit + gridDim.x < units) {   // or the next unit's first block
