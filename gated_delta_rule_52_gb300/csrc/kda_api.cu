@@ -102,10 +102,21 @@ kda_status launch(kda::Params &p, void *stream, int64_t tsplit = 0) {
         return KDA_ERR_CUDA;
     p.err = err;
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = tsplit > 0 ? kda::launch_tsplit(p, tsplit, p.ws, cs)
-                          : p.T == 1 ? kda::launch_decode(p, cs)
-                          : p.T <= kda::kShortMaxT ? kda::launch_short(p, cs)
-                                                    : kda::launch_cluster(p, cs);
+    cudaError_t e;
+    if (tsplit > 0) {
+        e = kda::launch_tsplit(p, tsplit, p.ws, cs);
+    } else if (p.T == 1) {
+        e = kda::launch_decode(p, cs);
+    } else if (p.T <= kda::kShortMaxT) {
+        e = kda::launch_short(p, cs);
+    } else if (p.cu_seqlens && p.T <= kda::kMixedMaxAvg * p.n_seqs) {
+        // mostly short sequences: each kernel on its own sequences, one after the other
+        p.mixed = 1;
+        e = kda::launch_short(p, cs);
+        if (e == cudaSuccess) e = kda::launch_cluster(p, cs);
+    } else {
+        e = kda::launch_cluster(p, cs);
+    }
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -118,7 +129,7 @@ kda_status kda_fwd(const void *q, const void *k, const void *v, const void *g, c
                    float lower_bound, const void *initial_state, void *final_state,
                    int state_dtype, const int64_t *cu_seqlens, int64_t num_seqs, int64_t B,
                    int64_t T, int64_t H, int64_t K, int64_t V, void *stream) {
-    kda::Params p;
+    kda::Params p{};   // every field zero until validate() fills it
     kda_status st = validate(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound,
                              initial_state, final_state, state_dtype, cu_seqlens, num_seqs, B, T,
                              H, K, V, p);
@@ -150,7 +161,7 @@ kda_status kda_fwd_ws(const void *q, const void *k, const void *v, const void *g
                       int state_dtype, const int64_t *cu_seqlens, int64_t num_seqs, int64_t B,
                       int64_t T, int64_t H, int64_t K, int64_t V, void *workspace,
                       size_t workspace_bytes, void *stream) {
-    kda::Params p;
+    kda::Params p{};   // every field zero until validate() fills it
     kda_status st = validate(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound,
                              initial_state, final_state, state_dtype, cu_seqlens, num_seqs, B, T,
                              H, K, V, p);

@@ -1020,6 +1020,7 @@ kda_cluster_kernel(const __grid_constant__ TmaMaps maps, Params p) {
     }
     int64_t b, t0, len;
     seq_range(p, n, b, t0, len);
+    if (p.mixed && len <= kShortMaxT) return;   // the short-step kernel's (both CTAs agree)
     const int64_t row_base = b * p.T + t0;
     const int nchunks = (int)((len + C - 1) / C);
 

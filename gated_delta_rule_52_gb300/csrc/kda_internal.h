@@ -33,6 +33,8 @@ struct Params {
     int64_t B, T, H;
     int *err;           // device error word (bounded waits that give up set it)
     unsigned char *ws;  // workspace: kWsBytesPerUnit bytes per (sequence, head), 16-byte aligned
+    int mixed;          // varlen call split by length: the short-step kernel takes the
+                        // sequences of at most kShortMaxT tokens, the cluster kernel the rest
 };
 
 // Token range of sequence n: packed batch row `b`, first token `t0`, `len` tokens.
@@ -55,6 +57,9 @@ __device__ __forceinline__ void seq_range(const Params &p, int64_t n, int64_t &b
 // tensor-core MMAs otherwise.
 constexpr int64_t kDecodeMaxT = 16;
 constexpr int64_t kShortMaxT = 64;
+// Varlen calls with more rows but at most this many per sequence on average run both
+// kernels, each on its own sequences (Params::mixed).
+constexpr int64_t kMixedMaxAvg = 256;
 
 // Launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_cluster(const Params &p, cudaStream_t stream);   // chunked, needs p.ws

@@ -148,8 +148,20 @@ __global__ void __launch_bounds__(NTS, 2) kda_short_kernel(Params p) {
     // unit's first block's) token rows are copied in as soon as the current ones are
     // dead (after the second barrier), and the next unit's state is prefetched into L2
     // at the same point.
-    if (blockIdx.x < units) load_inputs(blockIdx.x, 0);
-    for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
+    // In a mixed-length call the units longer than kShortMaxT tokens are the cluster
+    // kernel's: this kernel steps over them (the next unit it takes, from u on).
+    auto next_unit = [&](int64_t u) -> int64_t {
+        if (!p.mixed) return u;
+        for (; u < units; u += gridDim.x) {
+            int64_t ub, ut0, ulen;
+            seq_range(p, u / p.H, ub, ut0, ulen);
+            if (ulen <= kShortMaxT) break;
+        }
+        return u;
+    };
+    const int64_t first_unit = next_unit(blockIdx.x);
+    if (first_unit < units) load_inputs(first_unit, 0);
+    for (int64_t unit = first_unit; unit < units; unit = next_unit(unit + gridDim.x)) {
         const int64_t h = unit % p.H, n = unit / p.H;
         int64_t b, t0, len64;
         seq_range(p, n, b, t0, len64);
@@ -375,8 +387,8 @@ __global__ void __launch_bounds__(NTS, 2) kda_short_kernel(Params p) {
             __syncthreads();   // T' (warp 2), M' (warp 1) and every warp's R are in shared memory
             if (sc + 1 < nsub) {   // q, k, g, v are dead: the next block's rows go in
                 load_inputs(unit, sc + 1);
-            } else if (unit + gridDim.x < units) {   // or the next unit's first block
-                const int64_t nu = unit + gridDim.x;
+            } else if (next_unit(unit + gridDim.x) < units) {   // or the next unit's first block
+                const int64_t nu = next_unit(unit + gridDim.x);
                 load_inputs(nu, 0);
                 if (tid == 0 && p.init)
                     prefetch_l2(static_cast<const unsigned char *>(p.init) + (size_t)nu * DK * DK * selt,

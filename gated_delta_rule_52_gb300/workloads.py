@@ -93,6 +93,12 @@ WORKLOADS = {
     "step_64": Workload(
         name="step_64", B=64, T=64, H=64, seed=8, state_dtype="bf16", initial_state="normal",
         description="B=64 T=64 H=64 (64-token step); bf16 state N(0,0.02)"),
+    # A serving batch of short prompts: 512 sequences of 1..64 tokens (log-uniform), the
+    # 16-row-block kernel for every one of them.
+    "varlen_short": Workload(
+        name="varlen_short", B=1, T=0, H=32, seed=9, varlen="ragged", n_seqs=512,
+        ragged_len_range=(1, 64), state_dtype="fp32", initial_state="normal",
+        description="512 log-uniform lengths in [1,64] H=32; fp32 state N(0,0.02)"),
     # A long prefill with few heads (e.g. 8 heads on one GPU of a tensor-parallel group):
     # 8 (sequence, head) units, the sequence-parallel path.
     "prefill_64k_h8": Workload(

@@ -177,10 +177,12 @@ def test_binding_rejects_bad_tensors():
 
 def test_many_short_sequences_longest_first_order():
     # More clusters than SMs, zero-length and single-token sequences mixed in:
-    # every sequence must land on exactly one cluster whatever the order.
+    # every sequence must land on exactly one cluster whatever the order.  Three long
+    # sequences keep the average above 256 rows, so the cluster kernel takes them all.
     r = np.random.default_rng(7)
     lens = [int(x) for x in r.integers(0, 90, 300)]
     lens[0], lens[5], lens[-1] = 0, 1, 200
+    lens[-2], lens[-3], lens[-4] = 30000, 30000, 20000
     d = W.make_inputs(W.get("varlen_ragged", H=1, seqlens=tuple(lens)))
     out, fin = pu.run_gpu(d)
     ref_out, ref_fin = pu.run_oracle(d)
@@ -350,3 +352,20 @@ def test_sequence_parallel_state_options(init, want_final):
     out, fin = pu.run_gpu(d, want_final=want_final)
     ref_out, ref_fin = pu.run_oracle(d, want_final=want_final)
     pu.check(d, out, fin, ref_out, ref_fin, label=f"tsplit init={init} final={want_final}")
+
+
+# ---- varlen batches of mostly short sequences (packed T > 64, at most 256 rows per
+# sequence on average): the 16-row-block kernel takes the sequences of at most 64 tokens,
+# the cluster kernel the rest
+
+@pytest.mark.parametrize("seqlens,sd", [((3, 40, 64, 65, 0, 200, 17, 1, 50, 16, 33), "bf16"),
+                                        (tuple(range(1, 65, 3)), "fp32")])
+def test_mixed_length_batches(seqlens, sd):
+    d = W.make_inputs(W.get("varlen_ragged", H=3, seqlens=seqlens, state_dtype=sd, seed=40 + len(seqlens)))
+    assert d["T"] > 64 and d["T"] <= 256 * len(seqlens)
+    out, fin = pu.run_gpu(d)
+    ref_out, ref_fin = pu.run_oracle(d)
+    print("mixed", seqlens[:4], sd, pu.check(d, out, fin, ref_out, ref_fin, label="mixed-length varlen"))
+    n0 = seqlens.index(0) if 0 in seqlens else None
+    if n0 is not None:   # a zero-length sequence passes its state through
+        torch.testing.assert_close(fin[n0], d["initial_state"][n0].to(fin.dtype), rtol=0, atol=0)
