@@ -119,12 +119,21 @@ def tsplit_segments(N: int, T: int, H: int, varlen: bool, sms: int) -> int:
     return P if P >= 4 else 0
 
 
+MIXED_MAX_AVG = 256   # kda_internal.h kMixedMaxAvg
+
+
+def mixed_dispatch(d) -> bool:
+    """A varlen call of more than 64 rows with at most 256 per sequence on average: the
+    short-step kernel and the cluster kernel each take their own sequences."""
+    return d["cu_seqlens"] is not None and DECODE_MAX_T < d["T"] <= MIXED_MAX_AVG * d["N"]
+
+
 def launches_per_call(d, sms: int) -> int:
     """libkda kernel launches of one kda_fwd call on these inputs."""
     P = tsplit_segments(d["N"], d["T"], d["H"], d["cu_seqlens"] is not None, sms)
     if P:   # segment bounds, segment states, 2 state-only runs, scan, output run (+ final copy)
         return 6 + (d["state_dtype"] is not None)
-    return 1
+    return 2 if mixed_dispatch(d) else 1
 
 
 def kernel_source_hash(kernel: str = "cluster") -> str:
@@ -447,7 +456,9 @@ def run_ours(args):
             "frac": achieved / hbm, "traffic": stored_traffic(w.name, kernel_of(d_cpu["T"])),
             "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
             else f"{src} {hbm} GB/s",
-            "kernel": KERNEL_NAMES[kernel_of(d_cpu["T"])] + (
+            "kernel": ("kda_short_kernel + kda_cluster_kernel (kda_fwd: each on its own sequences, "
+                       "2 launches per step, the time of the whole call)") if mixed_dispatch(d_cpu) else
+                      KERNEL_NAMES[kernel_of(d_cpu["T"])] + (
                 " (kda_fwd: one launch per step)" if lpc == 1 else
                 f" (kda_fwd: sequence-parallel path, {lpc} launches per step, the time of the whole call)"),
             "algorithmic_bytes_per_launch": abytes,

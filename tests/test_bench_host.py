@@ -102,3 +102,14 @@ def test_tsplit_rule_mirror():
     assert bench.tsplit_segments(1, 65536, 1, False, 152) == 32     # capped at 32 segments
     assert bench.tsplit_segments(1, 65536, 8, True, 152) == 0       # varlen calls never split
     assert bench.tsplit_segments(1, 4096, 1, False, 152) == 0       # too short
+
+
+def test_mixed_dispatch_rule_mirror():
+    # varlen calls of more than 64 rows with at most 256 per sequence on average run the
+    # short-step kernel beside the cluster kernel (kda_api.cu), as bench.py mirrors it
+    import bench
+    from gated_delta_rule_52_gb300 import workloads as W
+    assert bench.mixed_dispatch(W.make_inputs(W.get("varlen_ragged", H=1, seqlens=(40, 30, 20))))
+    assert not bench.mixed_dispatch(W.make_inputs(W.get("varlen_ragged", H=1, seqlens=(40, 20))))   # 60 rows
+    assert not bench.mixed_dispatch(W.make_inputs(W.get("varlen_ragged", H=1, seqlens=(600, 20))))  # avg 310
+    assert not bench.mixed_dispatch(W.make_inputs(W.get("tiny")))                                   # fixed length
