@@ -96,10 +96,41 @@ cudaMemPool_t workspace_pool(int device) {
 
 // tsplit > 0: the sequence-parallel path with that many segments per sequence (p.ws is
 // then its scratch, tsplit_scratch_bytes long).
+}  // namespace
+
+namespace kda {
+cudaError_t sm_count(int &sms) {
+    static std::atomic<bool> done[kMaxDevices];
+    static int count[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= kMaxDevices) return cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    e = once_per_device(done, [&](int d) { return cudaDeviceGetAttribute(&count[d], cudaDevAttrMultiProcessorCount, d); });
+    sms = count[dev];
+    return e;
+}
+}  // namespace kda
+
+namespace {
+
 kda_status launch(kda::Params &p, void *stream, int64_t tsplit = 0) {
+    // the device error word's address, looked up once per device
+    static std::atomic<bool> done[kda::kMaxDevices];
+    static int *err_of[kda::kMaxDevices];
     int *err = nullptr;
-    if (cudaGetSymbolAddress(reinterpret_cast<void **>(&err), g_kda_error) != cudaSuccess)
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+    if (kda::once_per_device(done, [&](int d) {
+            return cudaGetSymbolAddress(reinterpret_cast<void **>(&err_of[d < kda::kMaxDevices ? d : 0]),
+                                        g_kda_error);
+        }) != cudaSuccess)
         return KDA_ERR_CUDA;
+    if (dev < kda::kMaxDevices) {
+        err = err_of[dev];
+    } else if (cudaGetSymbolAddress(reinterpret_cast<void **>(&err), g_kda_error) != cudaSuccess) {
+        return KDA_ERR_CUDA;
+    }
     p.err = err;
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e;
@@ -143,7 +174,7 @@ kda_status kda_fwd(const void *q, const void *k, const void *v, const void *g, c
     if (!pool) return KDA_ERR_CUDA;
     // Few (sequence, head) units on a long fixed-length call: the sequence-parallel path
     int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return KDA_ERR_CUDA;
+    if (kda::sm_count(sms) != cudaSuccess) return KDA_ERR_CUDA;
     const int64_t tsplit = kda::tsplit_segments(p, sms);
     const size_t bytes = tsplit > 0 ? kda::tsplit_scratch_bytes(p.n_seqs, p.H, tsplit)
                                     : (size_t)(p.n_seqs * p.H) * kda::kWsBytesPerUnit;

@@ -1103,8 +1103,10 @@ cudaError_t launch_cluster(const Params &p, cudaStream_t stream) {
         !encode_map(&maps.g, p.g ? p.g : dummy, rows, p.H) ||
         !encode_map(&maps.v, p.v ? p.v : dummy, rows, p.H))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(kda_cluster_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    static std::atomic<bool> attr_done[kMaxDevices];
+    cudaError_t e = once_per_device(attr_done, [](int) {
+        return cudaFuncSetAttribute(kda_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    });
     if (e != cudaSuccess) return e;
     kda_cluster_kernel<<<(unsigned)(2 * units), NT, SMEM_BYTES, stream>>>(maps, p);
     return cudaGetLastError();

@@ -2,6 +2,7 @@
 // libkda.so.  Not part of the public ABI (that is include/kda.h).
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -60,6 +61,23 @@ constexpr int64_t kShortMaxT = 64;
 // Varlen calls with more rows but at most this many per sequence on average run both
 // kernels, each on its own sequences (Params::mixed).
 constexpr int64_t kMixedMaxAvg = 256;
+
+// Per-device values that a launcher sets up once (a kernel's shared-memory limit, the SM
+// count): `f(device)` runs until it succeeds on that device; two threads racing both run
+// it, which is harmless.  Devices beyond kMaxDevices run it every time.
+constexpr int kMaxDevices = 64;
+template <typename F>
+cudaError_t once_per_device(std::atomic<bool> (&done)[kMaxDevices], F &&f) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < kMaxDevices && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    e = f(dev);
+    if (e == cudaSuccess && dev < kMaxDevices) done[dev].store(true, std::memory_order_release);
+    return e;
+}
+// The SM count of the current device (cached).
+cudaError_t sm_count(int &sms);
 
 // Launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_cluster(const Params &p, cudaStream_t stream);   // chunked, needs p.ws

@@ -463,12 +463,14 @@ cudaError_t launch_short(const Params &p, cudaStream_t stream) {
     if (units == 0) return cudaSuccess;
     const int bytes = (int)sizeof(ShortSmem);
     const bool multi = p.T > LT;
-    cudaError_t e = multi ? cudaFuncSetAttribute(kda_short_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
-                          : cudaFuncSetAttribute(kda_short_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    static std::atomic<bool> attr_done[2][kMaxDevices];
+    cudaError_t e = once_per_device(attr_done[multi], [&](int) {
+        return multi ? cudaFuncSetAttribute(kda_short_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
+                     : cudaFuncSetAttribute(kda_short_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    });
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    int sms = 0;
+    if ((e = sm_count(sms)) != cudaSuccess) return e;
     const int64_t grid = units < 2 * (int64_t)sms ? units : 2 * (int64_t)sms;   // two CTAs per SM
     if (multi)
         kda_short_kernel<true><<<(unsigned)grid, NTS, bytes, stream>>>(p);

@@ -181,8 +181,10 @@ cudaError_t launch_tsplit(const Params &p, int64_t P, unsigned char *scratch, cu
     if ((e = launch_cluster(q, stream)) != cudaSuccess) return e;
     // 3. the scan
     const int scan_smem = (int)((kState + (int64_t)kScanRows * kZs) * 4);
-    if ((e = cudaFuncSetAttribute(seg_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, scan_smem)) !=
-        cudaSuccess)
+    static std::atomic<bool> attr_done[kMaxDevices];
+    if ((e = once_per_device(attr_done, [&](int) {
+             return cudaFuncSetAttribute(seg_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, scan_smem);
+         })) != cudaSuccess)
         return e;
     seg_scan_kernel<<<dim3((unsigned)(N * H), DK / kScanRows), 256, scan_smem, stream>>>(sin, R, Pst, P, H);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

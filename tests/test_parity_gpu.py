@@ -369,3 +369,36 @@ def test_mixed_length_batches(seqlens, sd):
     n0 = seqlens.index(0) if 0 in seqlens else None
     if n0 is not None:   # a zero-length sequence passes its state through
         torch.testing.assert_close(fin[n0], d["initial_state"][n0].to(fin.dtype), rtol=0, atol=0)
+
+
+@pytest.mark.parametrize("name,wl", [("decode", dict(B=2, T=1, H=2)), ("short", dict(B=2, T=8, H=2)),
+                                     ("prefill", dict(B=1, T=300, H=2))])
+def test_cuda_graph_capture_replays_the_call(name, wl):
+    # A serving loop captures kda_fwd in a CUDA graph: the workspace is stream-ordered
+    # pool memory and every launch goes to the capturing stream, so a replay must give
+    # the direct call's results exactly.
+    d = W.make_inputs(W.get("decode", state_dtype="fp32", seed=50, **wl))
+    e = pu.to_device(d)
+    out = torch.empty((d["B"], d["T"], d["H"], 128), dtype=torch.bfloat16, device="cuda")
+    fin = torch.empty((d["N"], d["H"], 128, 128), dtype=torch.float32, device="cuda")
+
+    def call():
+        kda.kda_fwd(e["q"], e["k"], e["v"], e["g"], e["beta"], d["scale"], out, e["A_log"], e["dt_bias"],
+                    d["lower_bound"], initial_state=e["initial_state"], final_state=fin)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    ref_out, ref_fin = out.clone(), fin.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    out.zero_()
+    fin.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert kda.get_device_status() == kda.KDA_OK
+    assert torch.equal(out, ref_out) and torch.equal(fin, ref_fin)
