@@ -1,11 +1,12 @@
-// KDA forward for short multi-token steps (2..64 token rows per call): the
-// sequence's tokens form chunks of 16 of the UT/WY form, evaluated with warp-level
-// tensor-core MMAs (mma.sync m16n8k16, fp32 accumulation), the state kept in
-// registers from one 16-token block to the next.
+// KDA forward for short multi-token steps (2..64 token rows per call, or the
+// sequences of at most 64 tokens of a mixed-length varlen call): the sequence's
+// tokens form chunks of 16 of the UT/WY form, evaluated with warp-level tensor-core
+// MMAs (mma.sync m16n8k16, fp32 accumulation), the state kept in registers from one
+// 16-token block to the next.
 //
-// Per (sequence, head) and 16-token block of L <= 16 tokens, G the cumulative log
-// decay from the start of the block (every exponent below is <= 0 except 2^-G, which stays below 2^116
-// since each token's log decay is >= the lower bound of -5):
+// Per (sequence, head) and 16-token block of L <= 16 tokens, with G the cumulative
+// log decay from the start of the block (every exponent below is <= 0 except 2^-G,
+// which stays below 2^116 since each token's log decay is >= the lower bound of -5):
 //   A[t,i] = beta_t sum_c k_hat[t,c] k_hat[i,c] 2^(G[t,c]-G[i,c])   (i < t)
 //   M[t,i] =        sum_c q_hat[t,c] k_hat[i,c] 2^(G[t,c]-G[i,c])   (i <= t)
 //   T' = (I + A)^-1 Diag(beta);   U = T' (V - K_hat Gamma S)
@@ -16,16 +17,16 @@
 // Work split: one CTA of 8 warps per (sequence, head).  Warp w owns state rows
 // v = 16w .. 16w+15 (storage [V][K]) as fp32 MMA accumulators in registers; the
 // same registers, packed to fp16, are the B operand of (K_hat Gamma; Q_hat Gamma) S^T,
-// so no warp needs another warp's state.  The CTA shares the per-token operands:
-// the gate and the decayed q/k tiles (threads = channel pairs and token halves),
-// the norms and beta,
-// A and M from one bf16 MMA each (raw q/k times 2^G against k times 2^-G, the
-// norms applied in fp32 afterwards, as in the chunked kernel), and the 16 x 16
-// inverse by forward substitution (on warp 2, after its own products).  CTAs are persistent (two per SM): a unit's
-// token rows are copied in while the previous unit finishes, and its state is
-// prefetched into L2 at the same time.  The row norms of k are folded into U
-// (U' = Diag(1/|k|) U) and out of M and Kbar, so every fp16 tile is the raw input
-// times decay factors in [0, 1].
+// so no warp needs another warp's state.  The CTA shares the per-block operands:
+// - the gate and the decayed q/k tiles (threads = channel pairs and token halves);
+// - the norms and beta;
+// - A and M from one bf16 MMA each (raw q/k times 2^G against k times 2^-G, the
+//   norms applied in fp32 afterwards, as in the chunked kernel);
+// - the 16 x 16 inverse by forward substitution (on warp 2, after its own products).
+// CTAs are persistent (two per SM): a unit's token rows are copied in while the
+// previous unit finishes, and its state is prefetched into L2 at the same time.  The
+// row norms of k are folded into U (U' = Diag(1/|k|) U) and out of M and Kbar, so
+// every fp16 tile is the raw input times decay factors in [0, 1].
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
