@@ -7,8 +7,8 @@ One step = one kda_fwd call (the whole hot path: prologue, intra-chunk UT/WY,
 chunk-sequential state pass, state load/store) over the long-prefill workload
 B=1, T=8192, H=64, K=V=128 with bf16 initial/final state.  Inputs are seeded
 synthetic data resident in HBM; out/final_state are preallocated.  The working
-set (~676 MB) is larger than L2 (129 MB) and a 256 MB L2-flush write runs
-between timed steps (outside the timed kernel).  Each step is timed with CUDA
+set (~600 MB of algorithmic traffic) is larger than L2 (129 MB) and a 256 MB
+L2-flush write runs between timed steps (outside the timed kernel).  Each step is timed with CUDA
 events on the launching stream; rank 0 prints one JSON line.
 
 --impl reference times the fp64 CPU oracle (the baseline, on the host cores) on
@@ -470,8 +470,10 @@ def run_ours(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "B": B, "T": T, "H": H, "K": 128, "V": 128,
                        "state": d_cpu["state_dtype"], "lower_bound": d_cpu["lower_bound"],
-                       "l2": "inputs (676 MB) larger than L2 and a 256 MB flush write between "
-                             "timed steps", "timing": "CUDA events around each kda_fwd call"},
+                       "l2": f"algorithmic traffic {abytes / 1e6:.0f} MB per step "
+                             f"({'larger' if abytes > 129e6 else 'smaller'} than the 129 MB L2); "
+                             "a 256 MB flush write between timed steps",
+                       "timing": "CUDA events around each kda_fwd call"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
             "gpu_launches": args.steps * lpc,
             "wall_s_timed_region": wall}

@@ -54,9 +54,7 @@ __device__ __forceinline__ void seq_range(const Params &p, int64_t n, int64_t &b
 
 // Calls with at most kShortMaxT token rows (T of the packed batch) run a kernel with
 // no workspace instead of the chunked cluster kernel: the token recurrence for one row
-// (decode; it handles up to kDecodeMaxT rows), blocks of 16 rows on warp-level
-// tensor-core MMAs otherwise.
-constexpr int64_t kDecodeMaxT = 16;
+// (decode), blocks of 16 rows on warp-level tensor-core MMAs otherwise.
 constexpr int64_t kShortMaxT = 64;
 // Varlen calls with more rows but at most this many per sequence on average run both
 // kernels, each on its own sequences (Params::mixed).
@@ -81,7 +79,7 @@ cudaError_t sm_count(int &sms);
 
 // Launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_cluster(const Params &p, cudaStream_t stream);   // chunked, needs p.ws
-cudaError_t launch_decode(const Params &p, cudaStream_t stream);    // token recurrence, T = 1
+cudaError_t launch_decode(const Params &p, cudaStream_t stream);    // token recurrence, T = 1 only
 cudaError_t launch_short(const Params &p, cudaStream_t stream);     // 16-row blocks, 2 <= T <= 64
 
 // Sequence-parallel prefill (fixed-length calls with few (sequence, head) units): each
