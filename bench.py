@@ -52,7 +52,7 @@ KERNEL_SOURCES = {
     "decode": ("kda_decode.cu", "sm103.cuh", "kda_internal.h"),
     "short": ("kda_short.cu", "sm103.cuh", "kda_internal.h"),
 }
-KERNEL_NAMES = {"cluster": "kda_cluster_kernel", "decode": "kda_decode_kernel", "short": "kda_short_kernel"}
+KERNEL_NAMES = {"cluster": "kda_cluster_kernel", "decode": "kda_decode1_kernel", "short": "kda_short_kernel"}
 CSRC = os.path.join("gated_delta_rule_52_gb300", "csrc")
 DECODE_MAX_T = 64   # calls with at most this many token rows run a kernel without workspace
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")

@@ -94,8 +94,6 @@ cudaMemPool_t workspace_pool(int device) {
     return pools[device];
 }
 
-// tsplit > 0: the sequence-parallel path with that many segments per sequence (p.ws is
-// then its scratch, tsplit_scratch_bytes long).
 }  // namespace
 
 namespace kda {
@@ -114,6 +112,8 @@ cudaError_t sm_count(int &sms) {
 
 namespace {
 
+// tsplit > 0: the sequence-parallel path with that many segments per sequence (p.ws is
+// then its scratch, tsplit_scratch_bytes long).
 kda_status launch(kda::Params &p, void *stream, int64_t tsplit = 0) {
     // the device error word's address, looked up once per device
     static std::atomic<bool> done[kda::kMaxDevices];

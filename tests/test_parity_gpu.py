@@ -212,8 +212,9 @@ def test_caller_workspace_entry_point():
 
 # ---- short steps (T <= 64 token rows): the token recurrence (T = 1) and the 16-row-block kernel
 
-@pytest.mark.parametrize("T,sd,init", [(1, "fp32", "normal"), (3, "bf16", "normal"),
-                                       (16, "fp32", "none"), (16, "bf16", "normal"), (5, None, "none")])
+@pytest.mark.parametrize("T,sd,init", [(1, "fp32", "normal"), (1, "bf16", "none"), (1, None, "normal"),
+                                       (3, "bf16", "normal"), (16, "fp32", "none"),
+                                       (16, "bf16", "normal"), (5, None, "none")])
 def test_short_step_all_elements(T, sd, init):
     d = W.make_inputs(W.get("decode", B=5, T=T, H=3, state_dtype=sd, initial_state=init))
     out, fin = pu.run_gpu(d, want_final=sd is not None)
@@ -221,14 +222,16 @@ def test_short_step_all_elements(T, sd, init):
     print("short", T, sd, init, pu.check(d, out, fin, ref_out, ref_fin, label=f"short T={T}"))
 
 
-def test_short_step_varlen_with_empty_sequences():
-    d = W.make_inputs(W.get("varlen_ragged", H=2, seqlens=(1, 0, 5, 10, 0)))
+@pytest.mark.parametrize("seqlens", [(1, 0, 5, 10, 0), (0, 1, 0, 0, 0)])
+def test_short_step_varlen_with_empty_sequences(seqlens):
+    # (0, 1, 0, 0, 0): one packed token, so the one-token kernel with cu_seqlens
+    d = W.make_inputs(W.get("varlen_ragged", H=2, seqlens=seqlens))
     assert d["T"] <= 16
     out, fin = pu.run_gpu(d)
     ref_out, ref_fin = pu.run_oracle(d)
     pu.check(d, out, fin, ref_out, ref_fin, label="short varlen")
     # zero-length sequences pass their state through unchanged
-    for n in (1, 4):
+    for n in [i for i, L in enumerate(seqlens) if L == 0]:
         torch.testing.assert_close(fin[n], d["initial_state"][n].to(fin.dtype), rtol=0, atol=0)
 
 
