@@ -79,6 +79,11 @@ def _p(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
+def _lb(lower_bound):
+    """None (no lower bound: the softplus gate) travels to the C code as NaN."""
+    return float("nan") if lower_bound is None else float(lower_bound)
+
+
 def max_threads() -> int:
     return int(_load().kda_oracle_max_threads())
 
@@ -88,7 +93,8 @@ def kda_fwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, initial_state=
     """Full KDA forward in fp64 from raw inputs (numpy arrays or torch tensors in the
     Kernel API layouts).  Returns ``(out, final_state)`` as fp64 numpy arrays;
     ``final_state`` is None when ``want_final`` is false.  ``pairs`` (optional, a list
-    of (sequence, head)) restricts the work; other outputs stay NaN."""
+    of (sequence, head)) restricts the work; other outputs stay NaN.  ``lower_bound``
+    None selects the gate without a lower bound (softplus; see kda_oracle.c)."""
     lib = _load()
     q, k, v, g, beta = _f64(q), _f64(k), _f64(v), _f64(g), _f64(beta)
     A_log, dt_bias, init = _f64(A_log), _f64(dt_bias), _f64(initial_state)
@@ -102,7 +108,7 @@ def kda_fwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, initial_state=
     if pairs is not None:
         pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int64).reshape(-1, 2))
     rc = lib.kda_oracle_fwd(_p(q), _p(k), _p(v), _p(g), _p(beta), float(scale), _p(A_log),
-                            _p(dt_bias), float(lower_bound), _p(init), _p(fin), _p(out), _p(cu),
+                            _p(dt_bias), _lb(lower_bound), _p(init), _p(fin), _p(out), _p(cu),
                             N if cu is not None else 0, B, T, H, K, V, _p(pr),
                             0 if pr is None else pr.shape[0], int(nthreads))
     if rc:
@@ -138,7 +144,7 @@ def activations(q, k, g, beta, A_log, dt_bias, lower_bound):
     qn, kn, gk = np.empty_like(q), np.empty_like(k), np.empty_like(g)
     bo = np.empty_like(beta)
     rc = lib.kda_oracle_activations(_p(q), _p(k), _p(g), _p(beta), _p(A_log), _p(dt_bias),
-                                    float(lower_bound), B, T, H, K, _p(qn), _p(kn), _p(gk), _p(bo))
+                                    _lb(lower_bound), B, T, H, K, _p(qn), _p(kn), _p(gk), _p(bo))
     if rc:
         raise ValueError("oracle rejected the sizes")
     return qn, kn, gk, bo

@@ -14,6 +14,10 @@
  *   q_hat = q / sqrt(|q|^2 + eps),  k_hat likewise           (q/k L2 norm)
  *   beta  = 1 / (1 + exp(-beta_logit))                      (beta sigmoid)
  *   gk[c] = lower_bound * sigmoid(exp(A_log[h]) * (g[c] + dt_bias[h][c]))
+ *           (the bounded gate, safe_gate on; lower_bound in [-5, 0]), or, when the
+ *           call has no lower bound (safe_gate off; passed here as a NaN lower_bound),
+ *   gk[c] = -exp(A_log[h]) * softplus(g[c] + dt_bias[h][c]),
+ *           softplus(x) = log(1 + exp(x)), a log decay in (-inf, 0)
  *   S_t   = (I - beta_t k_t k_t^T) Diag(exp(gk_t)) S_{t-1} + beta_t k_t v_t^T
  *   o_t   = scale * S_t^T q_t
  *
@@ -39,6 +43,9 @@
 
 static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
 
+/* log(1 + exp(x)) without overflow: max(x, 0) + log1p(exp(-|x|)). */
+static double softplus(double x) { return (x > 0.0 ? x : 0.0) + log1p(exp(-fabs(x))); }
+
 /* Activations of one token of one head: L2-normalised q and k, beta and the
  * per-channel log decay gk. */
 static void activations(const double *q, const double *k, const double *g, double beta_logit,
@@ -56,7 +63,11 @@ static void activations(const double *q, const double *k, const double *g, doubl
     }
     *beta = sigmoid(beta_logit);
     double a = exp(A_log_h);
-    for (int64_t c = 0; c < K; ++c) gk[c] = lower_bound * sigmoid(a * (g[c] + dt_bias_h[c]));
+    if (isnan(lower_bound)) {
+        for (int64_t c = 0; c < K; ++c) gk[c] = -a * softplus(g[c] + dt_bias_h[c]);
+    } else {
+        for (int64_t c = 0; c < K; ++c) gk[c] = lower_bound * sigmoid(a * (g[c] + dt_bias_h[c]));
+    }
 }
 
 /* One step of the recurrence on S (K x V, row-major S[c*V+v]):

@@ -205,6 +205,53 @@ def test_gate_special_values():
     assert np.all(gk0 == 0.0)
 
 
+def test_unbounded_gate_special_values():
+    # The gate without a lower bound (lower_bound None): gk = -exp(A_log) softplus(g + dt_bias).
+    #   g + dt = 0 -> -exp(A_log) ln 2;  g + dt = ln(e - 1) -> softplus 1 -> -exp(A_log);
+    #   g + dt = 1e4 -> -exp(A_log) 1e4 (no overflow);  g + dt = -800 -> 0 (to 1e-300);
+    #   A_log -> -inf -> 0.
+    H, K = 3, 4
+    dt = rng(27).standard_normal((H, K))
+    A_log = np.array([0.0, np.log(2.0), -800.0])
+    g = np.empty((1, 4, H, K))
+    g[0, 0] = -dt
+    g[0, 1] = np.log(np.e - 1.0) - dt
+    g[0, 2] = 1e4 - dt
+    g[0, 3] = -800.0 - dt
+    z = np.zeros((1, 4, H, K)); zb = np.zeros((1, 4, H))
+    _, _, gk, _ = oracle.activations(z + 1, z + 1, g, zb, A_log, dt, None)
+    np.testing.assert_allclose(gk[0, 0, :2], -np.array([1.0, 2.0])[:, None] * np.log(2.0) * np.ones(K), rtol=1e-14)
+    np.testing.assert_allclose(gk[0, 1, :2], -np.array([1.0, 2.0])[:, None] * np.ones(K), rtol=1e-12)
+    np.testing.assert_allclose(gk[0, 2, :2], -np.array([1.0, 2.0])[:, None] * 1e4 * np.ones(K), rtol=1e-14)
+    assert np.all(np.abs(gk[0, 3]) < 1e-300) and np.all(gk[0, 3] <= 0.0)
+    assert np.all(np.abs(gk[0, :, 2]) < 1e-300)          # exp(A_log) = 0
+    # strictly decreasing in g, and below every bounded gate's floor for large g
+    xs = np.linspace(-6.0, 6.0, 25)
+    gg = (xs[:, None] - dt[0][None, :])[None, :, None, :] * np.ones((1, 25, 1, K))
+    _, _, gk1, _ = oracle.activations(gg + 1, gg + 1, gg, np.zeros((1, 25, 1)), A_log[:1], dt[:1], None)
+    assert np.all(np.diff(gk1[0, :, 0, 0]) < 0.0)
+    assert gk1[0, -1, 0, 0] < -5.0
+
+
+def test_unbounded_gate_forward_composes():
+    r = rng(28)
+    B, T, H, K, V = 2, 6, 2, 8, 5
+    q, k = r.standard_normal((B, T, H, K)), r.standard_normal((B, T, H, K))
+    g = 2.0 * r.standard_normal((B, T, H, K))
+    v = r.standard_normal((B, T, H, V)); bl = r.standard_normal((B, T, H))
+    A_log = np.log(r.uniform(1, 16, H)); dt = 0.1 * r.standard_normal((H, K))
+    S0 = 0.02 * r.standard_normal((B, H, V, K))
+    out, fin = oracle.kda_fwd(q, k, v, g, bl, 0.3, A_log, dt, None, initial_state=S0)
+    qn, kn, gk, b = oracle.activations(q, k, g, bl, A_log, dt, None)
+    assert np.all(gk < 0.0)
+    o2, f2 = oracle.recurrence(qn, kn, v, gk, b, 0.3, initial_state=S0)
+    np.testing.assert_array_equal(out, o2)
+    np.testing.assert_array_equal(fin, f2)
+    # and it differs from every bounded gate on these inputs (the flag is honoured)
+    o3, _ = oracle.kda_fwd(q, k, v, g, bl, 0.3, A_log, dt, -5.0, initial_state=S0)
+    assert np.abs(o3 - out).max() > 1e-3
+
+
 def test_beta_sigmoid_and_l2_norm():
     r = rng(18)
     B, T, H, K = 1, 5, 2, 128
