@@ -51,8 +51,10 @@ KERNEL_SOURCES = {
     "cluster": ("kda_cluster.cu", "sm103.cuh", "kda_internal.h"),
     "decode": ("kda_decode.cu", "sm103.cuh", "kda_internal.h"),
     "short": ("kda_short.cu", "sm103.cuh", "kda_internal.h"),
+    "recur": ("kda_recur.cu", "sm103.cuh", "kda_internal.h"),
 }
-KERNEL_NAMES = {"cluster": "kda_cluster_kernel", "decode": "kda_decode1_kernel", "short": "kda_short_kernel"}
+KERNEL_NAMES = {"cluster": "kda_cluster_kernel", "decode": "kda_decode1_kernel", "short": "kda_short_kernel",
+                "recur": "kda_recur_kernel"}
 CSRC = os.path.join("gated_delta_rule_52_gb300", "csrc")
 DECODE_MAX_T = 64   # calls with at most this many token rows run a kernel without workspace
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
@@ -97,13 +99,26 @@ def algorithmic_bytes(d) -> int:
     return th * BYTES_PER_TOKEN_HEAD + d["N"] * d["H"] * 128 * 128 * sb * n_state
 
 
+# The token recurrence (the gate without a lower bound): per token-head, the decay,
+# k^T S, the rank-1 update and q^T S, each K x V multiply-adds, 2 flops each.
+RECUR_FLOPS_PER_TOKEN_HEAD = 4 * 128 * 128 * 2
+SM_MAX_MHZ = 2070   # GB300 maximum SM clock, used when nvidia-smi reports none
+
+
 def algorithmic_flops(d) -> int:
     return d["B"] * d["T"] * d["H"] * FLOPS_PER_TOKEN_HEAD
 
 
-def kernel_of(T: int) -> str:
-    """The kernel libkda runs for a call of T packed token rows."""
+def kernel_of(T: int, unbounded: bool = False) -> str:
+    """The kernel libkda runs for a call of T packed token rows (the gate without a
+    lower bound always runs the token recurrence)."""
+    if unbounded:
+        return "recur"
     return "decode" if T == 1 else ("short" if T <= DECODE_MAX_T else "cluster")
+
+
+def kernel_for(d) -> str:
+    return kernel_of(d["T"], d["lower_bound"] is None)
 
 
 # The dispatch rule of kda_fwd for the sequence-parallel path (kda_internal.h,
@@ -125,11 +140,14 @@ MIXED_MAX_AVG = 256   # kda_internal.h kMixedMaxAvg
 def mixed_dispatch(d) -> bool:
     """A varlen call of more than 64 rows with at most 256 per sequence on average: the
     short-step kernel and the cluster kernel each take their own sequences."""
-    return d["cu_seqlens"] is not None and DECODE_MAX_T < d["T"] <= MIXED_MAX_AVG * d["N"]
+    return (d["lower_bound"] is not None and d["cu_seqlens"] is not None
+            and DECODE_MAX_T < d["T"] <= MIXED_MAX_AVG * d["N"])
 
 
 def launches_per_call(d, sms: int) -> int:
     """libkda kernel launches of one kda_fwd call on these inputs."""
+    if d["lower_bound"] is None:
+        return 1
     P = tsplit_segments(d["N"], d["T"], d["H"], d["cu_seqlens"] is not None, sms)
     if P:   # segment bounds, segment states, 2 state-only runs, scan, output run (+ final copy)
         return 6 + (d["state_dtype"] is not None)
@@ -464,23 +482,39 @@ def run_ours(args):
     abytes = algorithmic_bytes(d_cpu)
     achieved = abytes / (avg_launch_ms / 1e3) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-            "frac": achieved / hbm, "traffic": stored_traffic(w.name, kernel_of(d_cpu["T"])),
+            "frac": achieved / hbm, "traffic": stored_traffic(w.name, kernel_for(d_cpu)),
             "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
             else f"{src} {hbm} GB/s",
             "kernel": ("kda_short_kernel + kda_cluster_kernel (kda_fwd: each on its own sequences, "
                        "2 launches per step, the time of the whole call)") if mixed_dispatch(d_cpu) else
-                      KERNEL_NAMES[kernel_of(d_cpu["T"])] + (
+                      KERNEL_NAMES[kernel_for(d_cpu)] + (
                 " (kda_fwd: one launch per step)" if lpc == 1 else
                 f" (kda_fwd: sequence-parallel path, {lpc} launches per step, the time of the whole call)"),
             "algorithmic_bytes_per_launch": abytes,
             "algorithmic_flops_per_launch": algorithmic_flops(d_cpu),
             "tensor_frac": algorithmic_flops(d_cpu) / (avg_launch_ms / 1e3) / (tflops * 1e12)}
+    if kernel_for(d_cpu) == "recur":
+        # The token recurrence runs on the fp32 CUDA cores: 4 K V multiply-adds per
+        # token-head (decay, k^T S, the rank-1 update, q^T S), against 128 fp32 lanes per
+        # SM at the maximum SM clock.
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        mhz = (clk or {}).get("sm_max_mhz") or SM_MAX_MHZ
+        peak_alu = sms * 128 * 2 * mhz * 1e6 / 1e12
+        rflops = B * T * H * RECUR_FLOPS_PER_TOKEN_HEAD
+        ach = rflops / (avg_launch_ms / 1e3) / 1e12
+        roof = dict(roof, bound="alu", achieved=ach, peak=peak_alu, unit="TFLOP/s", frac=ach / peak_alu,
+                    peak_source=f"derived: {sms} SMs x 128 fp32 lanes x 2 flops x {mhz:.0f} MHz",
+                    hbm_view={"achieved_gbs": achieved, "peak_gbs": hbm, "frac": achieved / hbm},
+                    algorithmic_flops_per_launch=rflops)
     cpu = cpu_baseline(d_cpu) if ws == 1 else None
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "B": B, "T": T, "H": H, "K": 128, "V": 128,
                        "state": d_cpu["state_dtype"], "lower_bound": d_cpu["lower_bound"],
+                       "gate": ("-exp(A_log) softplus(g + dt_bias), no lower bound"
+                                if d_cpu["lower_bound"] is None else
+                                "lower_bound sigmoid(exp(A_log) (g + dt_bias))"),
                        "l2": f"algorithmic traffic {abytes / 1e6:.0f} MB per step "
                              f"({'larger' if abytes > 129e6 else 'smaller'} than the 129 MB L2); "
                              "a 256 MB flush write between timed steps",

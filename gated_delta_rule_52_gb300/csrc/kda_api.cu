@@ -97,6 +97,9 @@ cudaMemPool_t workspace_pool(int device) {
 }  // namespace
 
 namespace kda {
+// The token recurrence with the gate that has no lower bound (csrc/kda_recur.cu).
+cudaError_t launch_recur(const Params &p, cudaStream_t stream);
+
 cudaError_t sm_count(int &sms) {
     static std::atomic<bool> done[kMaxDevices];
     static int count[kMaxDevices];
@@ -204,6 +207,21 @@ kda_status kda_fwd_ws(const void *q, const void *k, const void *v, const void *g
     if (units == 0) return KDA_OK;
     p.ws = static_cast<unsigned char *>(workspace);
     return launch(p, stream);
+}
+
+kda_status kda_fwd_unbounded(const void *q, const void *k, const void *v, const void *g,
+                             const void *beta, float scale, void *out, const float *A_log,
+                             const float *dt_bias, const void *initial_state, void *final_state,
+                             int state_dtype, const int64_t *cu_seqlens, int64_t num_seqs,
+                             int64_t B, int64_t T, int64_t H, int64_t K, int64_t V, void *stream) {
+    kda::Params p{};   // every field zero until validate() fills it
+    // the lower bound is not an argument here; 0 passes its range check
+    kda_status st = validate(q, k, v, g, beta, scale, out, A_log, dt_bias, 0.f, initial_state,
+                             final_state, state_dtype, cu_seqlens, num_seqs, B, T, H, K, V, p);
+    if (st != KDA_OK) return st;
+    if (p.n_seqs == 0 || p.H == 0) return KDA_OK;
+    return kda::launch_recur(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KDA_OK
+                                                                                : KDA_ERR_CUDA;
 }
 
 const char *kda_status_string(int status) {

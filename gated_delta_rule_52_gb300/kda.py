@@ -36,7 +36,8 @@ KDA_STATE_BF16 = 1
 KDA_STATE_FP32 = 2
 
 # Every symbol include/kda.h declares.
-EXPORTED = ("kda_fwd", "kda_fwd_ws", "kda_status_string", "kda_get_device_status", "kda_version")
+EXPORTED = ("kda_fwd", "kda_fwd_ws", "kda_fwd_unbounded", "kda_status_string",
+            "kda_get_device_status", "kda_version")
 
 # Workspace bytes per (sequence, head) of kda_fwd_ws (KDA_WORKSPACE_BYTES_PER_UNIT).
 WORKSPACE_BYTES_PER_UNIT = 99328
@@ -67,6 +68,9 @@ def lib() -> ctypes.CDLL:
             L.kda_fwd_ws.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp, f, vp, vp, ci, vp, i64,
                                      i64, i64, i64, i64, i64, vp, ctypes.c_size_t, vp]
             L.kda_fwd_ws.restype = ci
+            L.kda_fwd_unbounded.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp, vp, vp, ci, vp, i64,
+                                            i64, i64, i64, i64, i64, vp]
+            L.kda_fwd_unbounded.restype = ci
             L.kda_status_string.argtypes = [ci]
             L.kda_status_string.restype = ctypes.c_char_p
             L.kda_get_device_status.argtypes = [vp]
@@ -128,7 +132,9 @@ def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_s
     """KDA forward through libkda.so.  Writes ``out`` [B,T,H,V] (and ``final_state``)
     in place, asynchronously on ``stream`` (default: the current torch stream).
     With ``workspace`` (a CUDA uint8 tensor of at least ``workspace_bytes(N, H)``
-    bytes) the call goes to kda_fwd_ws and allocates nothing."""
+    bytes) the call goes to kda_fwd_ws and allocates nothing.  ``lower_bound=None``
+    selects the gate without a lower bound (kda_fwd_unbounded: -exp(A_log) softplus(g +
+    dt_bias), the token recurrence)."""
     if q.dim() != 4:
         raise ValueError("q must be [B, T, H, K]")
     B, T, H, K = q.shape
@@ -152,6 +158,16 @@ def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_s
     for name, s in (("initial_state", initial_state), ("final_state", final_state)):
         if s is not None:
             _check_tensor(name, s, s.dtype, (N, H, V, K))
+    if lower_bound is None:
+        if workspace is not None:
+            raise ValueError("the gate without a lower bound takes no workspace")
+        st = lib().kda_fwd_unbounded(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                     _ptr(out), _ptr(A_log), _ptr(dt_bias), _ptr(initial_state),
+                                     _ptr(final_state), code, _ptr(cu_seqlens), num_seqs, B, T, H,
+                                     K, V, _stream_handle(stream))
+        if st != KDA_OK:
+            raise KDAError(st, status_string(st))
+        return
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(out), _ptr(A_log),
             _ptr(dt_bias), float(lower_bound), _ptr(initial_state), _ptr(final_state), code,
             _ptr(cu_seqlens), num_seqs, B, T, H, K, V)

@@ -42,7 +42,7 @@ class Workload:
     varlen: Optional[str] = None
     n_seqs: int = 0
     seqlens: Optional[tuple] = None          # explicit lengths (overrides varlen draw)
-    lower_bound: float = -5.0
+    lower_bound: Optional[float] = -5.0      # None: the gate without a lower bound (softplus)
     lower_bound_range: Optional[tuple] = None  # draw lb ~ U[lo, hi] if set
     state_dtype: Optional[str] = None        # None | "fp32" | "bf16"
     initial_state: str = "none"              # "none" | "normal" | "alternate" (zeros on even seqs)
@@ -104,6 +104,12 @@ WORKLOADS = {
     "prefill_64k_h8": Workload(
         name="prefill_64k_h8", B=1, T=65536, H=8, seed=7, state_dtype="bf16", initial_state="normal",
         description="B=1 T=65536 H=8; bf16 initial/final state N(0,0.02)"),
+    # The long prefill with the gate that has no lower bound (softplus), which runs the
+    # token recurrence instead of the chunked kernel.
+    "prefill_8k_unbounded": Workload(
+        name="prefill_8k_unbounded", B=1, T=8192, H=64, seed=10, lower_bound=None,
+        state_dtype="bf16", initial_state="normal",
+        description="B=1 T=8192 H=64, gate without a lower bound; bf16 state N(0,0.02)"),
 }
 
 # The throughput workload timed by bench.py.
@@ -187,7 +193,7 @@ def make_inputs(w: Workload, device="cpu") -> dict:
         lo, hi = w.lower_bound_range
         lb = float(lo + (hi - lo) * torch.rand((), generator=gen, dtype=torch.float64).item())
     else:
-        lb = float(w.lower_bound)
+        lb = None if w.lower_bound is None else float(w.lower_bound)
     d = dict(q=q, k=k, v=v, g=g, beta=beta, A_log=A_log, dt_bias=dt_bias,
              scale=1.0 / math.sqrt(K), lower_bound=lb, initial_state=init,
              state_dtype=w.state_dtype, cu_seqlens=cu, seqlens=lens,

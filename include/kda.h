@@ -136,6 +136,29 @@ kda_status kda_fwd_ws(const void *q, const void *k, const void *v, const void *g
                       int64_t T, int64_t H, int64_t K, int64_t V, void *workspace,
                       size_t workspace_bytes, void *stream);
 
+/*
+ * kda_fwd_unbounded — KDA forward with the gate that has no lower bound (the
+ * FlashKDA usage notes' safe_gate switched off; the pages give no formula for this
+ * gate, the one below is this library's reading):
+ *
+ *   gk_t[c] = -exp(A_log[h]) * softplus(g_t[c] + dt_bias[h][c]),
+ *   softplus(x) = log(1 + exp(x)),
+ *
+ * a per-token log decay in (-inf, 0) with no floor.  Everything else (norms, beta,
+ * the recurrence, scale, states, cu_seqlens) is as for kda_fwd, whose argument list
+ * this is without lower_bound.  Without the floor the decay over a few tokens can
+ * leave the fp32 exponent range, so this call applies the recurrence token by token
+ * (exact for any decay, down to zero) instead of the chunked tensor-core form; it is
+ * the slower path.  It allocates nothing and needs no workspace; asynchronous like
+ * kda_fwd.  Same argument errors as kda_fwd (no lower_bound check), KDA_ERR_CUDA if
+ * the launch failed.
+ */
+kda_status kda_fwd_unbounded(const void *q, const void *k, const void *v, const void *g,
+                             const void *beta, float scale, void *out, const float *A_log,
+                             const float *dt_bias, const void *initial_state, void *final_state,
+                             int state_dtype, const int64_t *cu_seqlens, int64_t num_seqs,
+                             int64_t B, int64_t T, int64_t H, int64_t K, int64_t V, void *stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *kda_status_string(int status);
 

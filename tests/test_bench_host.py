@@ -113,3 +113,12 @@ def test_mixed_dispatch_rule_mirror():
     assert not bench.mixed_dispatch(W.make_inputs(W.get("varlen_ragged", H=1, seqlens=(40, 20))))   # 60 rows
     assert not bench.mixed_dispatch(W.make_inputs(W.get("varlen_ragged", H=1, seqlens=(600, 20))))  # avg 310
     assert not bench.mixed_dispatch(W.make_inputs(W.get("tiny")))                                   # fixed length
+
+
+def test_gate_without_lower_bound_runs_the_recurrence():
+    d = W.make_inputs(W.get("varlen_ragged", H=1, seqlens=(40, 30, 20), lower_bound=None))
+    assert d["lower_bound"] is None
+    assert bench.kernel_for(d) == "recur" and not bench.mixed_dispatch(d)
+    assert bench.launches_per_call(d, 152) == 1
+    assert bench.kernel_of(8192, unbounded=True) == "recur" and bench.kernel_of(8192) == "cluster"
+    assert "recur" in bench.KERNEL_NAMES and len(bench.kernel_source_hash("recur")) == 16

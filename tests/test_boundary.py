@@ -159,3 +159,27 @@ def test_ws_entry_point_validates_workspace(L):
     # no work: a NULL workspace of size 0 is accepted without touching the device
     assert call_ws(ws=None, ws_bytes=0, q=None, k=None, v=None, g=None, beta=None, out=None,
                    B=0) == kda.KDA_OK
+
+
+def call_unbounded(**over):
+    a = dict(q=P[0], k=P[1], v=P[2], g=P[3], beta=P[4], scale=0.088, out=P[5], A_log=P[6],
+             dt_bias=P[7], init=None, fin=None, sdt=0, cu=None, nseq=0,
+             B=1, T=64, H=2, K=128, V=128, stream=None)
+    a.update(over)
+    return kda.lib().kda_fwd_unbounded(a["q"], a["k"], a["v"], a["g"], a["beta"],
+                                       ctypes.c_float(a["scale"]), a["out"], a["A_log"],
+                                       a["dt_bias"], a["init"], a["fin"], a["sdt"], a["cu"],
+                                       a["nseq"], a["B"], a["T"], a["H"], a["K"], a["V"],
+                                       a["stream"])
+
+
+def test_unbounded_gate_entry_point_validates(L):
+    # every case fails validation (nothing launched on the fake pointers), except the
+    # last, which has no work
+    assert call_unbounded(K=64) == kda.KDA_ERR_UNSUPPORTED
+    assert call_unbounded(q=None) == kda.KDA_ERR_NULL
+    assert call_unbounded(out=ctypes.c_void_p(0x10008)) == kda.KDA_ERR_ALIGN
+    assert call_unbounded(scale=float("inf")) == kda.KDA_ERR_VALUE
+    assert call_unbounded(init=P[9], sdt=kda.KDA_STATE_NONE) == kda.KDA_ERR_DTYPE
+    assert call_unbounded(cu=P[8], nseq=2, B=3) == kda.KDA_ERR_SHAPE
+    assert call_unbounded(q=None, k=None, v=None, g=None, beta=None, out=None, B=0) == kda.KDA_OK

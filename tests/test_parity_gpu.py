@@ -405,3 +405,48 @@ def test_cuda_graph_capture_replays_the_call(name, wl):
     torch.cuda.synchronize()
     assert kda.get_device_status() == kda.KDA_OK
     assert torch.equal(out, ref_out) and torch.equal(fin, ref_fin)
+
+
+# ---- the gate without a lower bound (kda_fwd_unbounded, the token recurrence)
+
+@pytest.mark.parametrize("B,T,H,sd,init,g_std", [(2, 300, 3, "fp32", "normal", 1.0),
+                                                 (1, 1, 4, "bf16", "normal", 1.0),
+                                                 (3, 70, 2, None, "none", 1.0),
+                                                 (2, 17, 2, "bf16", "none", 1.0),
+                                                 (1, 200, 2, "fp32", "alternate", 3.0)])
+def test_unbounded_gate_all_elements(B, T, H, sd, init, g_std):
+    d = W.make_inputs(W.get("tiny", B=B, T=T, H=H, state_dtype=sd, initial_state=init, g_std=g_std,
+                            lower_bound=None, seed=40 + T))
+    assert d["lower_bound"] is None
+    out, fin = pu.run_gpu(d, want_final=sd is not None)
+    ref_out, ref_fin = pu.run_oracle(d, want_final=sd is not None)
+    print("unbounded", B, T, H, sd, init, pu.check(d, out, fin, ref_out, ref_fin, label=f"unbounded T={T}"))
+
+
+def test_unbounded_gate_varlen_with_empty_sequences():
+    seqlens = (0, 5, 130, 0, 1, 64)
+    d = W.make_inputs(W.get("varlen_ragged", H=2, seqlens=seqlens, lower_bound=None))
+    out, fin = pu.run_gpu(d)
+    ref_out, ref_fin = pu.run_oracle(d)
+    pu.check(d, out, fin, ref_out, ref_fin, label="unbounded varlen")
+    for n in [i for i, L in enumerate(seqlens) if L == 0]:
+        torch.testing.assert_close(fin[n], d["initial_state"][n].to(fin.dtype), rtol=0, atol=0)
+
+
+def test_unbounded_gate_full_size_sampled():
+    d = W.make_inputs(W.get("prefill_8k_unbounded"))
+    out, fin = pu.run_gpu(d)
+    pairs = _sample_pairs(d, 4, seed=11)
+    ref_out, ref_fin = pu.run_oracle(d, pairs=pairs)
+    print("prefill_8k_unbounded", pu.check(d, out, fin, ref_out, ref_fin, pairs=pairs,
+                                           label="prefill_8k_unbounded"))
+    assert torch.isfinite(out.float()).all() and torch.isfinite(fin.float()).all()
+
+
+def test_unbounded_and_bounded_gates_differ():
+    # the two entry points compute different gates on the same inputs
+    d = W.make_inputs(W.get("tiny", T=64, H=2))
+    du = dict(d, lower_bound=None)
+    o_b, _ = pu.run_gpu(d)
+    o_u, _ = pu.run_gpu(du)
+    assert (o_b.float() - o_u.float()).abs().max() > 1e-2
