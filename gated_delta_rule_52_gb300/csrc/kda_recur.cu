@@ -12,11 +12,15 @@
 //   out = scale * S^T q_hat,
 // where any decay down to zero is exact in fp32.
 //
-// Work split as in the one-token kernel: warp = (sequence, head, 8 state columns),
-// lane = (column quad, channel chunk) holding 4 columns x 8 channels; per token each
-// warp forms the activations of its channels and sums over K with shuffles among the
-// 16 lanes of its column quad.  The next token's inputs are loaded while the current
-// one is computed.
+// Work split: two CTAs of 8 warps per (sequence, head), 64 state columns each; warp =
+// 8 columns, lane = (column quad, channel chunk) holding 4 columns x 8 channels of the
+// state for the whole sequence.  The tokens go in blocks of 16: (A) all 256 threads
+// form the block's activations once (thread = token x 8 channels: norms by shuffles
+// over 16 threads, beta, the gate) into shared memory with the block's v rows, then
+// (B) every warp runs the block's 16 steps from there, summing over K with shuffles
+// among the 16 lanes of a column quad.  The next block's raw inputs are loaded during
+// (B).  Against one warp per 8 columns forming every token's activations itself, this
+// halves the time (the activations were computed 16 times per token).
 #include <cuda_bf16.h>
 
 #include "kda_internal.h"
@@ -31,26 +35,6 @@ constexpr int DK = kHeadDim;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kWarpsR = 8;   // warps per CTA
 
-// One token's raw inputs for one lane: q, k, g at channels ca..ca+3 and cb..cb+3,
-// v at the lane's 4 columns, the beta logit.
-struct TokIn {
-    uint2 qa, qc, ka, kc, ga, gc, vv;
-    float bl;
-};
-
-__device__ __forceinline__ void load_tok(const Params &p, int64_t row, int64_t h, int ca, int cb,
-                                         int vb, TokIn &x) {
-    const int64_t tok = (row * p.H + h) * DK;
-    x.qa = *reinterpret_cast<const uint2 *>(p.q + tok + ca);
-    x.qc = *reinterpret_cast<const uint2 *>(p.q + tok + cb);
-    x.ka = *reinterpret_cast<const uint2 *>(p.k + tok + ca);
-    x.kc = *reinterpret_cast<const uint2 *>(p.k + tok + cb);
-    x.ga = *reinterpret_cast<const uint2 *>(p.g + tok + ca);
-    x.gc = *reinterpret_cast<const uint2 *>(p.g + tok + cb);
-    x.vv = *reinterpret_cast<const uint2 *>(p.v + tok + vb);
-    x.bl = __bfloat162float(p.beta[row * p.H + h]);
-}
-
 // log2(1 + 2^-y) for y >= 0: the lg2 unit where 2^-y is not tiny, else the first two
 // terms of the series (relative error below 1e-7 there).
 __device__ __forceinline__ float log2_1p_exp2_neg(float y) {
@@ -58,18 +42,28 @@ __device__ __forceinline__ float log2_1p_exp2_neg(float y) {
     return e > 1e-3f ? __log2f(1.f + e) : e * (1.f - 0.5f * e) * kLog2e;
 }
 
+// Tokens per staged block: the CTA forms the block's activations once in shared
+// memory, then every warp runs the block's recurrence steps from there.
+constexpr int TB = 16;
+
 __global__ void __launch_bounds__(32 * kWarpsR) kda_recur_kernel(Params p) {
-    const int lane = threadIdx.x & 31;
-    const int64_t task = (int64_t)blockIdx.x * kWarpsR + (threadIdx.x >> 5);
-    const int64_t tasks = p.n_seqs * p.H * (DK / 8);
-    if (task >= tasks) return;
-    const int cg = (int)(task % (DK / 8));
-    const int64_t unit = task / (DK / 8), h = unit % p.H, n = unit / p.H;
+    __shared__ __align__(16) float qs[TB][DK], kks[TB][DK], als[TB][DK];
+    __shared__ float bs[TB];
+    __shared__ __align__(16) __nv_bfloat16 vs[TB][DK];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t unit = blockIdx.x >> 1;   // two CTAs (64 columns each) per (sequence, head)
+    const int qc = (int)(blockIdx.x & 1);
+    if (unit >= p.n_seqs * p.H) return;     // the grid is exactly 2 CTAs per unit; never taken
+    const int64_t h = unit % p.H, n = unit / p.H;
     int64_t b, t0, len;
     seq_range(p, n, b, t0, len);
+    const int64_t row0 = b * p.T + t0;
+    // recurrence role: lane = (column quad, channel chunk)
     const int cl = lane >> 4, r = lane & 15;
-    const int vb = 8 * cg + 4 * cl;                 // first of this lane's 4 columns
+    const int vb = 64 * qc + 8 * warp + 4 * cl;     // first of this lane's 4 columns
     const int ca = 4 * r, cb = 64 + 4 * r;          // its two channel chunks
+    // activation role: thread = (token of the block, 8 consecutive channels)
+    const int aj = tid >> 4, ac = 8 * (tid & 15);
     const size_t sbase = (size_t)(n * p.H + h) * DK * DK;
     const bool sbf = p.state_type == kStateBF16;
 
@@ -97,95 +91,140 @@ __global__ void __launch_bounds__(32 * kWarpsR) kda_recur_kernel(Params p) {
         for (int i = 0; i < 4; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = make_float2(0.f, 0.f);
     }
 
-    // per-head constants: the gate bias of this lane's channels (in log2 units) and
-    // -exp(A_log) (the softplus below is in log2 units, so alpha = 2^(ea * sp2))
+    // the activation role's gate bias (log2 units) and -exp(A_log)
     float2 db[4];
     {
-        const float4 da = *reinterpret_cast<const float4 *>(p.dt_bias + h * DK + ca);
-        const float4 dc = *reinterpret_cast<const float4 *>(p.dt_bias + h * DK + cb);
-        db[0] = make_float2(da.x * kLog2e, da.y * kLog2e); db[1] = make_float2(da.z * kLog2e, da.w * kLog2e);
-        db[2] = make_float2(dc.x * kLog2e, dc.y * kLog2e); db[3] = make_float2(dc.z * kLog2e, dc.w * kLog2e);
+        const float4 d0 = *reinterpret_cast<const float4 *>(p.dt_bias + h * DK + ac);
+        const float4 d1 = *reinterpret_cast<const float4 *>(p.dt_bias + h * DK + ac + 4);
+        db[0] = make_float2(d0.x * kLog2e, d0.y * kLog2e); db[1] = make_float2(d0.z * kLog2e, d0.w * kLog2e);
+        db[2] = make_float2(d1.x * kLog2e, d1.y * kLog2e); db[3] = make_float2(d1.z * kLog2e, d1.w * kLog2e);
     }
     const float ea = -__expf(p.A_log[h]);
     const float2 l2e = make_float2(kLog2e, kLog2e);
 
-    TokIn nxt;
-    if (len > 0) load_tok(p, b * p.T + t0, h, ca, cb, vb, nxt);
-    for (int64_t t = 0; t < len; ++t) {
-        const TokIn cur = nxt;
-        const int64_t row = b * p.T + t0 + t;
-        if (t + 1 < len) load_tok(p, row + 1, h, ca, cb, vb, nxt);
+    // raw inputs of the next block, loaded one block ahead
+    uint4 xq = make_uint4(0u, 0u, 0u, 0u), xk = xq, xg = xq;
+    float xb = 0.f;
+    uint4 xv = make_uint4(0u, 0u, 0u, 0u);
+    auto load_block = [&](int64_t blk) {
+        const int64_t j = blk + aj;
+        if (j < len) {
+            const int64_t tok = ((row0 + j) * p.H + h) * DK + ac;
+            xq = *reinterpret_cast<const uint4 *>(p.q + tok);
+            xk = *reinterpret_cast<const uint4 *>(p.k + tok);
+            xg = *reinterpret_cast<const uint4 *>(p.g + tok);
+            xv = *reinterpret_cast<const uint4 *>(p.v + tok);
+            if ((tid & 15) == 0) xb = __bfloat162float(p.beta[(row0 + j) * p.H + h]);
+        }
+    };
+    if (len > 0) load_block(0);
 
-        const float2 q2[4] = {bf16x2_to_f2(cur.qa.x), bf16x2_to_f2(cur.qa.y), bf16x2_to_f2(cur.qc.x),
-                              bf16x2_to_f2(cur.qc.y)};
-        const float2 k2[4] = {bf16x2_to_f2(cur.ka.x), bf16x2_to_f2(cur.ka.y), bf16x2_to_f2(cur.kc.x),
-                              bf16x2_to_f2(cur.kc.y)};
-        const float2 g2[4] = {bf16x2_to_f2(cur.ga.x), bf16x2_to_f2(cur.ga.y), bf16x2_to_f2(cur.gc.x),
-                              bf16x2_to_f2(cur.gc.y)};
-        // norms over K: this lane's 8 channels, then the 16 lanes of the column quad
-        float2 sq2 = make_float2(0.f, 0.f), sk2 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            sq2 = fma2(q2[e], q2[e], sq2);
-            sk2 = fma2(k2[e], k2[e], sk2);
-        }
-        float sq = sq2.x + sq2.y, sk = sk2.x + sk2.y;
-#pragma unroll
-        for (int o = 1; o < 16; o <<= 1) {
-            sq += __shfl_xor_sync(0xffffffffu, sq, o);
-            sk += __shfl_xor_sync(0xffffffffu, sk, o);
-        }
-        const float rq = rsqrtf(sq + 1e-6f), rk = rsqrtf(sk + 1e-6f);
-        const float beta = 1.f / (1.f + exp2f(-cur.bl * kLog2e));
-        // alpha = exp(-exp(A_log) softplus(x)) with x = g + dt_bias; in log2 units
-        // softplus(x) log2(e) = max(y, 0) + log2(1 + 2^-|y|), y = x log2(e)
-        float2 al[4], kn[4], qn[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 y = fma2(g2[e], l2e, db[e]);
-            const float spx = fmaxf(y.x, 0.f) + log2_1p_exp2_neg(fabsf(y.x));
-            const float spy = fmaxf(y.y, 0.f) + log2_1p_exp2_neg(fabsf(y.y));
-            al[e] = make_float2(exp2f(ea * spx), exp2f(ea * spy));
-            kn[e] = mul2(k2[e], make_float2(rk, rk));
-            qn[e] = mul2(q2[e], make_float2(rq, rq));
-        }
-        const float2 vf[2] = {bf16x2_to_f2(cur.vv.x), bf16x2_to_f2(cur.vv.y)};
-        // decay, then k_hat^T S per column (the four columns' sums interleaved)
-        float ks[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float2 acc = make_float2(0.f, 0.f);
+    for (int64_t blk = 0; blk < len; blk += TB) {
+        const int L = (int)((len - blk) < TB ? (len - blk) : TB);
+        // (A) activations of the block's tokens into shared memory
+        {
+            const bool ok = aj < L;
+            const uint32_t qw[4] = {xq.x, xq.y, xq.z, xq.w}, kw[4] = {xk.x, xk.y, xk.z, xk.w},
+                           gw[4] = {xg.x, xg.y, xg.z, xg.w};
+            float2 q2[4], k2[4];
+            float2 sq2 = make_float2(0.f, 0.f), sk2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                s[i][e] = mul2(s[i][e], al[e]);
-                acc = fma2(kn[e], s[i][e], acc);
+                q2[e] = bf16x2_to_f2(qw[e]);
+                k2[e] = bf16x2_to_f2(kw[e]);
+                sq2 = fma2(q2[e], q2[e], sq2);
+                sk2 = fma2(k2[e], k2[e], sk2);
             }
-            ks[i] = acc.x + acc.y;
-        }
+            float sq = sq2.x + sq2.y, sk = sk2.x + sk2.y;
 #pragma unroll
-        for (int o = 1; o < 16; o <<= 1)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) ks[i] += __shfl_xor_sync(0xffffffffu, ks[i], o);
-        float os[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float vi = (i & 1) ? vf[i >> 1].y : vf[i >> 1].x;
-            const float u = beta * (vi - ks[i]);
-            float2 oc = make_float2(0.f, 0.f);
+            for (int o = 1; o < 16; o <<= 1) {
+                sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                sk += __shfl_xor_sync(0xffffffffu, sk, o);
+            }
+            const float rq = rsqrtf(sq + 1e-6f), rk = rsqrtf(sk + 1e-6f);
+            float2 al[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                s[i][e] = fma2(kn[e], make_float2(u, u), s[i][e]);
-                oc = fma2(qn[e], s[i][e], oc);
+                const float2 y = fma2(bf16x2_to_f2(gw[e]), l2e, db[e]);
+                const float spx = fmaxf(y.x, 0.f) + log2_1p_exp2_neg(fabsf(y.x));
+                const float spy = fmaxf(y.y, 0.f) + log2_1p_exp2_neg(fabsf(y.y));
+                al[e] = make_float2(exp2f(ea * spx), exp2f(ea * spy));
+                q2[e] = mul2(q2[e], make_float2(rq, rq));
+                k2[e] = mul2(k2[e], make_float2(rk, rk));
             }
-            os[i] = oc.x + oc.y;
+            const float beta = 1.f / (1.f + exp2f(-xb * kLog2e));
+            __syncthreads();   // the previous block's steps are done with the tiles
+            if (ok) {
+                float4 *dq = reinterpret_cast<float4 *>(&qs[aj][ac]);
+                float4 *dk = reinterpret_cast<float4 *>(&kks[aj][ac]);
+                float4 *da = reinterpret_cast<float4 *>(&als[aj][ac]);
+                dq[0] = make_float4(q2[0].x, q2[0].y, q2[1].x, q2[1].y);
+                dq[1] = make_float4(q2[2].x, q2[2].y, q2[3].x, q2[3].y);
+                dk[0] = make_float4(k2[0].x, k2[0].y, k2[1].x, k2[1].y);
+                dk[1] = make_float4(k2[2].x, k2[2].y, k2[3].x, k2[3].y);
+                da[0] = make_float4(al[0].x, al[0].y, al[1].x, al[1].y);
+                da[1] = make_float4(al[2].x, al[2].y, al[3].x, al[3].y);
+                if ((tid & 15) == 0) bs[aj] = beta;
+                *reinterpret_cast<uint4 *>(&vs[aj][ac]) = xv;
+            }
         }
+        if (blk + TB < len) load_block(blk + TB);
+        __syncthreads();   // the block's activations are in shared memory
+
+        // (B) the block's recurrence steps
+#pragma unroll 1
+        for (int j = 0; j < L; ++j) {
+            const float4 qa = *reinterpret_cast<const float4 *>(&qs[j][ca]);
+            const float4 qb = *reinterpret_cast<const float4 *>(&qs[j][cb]);
+            const float4 ka = *reinterpret_cast<const float4 *>(&kks[j][ca]);
+            const float4 kb = *reinterpret_cast<const float4 *>(&kks[j][cb]);
+            const float4 aa = *reinterpret_cast<const float4 *>(&als[j][ca]);
+            const float4 ab = *reinterpret_cast<const float4 *>(&als[j][cb]);
+            const float beta = bs[j];
+            const float2 qn[4] = {make_float2(qa.x, qa.y), make_float2(qa.z, qa.w), make_float2(qb.x, qb.y),
+                                  make_float2(qb.z, qb.w)};
+            const float2 kn[4] = {make_float2(ka.x, ka.y), make_float2(ka.z, ka.w), make_float2(kb.x, kb.y),
+                                  make_float2(kb.z, kb.w)};
+            const float2 al[4] = {make_float2(aa.x, aa.y), make_float2(aa.z, aa.w), make_float2(ab.x, ab.y),
+                                  make_float2(ab.z, ab.w)};
+            const uint2 vw = *reinterpret_cast<const uint2 *>(&vs[j][vb]);
+            const float2 vf[2] = {bf16x2_to_f2(vw.x), bf16x2_to_f2(vw.y)};
+            float ks[4];
 #pragma unroll
-        for (int o = 1; o < 16; o <<= 1)
+            for (int i = 0; i < 4; ++i) {
+                float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) os[i] += __shfl_xor_sync(0xffffffffu, os[i], o);
-        if (r == 0)
-            *reinterpret_cast<uint2 *>(p.out + (row * p.H + h) * DK + vb) =
-                make_uint2(pack_bf16(p.scale * os[0], p.scale * os[1]), pack_bf16(p.scale * os[2], p.scale * os[3]));
+                for (int e = 0; e < 4; ++e) {
+                    s[i][e] = mul2(s[i][e], al[e]);
+                    acc = fma2(kn[e], s[i][e], acc);
+                }
+                ks[i] = acc.x + acc.y;
+            }
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) ks[i] += __shfl_xor_sync(0xffffffffu, ks[i], o);
+            float os[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float u = beta * (((i & 1) ? vf[i >> 1].y : vf[i >> 1].x) - ks[i]);
+                float2 oc = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    s[i][e] = fma2(kn[e], make_float2(u, u), s[i][e]);
+                    oc = fma2(qn[e], s[i][e], oc);
+                }
+                os[i] = oc.x + oc.y;
+            }
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) os[i] += __shfl_xor_sync(0xffffffffu, os[i], o);
+            if (r == 0)
+                *reinterpret_cast<uint2 *>(p.out + ((row0 + blk + j) * p.H + h) * DK + vb) =
+                    make_uint2(pack_bf16(p.scale * os[0], p.scale * os[1]),
+                               pack_bf16(p.scale * os[2], p.scale * os[3]));
+        }
     }
 
     if (p.fin) {
@@ -207,9 +246,9 @@ __global__ void __launch_bounds__(32 * kWarpsR) kda_recur_kernel(Params p) {
 }  // namespace
 
 cudaError_t launch_recur(const Params &p, cudaStream_t stream) {
-    const int64_t tasks = p.n_seqs * p.H * (DK / 8);
-    if (tasks == 0) return cudaSuccess;
-    kda_recur_kernel<<<(unsigned)((tasks + kWarpsR - 1) / kWarpsR), 32 * kWarpsR, 0, stream>>>(p);
+    const int64_t units = p.n_seqs * p.H;
+    if (units == 0) return cudaSuccess;
+    kda_recur_kernel<<<(unsigned)(units * 2), 32 * kWarpsR, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
