@@ -2,7 +2,8 @@
 // A and B from global memory into 128B-swizzled shared-memory tiles in the
 // K-major or MN-major layouts the KDA kernel uses, runs D = A*B with
 // tcgen05.mma (M = 128, bf16 in, fp32 out), and copies D out of tensor memory.
-// The pytest suite compares D with torch.matmul.
+// The pytest suite compares D with torch.matmul.  A second probe runs the bounded
+// mbarrier wait on a barrier nothing completes, to check that it gives up.
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -147,6 +148,25 @@ __global__ void tma_probe_kernel(const __grid_constant__ CUtensorMap tmap, int h
     }
 }
 
+// The bounded mbarrier wait every libkda kernel uses, on a barrier that nothing
+// arrives on (arrive == 0) or that one thread has completed (arrive == 1): out[0] = 1
+// if the wait succeeded, 2 if it gave up; out[1] = nanoseconds spent in it.
+__global__ void wait_probe_kernel(unsigned long long limit_ns, int arrive, unsigned long long *out) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (arrive) mbar_arrive(&bar);
+        const uint64_t t0 = globaltimer_ns();
+        const bool ok = mbar_wait(&bar, 0, limit_ns);
+        out[1] = globaltimer_ns() - t0;
+        out[0] = ok ? 1ull : 2ull;
+    }
+}
+
 }  // namespace
 
 extern "C" int kda_probe_tma(const void *src, int T, int H, int h, int t0, int c0, void *out,
@@ -164,5 +184,12 @@ extern "C" int kda_probe_tma(const void *src, int T, int H, int h, int t0, int c
     if (r != CUDA_SUCCESS) return 10 + (int)r;
     tma_probe_kernel<<<1, 128, 2048 + 8192, static_cast<cudaStream_t>(stream)>>>(
         tm, h, t0, c0, static_cast<__nv_bfloat16 *>(out), status);
+    return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+extern "C" int kda_probe_wait(unsigned long long limit_ns, int arrive, unsigned long long *out,
+                              void *stream) {
+    if (limit_ns > 1000000000ull) return 1;   // at most 1 s
+    wait_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_ns, arrive, out);
     return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }

@@ -61,3 +61,23 @@ def test_tma_3d_swizzled_load(probe, T, H, h, t0, c0):
     n = max(0, min(64, T - t0))
     ref[:n] = src[t0:t0 + n, h, c0:c0 + 64]
     assert torch.equal(out, ref)
+
+
+def test_bounded_wait_gives_up_and_the_context_stays_usable(probe):
+    # The wait every libkda kernel uses, on a barrier that nothing arrives on: it must
+    # give up after its limit (the kernels then set the device error word and unwind).
+    probe.kda_probe_wait.argtypes = [ctypes.c_ulonglong, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    probe.kda_probe_wait.restype = ctypes.c_int
+    out = torch.zeros(2, dtype=torch.int64, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    assert probe.kda_probe_wait(5_000_000, 0, out.data_ptr(), s) == 0   # 5 ms, never arrived
+    torch.cuda.synchronize()
+    status, ns = out.tolist()
+    assert status == 2 and 5_000_000 <= ns < 500_000_000, (status, ns)
+    assert probe.kda_probe_wait(5_000_000, 1, out.data_ptr(), s) == 0   # completed barrier
+    torch.cuda.synchronize()
+    status, ns = out.tolist()
+    assert status == 1 and ns < 5_000_000, (status, ns)
+    # the context still runs work afterwards
+    x = torch.arange(1024, device="cuda", dtype=torch.float32)
+    assert float(x.sum().item()) == 1024 * 1023 / 2
