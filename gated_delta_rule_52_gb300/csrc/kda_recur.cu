@@ -20,7 +20,9 @@
 // (B) every warp runs the block's 16 steps from there, summing over K with shuffles
 // among the 16 lanes of a column quad.  The next block's raw inputs are loaded during
 // (B).  Against one warp per 8 columns forming every token's activations itself, this
-// halves the time (the activations were computed 16 times per token).
+// halves the time (the activations were computed 16 times per token).  Calls with at most
+// one CTA per SM sum k_hat^T and q_hat^T of the decayed state in one reduction per token
+// (kOneSum); larger calls keep the second sum after the update.
 #include <cuda_bf16.h>
 
 #include "kda_internal.h"
@@ -46,9 +48,14 @@ __device__ __forceinline__ float log2_1p_exp2_neg(float y) {
 // memory, then every warp runs the block's recurrence steps from there.
 constexpr int TB = 16;
 
+// kOneSum: k_hat^T S' and q_hat^T S' of the decayed state S' = Diag(alpha) S summed in
+// one reduction, out = q_hat^T S' + (q_hat . k_hat) u (a shorter chain per token, faster
+// with one CTA per SM); otherwise q_hat^T S is summed after the update, which overlaps the
+// next token's decay (faster when two CTAs share an SM).
+template <bool kOneSum>
 __global__ void __launch_bounds__(32 * kWarpsR) kda_recur_kernel(Params p) {
     __shared__ __align__(16) float qs[TB][DK], kks[TB][DK], als[TB][DK];
-    __shared__ float bs[TB];
+    __shared__ float bs[TB], qks[TB];
     __shared__ __align__(16) __nv_bfloat16 vs[TB][DK];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t unit = blockIdx.x >> 1;   // two CTAs (64 columns each) per (sequence, head)
@@ -127,19 +134,21 @@ __global__ void __launch_bounds__(32 * kWarpsR) kda_recur_kernel(Params p) {
             const uint32_t qw[4] = {xq.x, xq.y, xq.z, xq.w}, kw[4] = {xk.x, xk.y, xk.z, xk.w},
                            gw[4] = {xg.x, xg.y, xg.z, xg.w};
             float2 q2[4], k2[4];
-            float2 sq2 = make_float2(0.f, 0.f), sk2 = make_float2(0.f, 0.f);
+            float2 sq2 = make_float2(0.f, 0.f), sk2 = make_float2(0.f, 0.f), sqk2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 q2[e] = bf16x2_to_f2(qw[e]);
                 k2[e] = bf16x2_to_f2(kw[e]);
                 sq2 = fma2(q2[e], q2[e], sq2);
                 sk2 = fma2(k2[e], k2[e], sk2);
+                if (kOneSum) sqk2 = fma2(q2[e], k2[e], sqk2);
             }
-            float sq = sq2.x + sq2.y, sk = sk2.x + sk2.y;
+            float sq = sq2.x + sq2.y, sk = sk2.x + sk2.y, sqk = sqk2.x + sqk2.y;
 #pragma unroll
             for (int o = 1; o < 16; o <<= 1) {
                 sq += __shfl_xor_sync(0xffffffffu, sq, o);
                 sk += __shfl_xor_sync(0xffffffffu, sk, o);
+                if (kOneSum) sqk += __shfl_xor_sync(0xffffffffu, sqk, o);
             }
             const float rq = rsqrtf(sq + 1e-6f), rk = rsqrtf(sk + 1e-6f);
             float2 al[4];
@@ -164,7 +173,10 @@ __global__ void __launch_bounds__(32 * kWarpsR) kda_recur_kernel(Params p) {
                 dk[1] = make_float4(k2[2].x, k2[2].y, k2[3].x, k2[3].y);
                 da[0] = make_float4(al[0].x, al[0].y, al[1].x, al[1].y);
                 da[1] = make_float4(al[2].x, al[2].y, al[3].x, al[3].y);
-                if ((tid & 15) == 0) bs[aj] = beta;
+                if ((tid & 15) == 0) {
+                    bs[aj] = beta;
+                    qks[aj] = sqk * rq * rk;   // q_hat . k_hat (used with kOneSum)
+                }
                 *reinterpret_cast<uint4 *>(&vs[aj][ac]) = xv;
             }
         }
@@ -180,7 +192,7 @@ __global__ void __launch_bounds__(32 * kWarpsR) kda_recur_kernel(Params p) {
             const float4 kb = *reinterpret_cast<const float4 *>(&kks[j][cb]);
             const float4 aa = *reinterpret_cast<const float4 *>(&als[j][ca]);
             const float4 ab = *reinterpret_cast<const float4 *>(&als[j][cb]);
-            const float beta = bs[j];
+            const float beta = bs[j], qk = qks[j];
             const float2 qn[4] = {make_float2(qa.x, qa.y), make_float2(qa.z, qa.w), make_float2(qb.x, qb.y),
                                   make_float2(qb.z, qb.w)};
             const float2 kn[4] = {make_float2(ka.x, ka.y), make_float2(ka.z, ka.w), make_float2(kb.x, kb.y),
@@ -189,37 +201,66 @@ __global__ void __launch_bounds__(32 * kWarpsR) kda_recur_kernel(Params p) {
                                   make_float2(ab.z, ab.w)};
             const uint2 vw = *reinterpret_cast<const uint2 *>(&vs[j][vb]);
             const float2 vf[2] = {bf16x2_to_f2(vw.x), bf16x2_to_f2(vw.y)};
-            float ks[4];
+            float ks[4], os[4];
+            if (kOneSum) {
+                float qs[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float2 acc = make_float2(0.f, 0.f);
+                for (int i = 0; i < 4; ++i) {
+                    float2 ak = make_float2(0.f, 0.f), aq = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    s[i][e] = mul2(s[i][e], al[e]);
-                    acc = fma2(kn[e], s[i][e], acc);
+                    for (int e = 0; e < 4; ++e) {
+                        s[i][e] = mul2(s[i][e], al[e]);
+                        ak = fma2(kn[e], s[i][e], ak);
+                        aq = fma2(qn[e], s[i][e], aq);
+                    }
+                    ks[i] = ak.x + ak.y;
+                    qs[i] = aq.x + aq.y;
                 }
-                ks[i] = acc.x + acc.y;
-            }
 #pragma unroll
-            for (int o = 1; o < 16; o <<= 1)
+                for (int o = 1; o < 16; o <<= 1)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) ks[i] += __shfl_xor_sync(0xffffffffu, ks[i], o);
-            float os[4];
+                    for (int i = 0; i < 4; ++i) {
+                        ks[i] += __shfl_xor_sync(0xffffffffu, ks[i], o);
+                        qs[i] += __shfl_xor_sync(0xffffffffu, qs[i], o);
+                    }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float u = beta * (((i & 1) ? vf[i >> 1].y : vf[i >> 1].x) - ks[i]);
-                float2 oc = make_float2(0.f, 0.f);
+                for (int i = 0; i < 4; ++i) {
+                    const float u = beta * (((i & 1) ? vf[i >> 1].y : vf[i >> 1].x) - ks[i]);
+                    os[i] = fmaf(qk, u, qs[i]);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    s[i][e] = fma2(kn[e], make_float2(u, u), s[i][e]);
-                    oc = fma2(qn[e], s[i][e], oc);
+                    for (int e = 0; e < 4; ++e) s[i][e] = fma2(kn[e], make_float2(u, u), s[i][e]);
                 }
-                os[i] = oc.x + oc.y;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        s[i][e] = mul2(s[i][e], al[e]);
+                        acc = fma2(kn[e], s[i][e], acc);
+                    }
+                    ks[i] = acc.x + acc.y;
+                }
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) ks[i] += __shfl_xor_sync(0xffffffffu, ks[i], o);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float u = beta * (((i & 1) ? vf[i >> 1].y : vf[i >> 1].x) - ks[i]);
+                    float2 oc = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        s[i][e] = fma2(kn[e], make_float2(u, u), s[i][e]);
+                        oc = fma2(qn[e], s[i][e], oc);
+                    }
+                    os[i] = oc.x + oc.y;
+                }
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) os[i] += __shfl_xor_sync(0xffffffffu, os[i], o);
             }
-#pragma unroll
-            for (int o = 1; o < 16; o <<= 1)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) os[i] += __shfl_xor_sync(0xffffffffu, os[i], o);
             if (r == 0)
                 *reinterpret_cast<uint2 *>(p.out + ((row0 + blk + j) * p.H + h) * DK + vb) =
                     make_uint2(pack_bf16(p.scale * os[0], p.scale * os[1]),
@@ -248,7 +289,14 @@ __global__ void __launch_bounds__(32 * kWarpsR) kda_recur_kernel(Params p) {
 cudaError_t launch_recur(const Params &p, cudaStream_t stream) {
     const int64_t units = p.n_seqs * p.H;
     if (units == 0) return cudaSuccess;
-    kda_recur_kernel<<<(unsigned)(units * 2), 32 * kWarpsR, 0, stream>>>(p);
+    int sms = 0;
+    const cudaError_t e = sm_count(sms);
+    if (e != cudaSuccess) return e;
+    // one CTA per SM or fewer: the latency of the per-token chain decides, so one sum
+    if (units * 2 <= sms)
+        kda_recur_kernel<true><<<(unsigned)(units * 2), 32 * kWarpsR, 0, stream>>>(p);
+    else
+        kda_recur_kernel<false><<<(unsigned)(units * 2), 32 * kWarpsR, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -413,8 +413,11 @@ def test_cuda_graph_capture_replays_the_call(name, wl):
                                                  (1, 1, 4, "bf16", "normal", 1.0),
                                                  (3, 70, 2, None, "none", 1.0),
                                                  (2, 17, 2, "bf16", "none", 1.0),
-                                                 (1, 200, 2, "fp32", "alternate", 3.0)])
+                                                 (1, 200, 2, "fp32", "alternate", 3.0),
+                                                 (40, 33, 2, "bf16", "normal", 1.0)])
 def test_unbounded_gate_all_elements(B, T, H, sd, init, g_std):
+    # up to 76 (sequence, head) units the kernel sums k^T S and q^T S in one reduction;
+    # the 80-unit case (160 CTAs on 152 SMs) takes the two-reduction form
     d = W.make_inputs(W.get("tiny", B=B, T=T, H=H, state_dtype=sd, initial_state=init, g_std=g_std,
                             lower_bound=None, seed=40 + T))
     assert d["lower_bound"] is None
