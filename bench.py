@@ -109,6 +109,14 @@ def algorithmic_flops(d) -> int:
     return d["B"] * d["T"] * d["H"] * FLOPS_PER_TOKEN_HEAD
 
 
+def workload_config(name: str, d) -> dict:
+    """The `config` keys both arms report for a workload."""
+    return {"workload": name, "B": d["B"], "T": d["T"], "H": d["H"], "K": 128, "V": 128,
+            "state": d["state_dtype"], "lower_bound": d["lower_bound"],
+            "gate": ("-exp(A_log) softplus(g + dt_bias), no lower bound"
+                     if d["lower_bound"] is None else "lower_bound sigmoid(exp(A_log) (g + dt_bias))")}
+
+
 def kernel_of(T: int, unbounded: bool = False) -> str:
     """The kernel libkda runs for a call of T packed token rows (the gate without a
     lower bound always runs the token recurrence)."""
@@ -321,8 +329,7 @@ def run_reference(args):
             "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / max(1, args.steps),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": w.name, "B": d["B"], "T": d["T"], "H": d["H"], "K": 128,
-                       "V": 128, "state": d["state_dtype"]},
+            "config": workload_config(w.name, d),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle",
                              "sample": f"per step {nthreads} (sequence, head) pairs x {tokens} "
                                        f"tokens, fp64"},
@@ -510,15 +517,11 @@ def run_ours(args):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "B": B, "T": T, "H": H, "K": 128, "V": 128,
-                       "state": d_cpu["state_dtype"], "lower_bound": d_cpu["lower_bound"],
-                       "gate": ("-exp(A_log) softplus(g + dt_bias), no lower bound"
-                                if d_cpu["lower_bound"] is None else
-                                "lower_bound sigmoid(exp(A_log) (g + dt_bias))"),
-                       "l2": f"algorithmic traffic {abytes / 1e6:.0f} MB per step "
-                             f"({'larger' if abytes > 129e6 else 'smaller'} than the 129 MB L2); "
-                             "a 256 MB flush write between timed steps",
-                       "timing": "CUDA events around each kda_fwd call"},
+            "config": dict(workload_config(w.name, d_cpu),
+                       l2=f"algorithmic traffic {abytes / 1e6:.0f} MB per step "
+                          f"({'larger' if abytes > 129e6 else 'smaller'} than the 129 MB L2); "
+                          "a 256 MB flush write between timed steps",
+                       timing="CUDA events around each kda_fwd call"),
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
             "gpu_launches": args.steps * lpc,
             "wall_s_timed_region": wall}

@@ -122,3 +122,13 @@ def test_gate_without_lower_bound_runs_the_recurrence():
     assert bench.launches_per_call(d, 152) == 1
     assert bench.kernel_of(8192, unbounded=True) == "recur" and bench.kernel_of(8192) == "cluster"
     assert "recur" in bench.KERNEL_NAMES and len(bench.kernel_source_hash("recur")) == 16
+
+
+def test_both_arms_report_the_same_workload_config():
+    d = W.make_inputs(W.get("tiny"))
+    c = bench.workload_config("tiny", d)
+    assert c["workload"] == "tiny" and c["T"] == 256 and c["lower_bound"] == -5.0
+    assert "sigmoid" in c["gate"]
+    du = W.make_inputs(W.get("tiny", lower_bound=None))
+    cu = bench.workload_config("tiny", du)
+    assert cu["lower_bound"] is None and "softplus" in cu["gate"]
