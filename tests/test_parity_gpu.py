@@ -453,3 +453,16 @@ def test_unbounded_and_bounded_gates_differ():
     o_b, _ = pu.run_gpu(d)
     o_u, _ = pu.run_gpu(du)
     assert (o_b.float() - o_u.float()).abs().max() > 1e-2
+
+
+@pytest.mark.parametrize("sd", ["fp32", "bf16"])
+def test_unbounded_gate_zero_length_passes_state_through(sd):
+    d = W.make_inputs(W.get("batch_state", B=2, T=0, H=3, state_dtype=sd, lower_bound=None))
+    out, fin = pu.run_gpu(d)
+    assert out.numel() == 0
+    torch.testing.assert_close(fin, d["initial_state"].to(fin.dtype), rtol=0, atol=0)
+    # and a varlen call whose sequences are all empty
+    dv = W.make_inputs(W.get("varlen_ragged", H=2, seqlens=(0, 0, 0), lower_bound=None))
+    assert dv["T"] == 0
+    out, fin = pu.run_gpu(dv)
+    torch.testing.assert_close(fin, dv["initial_state"].to(fin.dtype), rtol=0, atol=0)
