@@ -18,6 +18,10 @@ __device__ int g_kda_error = 0;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Most (sequence, head) units one call may hold: the widest launch (the sequence-parallel
+// path's per-segment kernels, up to 32 segments per unit) must stay within 2^31 - 1 CTAs.
+constexpr int64_t kMaxUnits = ((int64_t(1) << 31) - 1) / 32;
+
 // Validates the arguments of kda_fwd and fills `p`.  Touches no device state.
 kda_status validate(const void *q, const void *k, const void *v, const void *g, const void *beta,
                     float scale, void *out, const float *A_log, const float *dt_bias,
@@ -35,6 +39,7 @@ kda_status validate(const void *q, const void *k, const void *v, const void *g, 
     }
     const int64_t N = cu_seqlens ? num_seqs : B;
     if (H == 0 && N > 0 && T > 0) return KDA_ERR_SHAPE;
+    if (N > 0 && H > 0 && N > kMaxUnits / H) return KDA_ERR_SHAPE;
     if (initial_state || final_state) {
         if (state_dtype != KDA_STATE_BF16 && state_dtype != KDA_STATE_FP32) return KDA_ERR_DTYPE;
     } else if (state_dtype != KDA_STATE_NONE && state_dtype != KDA_STATE_BF16 &&

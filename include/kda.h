@@ -38,7 +38,8 @@ typedef enum {
     KDA_ERR_DTYPE = 2,       /* state pointer given with state_dtype KDA_STATE_NONE,
                                 or an unknown state_dtype code                          */
     KDA_ERR_SHAPE = 3,       /* negative size, H == 0 with work to do, B != 1 with
-                                cu_seqlens, num_seqs < 1 with cu_seqlens                */
+                                cu_seqlens, num_seqs < 1 with cu_seqlens, or more than
+                                2^26 - 1 (sequence, head) units (N * H) in one call    */
     KDA_ERR_UNSUPPORTED = 4, /* K != 128 or V != 128 (the only head size supported)    */
     KDA_ERR_ALIGN = 5,       /* a tensor pointer is not 16-byte aligned                 */
     KDA_ERR_VALUE = 6,       /* lower_bound outside [-5, 0], non-finite scale, or (for

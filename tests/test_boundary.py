@@ -183,3 +183,10 @@ def test_unbounded_gate_entry_point_validates(L):
     assert call_unbounded(init=P[9], sdt=kda.KDA_STATE_NONE) == kda.KDA_ERR_DTYPE
     assert call_unbounded(cu=P[8], nseq=2, B=3) == kda.KDA_ERR_SHAPE
     assert call_unbounded(q=None, k=None, v=None, g=None, beta=None, out=None, B=0) == kda.KDA_OK
+
+
+def test_too_many_units_rejected(L):
+    # N * H above 2^26 - 1 would overflow the widest grid; rejected before any launch
+    assert call(B=1 << 20, H=128, T=1) == kda.KDA_ERR_SHAPE
+    assert call(B=1 << 40, H=1 << 30, T=1) == kda.KDA_ERR_SHAPE   # no int64 overflow either
+    assert call_unbounded(B=1 << 20, H=128, T=1) == kda.KDA_ERR_SHAPE
