@@ -181,6 +181,27 @@ def test_chunked_formula_equals_recurrence(C):
         np.testing.assert_allclose(fin[0, h], S.T, rtol=1e-9, atol=1e-10)
 
 
+@pytest.mark.parametrize("C", [1, 3, 64])
+def test_chunked_formula_equals_recurrence_unbounded_gate(C):
+    # the gate without a lower bound decays by up to ~e^-60 per token here; the chunked
+    # formula (explicit exp(G_t - G_i) <= 1) must still equal the token recurrence
+    r = rng(40 + C)
+    B, T, H, K, V = 1, 140, 2, 16, 12
+    q, k = r.standard_normal((B, T, H, K)), r.standard_normal((B, T, H, K))
+    g = 2.0 * r.standard_normal((B, T, H, K))
+    v = r.standard_normal((B, T, H, V)); bl = r.standard_normal((B, T, H))
+    A_log = np.log(np.array([1.0, 16.0])); dt = 0.1 * r.standard_normal((H, K))
+    S0 = 0.1 * r.standard_normal((B, H, V, K))
+    out, fin = oracle.kda_fwd(q, k, v, g, bl, 0.3, A_log, dt, None, initial_state=S0)
+    qn, kn, gk, b = oracle.activations(q, k, g, bl, A_log, dt, None)
+    assert gk.min() < -40.0
+    for h in range(H):
+        o, S = chunked_pair(qn[0, :, h], kn[0, :, h], v[0, :, h], gk[0, :, h], b[0, :, h], 0.3,
+                            S0[0, h].T, C)
+        np.testing.assert_allclose(out[0, :, h], o, rtol=1e-9, atol=1e-10)
+        np.testing.assert_allclose(fin[0, h], S.T, rtol=1e-9, atol=1e-10)
+
+
 # ---------------------------------------------------------------- activations
 def test_gate_special_values():
     # gk = lb * sigmoid(exp(A_log) * (g + dt_bias)):
