@@ -7,9 +7,15 @@ One step = one kda_fwd call (the whole hot path: prologue, intra-chunk UT/WY,
 chunk-sequential state pass, state load/store) over the long-prefill workload
 B=1, T=8192, H=64, K=V=128 with bf16 initial/final state.  Inputs are seeded
 synthetic data resident in HBM; out/final_state are preallocated.  The working
-set (~600 MB of algorithmic traffic) is larger than L2 (129 MB) and a 256 MB
-L2-flush write runs between timed steps (outside the timed kernel).  Each step is timed with CUDA
-events on the launching stream; rank 0 prints one JSON line.
+set (676 MB of algorithmic traffic) is larger than L2 (129 MB) and a 256 MB
+L2-flush write runs between timed steps (outside the timed kernel).  Each step is timed
+with CUDA events on the launching stream; rank 0 prints one JSON line.
+
+--workload picks another named workload (gated_delta_rule_52_gb300/workloads.py): the
+other prefill/varlen shapes, the decode and short-step batches (decode, decode_16, step_64,
+varlen_short), the few-head long prefill (prefill_64k_h8, sequence-parallel path) and the
+gate without a lower bound (prefill_8k_unbounded, token recurrence, roofline on the fp32
+lanes).  Every kernel's time is the whole kda_fwd call.
 
 --impl reference times the fp64 CPU oracle (the baseline, on the host cores) on
 a bounded sample of the same workload.
