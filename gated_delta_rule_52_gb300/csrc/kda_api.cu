@@ -229,6 +229,15 @@ kda_status kda_fwd_unbounded(const void *q, const void *k, const void *v, const 
                                                                                 : KDA_ERR_CUDA;
 }
 
+size_t kda_workspace_size(int64_t num_seqs, int64_t H) {
+    if (num_seqs < 0 || H < 0) return 0;
+    if (num_seqs == 0 || H == 0) return 0;
+    const uint64_t per = (uint64_t)KDA_WORKSPACE_BYTES_PER_UNIT;
+    const uint64_t n = (uint64_t)num_seqs, h = (uint64_t)H;
+    if (n > SIZE_MAX / h || n * h > SIZE_MAX / per) return 0;
+    return (size_t)(n * h * per);
+}
+
 const char *kda_status_string(int status) {
     switch (status) {
         case KDA_OK: return "KDA_OK";

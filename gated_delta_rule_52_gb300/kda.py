@@ -36,8 +36,8 @@ KDA_STATE_BF16 = 1
 KDA_STATE_FP32 = 2
 
 # Every symbol include/kda.h declares.
-EXPORTED = ("kda_fwd", "kda_fwd_ws", "kda_fwd_unbounded", "kda_status_string",
-            "kda_get_device_status", "kda_version")
+EXPORTED = ("kda_fwd", "kda_fwd_ws", "kda_fwd_unbounded", "kda_workspace_size",
+            "kda_status_string", "kda_get_device_status", "kda_version")
 
 # Workspace bytes per (sequence, head) of kda_fwd_ws (KDA_WORKSPACE_BYTES_PER_UNIT).
 WORKSPACE_BYTES_PER_UNIT = 99328
@@ -71,6 +71,8 @@ def lib() -> ctypes.CDLL:
             L.kda_fwd_unbounded.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp, vp, vp, ci, vp, i64,
                                             i64, i64, i64, i64, i64, vp]
             L.kda_fwd_unbounded.restype = ci
+            L.kda_workspace_size.argtypes = [i64, i64]
+            L.kda_workspace_size.restype = ctypes.c_size_t
             L.kda_status_string.argtypes = [ci]
             L.kda_status_string.restype = ctypes.c_char_p
             L.kda_get_device_status.argtypes = [vp]

@@ -116,6 +116,11 @@ kda_status kda_fwd(const void *q, const void *k, const void *v, const void *g, c
  * total (N = num_seqs with cu_seqlens, else B). */
 #define KDA_WORKSPACE_BYTES_PER_UNIT 99328
 
+/* Bytes of the workspace kda_fwd_ws needs for N sequences of H heads (N = num_seqs with
+ * cu_seqlens, else B): N * H * KDA_WORKSPACE_BYTES_PER_UNIT.  Returns 0 for negative
+ * sizes or a product that does not fit in size_t.  Pure host arithmetic. */
+size_t kda_workspace_size(int64_t num_seqs, int64_t H);
+
 /*
  * kda_fwd_ws — kda_fwd without any allocation: the caller passes the workspace.
  * Same arguments and semantics as kda_fwd, plus

@@ -190,3 +190,10 @@ def test_too_many_units_rejected(L):
     assert call(B=1 << 20, H=128, T=1) == kda.KDA_ERR_SHAPE
     assert call(B=1 << 40, H=1 << 30, T=1) == kda.KDA_ERR_SHAPE   # no int64 overflow either
     assert call_unbounded(B=1 << 20, H=128, T=1) == kda.KDA_ERR_SHAPE
+
+
+def test_workspace_size_query(L):
+    assert L.kda_workspace_size(3, 5) == 3 * 5 * kda.WORKSPACE_BYTES_PER_UNIT == kda.workspace_bytes(3, 5)
+    assert L.kda_workspace_size(0, 5) == 0 and L.kda_workspace_size(3, 0) == 0
+    assert L.kda_workspace_size(-1, 5) == 0 and L.kda_workspace_size(3, -2) == 0
+    assert L.kda_workspace_size(1 << 40, 1 << 30) == 0   # does not fit in size_t
