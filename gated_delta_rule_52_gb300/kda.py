@@ -8,7 +8,8 @@ or fails to load this module raises, it never falls back to anything else.
 The Python signature mirrors flash_kda.fwd from the FlashKDA README "Kernel
 API" section: ``kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias,
 lower_bound, initial_state=None, final_state=None, cu_seqlens=None)``; it
-returns nothing and writes ``out`` (and ``final_state``) in place.
+returns nothing and writes ``out`` (and ``final_state``) in place.  ``lower_bound=None``
+selects the gate without a lower bound (the C entry point kda_fwd_unbounded).
 """
 from __future__ import annotations
 
