@@ -14,8 +14,9 @@
  *
  * The pages name the gate inputs (A_log "log-gate parameter", dt_bias "gate
  * bias", lower_bound "gate lower bound, -5.0 to 0") but print no formula; the
- * gate above is this library's reading.  The L2 norm uses eps = 1e-6 inside the
- * square root.
+ * gate above is this library's reading.  kda_fwd_unbounded takes the gate with no
+ * lower bound instead, -exp(A_log[h]) * softplus(g_t[c] + dt_bias[h][c]).  The L2
+ * norm uses eps = 1e-6 inside the square root.
  *
  * Everything here is plain C: device pointers, host scalars, a stream handle.
  */
