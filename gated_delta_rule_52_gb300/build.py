@@ -68,25 +68,5 @@ def build_library(force: bool = False, verbose: bool = False, extra=()) -> str:
     return OUT
 
 
-
-PROBE_SRC = os.path.join(PKG, "..", "tests", "csrc", "tc_probe.cu")
-PROBE_OUT = os.path.join(PKG, "..", "tests", "csrc", "libkda_probe.so")
-
-
-def build_probe(force: bool = False) -> str:
-    """Builds the test-only tcgen05 probe library (tests/csrc/libkda_probe.so)."""
-    hdrs = glob.glob(os.path.join(CSRC, "*.cuh"))
-    if not force and not _stale([PROBE_SRC], hdrs, PROBE_OUT):
-        return PROBE_OUT
-    tmp = PROBE_OUT + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *ARCH, *FLAGS, "-shared", "-o", tmp, PROBE_SRC, "-lcuda"]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode:
-        sys.stderr.write(r.stdout + r.stderr)
-        raise RuntimeError("building the tcgen05 probe failed")
-    os.replace(tmp, PROBE_OUT)
-    return PROBE_OUT
-
-
 if __name__ == "__main__":
     print(build_library(force="--force" in sys.argv, verbose="-v" in sys.argv))

@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(32 * kWarpsR) kda_recur_kernel(Params p) {
             const float2 vf[2] = {bf16x2_to_f2(vw.x), bf16x2_to_f2(vw.y)};
             float ks[4], os[4];
             if (kOneSum) {
-                float qs[4];
+                float qsum[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     float2 ak = make_float2(0.f, 0.f), aq = make_float2(0.f, 0.f);
@@ -214,19 +214,19 @@ __global__ void __launch_bounds__(32 * kWarpsR) kda_recur_kernel(Params p) {
                         aq = fma2(qn[e], s[i][e], aq);
                     }
                     ks[i] = ak.x + ak.y;
-                    qs[i] = aq.x + aq.y;
+                    qsum[i] = aq.x + aq.y;
                 }
 #pragma unroll
                 for (int o = 1; o < 16; o <<= 1)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         ks[i] += __shfl_xor_sync(0xffffffffu, ks[i], o);
-                        qs[i] += __shfl_xor_sync(0xffffffffu, qs[i], o);
+                        qsum[i] += __shfl_xor_sync(0xffffffffu, qsum[i], o);
                     }
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const float u = beta * (((i & 1) ? vf[i >> 1].y : vf[i >> 1].x) - ks[i]);
-                    os[i] = fmaf(qk, u, qs[i]);
+                    os[i] = fmaf(qk, u, qsum[i]);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) s[i][e] = fma2(kn[e], make_float2(u, u), s[i][e]);
                 }

@@ -189,12 +189,12 @@ def get_device_status(stream=None) -> int:
 
 
 def raw_call(*args):
-    """Direct call of the C entry point with already-marshalled arguments (tests of
+    """Direct call of the C entry point with already-marshalled arguments (checks of
     the validation path use this with host-side fake pointers; nothing is launched
     when validation fails)."""
     return int(lib().kda_fwd(*args))
 
 
 def raw_call_ws(*args):
-    """Direct call of kda_fwd_ws with already-marshalled arguments (validation tests)."""
+    """Direct call of kda_fwd_ws with already-marshalled arguments (validation checks)."""
     return int(lib().kda_fwd_ws(*args))

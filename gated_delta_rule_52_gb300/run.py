@@ -1,12 +1,11 @@
 """Runs kda_fwd on a seeded synthetic workload (for profiling and quick checks).
 
   python -m gated_delta_rule_52_gb300.run [--workload prefill_8k] [--T 2048] [--H 64]
-                                          [--iters 3] [--check]
+                                          [--iters 3]
 
 Builds libkda.so if needed, draws the workload's inputs on the GPU, calls
-kda_fwd `iters` times and prints the CUDA-event time of the last call.  With
---check it also compares a few (sequence, head) pairs with the fp64 oracle (a
-test-only dependency).
+kda_fwd `iters` times and prints the CUDA-event time of the last call and the
+device status.  It checks no numbers: a profiling and timing runner only.
 """
 import argparse
 import os
@@ -28,7 +27,6 @@ def main(argv=None):
     ap.add_argument("--T", type=int, default=None)
     ap.add_argument("--H", type=int, default=None)
     ap.add_argument("--iters", type=int, default=3)
-    ap.add_argument("--check", action="store_true")
     a = ap.parse_args(argv)
     over = {}
     if a.T is not None:
@@ -54,15 +52,7 @@ def main(argv=None):
     st = kda.get_device_status()
     print(f"{a.workload} B={d['B']} T={d['T']} H={d['H']}: {s.elapsed_time(t):.3f} ms "
           f"(last call), device status {st}")
-    if st != kda.KDA_OK:
-        return 1
-    if a.check:
-        sys.path.insert(0, ROOT)
-        from tests import parity_util as pu
-        pairs = [(0, 0), (d["N"] - 1, d["H"] - 1)]
-        ro, rf = pu.run_oracle(d, pairs=pairs)
-        print(pu.check(d, out.cpu(), fin.cpu() if fin is not None else None, ro, rf, pairs=pairs))
-    return 0
+    return 0 if st == kda.KDA_OK else 1
 
 
 if __name__ == "__main__":

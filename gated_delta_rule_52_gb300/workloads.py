@@ -2,7 +2,7 @@
 
 This module only draws random numbers and lays them out; it holds none of the
 method's arithmetic (no gate, no normalisation, no recurrence).  Both the fp64
-oracle tests and the CUDA path take their inputs from here, so the two sides see
+reference and the CUDA path take their inputs from here, so the two sides see
 identical bf16/fp32 values.
 
 Shapes and dtypes follow the FlashKDA README's Kernel API table ("Kernel API",

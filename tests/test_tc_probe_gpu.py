@@ -3,17 +3,38 @@ descriptor encodings (K-major and MN-major 128B-swizzled tiles, M = 128, the N
 and K extents the KDA kernel uses) against torch.matmul, plus a TMEM store/load
 round trip."""
 import ctypes
+import glob
+import os
+import subprocess
 
 import pytest
 import torch
 
 pytestmark = pytest.mark.gpu
 
+HERE = os.path.dirname(os.path.abspath(__file__))
+PROBE_SRC = os.path.join(HERE, "csrc", "tc_probe.cu")
+PROBE_OUT = os.path.join(HERE, "csrc", "libkda_probe.so")
+
+
+def build_probe() -> str:
+    """Builds the probe library (tests/csrc/libkda_probe.so) with the product's flags."""
+    from gated_delta_rule_52_gb300 import build
+    hdrs = glob.glob(os.path.join(build.CSRC, "*.cuh"))
+    if os.path.exists(PROBE_OUT) and all(os.path.getmtime(f) <= os.path.getmtime(PROBE_OUT)
+                                         for f in [PROBE_SRC, *hdrs]):
+        return PROBE_OUT
+    tmp = PROBE_OUT + f".tmp{os.getpid()}"
+    cmd = [build.nvcc(), *build.ARCH, *build.FLAGS, "-shared", "-o", tmp, PROBE_SRC, "-lcuda"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    os.replace(tmp, PROBE_OUT)
+    return PROBE_OUT
+
 
 @pytest.fixture(scope="module")
 def probe():
-    from gated_delta_rule_52_gb300 import build
-    L = ctypes.CDLL(build.build_probe())
+    L = ctypes.CDLL(build_probe())
     L.kda_probe_mma.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 5 + [ctypes.c_void_p] * 2
     L.kda_probe_mma.restype = ctypes.c_int
     return L
