@@ -10,6 +10,13 @@
 
 static_assert(KDA_WORKSPACE_BYTES_PER_UNIT == kda::kWsBytesPerUnit, "workspace size in kda.h");
 
+// Scratch of kda_fwd_static, for callers that cannot allocate: a fixed array in the
+// library's own device memory, present on every device that loads the library.  Host
+// code must not pass its name to a kernel (on the host it names a host-side stand-in);
+// the device address comes from cudaGetSymbolAddress (static_workspace below).
+static __device__ __align__(256) unsigned char
+    g_kda_static_ws[(size_t)KDA_STATIC_MAX_UNITS * KDA_WORKSPACE_BYTES_PER_UNIT];
+
 namespace {
 
 // Set by kernels whose bounded waits give up; read and cleared by
@@ -159,6 +166,23 @@ kda_status launch(kda::Params &p, void *stream, int64_t tsplit = 0) {
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+// Device address of g_kda_static_ws on the current device, looked up once per device
+// (with that device current) and cached.
+cudaError_t static_workspace(unsigned char *&ws) {
+    static std::atomic<bool> done[kda::kMaxDevices];
+    static unsigned char *addr_of[kda::kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= kda::kMaxDevices) return cudaGetSymbolAddress(reinterpret_cast<void **>(&ws), g_kda_static_ws);
+    e = kda::once_per_device(done, [&](int d) {
+        return cudaGetSymbolAddress(reinterpret_cast<void **>(&addr_of[d]), g_kda_static_ws);
+    });
+    if (e != cudaSuccess) return e;
+    ws = addr_of[dev];
+    return cudaSuccess;
+}
+
 }  // namespace
 
 extern "C" {
@@ -229,6 +253,26 @@ kda_status kda_fwd_unbounded(const void *q, const void *k, const void *v, const 
                                                                                 : KDA_ERR_CUDA;
 }
 
+kda_status kda_fwd_static(const void *q, const void *k, const void *v, const void *g,
+                          const void *beta, float scale, void *out, const float *A_log,
+                          const float *dt_bias, float lower_bound, const void *initial_state,
+                          void *final_state, int state_dtype, const int64_t *cu_seqlens,
+                          int64_t num_seqs, int64_t B, int64_t T, int64_t H, int64_t K, int64_t V,
+                          void *stream) {
+    kda::Params p{};   // every field zero until validate() fills it
+    kda_status st = validate(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound,
+                             initial_state, final_state, state_dtype, cu_seqlens, num_seqs, B, T,
+                             H, K, V, p);
+    if (st != KDA_OK) return st;
+    const int64_t units = p.n_seqs * p.H;
+    if (units > KDA_STATIC_MAX_UNITS) return KDA_ERR_LIMIT;
+    if (units == 0) return KDA_OK;
+    unsigned char *ws = nullptr;
+    if (static_workspace(ws) != cudaSuccess) return KDA_ERR_CUDA;
+    p.ws = ws;
+    return launch(p, stream);
+}
+
 size_t kda_workspace_size(int64_t num_seqs, int64_t H) {
     if (num_seqs < 0 || H < 0) return 0;
     if (num_seqs == 0 || H == 0) return 0;
@@ -249,6 +293,7 @@ const char *kda_status_string(int status) {
         case KDA_ERR_VALUE: return "KDA_ERR_VALUE: lower_bound outside [-5, 0], non-finite scale or workspace too small";
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA call or launch failed";
         case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded device wait expired";
+        case KDA_ERR_LIMIT: return "KDA_ERR_LIMIT: kda_fwd_static takes at most KDA_STATIC_MAX_UNITS (sequence, head) units";
         default: return "KDA: unknown status";
     }
 }

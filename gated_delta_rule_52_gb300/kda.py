@@ -31,6 +31,7 @@ KDA_ERR_ALIGN = 5
 KDA_ERR_VALUE = 6
 KDA_ERR_CUDA = 7
 KDA_ERR_TIMEOUT = 8
+KDA_ERR_LIMIT = 9
 
 KDA_STATE_NONE = 0
 KDA_STATE_BF16 = 1
@@ -38,10 +39,12 @@ KDA_STATE_FP32 = 2
 
 # Every symbol include/kda.h declares.
 EXPORTED = ("kda_fwd", "kda_fwd_ws", "kda_fwd_unbounded", "kda_workspace_size",
-            "kda_status_string", "kda_get_device_status", "kda_version")
+            "kda_status_string", "kda_get_device_status", "kda_version", "kda_fwd_static")
 
 # Workspace bytes per (sequence, head) of kda_fwd_ws (KDA_WORKSPACE_BYTES_PER_UNIT).
 WORKSPACE_BYTES_PER_UNIT = 99328
+# Most (sequence, head) units of one kda_fwd_static call (KDA_STATIC_MAX_UNITS).
+STATIC_MAX_UNITS = 128
 
 _lock = threading.Lock()
 _lib = None
@@ -72,6 +75,9 @@ def lib() -> ctypes.CDLL:
             L.kda_fwd_unbounded.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp, vp, vp, ci, vp, i64,
                                             i64, i64, i64, i64, i64, vp]
             L.kda_fwd_unbounded.restype = ci
+            L.kda_fwd_static.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp, f, vp, vp, ci, vp,
+                                         i64, i64, i64, i64, i64, i64, vp]
+            L.kda_fwd_static.restype = ci
             L.kda_workspace_size.argtypes = [i64, i64]
             L.kda_workspace_size.restype = ctypes.c_size_t
             L.kda_status_string.argtypes = [ci]
@@ -179,6 +185,43 @@ def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_s
     else:
         _check_tensor("workspace", workspace, torch.uint8)
         st = lib().kda_fwd_ws(*args, _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    if st != KDA_OK:
+        raise KDAError(st, status_string(st))
+
+
+def kda_fwd_static(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound,
+                   initial_state=None, final_state=None, cu_seqlens=None, stream=None) -> None:
+    """kda_fwd through the C entry point kda_fwd_static, which allocates nothing: for
+    callers that cannot allocate device memory (an engine that owns all of it, a
+    plug-in host that hands over only the inputs and outputs).  Its scratch is a fixed
+    array inside libkda.so, so a call holds at most ``STATIC_MAX_UNITS`` (sequence,
+    head) units, and calls that may overlap on the GPU race on that array.  Same
+    arguments and results as ``kda_fwd`` with a lower bound."""
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, H, K]")
+    B, T, H, K = q.shape
+    V = v.shape[-1] if v.dim() == 4 else -1
+    for name, t, shape in (("q", q, None), ("k", k, (B, T, H, K)), ("g", g, (B, T, H, K)),
+                           ("v", v, (B, T, H, V)), ("beta", beta, (B, T, H)),
+                           ("out", out, (B, T, H, V))):
+        _check_tensor(name, t, torch.bfloat16, shape)
+    _check_tensor("A_log", A_log, torch.float32, (H,))
+    _check_tensor("dt_bias", dt_bias, torch.float32, (H, K))
+    num_seqs = 0
+    if cu_seqlens is not None:
+        _check_tensor("cu_seqlens", cu_seqlens, torch.int64)
+        if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+            raise ValueError("cu_seqlens must be 1-D with at least 2 entries")
+        num_seqs = cu_seqlens.numel() - 1
+    N = num_seqs if cu_seqlens is not None else B
+    code = state_dtype_code(initial_state, final_state)
+    for name, s in (("initial_state", initial_state), ("final_state", final_state)):
+        if s is not None:
+            _check_tensor(name, s, s.dtype, (N, H, V, K))
+    st = lib().kda_fwd_static(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                              _ptr(out), _ptr(A_log), _ptr(dt_bias), float(lower_bound),
+                              _ptr(initial_state), _ptr(final_state), code, _ptr(cu_seqlens),
+                              num_seqs, B, T, H, K, V, _stream_handle(stream))
     if st != KDA_OK:
         raise KDAError(st, status_string(st))
 

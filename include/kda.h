@@ -46,7 +46,8 @@ typedef enum {
     KDA_ERR_VALUE = 6,       /* lower_bound outside [-5, 0], non-finite scale, or (for
                                 kda_fwd_ws) a workspace smaller than required          */
     KDA_ERR_CUDA = 7,        /* a CUDA runtime call or kernel launch failed             */
-    KDA_ERR_TIMEOUT = 8      /* a bounded on-device wait expired (kda_get_device_status) */
+    KDA_ERR_TIMEOUT = 8,     /* a bounded on-device wait expired (kda_get_device_status) */
+    KDA_ERR_LIMIT = 9        /* kda_fwd_static: N * H above KDA_STATIC_MAX_UNITS          */
 } kda_status;
 
 /* Element type of initial_state / final_state (both, when both are given). */
@@ -165,6 +166,42 @@ kda_status kda_fwd_unbounded(const void *q, const void *k, const void *v, const 
                              const float *dt_bias, const void *initial_state, void *final_state,
                              int state_dtype, const int64_t *cu_seqlens, int64_t num_seqs,
                              int64_t B, int64_t T, int64_t H, int64_t K, int64_t V, void *stream);
+
+/* Most (sequence, head) units, N * H, that one kda_fwd_static call may hold. */
+#define KDA_STATIC_MAX_UNITS 128
+
+/*
+ * kda_fwd_static — kda_fwd for a caller that cannot allocate device memory.
+ * The pages describe nothing like it: it exists for callers such as a serving
+ * engine that reserves all device memory for its own pool up front (a library's
+ * cudaMalloc there fails, or breaks the engine's budget), a plug-in host whose
+ * interface hands a plug-in only its input and output buffers, or a request path
+ * that must not allocate because an allocation can block or synchronise the device.
+ *
+ * Same arguments, results and asynchrony as kda_fwd.  The caller passes the inputs
+ * and outputs only; the call allocates nothing (no cudaMalloc, cudaMallocAsync or
+ * cudaFree, no allocating library routine).  Its scratch is one array of
+ * KDA_STATIC_MAX_UNITS * KDA_WORKSPACE_BYTES_PER_UNIT bytes (12,713,984 bytes) in
+ * libkda.so's own device memory: every GPU that loads the library holds it until
+ * the process exits.  Consequences:
+ *   - calls with N * H > KDA_STATIC_MAX_UNITS return KDA_ERR_LIMIT (nothing enqueued);
+ *   - every call on a device shares that one array, and calls that can overlap on
+ *     the GPU (different streams, without an ordering between them) race on it and
+ *     give wrong results: order them, for instance on one stream;
+ *   - the array keeps what the last call left in it; the kernels write every part of
+ *     it they read within a call before reading it, so nothing needs clearing;
+ *   - the first call on a device looks up the array's device address (with that
+ *     device current) and caches it: make that first call before any stream capture.
+ * It always takes the plain path (no sequence-parallel split), like kda_fwd_ws.
+ * Returns what kda_fwd returns, plus KDA_ERR_LIMIT, and KDA_ERR_CUDA when the address
+ * lookup fails.
+ */
+kda_status kda_fwd_static(const void *q, const void *k, const void *v, const void *g,
+                          const void *beta, float scale, void *out, const float *A_log,
+                          const float *dt_bias, float lower_bound, const void *initial_state,
+                          void *final_state, int state_dtype, const int64_t *cu_seqlens,
+                          int64_t num_seqs, int64_t B, int64_t T, int64_t H, int64_t K, int64_t V,
+                          void *stream);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *kda_status_string(int status);

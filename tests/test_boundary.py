@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(L):
 
 def test_version_and_status_strings(L):
     assert kda.lib().kda_version() >= 100
-    for code in range(0, 9):
+    for code in range(0, 10):
         s = kda.status_string(code)
         assert s.startswith("KDA_")
     assert "unknown" in kda.status_string(99)
@@ -197,3 +197,21 @@ def test_workspace_size_query(L):
     assert L.kda_workspace_size(0, 5) == 0 and L.kda_workspace_size(3, 0) == 0
     assert L.kda_workspace_size(-1, 5) == 0 and L.kda_workspace_size(3, -2) == 0
     assert L.kda_workspace_size(1 << 40, 1 << 30) == 0   # does not fit in size_t
+
+
+def test_static_entry_point_rejects_calls_above_its_limit(L):
+    # the unit limit is checked after the ordinary validation and before any device call
+    def call_static(**over):
+        a = dict(q=P[0], k=P[1], v=P[2], g=P[3], beta=P[4], out=P[5], A_log=P[6], dt_bias=P[7],
+                 B=1, T=64, H=kda.STATIC_MAX_UNITS + 1, K=128)
+        a.update(over)
+        return L.kda_fwd_static(a["q"], a["k"], a["v"], a["g"], a["beta"], ctypes.c_float(0.088),
+                                a["out"], a["A_log"], a["dt_bias"], ctypes.c_float(-5.0), None,
+                                None, 0, None, 0, a["B"], a["T"], a["H"], a["K"], 128, None)
+    assert call_static() == kda.KDA_ERR_LIMIT
+    assert call_static(B=3, H=kda.STATIC_MAX_UNITS // 2) == kda.KDA_ERR_LIMIT
+    assert call_static(K=64) == kda.KDA_ERR_UNSUPPORTED
+    assert call_static(q=None, k=None, v=None, g=None, beta=None, out=None, B=0) == kda.KDA_OK
+    src = open(os.path.join(ROOT, "include", "kda.h")).read()
+    m = re.search(r"#define KDA_STATIC_MAX_UNITS (\d+)", src)
+    assert m and int(m.group(1)) == kda.STATIC_MAX_UNITS
