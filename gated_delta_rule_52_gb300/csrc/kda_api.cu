@@ -128,8 +128,9 @@ cudaError_t sm_count(int &sms) {
 namespace {
 
 // tsplit > 0: the sequence-parallel path with that many segments per sequence (p.ws is
-// then its scratch, tsplit_scratch_bytes long).
-kda_status launch(kda::Params &p, void *stream, int64_t tsplit = 0) {
+// then its scratch, tsplit_scratch_bytes long); pool_sms > 0: the persistent pool kernel
+// on that many SMs (p.ws its ring, pool_scratch_bytes long).
+kda_status launch(kda::Params &p, void *stream, int64_t tsplit = 0, int pool_sms = 0) {
     // the device error word's address, looked up once per device
     static std::atomic<bool> done[kda::kMaxDevices];
     static int *err_of[kda::kMaxDevices];
@@ -151,6 +152,8 @@ kda_status launch(kda::Params &p, void *stream, int64_t tsplit = 0) {
     cudaError_t e;
     if (tsplit > 0) {
         e = kda::launch_tsplit(p, tsplit, p.ws, cs);
+    } else if (pool_sms > 0) {
+        e = kda::launch_pool(p, pool_sms, cs);
     } else if (p.T == 1) {
         e = kda::launch_decode(p, cs);
     } else if (p.T <= kda::kShortMaxT) {
@@ -208,12 +211,15 @@ kda_status kda_fwd(const void *q, const void *k, const void *v, const void *g, c
     int sms = 0;
     if (kda::sm_count(sms) != cudaSuccess) return KDA_ERR_CUDA;
     const int64_t tsplit = kda::tsplit_segments(p, sms);
-    const size_t bytes = tsplit > 0 ? kda::tsplit_scratch_bytes(p.n_seqs, p.H, tsplit)
-                                    : (size_t)(p.n_seqs * p.H) * kda::kWsBytesPerUnit;
+    // fixed-length calls otherwise run the persistent pool kernel
+    const int pool_sms = (tsplit == 0 && !p.cu_seqlens) ? sms : 0;
+    const size_t bytes = tsplit > 0     ? kda::tsplit_scratch_bytes(p.n_seqs, p.H, tsplit)
+                         : pool_sms > 0 ? kda::pool_scratch_bytes(p.n_seqs * p.H, pool_sms)
+                                        : (size_t)(p.n_seqs * p.H) * kda::kWsBytesPerUnit;
     void *ws = nullptr;
     if (cudaMallocFromPoolAsync(&ws, bytes, pool, cs) != cudaSuccess) return KDA_ERR_CUDA;
     p.ws = static_cast<unsigned char *>(ws);
-    st = launch(p, stream, tsplit);
+    st = launch(p, stream, tsplit, pool_sms);
     if (cudaFreeAsync(ws, cs) != cudaSuccess) st = KDA_ERR_CUDA;
     return st;
 }

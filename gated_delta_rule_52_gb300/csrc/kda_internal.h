@@ -82,6 +82,13 @@ cudaError_t launch_cluster(const Params &p, cudaStream_t stream);   // chunked, 
 cudaError_t launch_decode(const Params &p, cudaStream_t stream);    // token recurrence, T = 1 only
 cudaError_t launch_short(const Params &p, cudaStream_t stream);     // 16-row blocks, 2 <= T <= 64
 
+// Persistent pool kernel for fixed-length calls (cu_seqlens == nullptr, T > kShortMaxT):
+// chain CTAs run the state recurrence, front CTAs the chunk-parallel work, handing each
+// chunk over through a ring in p.ws (pool_scratch_bytes long).
+int64_t pool_chains(int64_t units, int sms);
+size_t pool_scratch_bytes(int64_t units, int sms);
+cudaError_t launch_pool(const Params &p, int sms, cudaStream_t stream);
+
 // Sequence-parallel prefill (fixed-length calls with few (sequence, head) units): each
 // sequence cut into P segments of at least kTsplitMinSeg tokens, P in [4, kTsplitMaxSeg].
 constexpr int64_t kTsplitMinSeg = 2048;

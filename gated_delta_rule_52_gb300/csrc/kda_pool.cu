@@ -1,0 +1,1328 @@
+// KDA forward on sm_103a with a persistent pool of CTAs: "fronts" run the
+// chunk-parallel part of every chunk of every (sequence, head) unit, "chains" run
+// the sequential state recurrence, one unit at a time each.  Fronts hand each chunk's
+// operands to its chain through a ring of slots in global memory (resident in L2).
+//
+// The chunk algebra is that of the UT/WY (chunked) form of the KDA token recurrence
+// (FlashKDA README "Kernel API"; the recurrence is the gated delta rule with one decay
+// rate per key channel), over 64-token chunks with S the K x V state entering the chunk,
+// G the in-chunk cumulative log decay and Gamma = exp(G):
+//   A[t,i] = beta_t sum_c k[t,c] k[i,c] exp(G[t,c]-G[i,c])  (i < t)
+//   M[t,i] =        sum_c q[t,c] k[i,c] exp(G[t,c]-G[i,c])  (i <= t)
+//   T' = (I + A)^-1 Diag(beta);  W = T' (K_hat*Gamma);  U = T' V - W S
+//   O  = scale ((Q_hat*Gamma) S + M U);   S <- Diag(Gamma_C) S + Kbar^T U
+// Everything up to the last line's inputs depends only on the chunk's own tokens; only
+// the last line's two products carry the state from chunk to chunk.
+//
+// Grid: one CTA per SM, launched cooperatively (all CTAs resident at once, which the
+// flag waits between CTAs need).  CTAs 0 .. nc-1 are chains, the rest fronts.
+//   Chain c owns units c, c + nc, ...; its packets (chunks) j = 0, 1, ... are chunk
+//   j % nchunks of unit c + (j / nchunks) nc.
+//   Front f takes the packets of global index i = f, f + nf, f + 2 nf, ... in the order
+//   i = j * nc + c (packet j of chain c), so fronts produce packets in the order the
+//   chains consume them.  The packet of lowest index not yet produced can always be
+//   produced (the slot it needs holds a packet of lower index, which its chain
+//   consumes), so the pool cannot deadlock.
+// Packet (c, j) goes through ring slot (c, j % D): the front waits until the chain
+// has loaded packet j - D out of it ("freed" flag), stores the packet, then sets
+// the slot's "ready" flag; the chain's loader warp waits for "ready", bulk-loads the
+// packet and sets "freed".  Flags hold the launch's epoch plus the packet index, so the
+// ring needs no clearing between calls.
+//
+// Front CTA (per packet, pipelined as in the cluster kernel's front): warps 0-7 the
+// prologue (gate, block-local decay, the operands of G1 = [Kp; Qp] x Kn^T and the
+// chain tiles K_hat*Gamma, Q_hat*Gamma, Kbar), warps 13-15 row norms and beta, warp 12
+// G1 and the ring stores of the chain tiles, warps 8-11 the A/M readout, the blocked
+// inverse and T', stored with M.
+// Chain CTA: the state steps on tcgen05 with the fp32 state in TMEM (as the cluster
+// kernel's chain; -W is read out by warps 8 and 9 only), warp 12 the ring loader.
+//
+// Precision: G1 on bf16 operands of the raw q/k scaled by 16-token-block-local decay
+// factors, the other GEMMs on fp16 operands, fp32 accumulators, fp32 state.  Every wait
+// is bounded (2 s); a timeout sets the device error word and the CTA unwinds.
+#include "kda_chunk.cuh"
+
+namespace kda {
+namespace {
+
+using namespace sm103;
+using namespace chunk;
+
+constexpr int NT = 512;            // 16 warps
+constexpr int kLoaderWarp = 12;    // chain: ring loader (the control warp in a front)
+constexpr int NP = 256;            // front prologue group: warps 0-7
+constexpr int NS = 128;            // front solver group: warps 8-11
+constexpr int NH = 96;             // front helper group (norms, beta): warps 13-15
+constexpr int kHelp0 = 416;        // first helper thread
+constexpr int kProLead = 32;       // thread that waits for the prologue group (warp 1)
+constexpr int kSolLead = 64;       // index within the solver group of its waiting thread (warp 10)
+constexpr uint32_t kChunkBytes = 16384 * 3 + 512 + 8192 * 2;   // one packet
+// ring slot layout: Kbar, Q_hat*Gamma, K_hat*Gamma (fp16 tiles), exp(G_C) (fp32), T', M (fp16)
+constexpr uint32_t RS_KB = 0, RS_QG = 16384, RS_KG = 32768, RS_GC = 49152, RS_TP = 49664, RS_MM = 57856;
+static_assert(RS_MM + 8192 == kChunkBytes, "ring slot layout");
+
+// ---- front shared memory
+constexpr uint32_t F_RAW = 0;          // 2 slots x {q, k, g}: 16 KB each, 2 x [64 t][64 c]
+constexpr uint32_t F_SLOT = 49152;
+constexpr uint32_t F_AMA = 98304;      // [Kp; Qp]: 2 x [128][64] bf16
+constexpr uint32_t F_AMB = 131072;     // Kn variants: 2 x [160][64] bf16
+constexpr uint32_t F_MST = 172032;     // M staging fp16 [64 t][64 i]
+constexpr uint32_t F_AMAT = 180224;    // A fp32 [64][68]; T' staging (fp16) after the inverse
+constexpr uint32_t F_TF = 197632;      // T fp32 [64][68]
+// ---- chain shared memory
+constexpr uint32_t C_SH = 0;           // S^T fp16: 2 x [128 c][64 v] (A, MN-major)
+constexpr uint32_t C_UH = 32768;       // U^T fp16: [128 v][64 t] (K-major)
+constexpr uint32_t C_WT = 49152;       // -W^T fp16: [128 c][64 t] (B, MN-major)
+constexpr uint32_t C_V = 65536;        // 2 buffers x V [64 t][128 v] as 2 x [64][64] (bf16 -> fp16)
+constexpr uint32_t C_PK = 98304;       // 2 packet slots
+constexpr uint32_t C_PKSLOT = 65536;
+constexpr uint32_t PK_KB = 0, PK_QG = 16384, PK_KG = 32768, PK_TP = 49152, PK_MM = 57344;
+constexpr uint32_t C_END = C_PK + 2 * C_PKSLOT;
+constexpr uint32_t F_END = F_TF + 64 * LDA * 4;
+
+struct FrontSmall {
+    float rq[3][C], rk[3][C], beta[3][C];   // per norm slot (task % 3)
+    float btot[4][DK];
+    float fac[kFacRows][DK];                 // decay factors, see fac_base
+    float gamC_f[2][DK];                     // exp(G_C) per slot (store source)
+    float gb[2][DK];                         // gate bias a2 * dt_bias[h] per slot (log2 units)
+    float ga[2];                             // a2 = -exp(A_log[h]) log2(e) per slot
+    uint64_t raw_full[2], g1_done[2], am_free[2], pdone[2];
+    uint64_t s_done[3];   // the solver is done with norm slot task % 3
+    unsigned int ctl_count;   // tasks whose chain tiles the control warp has stored (complete)
+    int abort_p, abort_s;
+    int dec_p, dec_s;   // a group's abort decision, written by its lead thread only, before a barrier
+};
+struct ChainSmall {
+    float gamC[2][DK];   // exp(G_C) of the packet in each slot
+    // Barriers that complete once per packet are per packet parity ([2]) wherever a
+    // waiter could otherwise fall two phases behind
+    uint64_t full_e[2], full_l[2], vfull[2], vconv[2], u_done[2], o_done[2];
+    uint64_t w_done, s_done, o_free, sh_ready, s_scaled, uh_ready, wt_ready, fin;
+    int abort;
+};
+constexpr uint32_t F_SMALL = F_END;
+constexpr uint32_t C_SMALL = C_END;
+constexpr uint32_t COMMON_A = (F_SMALL + sizeof(FrontSmall) > C_SMALL + sizeof(ChainSmall)
+                                   ? F_SMALL + sizeof(FrontSmall)
+                                   : C_SMALL + sizeof(ChainSmall));
+constexpr uint32_t COMMON = (COMMON_A + 15u) & ~15u;   // TMEM base address
+constexpr uint32_t SMEM_BYTES = COMMON + 16 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+// ---------------------------------------------------------------- ring and flags
+// Ring depth D (slots per chain).  A front publishes a packet only once it has issued
+// the stores of its next one, whose slot it waits out first: that slot's earlier packet
+// has index (i + nf) - D nc, which must lie below the held packet's index i, or the
+// pool could wait in a circle.  So D > nf / nc, and at least kRingMin.
+constexpr int kRingMin = 4;
+__host__ __device__ constexpr int64_t ring_depth(int64_t nc, int64_t nf) {
+    return nf / nc + 2 > kRingMin ? nf / nc + 2 : kRingMin;
+}
+
+// Device side of the ring: D slots of kChunkBytes per chain, and per chain D "ready"
+// words then D "freed" words.
+struct PoolArgs {
+    unsigned char *ring;
+    unsigned long long *flags;
+    unsigned long long epoch;   // this launch's tag base (a per-process counter << 32)
+    int nc, nf;                 // chain CTAs, front CTAs
+    int depth;                  // ring slots per chain
+    int nchunks;                // chunks per unit (fixed-length calls)
+    int waves;                  // ceil(units / nc)
+
+    __device__ unsigned char *slot(int64_t c, int64_t j) const {
+        return ring + ((size_t)c * depth + (size_t)(j % depth)) * kChunkBytes;
+    }
+    __device__ unsigned long long *ready(int64_t c, int64_t j) const {
+        return flags + (size_t)c * 2 * depth + (size_t)(j % depth);
+    }
+    __device__ unsigned long long *freed(int64_t c, int64_t j) const {
+        return flags + (size_t)c * 2 * depth + depth + (size_t)(j % depth);
+    }
+    __device__ unsigned long long tag(int64_t j) const { return epoch + (unsigned long long)j + 1ull; }
+};
+
+__device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long *ptr) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ptr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(unsigned long long *ptr, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(ptr), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_release_cta(unsigned int *ptr, unsigned int v) {
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(ptr)), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned int ld_acquire_cta(const unsigned int *ptr) {
+    unsigned int v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(ptr)) : "memory");
+    return v;
+}
+// Waits until *ptr == want (another CTA's release store), giving up after limit_ns.
+__device__ __forceinline__ bool wait_flag(const unsigned long long *ptr, unsigned long long want,
+                                          uint64_t limit_ns) {
+    if (ld_acquire_gpu(ptr) == want) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (ld_acquire_gpu(ptr) != want)
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    return true;
+}
+
+// The packets of one front in order: global index i = f, f + nf, ...; i = j * nc + c.
+// The decomposition is carried along incrementally (no 64-bit divisions per packet).
+struct TaskIt {
+    int64_t i, end;       // current global index; one past the last
+    int units, H, nf, nc, nchunks, dj, dc;   // dj, dc: nf / nc and nf % nc
+    int c, m, w;          // chain, chunk of the unit, wave (unit = c + w nc)
+    // the current packet
+    int64_t j, row;       // packet index of its chain, first token row in [B*T]
+    int h, L;             // head; its token rows (<= 64)
+
+    __device__ bool decode(const Params &p) {
+        const int u = c + w * nc;
+        if (u >= units) return false;
+        const int n = u / H;
+        h = u - n * H;
+        j = (int64_t)w * nchunks + m;
+        row = (int64_t)n * p.T + (int64_t)m * C;
+        const int64_t rem = p.T - (int64_t)m * C;
+        L = (int)(rem < C ? rem : C);
+        return true;
+    }
+    // moves (c, m, w) on by nf global indices
+    __device__ void step() {
+        c += dc;
+        int add = dj;
+        if (c >= nc) {
+            c -= nc;
+            ++add;
+        }
+        m += add;
+        while (m >= nchunks) {
+            m -= nchunks;
+            ++w;
+        }
+    }
+    __device__ void advance(const Params &p) {
+        for (i += nf, step(); i < end; i += nf, step())
+            if (decode(p)) return;
+    }
+    __device__ void start(int f, const PoolArgs &a, int64_t units_, const Params &p) {
+        units = (int)units_;
+        H = (int)p.H;
+        nf = a.nf;
+        nc = a.nc;
+        nchunks = a.nchunks;
+        dj = nf / nc;
+        dc = nf - dj * nc;
+        end = (int64_t)a.waves * nchunks * nc;
+        i = f;
+        c = f % nc;
+        const int jf = f / nc;
+        m = jf % nchunks;
+        w = jf / nchunks;
+        if (i < end && !decode(p)) advance(p);
+    }
+    __device__ bool valid() const { return i < end; }
+};
+
+// ============================================================== front CTA
+__device__ __forceinline__ void pool_front(const TmaMaps &maps, const Params &p, const PoolArgs &a,
+                                           unsigned char *smem, FrontSmall &sm, uint32_t tmem, int f) {
+    const int64_t units = p.n_seqs * p.H;
+    const uint32_t sbase = smem_u32(smem);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // raw q, k, g tiles of packet `t` into raw slot m & 1
+    auto issue_raw = [&](int m, const TaskIt &t) {
+        const int s = m & 1;
+        unsigned char *base = smem + F_RAW + s * F_SLOT;
+        mbar_arrive_expect_tx(&sm.raw_full[s], 3 * 16384);
+        for (int kb = 0; kb < 2; ++kb) {
+            tma_load_3d(base + kb * 8192, &maps.q, &sm.raw_full[s], kb * 64, (int)t.h, (int)t.row);
+            tma_load_3d(base + 16384 + kb * 8192, &maps.k, &sm.raw_full[s], kb * 64, (int)t.h, (int)t.row);
+            tma_load_3d(base + 32768 + kb * 8192, &maps.g, &sm.raw_full[s], kb * 64, (int)t.h, (int)t.row);
+        }
+    };
+
+    if (tid < NP) {
+        // ------------------------------------------------ prologue group
+        // Thread layout for the gate and the operands: warp = (16-token block, 64-channel
+        // half), lane = (4-token quarter of the block, 8-channel group); every access to
+        // the tiles is one 16-byte vector (8 channels of one token).
+        const float lb2 = p.lower_bound * kLog2e;
+        const int blk = warp >> 1, kh = warp & 1;
+        const int cg = lane & 7, qr = lane >> 3;
+        const int c0 = 64 * kh + 8 * cg;             // first of this thread's 8 channels
+        const uint32_t kho = kh * 8192;              // the half inside a raw tile
+        TaskIt it;
+        it.start(f, a, units, p);
+        for (int m = 0; it.valid(); ++m, it.advance(p)) {   // m: this front's task count
+            const int s = m & 1;
+            const int L = it.L;
+            const uint32_t rq_off = F_RAW + s * F_SLOT, rk_off = rq_off + 16384, rg_off = rq_off + 32768;
+            if (tid == kProLead) {
+                bool ok = mbar_wait(&sm.raw_full[s], (m >> 1) & 1, kWait);
+                if (ok && m >= 3) ok = mbar_wait(&sm.s_done[m % 3], ((m - 3) / 3) & 1, kWait);
+                if (!ok) { set_err(p); sm.abort_p = 1; }
+                sm.dec_p = sm.abort_p;
+            }
+            named_bar(1, NP + NH);   // with the helpers: raw tiles and gate parameters of task m are in
+            if (sm.dec_p) break;
+            const float a2 = sm.ga[s];
+            float2 bias[4];
+            {
+                const float4 *gb4 = reinterpret_cast<const float4 *>(&sm.gb[s][c0]);
+                const float4 ba = gb4[0], bb = gb4[1];
+                bias[0] = make_float2(ba.x, ba.y);
+                bias[1] = make_float2(ba.z, ba.w);
+                bias[2] = make_float2(bb.x, bb.y);
+                bias[3] = make_float2(bb.z, bb.w);
+            }
+
+            // gate (log2 units) and its block-local inclusive cumulative sum H (channel pairs)
+            float2 H[4][4];
+            {
+                const float2 a2v = make_float2(a2, a2), lb2v = make_float2(lb2, lb2);
+                const float2 one = make_float2(1.f, 1.f);
+                float2 acc[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int t = 16 * blk + 4 * qr + j;
+                    const uint4 gv = *reinterpret_cast<const uint4 *>(smem + rg_off + kho + sw128_off(t, 8 * cg));
+                    if (t < L) {
+                        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float2 z = fma2(bf16x2_to_f2(gw[i]), a2v, bias[i]);
+                            const float2 d = add2(make_float2(exp2f(z.x), exp2f(z.y)), one);
+                            acc[i] = fma2(lb2v, make_float2(__fdividef(1.f, d.x), __fdividef(1.f, d.y)), acc[i]);
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) H[j][i] = acc[i];
+                }
+                // add the totals of the earlier quarters (lanes 8 and 16 apart share channels)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float2 v = acc[i];
+                    float2 u = make_float2(__shfl_up_sync(0xffffffffu, v.x, 8), __shfl_up_sync(0xffffffffu, v.y, 8));
+                    if (qr >= 1) v = add2(v, u);
+                    u = make_float2(__shfl_up_sync(0xffffffffu, v.x, 16), __shfl_up_sync(0xffffffffu, v.y, 16));
+                    if (qr >= 2) v = add2(v, u);
+                    float2 ex = make_float2(__shfl_up_sync(0xffffffffu, v.x, 8), __shfl_up_sync(0xffffffffu, v.y, 8));
+                    if (qr == 0) ex = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) H[j][i] = add2(H[j][i], ex);
+                    acc[i] = v;
+                }
+                if (qr == 3) {
+                    float4 *bt4 = reinterpret_cast<float4 *>(&sm.btot[blk][c0]);
+                    bt4[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+                    bt4[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
+                }
+            }
+            named_bar(1, NP + NH);   // gate totals, and the helpers' norms and beta
+
+            // decay factors per (block, channel): thread = channel, two blocks each
+            {
+                const int c = tid & (DK - 1), bh = tid >> 7;
+                float Gs[4], tot = 0.f;
+#pragma unroll
+                for (int bb = 0; bb < 4; ++bb) {
+                    Gs[bb] = tot;
+                    tot += sm.btot[bb][c];
+                }
+                if (bh == 0) sm.gamC_f[s][c] = exp2f(tot);
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    if ((b >> 1) != bh) continue;
+                    float *f = &sm.fac[fac_base(b)][c];
+                    f[0] = exp2f(Gs[b]);
+                    f[DK] = exp2f(tot - Gs[b]);
+#pragma unroll
+                    for (int bt = b + 1; bt < 4; ++bt) f[(1 + bt - b) * DK] = exp2f(Gs[bt] - Gs[b]);
+                }
+            }
+            // [Kp; Qp] and Kn are free once G1 of the previous chunk completed
+            if (tid == kProLead) {
+                if (m >= 1 && !mbar_wait(&sm.g1_done[(m - 1) & 1], ((m - 1) >> 1) & 1, kWait)) {
+                    set_err(p);
+                    sm.abort_p = 1;
+                }
+                sm.dec_p = sm.abort_p;
+            }
+            named_bar(3, NP);
+            if (sm.dec_p) {
+                named_bar(1, NP + NH);   // the helpers read the decision at their next barrier
+                break;
+            }
+
+            // Operands.  G1 (bf16, raw q/k times block-local decay): Kp = k 2^H and
+            // Qp = q 2^H at rows 32 blk + r and 32 blk + 16 + r of [Kp; Qp]; key
+            // variants Kn(bt) = k 2^(Gs[bt] - Gs[blk] - H) at row variant_off(bt) + t for
+            // bt >= blk.  Chain (fp16, in place of the raw tiles): Q_hat*Gamma,
+            // K_hat*Gamma and Kbar = k_hat 2^(G_C - G).
+            {
+                const int fb = fac_base(blk);
+                const float4 *fs4 = reinterpret_cast<const float4 *>(&sm.fac[fb][c0]);
+                const float4 *fc4 = reinterpret_cast<const float4 *>(&sm.fac[fb + 1][c0]);
+                const float4 fsa = fs4[0], fsb = fs4[1], fca = fc4[0], fcb = fc4[1];
+                const float2 Fs[4] = {make_float2(fsa.x, fsa.y), make_float2(fsa.z, fsa.w), make_float2(fsb.x, fsb.y),
+                                      make_float2(fsb.z, fsb.w)};
+                const float2 FC[4] = {make_float2(fca.x, fca.y), make_float2(fca.z, fca.w), make_float2(fcb.x, fcb.y),
+                                      make_float2(fcb.z, fcb.w)};
+                const uint32_t ama = sbase + F_AMA + kh * 16384, amb = sbase + F_AMB + kh * 20480;
+#pragma unroll 2
+                for (int j = 0; j < 4; ++j) {
+                    const int r = 4 * qr + j, t = 16 * blk + r;
+                    const uint32_t off = kho + sw128_off(t, 8 * cg);
+                    uint4 qv = *reinterpret_cast<const uint4 *>(smem + rq_off + off);
+                    uint4 kv = *reinterpret_cast<const uint4 *>(smem + rk_off + off);
+                    if (t >= L) qv = kv = make_uint4(0u, 0u, 0u, 0u);
+                    const float rq = sm.rq[m % 3][t], rk = sm.rk[m % 3][t];
+                    const float2 rq2 = make_float2(rq, rq), rk2 = make_float2(rk, rk);
+                    const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w}, kw[4] = {kv.x, kv.y, kv.z, kv.w};
+                    uint32_t wkp[4], wqp[4], wq[4], wk[4], wb[4], wn[4];
+                    float2 kn[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 k2 = bf16x2_to_f2(kw[i]), q2 = bf16x2_to_f2(qw[i]);
+                        const float2 e1 = make_float2(exp2f(H[0][i].x), exp2f(H[0][i].y));
+                        const float2 e2 = make_float2(exp2f(-H[0][i].x), exp2f(-H[0][i].y));
+                        const float2 kp = mul2(k2, e1), qp = mul2(q2, e1);
+                        kn[i] = mul2(k2, e2);
+                        wkp[i] = pack_bf16(kp.x, kp.y);
+                        wqp[i] = pack_bf16(qp.x, qp.y);
+                        wn[i] = pack_bf16(kn[i].x, kn[i].y);
+                        const float2 xq = mul2(qp, mul2(Fs[i], rq2));     // Q_hat*Gamma
+                        const float2 xk = mul2(kp, mul2(Fs[i], rk2));     // K_hat*Gamma
+                        const float2 xb = mul2(kn[i], mul2(FC[i], rk2));  // Kbar
+                        wq[i] = pack_f16(xq.x, xq.y);
+                        wk[i] = pack_f16(xk.x, xk.y);
+                        wb[i] = pack_f16(xb.x, xb.y);
+                    }
+                    sts128(ama + sw128_off(32 * blk + r, 8 * cg), wkp[0], wkp[1], wkp[2], wkp[3]);
+                    sts128(ama + sw128_off(32 * blk + 16 + r, 8 * cg), wqp[0], wqp[1], wqp[2], wqp[3]);
+                    sts128(amb + sw128_off(variant_off(blk) + t, 8 * cg), wn[0], wn[1], wn[2], wn[3]);
+                    sts128(sbase + rq_off + off, wq[0], wq[1], wq[2], wq[3]);
+                    sts128(sbase + rk_off + off, wk[0], wk[1], wk[2], wk[3]);
+                    sts128(sbase + rg_off + off, wb[0], wb[1], wb[2], wb[3]);
+#pragma unroll 1
+                    for (int bt = blk + 1; bt < 4; ++bt) {
+                        const float4 *d4 = reinterpret_cast<const float4 *>(&sm.fac[fb + 1 + bt - blk][c0]);
+                        const float4 da = d4[0], db = d4[1];
+                        const float2 v0 = mul2(kn[0], make_float2(da.x, da.y)), v1 = mul2(kn[1], make_float2(da.z, da.w));
+                        const float2 v2 = mul2(kn[2], make_float2(db.x, db.y)), v3 = mul2(kn[3], make_float2(db.z, db.w));
+                        sts128(amb + sw128_off(variant_off(bt) + t, 8 * cg), pack_bf16(v0.x, v0.y), pack_bf16(v1.x, v1.y),
+                               pack_bf16(v2.x, v2.y), pack_bf16(v3.x, v3.y));
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < 3; ++jj)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) H[jj][i] = H[jj + 1][i];
+                }
+            }
+            fence_proxy_async_smem();
+            named_bar(3, NP);
+
+            if (tid == kProLead) mbar_arrive(&sm.pdone[s]);   // operands and rq/rk/beta of chunk m ready
+        }
+    } else if (tid >= kHelp0 && tid < kHelp0 + NH) {
+        // ------------------------------------------------ helper group
+        // Row norms (one thread per row of q or k) and beta, beside the prologue's gate;
+        // published to the prologue by the barrier that ends its gate step.
+        const int htid = tid - kHelp0;
+        auto load_logit = [&](const TaskIt &t) {
+            return htid < t.L ? __bfloat162float(p.beta[(t.row + htid) * p.H + t.h]) : 0.f;
+        };
+        TaskIt it, nx;
+        it.start(f, a, units, p);
+        nx = it;
+        nx.advance(p);
+        // the gate parameters of task t into slot ps (read by the prologue after the
+        // first barrier of that task)
+        auto stage_gate = [&](const TaskIt &t, int ps) {
+            const float a2 = -__expf(p.A_log[t.h]) * kLog2e;
+            for (int cch = htid; cch < DK; cch += NH) sm.gb[ps][cch] = a2 * p.dt_bias[t.h * DK + cch];
+            if (htid == 0) sm.ga[ps] = a2;
+        };
+        float nb = 0.f;   // logit of token htid, loaded one task ahead
+        if (it.valid()) {
+            if (htid < C) nb = load_logit(it);
+            stage_gate(it, 0);
+        }
+        for (int m = 0; it.valid(); ++m, it.advance(p), nx.advance(p)) {
+            const int s = m & 1;
+            const int L = it.L;
+            const uint32_t rq_off = F_RAW + s * F_SLOT, rk_off = rq_off + 16384;
+            named_bar(1, NP + NH);
+            if (sm.dec_p) break;
+            if (nx.valid()) stage_gate(nx, s ^ 1);
+            const float bl = nb;
+            if (htid < C && nx.valid()) nb = load_logit(nx);
+            for (int i = htid; i < 2 * C; i += NH) {
+                const int t = i >> 1;
+                const uint32_t base = (i & 1) ? rk_off : rq_off;
+                float2 acc[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) acc[u] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int c16 = 0; c16 < 16; ++c16) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(
+                        smem + base + (c16 >> 3) * 8192 + sw128_off(t, (c16 & 7) * 8));
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float2 x = bf16x2_to_f2(w[u]);
+                        acc[u] = fma2(x, x, acc[u]);
+                    }
+                }
+                const float2 s01 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+                const float r = t < L ? rsqrtf(s01.x + s01.y + 1e-6f) : 0.f;
+                if (i & 1) sm.rk[m % 3][t] = r;
+                else sm.rq[m % 3][t] = r;
+            }
+            if (htid < C) sm.beta[m % 3][htid] = htid < L ? 1.f / (1.f + exp2f(-bl * kLog2e)) : 0.f;
+            named_bar(1, NP + NH);
+        }
+    } else if (warp == 12) {
+        // ------------------------------------------------ control warp (lane 0)
+        if (lane == 0) {
+            TaskIt it, ahead, nx;
+            it.start(f, a, units, p);
+            ahead = it;
+            nx = it;
+            nx.advance(p);
+            unsigned long long fv = 0;   // this task's ring-slot "freed" flag, read ahead
+            if (it.valid() && it.j >= a.depth) fv = ld_acquire_gpu(a.freed(it.c, it.j));
+            int issued = 0;   // raw tile loads requested
+            if (ahead.valid()) { issue_raw(0, ahead); ++issued; }
+            ahead.advance(p);
+            if (ahead.valid()) { issue_raw(1, ahead); ++issued; }
+            ahead.advance(p);
+            int m = 0;
+            for (; it.valid(); ++m, it.advance(p), ahead.advance(p), nx.advance(p)) {
+                const int s = m & 1;
+                bool ok = mbar_wait(&sm.pdone[s], (m >> 1) & 1, kWait);
+                if (ok && m >= 2) ok = mbar_wait(&sm.am_free[s], ((m - 2) >> 1) & 1, kWait);
+                if (ok) {
+                    tc_fence_after();
+                    const uint32_t id = idesc_bf16(128, 160, false, false);
+                    for (int ks = 0; ks < DK / 16; ++ks) {
+                        const uint64_t ad =
+                            sdesc_sw128(sbase + F_AMA + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+                        const uint64_t bd =
+                            sdesc_sw128(sbase + F_AMB + (ks >> 2) * 20480 + (ks & 3) * 32, 16, 1024);
+                        mma_bf16(tmem + 256 * s, ad, bd, id, ks > 0);
+                    }
+                    mma_commit(&sm.g1_done[s]);
+                }
+                // Kbar, Q_hat*Gamma, K_hat*Gamma and exp(G_C) of the task go to its ring slot
+                // once the chain has loaded the packet that slot held before (its "freed"
+                // flag was read one task ahead, so that the load latency is hidden)
+                if (ok && it.j >= a.depth && fv != a.tag(it.j - a.depth))
+                    ok = wait_flag(a.freed(it.c, it.j), a.tag(it.j - a.depth), kWait);
+                fv = 0;
+                if (nx.valid() && nx.j >= a.depth) fv = ld_acquire_gpu(a.freed(nx.c, nx.j));
+                if (ok) {
+                    const uint32_t rq_off = F_RAW + s * F_SLOT, rk_off = rq_off + 16384, rg_off = rq_off + 32768;
+                    unsigned char *slot = a.slot(it.c, it.j);
+                    fence_proxy_async_global();
+                    bulk_store(slot + RS_KB, smem + rg_off, 16384);
+                    bulk_store(slot + RS_QG, smem + rq_off, 16384);
+                    bulk_store(slot + RS_KG, smem + rk_off, 16384);
+                    bulk_store(slot + RS_GC, &sm.gamC_f[s][0], 512);
+                    bulk_commit();
+                    bulk_wait_read0();   // raw tiles and exp(G_C) of slot s may be overwritten
+                    if (ahead.valid()) { issue_raw(m + 2, ahead); ++issued; }
+                    bulk_wait0();        // the stores are complete in global memory
+                    fence_proxy_async_global();
+                    st_release_cta(&sm.ctl_count, (unsigned)(m + 1));
+                }
+                if (!ok) {
+                    set_err(p);
+                    sm.abort_p = 1;
+                    sm.abort_s = 1;
+                    break;
+                }
+            }
+            bulk_wait0();
+            // after an abort, raw loads of tasks nobody processes may be in flight: no copy
+            // into this CTA's shared memory may outlive it (bounded waits)
+            for (int k = m; k < issued; ++k) mbar_wait(&sm.raw_full[k & 1], (k >> 1) & 1, kWait);
+        }
+    } else {
+        // ------------------------------------------------ solver group
+        // Warp sw reads TMEM lane quarter sw of G1 = rows of token block sw: lanes 0-15
+        // are A rows (Kp), lanes 16-31 M rows (Qp); it needs the sw + 1 chunks of 16
+        // columns of variant sw.
+        const int stid = tid - NP, sw = warp - 8;
+        float *Amat = reinterpret_cast<float *>(smem + F_AMAT);
+        float *Tf = reinterpret_cast<float *>(smem + F_TF);
+        // the M staging tile above the diagonal blocks stays zero for the whole run
+        for (int k16 = stid; k16 < 512; k16 += NS) sts128(sbase + F_MST + k16 * 16, 0u, 0u, 0u, 0u);
+        // T above its diagonal blocks is never written: zero once, so T' needs no mask
+        for (int k4 = stid; k4 < 64 * LDA / 4; k4 += NS)
+            reinterpret_cast<float4 *>(Tf)[k4] = make_float4(0.f, 0.f, 0.f, 0.f);
+        named_bar(2, NS);
+        unsigned long long *pub_flag = nullptr, pub_tag = 0;   // the lead's packet awaiting publication
+        TaskIt it;
+        it.start(f, a, units, p);
+        for (int m = 0; it.valid(); ++m, it.advance(p)) {
+            const int s = m & 1;
+            if (stid == kSolLead) {
+                bulk_wait_read0();   // the previous T'/M staging is shipped
+                if (!mbar_wait(&sm.pdone[s], (m >> 1) & 1, kWait) ||
+                    !mbar_wait(&sm.g1_done[s], (m >> 1) & 1, kWait)) {
+                    set_err(p);
+                    sm.abort_s = 1;
+                }
+                sm.dec_s = sm.abort_s;
+            }
+            named_bar(2, NS);
+            if (sm.dec_s) break;
+            tc_fence_after();
+
+            // A (fp32, beta_t/|k_t| x 1/|k_i|; only i < t is used later) and
+            // M (fp16, 1/|q_t| x 1/|k_i|, zero for i > t); all column loads in flight at once
+            {
+                const bool is_m = lane >= 16;
+                const int t = 16 * sw + (lane & 15);
+                const float rowf = is_m ? sm.rq[m % 3][t] : sm.beta[m % 3][t] * sm.rk[m % 3][t];
+                const uint32_t col0 = 256 * s + variant_off(sw);
+                float r[4][16];
+                tmem_ld16(tmem_addr(tmem, 32 * sw, col0), r[0]);
+                if (sw >= 1) tmem_ld16(tmem_addr(tmem, 32 * sw, col0 + 16), r[1]);
+                if (sw >= 2) tmem_ld16(tmem_addr(tmem, 32 * sw, col0 + 32), r[2]);
+                if (sw >= 3) tmem_ld16(tmem_addr(tmem, 32 * sw, col0 + 48), r[3]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    if (kk > sw) break;
+                    const float4 *rk4 = reinterpret_cast<const float4 *>(&sm.rk[m % 3][16 * kk]);
+#pragma unroll
+                    for (int e4 = 0; e4 < 4; ++e4) {
+                        const float4 x = rk4[e4];
+                        const float2 f0 = mul2(make_float2(rowf, rowf), make_float2(x.x, x.y));
+                        const float2 f1 = mul2(make_float2(rowf, rowf), make_float2(x.z, x.w));
+                        const float2 y0 = mul2(f0, make_float2(r[kk][4 * e4], r[kk][4 * e4 + 1]));
+                        const float2 y1 = mul2(f1, make_float2(r[kk][4 * e4 + 2], r[kk][4 * e4 + 3]));
+                        r[kk][4 * e4] = y0.x; r[kk][4 * e4 + 1] = y0.y;
+                        r[kk][4 * e4 + 2] = y1.x; r[kk][4 * e4 + 3] = y1.y;
+                    }
+                    if (is_m) {
+                        if (kk == sw) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) r[kk][e] = e <= (lane & 15) ? r[kk][e] : 0.f;
+                        }
+                        st_pack16<true>(sbase + F_MST, t, 16 * kk, r[kk]);
+                    } else {
+                        float4 *dst = reinterpret_cast<float4 *>(Amat + t * LDA + 16 * kk);
+#pragma unroll
+                        for (int e4 = 0; e4 < 4; ++e4)
+                            dst[e4] = make_float4(r[kk][4 * e4], r[kk][4 * e4 + 1], r[kk][4 * e4 + 2],
+                                                  r[kk][4 * e4 + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            named_bar(2, NS);
+            if (stid == kSolLead) mbar_arrive(&sm.am_free[s]);
+
+            // T = (I + A)^-1 in 16x16 blocks.  Diagonal blocks: forward substitution,
+            // thread = (block, column j), updating all later rows after each solved row.
+            if (stid < 64) {
+                const int bb = stid >> 4, j = stid & 15;
+                const float *Ab = Amat + (16 * bb) * LDA + 16 * bb;
+                float acc[16], x[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) acc[r] = 0.f;
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    x[q] = q == j ? 1.f : (q < j ? 0.f : -acc[q]);
+#pragma unroll
+                    for (int r = q + 1; r < 16; ++r) acc[r] = fmaf(Ab[r * LDA + q], x[q], acc[r]);
+                }
+#pragma unroll
+                for (int r = 0; r < 16; ++r) Tf[(16 * bb + r) * LDA + 16 * bb + j] = x[r];
+            }
+            named_bar(2, NS);
+            // B[bt][m] = T[bt][bt] A[bt][m] for m < bt, in place of A's blocks: twelve
+            // 16x8 tiles (bt, nt), three per warp, all operands loaded before the MMAs
+            {
+                uint32_t fa[3][2][4], fb[3][2][2];
+#pragma unroll
+                for (int u = 0; u < 3; ++u) {
+                    const int idx = sw + 4 * u;
+                    const int bt = idx < 2 ? 1 : (idx < 6 ? 2 : 3);
+                    const int nt = idx - (bt == 1 ? 0 : (bt == 2 ? 2 : 6));
+                    const float *Tb = Tf + (16 * bt) * LDA + 16 * bt;
+                    const float *Ab = Amat + (16 * bt) * LDA + 8 * nt;
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks) {
+                        frag_a(Tb + 8 * ks, LDA, lane, fa[u][ks]);
+                        frag_b(Ab + 8 * ks * LDA, LDA, lane, fb[u][ks]);
+                    }
+                }
+                float acc[3][4];
+#pragma unroll
+                for (int u = 0; u < 3; ++u) {
+                    acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.f;
+                    mma_tf32_16x8x8(acc[u], fa[u][0], fb[u][0]);
+                    mma_tf32_16x8x8(acc[u], fa[u][1], fb[u][1]);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int u = 0; u < 3; ++u) {
+                    const int idx = sw + 4 * u;
+                    const int bt = idx < 2 ? 1 : (idx < 6 ? 2 : 3);
+                    const int nt = idx - (bt == 1 ? 0 : (bt == 2 ? 2 : 6));
+                    store_16x8(Amat + (16 * bt) * LDA + 8 * nt, LDA, lane, acc[u], 1.f);
+                }
+            }
+            named_bar(2, NS);
+            // Off-diagonal blocks of column block ba (warp ba), right-looking: once
+            // T[m][ba] is final, B[bt][m] T[m][ba] is added to the sum of every bt > m,
+            // and T[m+1][ba] = -(its completed sum).
+            if (sw <= 2) {
+                const int ba = sw;
+                float P[3][2][4];   // [bt - 1][n tile]
+#pragma unroll
+                for (int i = 0; i < 3; ++i)
+#pragma unroll
+                    for (int n = 0; n < 2; ++n) P[i][n][0] = P[i][n][1] = P[i][n][2] = P[i][n][3] = 0.f;
+#pragma unroll
+                for (int m = 0; m < 3; ++m) {
+                    if (m < ba) continue;
+                    uint32_t tb[2][2][2];
+                    const float *Tm = Tf + (16 * m) * LDA + 16 * ba;
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+                        for (int n = 0; n < 2; ++n) frag_b(Tm + 8 * ks * LDA + 8 * n, LDA, lane, tb[ks][n]);
+#pragma unroll
+                    for (int bt = m + 1; bt < 4; ++bt) {
+                        uint32_t fa[2][4];
+                        const float *Bp = Amat + (16 * bt) * LDA + 16 * m;
+                        frag_a(Bp, LDA, lane, fa[0]);
+                        frag_a(Bp + 8, LDA, lane, fa[1]);
+#pragma unroll
+                        for (int n = 0; n < 2; ++n) {
+                            mma_tf32_16x8x8(P[bt - 1][n], fa[0], tb[0][n]);
+                            mma_tf32_16x8x8(P[bt - 1][n], fa[1], tb[1][n]);
+                        }
+                    }
+                    float *dst = Tf + (16 * (m + 1)) * LDA + 16 * ba;
+                    store_16x8(dst, LDA, lane, P[m][0], -1.f);
+                    store_16x8(dst + 8, LDA, lane, P[m][1], -1.f);
+                    __syncwarp();
+                }
+            }
+            named_bar(2, NS);
+            // T' = T Diag(beta), fp16, into the staging tile (over the dead A)
+            {
+                const int t = stid >> 1, i0 = (stid & 1) * 32;
+                const float4 *b4 = reinterpret_cast<const float4 *>(&sm.beta[m % 3][i0]);
+                const float4 *t4 = reinterpret_cast<const float4 *>(Tf + t * LDA + i0);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    float r[16];
+#pragma unroll
+                    for (int e4 = 0; e4 < 4; ++e4) {
+                        const float4 tv = t4[4 * hh + e4], bv = b4[4 * hh + e4];
+                        const float2 y0 = mul2(make_float2(tv.x, tv.y), make_float2(bv.x, bv.y));
+                        const float2 y1 = mul2(make_float2(tv.z, tv.w), make_float2(bv.z, bv.w));
+                        r[4 * e4] = y0.x; r[4 * e4 + 1] = y0.y; r[4 * e4 + 2] = y1.x; r[4 * e4 + 3] = y1.y;
+                    }
+                    st_pack16<true>(sbase + F_AMAT, t, i0 + 16 * hh, r);
+                }
+            }
+            fence_proxy_async_smem();
+            named_bar(2, NS);
+            if (stid == kSolLead) {
+                mbar_arrive(&sm.s_done[m % 3]);
+                // T' and M complete the packet, once the control warp has stored the rest
+                // (which also means the slot's earlier packet is out).  The packet is
+                // published one task later, when all its stores have completed for sure, so
+                // that the solver does not wait for them here (the ring depth makes that
+                // safe, see ring_depth).
+                bool ok = true;
+                if (ld_acquire_cta(&sm.ctl_count) <= (unsigned)m) {
+                    const uint64_t t0 = globaltimer_ns();
+                    while (ld_acquire_cta(&sm.ctl_count) <= (unsigned)m)
+                        if (globaltimer_ns() - t0 > kWait || *(volatile int *)&sm.abort_s) { ok = false; break; }
+                }
+                if (ok) {
+                    unsigned char *slot = a.slot(it.c, it.j);
+                    bulk_store(slot + RS_TP, smem + F_AMAT, 8192);
+                    bulk_store(slot + RS_MM, smem + F_MST, 8192);
+                    bulk_commit();
+                    if (pub_flag) {
+                        bulk_wait1();   // every group but this one is complete
+                        fence_proxy_async_global();
+                        st_release_gpu(pub_flag, pub_tag);
+                    }
+                    pub_flag = a.ready(it.c, it.j);
+                    pub_tag = a.tag(it.j);
+                } else {
+                    set_err(p);
+                    sm.abort_s = 1;
+                    sm.abort_p = 1;
+                }
+            }
+        }
+        if (stid == kSolLead) {
+            bulk_wait0();
+            if (pub_flag && !sm.abort_s) {
+                fence_proxy_async_global();
+                st_release_gpu(pub_flag, pub_tag);
+            }
+        }
+    }
+}
+
+// ============================================================== chain CTA
+// Chain c runs units c, c + nc, ...; its packets j = 0, 1, ... are chunk j % nchunks of
+// unit c + (j / nchunks) nc, in that order.
+//
+// The accumulators the sequential path reads out span all 128 TMEM lanes (one lane per
+// value column v, or per key channel c), so four warps on four schedulers read them:
+//   G2w: W^T    = (K_hat*Gamma)^T T'^T            [c x t]  (one packet ahead)
+//   G2u: U^T    = V^T T'^T                        [v x t]  (one packet ahead)
+//   G3u: U^T   += S^T (-W^T)                      [v x t]  (needs S of this chunk)
+//   G4 : S     += Kbar^T U                        [c x v]  (S pre-scaled by Gamma_C)
+//   G3o: O      = (Q_hat*Gamma) S                 [t x v]  (A rows 64-127; lanes 64-127)
+//   G5 : O     += M U                             [t x v]
+// The sequential path per chunk is G3u -> U readout -> G4 -> S readout; the MMA warp
+// issues G2w of the next packet between G3u and G4, and G3o, G5 and the next G2u after G4.
+// Roles (warp w reaches TMEM lanes 32 (w % 4) ..): warps 0-7 the state (S readout to
+// its fp16 operand copy, decay by the next Gamma_C, initial and final state) and the
+// conversion of the next V to fp16, 8-11 the U and -W^T readouts, 12 the loader (ring
+// packets, V), 13 the MMA issuer, 14-15 the O readout (token rows, 16-byte stores).
+__device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p, const PoolArgs &a,
+                                           unsigned char *smem, ChainSmall &cs, uint32_t tmem, int c) {
+    const uint32_t sbase = smem_u32(smem);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3;
+    const uint32_t D_S = tmem, D_W = tmem + 128, D_U0 = tmem + 192, D_O = tmem + 320;
+    const int nchunks = a.nchunks;
+    const int64_t units = p.n_seqs * p.H;
+    const int64_t nunits = (units - c + a.nc - 1) / a.nc;
+    const int64_t npk = nunits * nchunks;   // this chain's packets
+    auto pk_unit = [&](int64_t j) { return (int64_t)c + (j / nchunks) * a.nc; };
+    auto pk_row = [&](int64_t j) {   // first token row of packet j in the [B*T] token rows
+        return (pk_unit(j) / p.H) * p.T + (j % nchunks) * (int64_t)C;
+    };
+    auto pk_slot = [&](int64_t j) { return sbase + C_PK + (uint32_t)(j & 1) * C_PKSLOT; };
+    auto par2 = [](int64_t j) { return (uint32_t)((j >> 1) & 1); };   // phase of a [j & 1] barrier
+    auto par1 = [](int64_t j) { return (uint32_t)(j & 1); };          // phase of a per-packet barrier
+    // bounded wait that also gives up once another role has aborted
+    auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+        if (mbar_try_wait(bar, parity)) return true;
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar, parity)) {
+            if (*(volatile int *)&cs.abort) return false;
+            if (globaltimer_ns() - t0 > kWait) {
+                set_err(p);
+                *(volatile int *)&cs.abort = 1;
+                return false;
+            }
+        }
+        return true;
+    };
+    auto warp_arrive = [&](uint64_t *bar) {   // one arrival per warp, after all its lanes
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar);
+    };
+
+    if (warp == kLoaderWarp) {
+        // ------------------------------------------------ loader: V and the ring packets
+        // Three tracks, advanced by one thread in whatever order their conditions allow:
+        //   early(je)  K_hat*Gamma, T' of a published packet into slot je & 1 once G2u of
+        //              packet je - 2 is done (u_done);
+        //   late(jl)   Kbar, Q_hat*Gamma, M, exp(G_C) once G5 of packet jl - 2 is done (o_done);
+        //   release(jr) the ring slot of packet jr once both of its parts have landed.
+        if (lane != 0) return;
+        int64_t je = 0, jl = 0, jr = 0;
+        bool ready_je = false;   // packet je seen published
+        [&]() {
+            uint64_t t0 = globaltimer_ns();
+            while (jr < npk) {
+                bool progress = false;
+                if (*(volatile int *)&cs.abort) return;
+                if (je < npk && je < jr + 2 && (je < 2 || mbar_try_wait(&cs.u_done[je & 1], par2(je - 2)))) {
+                    if (!ready_je) ready_je = ld_acquire_gpu(a.ready(c, je)) == a.tag(je);
+                    if (ready_je) {
+                        fence_proxy_async_global();
+                        const unsigned char *slot = a.slot(c, je);
+                        const uint32_t dst = pk_slot(je), fb = smem_u32(&cs.full_e[je & 1]);
+                        mbar_arrive_expect_tx(&cs.full_e[je & 1], 16384 + 8192);
+                        bulk_load(dst + PK_KG, slot + RS_KG, 16384, fb);
+                        bulk_load(dst + PK_TP, slot + RS_TP, 8192, fb);
+                        ++je;
+                        ready_je = false;
+                        progress = true;
+                    }
+                }
+                if (jl < je && (jl < 2 || mbar_try_wait(&cs.o_done[jl & 1], par2(jl - 2)))) {
+                    const unsigned char *slot = a.slot(c, jl);
+                    const uint32_t dst = pk_slot(jl), fb = smem_u32(&cs.full_l[jl & 1]);
+                    mbar_arrive_expect_tx(&cs.full_l[jl & 1], 16384 * 2 + 8192 + 512);
+                    bulk_load(dst + PK_KB, slot + RS_KB, 16384, fb);
+                    bulk_load(dst + PK_QG, slot + RS_QG, 16384, fb);
+                    bulk_load(dst + PK_MM, slot + RS_MM, 8192, fb);
+                    bulk_load(smem_u32(&cs.gamC[jl & 1][0]), slot + RS_GC, 512, fb);
+                    ++jl;
+                    progress = true;
+                }
+                if (jr < jl && mbar_try_wait(&cs.full_e[jr & 1], par2(jr)) &&
+                    mbar_try_wait(&cs.full_l[jr & 1], par2(jr))) {
+                    fence_proxy_async_global();
+                    st_release_gpu(a.freed(c, jr), a.tag(jr));
+                    ++jr;
+                    progress = true;
+                }
+                if (progress) {
+                    t0 = globaltimer_ns();
+                } else if (globaltimer_ns() - t0 > kWait) {
+                    set_err(p);
+                    *(volatile int *)&cs.abort = 1;
+                    return;
+                }
+            }
+        }();
+        // no copy into this CTA's shared memory may outlive it: wait (bounded) for the
+        // last ones requested (release waited for every part up to jr)
+        for (int64_t k = jr; k < je; ++k) mbar_wait(&cs.full_e[k & 1], par2(k), kWait);
+        for (int64_t k = jr; k < jl; ++k) mbar_wait(&cs.full_l[k & 1], par2(k), kWait);
+        return;
+    }
+
+    if (warp == 13) {
+        // ------------------------------------------------ MMA issuer
+        if (lane != 0) return;
+        [&]() {
+            const uint32_t id_n64_mk = idesc_fp16(128, 64, true, false);    // A MN-major, B K-major
+            const uint32_t id_n64_mm = idesc_fp16(128, 64, true, true);     // A MN-major, B MN-major
+            const uint32_t id_n128_mk = idesc_fp16(128, 128, true, false);  // A MN-major, B K-major
+            const uint32_t id_n128_km = idesc_fp16(128, 128, false, true);  // A K-major, B MN-major
+            const uint32_t id_n128_kk = idesc_fp16(128, 128, false, false); // A K-major, B K-major
+            const uint64_t dSH = sdesc_sw128(sbase + C_SH, 16384, 1024);    // S^T, A MN-major
+            const uint64_t dWT = sdesc_sw128(sbase + C_WT, 16384, 1024);    // -W^T, B MN-major
+            const uint64_t dUH = sdesc_sw128(sbase + C_UH, 16, 1024);       // U^T as A / U as B, K-major
+            auto issue_g2w = [&](int64_t jn) {   // G2w of packet jn
+                const uint32_t pk = pk_slot(jn);
+                const uint64_t dKG = sdesc_sw128(pk + PK_KG, 8192, 1024);
+                const uint64_t dTP = sdesc_sw128(pk + PK_TP, 16, 1024);
+                tc_fence_after();
+                for (int ks = 0; ks < C / 16; ++ks)
+                    mma_bf16(D_W, dKG + (uint64_t)(ks * 128), dTP + (uint64_t)(ks * 2), id_n64_mk, ks > 0);
+                mma_commit(&cs.w_done);
+            };
+            auto issue_g2u = [&](int64_t jn) {   // G2u of packet jn, once its V is fp16
+                const uint64_t dTP = sdesc_sw128(pk_slot(jn) + PK_TP, 16, 1024);
+                const uint64_t dV = sdesc_sw128(sbase + C_V + (uint32_t)(jn & 1) * 16384, 8192, 1024);
+                if (!wait(&cs.vconv[jn & 1], par2(jn))) return false;
+                tc_fence_after();
+                const uint32_t du = D_U0 + (uint32_t)(jn & 1) * 64;
+                for (int ks = 0; ks < C / 16; ++ks)
+                    mma_bf16(du, dV + (uint64_t)(ks * 128), dTP + (uint64_t)(ks * 2), id_n64_mk, ks > 0);
+                return true;
+            };
+            if (npk > 0) {
+                if (!wait(&cs.full_e[0], 0)) return;
+                issue_g2w(0);
+                if (!issue_g2u(0)) return;
+            }
+            for (int64_t j = 0; j < npk; ++j) {
+                const int sj = (int)(j & 1);
+                const uint32_t pk = pk_slot(j);
+                const uint32_t du = D_U0 + (uint32_t)sj * 64;
+                // G3u: U^T += S^T (-W^T)
+                if (!wait(&cs.sh_ready, par1(j)) || !wait(&cs.wt_ready, par1(j))) return;
+                tc_fence_after();
+                for (int ks = 0; ks < DK / 16; ++ks)
+                    mma_bf16(du, dSH + (uint64_t)(ks * 128), dWT + (uint64_t)(ks * 128), id_n64_mm, true);
+                mma_commit(&cs.u_done[sj]);
+                // G3o: O = (Q_hat Gamma) S into lanes 64-127 (the A operand starts 64 rows
+                // before Q_hat Gamma; rows 0-63 of O are unused), right behind G3u, so that
+                // the S copy is free again when G4 completes
+                if (!wait(&cs.full_l[sj], par2(j))) return;
+                if (j >= 1 && !wait(&cs.o_free, par1(j - 1))) return;
+                tc_fence_after();
+                {
+                    const uint64_t dQG = sdesc_sw128(pk + PK_QG - 8192, 16, 1024);
+                    for (int ks = 0; ks < DK / 16; ++ks)
+                        mma_bf16(D_O, dQG + (uint64_t)((ks >> 2) * 512 + (ks & 3) * 2), dSH + (uint64_t)(ks * 128),
+                                 id_n128_km, ks > 0);
+                }
+                // G4: S += Kbar^T U
+                if (!wait(&cs.uh_ready, par1(j)) || !wait(&cs.s_scaled, par1(j))) return;
+                tc_fence_after();
+                {
+                    const uint64_t dKB = sdesc_sw128(pk + PK_KB, 8192, 1024);
+                    for (int ks = 0; ks < C / 16; ++ks)
+                        mma_bf16(D_S, dKB + (uint64_t)(ks * 128), dUH + (uint64_t)(ks * 2), id_n128_mk, true);
+                    mma_commit(&cs.s_done);
+                }
+                // G2w of the next packet (the -W^T readout of this one is done), so that its
+                // readout runs beside the S readout
+                const bool more = j + 1 < npk;
+                if (more) {
+                    if (!wait(&cs.full_e[sj ^ 1], par2(j + 1))) return;
+                    issue_g2w(j + 1);
+                }
+                // G5: O += M U
+                {
+                    const uint64_t dMM = sdesc_sw128(pk + PK_MM - 8192, 16, 1024);
+                    for (int ks = 0; ks < C / 16; ++ks)
+                        mma_bf16(D_O, dMM + (uint64_t)(ks * 2), dUH + (uint64_t)(ks * 2), id_n128_kk, true);
+                    mma_commit(&cs.o_done[sj]);
+                }
+                // G2u of the next packet (U^T buffer (j + 1) & 1 was read out for packet j - 1)
+                if (more && !issue_g2u(j + 1)) return;
+            }
+        }();
+        // every MMA issued here completes before the CTA releases its tensor memory
+        mma_commit(&cs.fin);
+        mbar_wait(&cs.fin, 0, kWait);
+        return;
+    }
+
+    if (warp >= 14) {
+        // ------------------------------------------------ O readout: token rows (TMEM lanes 64-127)
+        const int t = (quarter - 2) * 32 + lane;   // token of the chunk
+        for (int64_t j = 0; j < npk; ++j) {
+            if (!wait(&cs.o_done[j & 1], par2(j))) return;
+            tc_fence_after();
+            uint32_t pk0[32];   // columns 0-63 as bf16 pairs
+            float r[4][16];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) tmem_ld16(tmem_addr(D_O, quarter * 32, 16 * jj), r[jj]);
+            tmem_ld_wait();
+            const float sc = p.scale;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) pk0[8 * jj + e] = pack_bf16(sc * r[jj][2 * e], sc * r[jj][2 * e + 1]);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) tmem_ld16(tmem_addr(D_O, quarter * 32, 64 + 16 * jj), r[jj]);
+            tmem_ld_wait();
+            tc_fence_before();
+            warp_arrive(&cs.o_free);
+            const int rem = (int)(p.T - (j % nchunks) * (int64_t)C);
+            if (p.out && t < (rem < C ? rem : C)) {
+                const int64_t u = pk_unit(j);
+                uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((pk_row(j) + t) * p.H + u % p.H) * DK);
+#pragma unroll
+                for (int q8 = 0; q8 < 8; ++q8)
+                    dst[q8] = make_uint4(pk0[4 * q8], pk0[4 * q8 + 1], pk0[4 * q8 + 2], pk0[4 * q8 + 3]);
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    dst[8 + 2 * jj] = make_uint4(pack_bf16(sc * r[jj][0], sc * r[jj][1]), pack_bf16(sc * r[jj][2], sc * r[jj][3]),
+                                                 pack_bf16(sc * r[jj][4], sc * r[jj][5]), pack_bf16(sc * r[jj][6], sc * r[jj][7]));
+                    dst[9 + 2 * jj] = make_uint4(pack_bf16(sc * r[jj][8], sc * r[jj][9]), pack_bf16(sc * r[jj][10], sc * r[jj][11]),
+                                                 pack_bf16(sc * r[jj][12], sc * r[jj][13]), pack_bf16(sc * r[jj][14], sc * r[jj][15]));
+                }
+            }
+        }
+        return;
+    }
+
+    if (warp >= 8) {
+        // ------------------------------------------------ U and -W^T readouts (lane quarter)
+        const int lv = quarter * 32 + lane;   // this thread's TMEM lane: v for U, c for W
+        auto read64 = [&](uint32_t col, float (&r)[4][16]) {
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) tmem_ld16(tmem_addr(col, quarter * 32, 16 * jj), r[jj]);
+            tmem_ld_wait();
+        };
+        auto w_readout = [&](int64_t jw) -> bool {   // -W^T of packet jw
+            if (!wait(&cs.w_done, par1(jw))) return false;
+            tc_fence_after();
+            float r[4][16];
+            read64(D_W, r);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) r[jj][e] = -r[jj][e];
+                st_pack16<true>(sbase + C_WT, lv, 16 * jj, r[jj]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            warp_arrive(&cs.wt_ready);
+            return true;
+        };
+        // V of packet jv into V buffer jv & 1 (warp 8, lane 0), free once G2u of packet
+        // jv - 2 is done
+        int64_t v_issued = 0;
+        auto issue_v = [&](int64_t jv) {
+            const int sv = (int)(jv & 1);
+            if (p.v) {
+                const int row = (int)pk_row(jv), h = (int)(pk_unit(jv) % p.H);
+                unsigned char *vb = smem + C_V + sv * 16384;
+                mbar_arrive_expect_tx(&cs.vfull[sv], 16384);
+                tma_load_3d(vb, &maps.v, &cs.vfull[sv], 0, h, row);
+                tma_load_3d(vb + 8192, &maps.v, &cs.vfull[sv], 64, h, row);
+            } else {
+                mbar_arrive(&cs.vfull[sv]);   // values of zero: the buffer stays zero
+            }
+            v_issued = jv + 1;
+        };
+        // V of packet jv to fp16, in place (the 128 threads of warps 8-11)
+        auto convert_v = [&](int64_t jv) -> bool {
+            const int sv = (int)(jv & 1);
+            if (!wait(&cs.vfull[sv], par2(jv))) return false;
+            for (int k16 = tid - 256; k16 < 1024; k16 += 128) {
+                uint4 *ptr = reinterpret_cast<uint4 *>(smem + C_V + sv * 16384 + k16 * 16);
+                uint4 x = *ptr;
+                x.x = pack_f16(bf16lo(x.x), bf16hi(x.x));
+                x.y = pack_f16(bf16lo(x.y), bf16hi(x.y));
+                x.z = pack_f16(bf16lo(x.z), bf16hi(x.z));
+                x.w = pack_f16(bf16lo(x.w), bf16hi(x.w));
+                *ptr = x;
+            }
+            fence_proxy_async_smem();
+            warp_arrive(&cs.vconv[sv]);
+            return true;
+        };
+        const bool vlead = warp == 8 && lane == 0;
+        [&]() {
+        if (vlead) {
+            if (npk > 0) issue_v(0);
+            if (npk > 1) issue_v(1);
+        }
+        if (npk > 0 && !convert_v(0)) return;
+        if (npk > 0 && !w_readout(0)) return;
+        for (int64_t j = 0; j < npk; ++j) {
+            const int sj = (int)(j & 1);
+            // U^T -> fp16 rows of U^T (K-major)
+            if (!wait(&cs.u_done[sj], par2(j))) return;
+            // G2u of packet j is done: V of packet j + 2 may land in its buffer
+            if (vlead && j + 2 < npk) issue_v(j + 2);
+            tc_fence_after();
+            {
+                float r[4][16];
+                read64(D_U0 + (uint32_t)sj * 64, r);
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) st_pack16<true>(sbase + C_UH, lv, 16 * jj, r[jj]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            warp_arrive(&cs.uh_ready);
+            if (j + 1 < npk && (!w_readout(j + 1) || !convert_v(j + 1))) return;
+        }
+        }();
+        // no V copy into this CTA's shared memory may outlive it (bounded waits)
+        if (vlead)
+            for (int64_t k = v_issued - 2; k < v_issued; ++k)
+                if (k >= 0) mbar_wait(&cs.vfull[k & 1], par2(k), kWait);
+        return;
+    }
+
+    // ------------------------------------------------ state warps 0-7 (lane quarter, column half)
+    const int half = warp >> 2;
+    const int cc = quarter * 32 + lane;   // key channel (TMEM lane of D_S)
+    auto ld_s = [&](float (&r)[4][16]) {
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) tmem_ld16(tmem_addr(D_S, quarter * 32, 64 * half + 16 * jj), r[jj]);
+        tmem_ld_wait();
+    };
+    int64_t j = 0;
+    for (int64_t w = 0; w < nunits; ++w) {
+        const int64_t unit = (int64_t)c + w * a.nc;
+        const int64_t h = unit % p.H, n = unit / p.H;
+        const size_t state_base = (size_t)(n * p.H + h) * DK * DK;
+        for (int m = 0; m < nchunks; ++m, ++j) {
+            const int sj = (int)(j & 1);
+            float r[4][16];
+            if (m == 0) {
+                // the unit's initial state (the previous unit's final state is out of D_S)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float x = 0.f;
+                        if (p.init) {
+                            const size_t off = state_base + (size_t)(64 * half + 16 * jj + e) * DK + cc;
+                            x = p.state_type == kStateBF16
+                                    ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p.init)[off])
+                                    : reinterpret_cast<const float *>(p.init)[off];
+                        }
+                        r[jj][e] = x;
+                    }
+            } else {
+                if (!wait(&cs.s_done, par1(j - 1))) return;
+                tc_fence_after();
+                ld_s(r);
+            }
+            // the S^T operand of this chunk (G3o of the previous one, which read the last
+            // copy, completed before G4 did)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) st_pack16<true>(sbase + C_SH + half * 16384, cc, 16 * jj, r[jj]);
+            fence_proxy_async_smem();
+            warp_arrive(&cs.sh_ready);
+            // D_S = Diag(Gamma_C) S, the decayed state G4 accumulates onto
+            if (!wait(&cs.full_l[sj], par2(j))) return;
+            const float g = cs.gamC[sj][cc];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) r[jj][e] *= g;
+                tmem_st16(tmem_addr(D_S, quarter * 32, 64 * half + 16 * jj), r[jj]);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            warp_arrive(&cs.s_scaled);
+        }
+        // final state from the fp32 master
+        if (!wait(&cs.s_done, par1(j - 1))) return;
+        tc_fence_after();
+        if (p.fin) {
+            float r[4][16];
+            ld_s(r);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const size_t off = state_base + (size_t)(64 * half + 16 * jj + e) * DK + cc;
+                    if (p.state_type == kStateBF16)
+                        reinterpret_cast<__nv_bfloat16 *>(p.fin)[off] = __float2bfloat16(r[jj][e]);
+                    else
+                        reinterpret_cast<float *>(p.fin)[off] = r[jj][e];
+                }
+        }
+        tc_fence_before();
+    }
+}
+
+__global__ void __launch_bounds__(NT, 1)
+kda_pool_kernel(const __grid_constant__ TmaMaps maps, Params p, PoolArgs a) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // 1024-byte alignment (128B-swizzled tiles) by pointer arithmetic on the shared
+    // array itself, so that every access through `smem` stays a shared-memory access
+    unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint32_t *tmem_base = reinterpret_cast<uint32_t *>(smem + COMMON);
+    const int cta = (int)blockIdx.x;
+    const bool chain = cta < a.nc;
+    FrontSmall &fs = *reinterpret_cast<FrontSmall *>(smem + F_SMALL);
+    ChainSmall &cs = *reinterpret_cast<ChainSmall *>(smem + C_SMALL);
+
+    if (threadIdx.x == 0) {
+        if (chain) {
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&cs.full_e[i], 1);
+                mbar_init(&cs.full_l[i], 1);
+                mbar_init(&cs.vfull[i], 1);
+                mbar_init(&cs.vconv[i], 4);     // the four U / W readout warps
+                mbar_init(&cs.u_done[i], 1);
+                mbar_init(&cs.o_done[i], 1);
+            }
+            mbar_init(&cs.o_free, 2);           // the two O readout warps
+            mbar_init(&cs.w_done, 1);
+            mbar_init(&cs.s_done, 1);
+            mbar_init(&cs.sh_ready, 8);         // the eight state warps
+            mbar_init(&cs.s_scaled, 8);
+            mbar_init(&cs.uh_ready, 4);
+            mbar_init(&cs.wt_ready, 4);
+            mbar_init(&cs.fin, 1);
+            cs.abort = 0;
+        } else {
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&fs.raw_full[i], 1);
+                mbar_init(&fs.g1_done[i], 1);
+                mbar_init(&fs.am_free[i], 1);
+                mbar_init(&fs.pdone[i], 1);
+            }
+            fs.ctl_count = 0;
+            for (int i = 0; i < 3; ++i) mbar_init(&fs.s_done[i], 1);
+            fs.abort_p = fs.abort_s = 0;
+            fs.dec_p = fs.dec_s = 0;
+        }
+        fence_mbar_init();
+    }
+    if (threadIdx.x < 32) {
+        tmem_alloc(tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_base;
+
+    if (chain)
+        pool_chain(maps, p, a, smem, cs, tmem, cta);
+    else
+        pool_front(maps, p, a, smem, fs, tmem, cta - a.nc);
+
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x < 32) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+int64_t pool_chains(int64_t units, int sms) {
+    // At most half the SMs run chains; the units are spread evenly over the fewest
+    // waves that this allows.
+    int64_t cap = sms / 2;
+    if (cap < 1) cap = 1;
+    const int64_t waves = (units + cap - 1) / cap;
+    return (units + waves - 1) / waves;
+}
+
+size_t pool_scratch_bytes(int64_t units, int sms) {
+    const int64_t nc = pool_chains(units, sms);
+    return (size_t)nc * ring_depth(nc, sms - nc) * (kChunkBytes + 2 * sizeof(unsigned long long));
+}
+
+cudaError_t launch_pool(const Params &p, int sms, cudaStream_t stream) {
+    const int64_t units = p.n_seqs * p.H;
+    if (units == 0) return cudaSuccess;
+    const int64_t nc = pool_chains(units, sms);
+    const int64_t nf = sms - nc;
+    const int64_t nchunks = (p.T + C - 1) / C;
+    if (nf < 1 || nchunks < 1) return cudaErrorInvalidValue;
+    PoolArgs a;
+    a.nc = (int)nc;
+    a.nf = (int)nf;
+    a.nchunks = (int)nchunks;
+    a.waves = (int)((units + nc - 1) / nc);
+    a.ring = p.ws;
+    a.depth = (int)ring_depth(nc, nf);
+    a.flags = reinterpret_cast<unsigned long long *>(p.ws + (size_t)nc * a.depth * kChunkBytes);
+    // A per-process counter in the high half: flags left by earlier calls never match
+    // this call's tags (packet indices stay below 2^32).
+    static std::atomic<unsigned long long> launches{0};
+    a.epoch = (launches.fetch_add(1) + 1) << 32;
+    if ((int64_t)a.waves * nchunks >= (int64_t(1) << 32)) return cudaErrorInvalidValue;
+    TmaMaps maps;
+    const int64_t rows = p.B * p.T;
+    if (!encode_map(&maps.q, p.q, rows, p.H) || !encode_map(&maps.k, p.k, rows, p.H) ||
+        !encode_map(&maps.g, p.g, rows, p.H) || !encode_map(&maps.v, p.v, rows, p.H))
+        return cudaErrorInvalidValue;
+    static std::atomic<bool> attr_done[kMaxDevices];
+    cudaError_t e = once_per_device(attr_done, [](int) {
+        return cudaFuncSetAttribute(kda_pool_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    });
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(nc + nf));
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kda_pool_kernel, maps, p, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -194,6 +194,10 @@ __device__ __forceinline__ void bulk_wait_read0() {
 __device__ __forceinline__ void bulk_wait0() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// Waits until at most one bulk group of this thread is still pending.
+__device__ __forceinline__ void bulk_wait1() {
+    asm volatile("cp.async.bulk.wait_group 1;" ::: "memory");
+}
 
 // ------------------------------------------------------------------ TMEM
 // Allocation is warp-wide: one full warp executes these.

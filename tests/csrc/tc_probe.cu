@@ -16,10 +16,12 @@ namespace {
 
 constexpr int M = 128;
 
-// A: row-major [M][K] in global.  B: row-major [K][N] in global.
+// A: row-major [M][K] in global.  B: row-major [K][N] in global.  The MMA runs with
+// mma_m rows (64 or 128; with 64 it reads the first 64 rows of the A tile); D returns
+// all 128 TMEM lanes, which start out NaN.
 __global__ void __launch_bounds__(128, 1)
 probe_kernel(const __nv_bfloat16 *A, const __nv_bfloat16 *B, float *D, int N, int K, int a_mn,
-             int b_mn, int fp16, int *status) {
+             int b_mn, int fp16, int *status, int mma_m) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -59,9 +61,18 @@ probe_kernel(const __nv_bfloat16 *A, const __nv_bfloat16 *B, float *D, int N, in
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = tmem_base;
+    {
+        float nanv[16];
+        for (int j = 0; j < 16; ++j) nanv[j] = __int_as_float(0x7fc00000);
+        for (int c0 = 0; c0 < N; c0 += 16) tmem_st16(tmem_addr(tbase, warp * 32, c0), nanv);
+        tmem_st_wait();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
 
     if (tid == 0) {
-        const uint32_t idesc = idesc_f16kind(M, N, a_mn != 0, b_mn != 0, fp16 != 0);
+        const uint32_t idesc = idesc_f16kind(mma_m, N, a_mn != 0, b_mn != 0, fp16 != 0);
         const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
         for (int ks = 0; ks < K / 16; ++ks) {
             uint64_t ad, bd;
@@ -102,9 +113,10 @@ probe_kernel(const __nv_bfloat16 *A, const __nv_bfloat16 *B, float *D, int N, in
 
 }  // namespace
 
-extern "C" int kda_probe_mma(const void *A, const void *B, float *D, int N, int K, int a_mn,
-                             int b_mn, int fp16, int *status, void *stream) {
-    if (N < 16 || N > 256 || N % 16 || (b_mn && N % 64) || K < 16 || K > 128 || K % 64)
+extern "C" int kda_probe_mma_m(const void *A, const void *B, float *D, int mma_m, int N, int K,
+                               int a_mn, int b_mn, int fp16, int *status, void *stream) {
+    if (N < 16 || N > 256 || N % 16 || (b_mn && N % 64) || K < 16 || K > 128 || K % 64 ||
+        (mma_m != 64 && mma_m != 128) || (mma_m == 64 && a_mn))
         return 1;
     const size_t smem = 1024 + (size_t)(M + N) * K * 2;
     cudaError_t e = cudaFuncSetAttribute(probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -112,8 +124,13 @@ extern "C" int kda_probe_mma(const void *A, const void *B, float *D, int N, int 
     if (e != cudaSuccess) return 2;
     probe_kernel<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const __nv_bfloat16 *>(A), static_cast<const __nv_bfloat16 *>(B), D, N, K,
-        a_mn, b_mn, fp16, status);
+        a_mn, b_mn, fp16, status, mma_m);
     return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+extern "C" int kda_probe_mma(const void *A, const void *B, float *D, int N, int K, int a_mn,
+                             int b_mn, int fp16, int *status, void *stream) {
+    return kda_probe_mma_m(A, B, D, 128, N, K, a_mn, b_mn, fp16, status, stream);
 }
 
 // ---------------------------------------------------------------------------
