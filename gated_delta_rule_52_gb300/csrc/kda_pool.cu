@@ -114,10 +114,11 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 // Ring depth D (slots per chain).  A front publishes a packet only once it has issued
 // the stores of its next one, whose slot it waits out first: that slot's earlier packet
 // has index (i + nf) - D nc, which must lie below the held packet's index i, or the
-// pool could wait in a circle.  So D > nf / nc, and at least kRingMin.
-constexpr int kRingMin = 4;
+// pool could wait in a circle.  So D > nf / nc; a few more slots (at least kRingMin)
+// let the fronts run ahead of the chains without waiting on the ring.
+constexpr int kRingMin = 8;
 __host__ __device__ constexpr int64_t ring_depth(int64_t nc, int64_t nf) {
-    return nf / nc + 2 > kRingMin ? nf / nc + 2 : kRingMin;
+    return nf / nc + 6 > kRingMin ? nf / nc + 6 : kRingMin;
 }
 
 // Device side of the ring: D slots of kChunkBytes per chain, and per chain D "ready"
