@@ -9,6 +9,7 @@
 #include "kda_internal.h"
 
 static_assert(KDA_WORKSPACE_BYTES_PER_UNIT == kda::kWsBytesPerUnit, "workspace size in kda.h");
+static_assert(KDA_ERR_TIMEOUT == kda::kErrTimeout && KDA_ERR_RANGE == kda::kErrRange, "device error codes");
 
 // Scratch of kda_fwd_static, for callers that cannot allocate: a fixed array in the
 // library's own device memory, present on every device that loads the library.  Host
@@ -299,6 +300,7 @@ const char *kda_status_string(int status) {
         case KDA_ERR_VALUE: return "KDA_ERR_VALUE: lower_bound outside [-5, 0], non-finite scale or workspace too small";
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA call or launch failed";
         case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded device wait expired";
+        case KDA_ERR_RANGE: return "KDA_ERR_RANGE: an fp16 operand (v, state, U, W, T', M; q, k on short steps) exceeded 65504";
         case KDA_ERR_LIMIT: return "KDA_ERR_LIMIT: kda_fwd_static takes at most KDA_STATIC_MAX_UNITS (sequence, head) units";
         default: return "KDA: unknown status";
     }

@@ -71,12 +71,38 @@ __device__ __forceinline__ void st_pack16(uint32_t base, int row, int col0, cons
            pack2(v[12], v[13], FP16), pack2(v[14], v[15], FP16));
 }
 
+// fp16 operand range: true when x lies beyond +-65504 (or is NaN), where its fp16 copy
+// would not hold it.
+__device__ __forceinline__ bool f16_out(float x) { return !(fabsf(x) <= 65504.f); }
+// st_pack16 that also records whether any value leaves the fp16 range (fp16 tiles only).
+template <bool FP16>
+__device__ __forceinline__ void st_pack16(uint32_t base, int row, int col0, const float (&v)[16], bool &bad) {
+    if (FP16) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) bad |= f16_out(v[e]);
+    }
+    st_pack16<FP16>(base, row, col0, v);
+}
+// bf16 -> fp16 of a 16-byte vector in place, recording values beyond the fp16 range.
+__device__ __forceinline__ uint4 bf16_to_f16x8(uint4 x, bool &bad) {
+    const float a0 = bf16lo(x.x), a1 = bf16hi(x.x), b0 = bf16lo(x.y), b1 = bf16hi(x.y);
+    const float c0 = bf16lo(x.z), c1 = bf16hi(x.z), d0 = bf16lo(x.w), d1 = bf16hi(x.w);
+    bad |= f16_out(a0) | f16_out(a1) | f16_out(b0) | f16_out(b1) | f16_out(c0) | f16_out(c1) |
+           f16_out(d0) | f16_out(d1);
+    return make_uint4(pack_f16(a0, a1), pack_f16(b0, b1), pack_f16(c0, c1), pack_f16(d0, d1));
+}
+
 struct TmaMaps {
     CUtensorMap q, k, g, v;
 };
 
+// Records (first error wins) that this thread met a value beyond the fp16 operand range.
+__device__ __forceinline__ void flag_range(const Params &p, bool bad) {
+    if (bad && p.err) atomicCAS(p.err, 0, kErrRange);
+}
+
 __device__ __forceinline__ void set_err(const Params &p) {
-    if (p.err) atomicExch(p.err, 8);
+    if (p.err) atomicExch(p.err, kErrTimeout);
 }
 
 // Host: the driver's tensor-map encoder and the 3-D tiled map of a [rows, H, 128] bf16

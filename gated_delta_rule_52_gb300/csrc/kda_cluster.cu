@@ -407,6 +407,7 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
         // are A rows (Kp), lanes 16-31 M rows (Qp); it needs the sw + 1 chunks of 16
         // columns of variant sw.
         const int stid = tid - NP, sw = warp - 8;
+        bool rbad = false;   // a T' or M value beyond the fp16 range
         float *Amat = reinterpret_cast<float *>(smem + F_AMAT);
         float *Tf = reinterpret_cast<float *>(smem + F_TF);
         // the M staging tile above the diagonal blocks stays zero for the whole run
@@ -462,7 +463,7 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
 #pragma unroll
                             for (int e = 0; e < 16; ++e) r[kk][e] = e <= (lane & 15) ? r[kk][e] : 0.f;
                         }
-                        st_pack16<true>(sbase + F_MST, t, 16 * kk, r[kk]);
+                        st_pack16<true>(sbase + F_MST, t, 16 * kk, r[kk], rbad);
                     } else {
                         float4 *dst = reinterpret_cast<float4 *>(Amat + t * LDA + 16 * kk);
 #pragma unroll
@@ -581,7 +582,7 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                         const float2 y1 = mul2(make_float2(tv.z, tv.w), make_float2(bv.z, bv.w));
                         r[4 * e4] = y0.x; r[4 * e4 + 1] = y0.y; r[4 * e4 + 2] = y1.x; r[4 * e4 + 3] = y1.y;
                     }
-                    st_pack16<true>(sbase + F_AMAT, t, i0 + 16 * hh, r);
+                    st_pack16<true>(sbase + F_AMAT, t, i0 + 16 * hh, r, rbad);
                 }
             }
             fence_proxy_async_smem();
@@ -599,6 +600,7 @@ __device__ __forceinline__ void run_front(const TmaMaps &maps, const Params &p, 
                 if (!ok) { set_err(p); sm.abort_s = 1; sm.abort_p = 1; }
             }
         }
+        flag_range(p, rbad);
         if (stid == kSolLead) bulk_wait0();
     }
 }
@@ -649,15 +651,11 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
         __syncthreads();
         return sm.abort_c != 0;
     };
+    bool rbad = false;   // a V, U, W or state value beyond the fp16 range
     auto convert_v = [&]() {
         for (int k16 = tid; k16 < 1024; k16 += NT) {
             uint4 *ptr = reinterpret_cast<uint4 *>(smem + C_B2 + 16384 + k16 * 16);
-            uint4 x = *ptr;
-            x.x = pack_f16(bf16lo(x.x), bf16hi(x.x));
-            x.y = pack_f16(bf16lo(x.y), bf16hi(x.y));
-            x.z = pack_f16(bf16lo(x.z), bf16hi(x.z));
-            x.w = pack_f16(bf16lo(x.w), bf16hi(x.w));
-            *ptr = x;
+            *ptr = bf16_to_f16x8(*ptr, rbad);
         }
     };
     // -W (D_W lanes 0..63) -> rows 0..63 of the G3 A operand: warps 8, 9, 12, 13
@@ -675,7 +673,7 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
                 for (int jj = 0; jj < 4; ++jj) {
 #pragma unroll
                     for (int e = 0; e < 16; ++e) r[jj][e] = -r[jj][e];
-                    st_pack16<true>(sbase + C_G3A + cb * 16384, t, 16 * jj, r[jj]);
+                    st_pack16<true>(sbase + C_G3A + cb * 16384, t, 16 * jj, r[jj], rbad);
                 }
             }
         }
@@ -729,7 +727,7 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
                 r[e] = x;
             }
             tmem_st16(tmem_addr(D_S, quarter * 32, 64 * half + 16 * jj), r);
-            st_pack16<true>(sbase + C_SB + half * 16384, c, 16 * jj, r);
+            st_pack16<true>(sbase + C_SB + half * 16384, c, 16 * jj, r, rbad);
         }
         tmem_st_wait();
     }
@@ -811,7 +809,7 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
             for (int jj = 0; jj < 4; ++jj) tmem_ld16(tmem_addr(D_U, quarter * 32, 64 * half + 16 * jj), r[jj]);
             tmem_ld_wait();
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) st_pack16<true>(sbase + C_UT + half * 8192, t, 16 * jj, r[jj]);
+            for (int jj = 0; jj < 4; ++jj) st_pack16<true>(sbase + C_UT + half * 8192, t, 16 * jj, r[jj], rbad);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -859,7 +857,7 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
                 tmem_ld16(tmem_addr(D_S, quarter * 32, 64 * half + 16 * jj), r[jj]);
             tmem_ld_wait();
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) st_pack16<true>(sbase + C_SB + half * 16384, c, 16 * jj, r[jj]);
+            for (int jj = 0; jj < 4; ++jj) st_pack16<true>(sbase + C_SB + half * 16384, c, 16 * jj, r[jj], rbad);
             if (m + 1 < nchunks) {
                 const float g = sm.gamC_c[s ^ 1][c];
 #pragma unroll
@@ -904,6 +902,7 @@ __device__ __forceinline__ void run_chain(const TmaMaps &maps, const Params &p, 
         __syncthreads();
     }
 
+    flag_range(p, rbad);
     // final state from the fp32 master
     if (!sm.abort_c && p.fin && warp < 8) {
         tc_fence_after();

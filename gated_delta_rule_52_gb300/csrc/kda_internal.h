@@ -18,6 +18,10 @@ constexpr int64_t kWsBytesPerUnit = 2 * kWsSlot;
 
 enum StateType : int { kStateNone = 0, kStateBF16 = 1, kStateFP32 = 2 };
 
+// Device error word values (kda_status codes of include/kda.h).
+constexpr int kErrTimeout = 8;   // a bounded wait gave up
+constexpr int kErrRange = 10;    // an fp16 operand (v, state, U, W, T', M) left +-65504
+
 // Problem description after host-side validation.  Tensor layouts are those of
 // the FlashKDA README "Kernel API" table: q,k,g [B,T,H,128], v,out [B,T,H,128],
 // beta [B,T,H], A_log [H], dt_bias [H,128], states [N,H,V,K].

@@ -571,6 +571,7 @@ __device__ __forceinline__ void pool_front(const TmaMaps &maps, const Params &p,
             reinterpret_cast<float4 *>(Tf)[k4] = make_float4(0.f, 0.f, 0.f, 0.f);
         named_bar(2, NS);
         unsigned long long *pub_flag = nullptr, pub_tag = 0;   // the lead's packet awaiting publication
+        bool rbad = false;   // a T' or M value beyond the fp16 range
         TaskIt it;
         it.start(f, a, units, p);
         for (int m = 0; it.valid(); ++m, it.advance(p)) {
@@ -620,7 +621,7 @@ __device__ __forceinline__ void pool_front(const TmaMaps &maps, const Params &p,
 #pragma unroll
                             for (int e = 0; e < 16; ++e) r[kk][e] = e <= (lane & 15) ? r[kk][e] : 0.f;
                         }
-                        st_pack16<true>(sbase + F_MST, t, 16 * kk, r[kk]);
+                        st_pack16<true>(sbase + F_MST, t, 16 * kk, r[kk], rbad);
                     } else {
                         float4 *dst = reinterpret_cast<float4 *>(Amat + t * LDA + 16 * kk);
 #pragma unroll
@@ -739,7 +740,7 @@ __device__ __forceinline__ void pool_front(const TmaMaps &maps, const Params &p,
                         const float2 y1 = mul2(make_float2(tv.z, tv.w), make_float2(bv.z, bv.w));
                         r[4 * e4] = y0.x; r[4 * e4 + 1] = y0.y; r[4 * e4 + 2] = y1.x; r[4 * e4 + 3] = y1.y;
                     }
-                    st_pack16<true>(sbase + F_AMAT, t, i0 + 16 * hh, r);
+                    st_pack16<true>(sbase + F_AMAT, t, i0 + 16 * hh, r, rbad);
                 }
             }
             fence_proxy_async_smem();
@@ -776,6 +777,7 @@ __device__ __forceinline__ void pool_front(const TmaMaps &maps, const Params &p,
                 }
             }
         }
+        flag_range(p, rbad);
         if (stid == kSolLead) {
             bulk_wait0();
             if (pub_flag && !sm.abort_s) {
@@ -1037,6 +1039,7 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
     if (warp >= 8) {
         // ------------------------------------------------ U and -W^T readouts (lane quarter)
         const int lv = quarter * 32 + lane;   // this thread's TMEM lane: v for U, c for W
+        bool rbad = false;                    // a V, U or W value beyond the fp16 range
         auto read64 = [&](uint32_t col, float (&r)[4][16]) {
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) tmem_ld16(tmem_addr(col, quarter * 32, 16 * jj), r[jj]);
@@ -1051,7 +1054,7 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
             for (int jj = 0; jj < 4; ++jj) {
 #pragma unroll
                 for (int e = 0; e < 16; ++e) r[jj][e] = -r[jj][e];
-                st_pack16<true>(sbase + C_WT, lv, 16 * jj, r[jj]);
+                st_pack16<true>(sbase + C_WT, lv, 16 * jj, r[jj], rbad);
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -1080,12 +1083,7 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
             if (!wait(&cs.vfull[sv], par2(jv))) return false;
             for (int k16 = tid - 256; k16 < 1024; k16 += 128) {
                 uint4 *ptr = reinterpret_cast<uint4 *>(smem + C_V + sv * 16384 + k16 * 16);
-                uint4 x = *ptr;
-                x.x = pack_f16(bf16lo(x.x), bf16hi(x.x));
-                x.y = pack_f16(bf16lo(x.y), bf16hi(x.y));
-                x.z = pack_f16(bf16lo(x.z), bf16hi(x.z));
-                x.w = pack_f16(bf16lo(x.w), bf16hi(x.w));
-                *ptr = x;
+                *ptr = bf16_to_f16x8(*ptr, rbad);
             }
             fence_proxy_async_smem();
             warp_arrive(&cs.vconv[sv]);
@@ -1110,7 +1108,7 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
                 float r[4][16];
                 read64(D_U0 + (uint32_t)sj * 64, r);
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) st_pack16<true>(sbase + C_UH, lv, 16 * jj, r[jj]);
+                for (int jj = 0; jj < 4; ++jj) st_pack16<true>(sbase + C_UH, lv, 16 * jj, r[jj], rbad);
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -1118,6 +1116,7 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
             if (j + 1 < npk && (!w_readout(j + 1) || !convert_v(j + 1))) return;
         }
         }();
+        flag_range(p, rbad);
         // no V copy into this CTA's shared memory may outlive it (bounded waits)
         if (vlead)
             for (int64_t k = v_issued - 2; k < v_issued; ++k)
@@ -1133,6 +1132,7 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
         for (int jj = 0; jj < 4; ++jj) tmem_ld16(tmem_addr(D_S, quarter * 32, 64 * half + 16 * jj), r[jj]);
         tmem_ld_wait();
     };
+    bool rbad = false;   // a state value beyond the fp16 range of its operand copy
     int64_t j = 0;
     for (int64_t w = 0; w < nunits; ++w) {
         const int64_t unit = (int64_t)c + w * a.nc;
@@ -1164,7 +1164,7 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
             // the S^T operand of this chunk (G3o of the previous one, which read the last
             // copy, completed before G4 did)
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) st_pack16<true>(sbase + C_SH + half * 16384, cc, 16 * jj, r[jj]);
+            for (int jj = 0; jj < 4; ++jj) st_pack16<true>(sbase + C_SH + half * 16384, cc, 16 * jj, r[jj], rbad);
             fence_proxy_async_smem();
             warp_arrive(&cs.sh_ready);
             // D_S = Diag(Gamma_C) S, the decayed state G4 accumulates onto
@@ -1199,6 +1199,7 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
         }
         tc_fence_before();
     }
+    flag_range(p, rbad);
 }
 
 __global__ void __launch_bounds__(NT, 1)

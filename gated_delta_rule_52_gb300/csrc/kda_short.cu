@@ -92,7 +92,11 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void *row) {
 __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
-__device__ __forceinline__ uint32_t h2_bits(float lo, float hi) { return pack_f16(lo, hi); }
+// fp16 pair of operand values, recording in `bad` any value beyond +-65504 (or NaN)
+__device__ __forceinline__ uint32_t h2c(bool &bad, float lo, float hi) {
+    bad |= !(fabsf(lo) <= 65504.f) | !(fabsf(hi) <= 65504.f);
+    return pack_f16(lo, hi);
+}
 // Bulk prefetch of a contiguous global range into L2 (16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
@@ -113,6 +117,7 @@ __device__ __forceinline__ int tau(int c) {
 // instantiation keeps the single-block case free of the block loop's registers.
 template <bool kMulti>
 __global__ void __launch_bounds__(NTS, 2) kda_short_kernel(Params p) {
+    bool rbad = false;   // some fp16 operand value (k, q, state, R, T', U') beyond +-65504
     extern __shared__ __align__(16) unsigned char dsm[];
     ShortSmem &sm = *reinterpret_cast<ShortSmem *>(dsm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -263,9 +268,9 @@ __global__ void __launch_bounds__(NTS, 2) kda_short_kernel(Params p) {
                     *reinterpret_cast<uint32_t *>(&sm.kp[t][col]) = pack_bf16(ke.x, ke.y);
                     *reinterpret_cast<uint32_t *>(&sm.qp[t][col]) = pack_bf16(qe.x, qe.y);
                     *reinterpret_cast<uint32_t *>(&sm.kn[t][col]) = pack_bf16(ki.x, ki.y);
-                    *reinterpret_cast<uint32_t *>(&sm.y[t][col]) = h2_bits(ke.x, ke.y);
-                    *reinterpret_cast<uint32_t *>(&sm.y[LT + t][col]) = h2_bits(qe.x, qe.y);
-                    *reinterpret_cast<uint32_t *>(&sm.kc[t][col]) = h2_bits(kc.x, kc.y);
+                    *reinterpret_cast<uint32_t *>(&sm.y[t][col]) = h2c(rbad, ke.x, ke.y);
+                    *reinterpret_cast<uint32_t *>(&sm.y[LT + t][col]) = h2c(rbad, qe.x, qe.y);
+                    *reinterpret_cast<uint32_t *>(&sm.kc[t][col]) = h2c(rbad, kc.x, kc.y);
                 }
                 if (hf == 0) *reinterpret_cast<float2 *>(&sm.gam[col]) = eL;
             } else {
@@ -327,7 +332,7 @@ __global__ void __launch_bounds__(NTS, 2) kda_short_kernel(Params p) {
                         } else {
                             const float f = sm.rq[t];
                             *reinterpret_cast<uint32_t *>(&sm.mp[t][i0]) =
-                                h2_bits(i0 <= t ? f * d[nt][2 * hr] : 0.f, i0 + 1 <= t ? f * d[nt][2 * hr + 1] : 0.f);
+                                h2c(rbad, i0 <= t ? f * d[nt][2 * hr] : 0.f, i0 + 1 <= t ? f * d[nt][2 * hr + 1] : 0.f);
                         }
                     }
                 }
@@ -345,8 +350,8 @@ __global__ void __launch_bounds__(NTS, 2) kda_short_kernel(Params p) {
                 ldsm_x4(a1, &sm.y[LT + (lane & 7) + 8 * ((lane >> 3) & 1)][16 * s + 8 * (lane >> 4)]);
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
-                    const uint32_t b0 = h2_bits(z[2 * s][2 * nt], z[2 * s][2 * nt + 1]);
-                    const uint32_t b1 = h2_bits(z[2 * s + 1][2 * nt], z[2 * s + 1][2 * nt + 1]);
+                    const uint32_t b0 = h2c(rbad, z[2 * s][2 * nt], z[2 * s][2 * nt + 1]);
+                    const uint32_t b1 = h2c(rbad, z[2 * s + 1][2 * nt], z[2 * s + 1][2 * nt + 1]);
                     mma_f16(x[0][nt], a0, b0, b1);
                     mma_f16(x[1][nt], a1, b0, b1);
                 }
@@ -359,9 +364,9 @@ __global__ void __launch_bounds__(NTS, 2) kda_short_kernel(Params p) {
                 const float2 va = bf16x2_to_f2(*reinterpret_cast<const uint32_t *>(&sm.v[gq][vg]));
                 const float2 vb = bf16x2_to_f2(*reinterpret_cast<const uint32_t *>(&sm.v[gq + 8][vg]));
                 *reinterpret_cast<uint32_t *>(&sm.wr[warp][gq][vl]) =
-                    h2_bits(va.x - rk0 * x[0][nt][0], va.y - rk0 * x[0][nt][1]);
+                    h2c(rbad, va.x - rk0 * x[0][nt][0], va.y - rk0 * x[0][nt][1]);
                 *reinterpret_cast<uint32_t *>(&sm.wr[warp][gq + 8][vl]) =
-                    h2_bits(vb.x - rk1 * x[0][nt][2], vb.y - rk1 * x[0][nt][3]);
+                    h2c(rbad, vb.x - rk1 * x[0][nt][2], vb.y - rk1 * x[0][nt][3]);
                 x[1][nt][0] *= rq0; x[1][nt][1] *= rq0; x[1][nt][2] *= rq1; x[1][nt][3] *= rq1;
             }
             if (warp == 2) {
@@ -382,7 +387,10 @@ __global__ void __launch_bounds__(NTS, 2) kda_short_kernel(Params p) {
                 const float bj = sm.beta[j];
                 if (lane < LT) {
 #pragma unroll
-                    for (int r = 0; r < LT; ++r) sm.tp[r][j] = __float2half_rn(xs[r] * bj);
+                    for (int r = 0; r < LT; ++r) {
+                        rbad |= !(fabsf(xs[r] * bj) <= 65504.f);
+                        sm.tp[r][j] = __float2half_rn(xs[r] * bj);
+                    }
                 }
             }
             __syncthreads();   // T' (warp 2), M' (warp 1) and every warp's R are in shared memory
@@ -407,8 +415,8 @@ __global__ void __launch_bounds__(NTS, 2) kda_short_kernel(Params p) {
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
                     const int vl = 8 * nt + 2 * qq;
-                    *reinterpret_cast<uint32_t *>(&sm.wu[warp][gq][vl]) = h2_bits(rk0 * u[nt][0], rk0 * u[nt][1]);
-                    *reinterpret_cast<uint32_t *>(&sm.wu[warp][gq + 8][vl]) = h2_bits(rk1 * u[nt][2], rk1 * u[nt][3]);
+                    *reinterpret_cast<uint32_t *>(&sm.wu[warp][gq][vl]) = h2c(rbad, rk0 * u[nt][0], rk0 * u[nt][1]);
+                    *reinterpret_cast<uint32_t *>(&sm.wu[warp][gq + 8][vl]) = h2c(rbad, rk1 * u[nt][2], rk1 * u[nt][3]);
                 }
             }
             __syncwarp();
@@ -455,6 +463,7 @@ __global__ void __launch_bounds__(NTS, 2) kda_short_kernel(Params p) {
         }   // blocks of the unit
         if (kMulti && p.fin) store_state();
     }
+    if (rbad && p.err) atomicCAS(p.err, 0, kErrRange);   // an fp16 operand left its range
 }
 
 }  // namespace

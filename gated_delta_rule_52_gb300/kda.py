@@ -32,6 +32,7 @@ KDA_ERR_VALUE = 6
 KDA_ERR_CUDA = 7
 KDA_ERR_TIMEOUT = 8
 KDA_ERR_LIMIT = 9
+KDA_ERR_RANGE = 10
 
 KDA_STATE_NONE = 0
 KDA_STATE_BF16 = 1

@@ -47,7 +47,9 @@ typedef enum {
                                 kda_fwd_ws) a workspace smaller than required          */
     KDA_ERR_CUDA = 7,        /* a CUDA runtime call or kernel launch failed             */
     KDA_ERR_TIMEOUT = 8,     /* a bounded on-device wait expired (kda_get_device_status) */
-    KDA_ERR_LIMIT = 9        /* kda_fwd_static: N * H above KDA_STATIC_MAX_UNITS          */
+    KDA_ERR_LIMIT = 9,       /* kda_fwd_static: N * H above KDA_STATIC_MAX_UNITS          */
+    KDA_ERR_RANGE = 10       /* an fp16 operand left +-65504 (kda_get_device_status; see
+                                "Value range" at kda_fwd)                              */
 } kda_status;
 
 /* Element type of initial_state / final_state (both, when both are given). */
@@ -104,6 +106,15 @@ typedef enum {
  * without synchronising.
  * q/k/v/g/beta/out/A_log/dt_bias/states must be 16-byte aligned.  `out` must not
  * alias an input.
+ *
+ * Value range: the tensor-core paths (every call of more than one token row) hold v,
+ * the recurrent state and the intermediate products U, W, T' and M as fp16 MMA
+ * operands (fp32 accumulation), and calls of 2-64 rows also q and k scaled by their
+ * decay.  Those values must stay within +-65504.  A call that meets a larger value (or
+ * a NaN) sets KDA_ERR_RANGE in the device status word that kda_get_device_status
+ * returns, and its outputs are then undefined; the call itself still returns KDA_OK
+ * (the check runs on the device).  Calls of one token row (the fp32 token recurrence)
+ * and kda_fwd_unbounded have no such limit.
  *
  * Returns KDA_OK, or an argument error (nothing enqueued), or KDA_ERR_CUDA if
  * the workspace allocation or the launch failed.
@@ -209,8 +220,9 @@ const char *kda_status_string(int status);
 /*
  * kda_get_device_status — synchronises `stream`, then reads and clears the
  * device-side error word that kernels set when a bounded wait gives up
- * (KDA_ERR_TIMEOUT).  Returns KDA_OK when no kernel reported a problem, or
- * KDA_ERR_CUDA if the synchronisation itself failed.
+ * (KDA_ERR_TIMEOUT) or an fp16 operand leaves its range (KDA_ERR_RANGE).  Returns
+ * KDA_OK when no kernel reported a problem, the reported code, or KDA_ERR_CUDA if the
+ * synchronisation itself failed.
  */
 kda_status kda_get_device_status(void *stream);
 

@@ -98,3 +98,66 @@ def check(d, got_out, got_fin, ref_out, ref_fin, pairs=None, label=""):
         tol = STATE_REL_L2[d["state_dtype"]]
         assert srl <= tol, f"{label}: final_state rel-L2 {srl:.3e} > {tol}"
     return res
+
+
+def check_full(d, got_out, got_fin, label="", max_tokens=16384):
+    """Compares every element of a full-size call with the oracle, one batch row (or a
+    group of whole varlen sequences of at most ``max_tokens`` packed tokens) at a time, so
+    that the fp64 copies stay small; the error figures are those of the whole tensors."""
+    go = got_out.float()
+    gf = got_fin.float() if got_fin is not None else None
+    acc = {"d_out": 0.0, "r_out": 0.0, "max": 0.0, "d_fin": 0.0, "r_fin": 0.0}
+
+    def compare(sub, o_slice, f_slice):
+        ro, rf = run_oracle(sub, want_final=f_slice is not None)
+        o = o_slice.numpy().astype(np.float64)
+        assert np.all(np.isfinite(o)), f"{label}: non-finite output"
+        diff = o - ro
+        acc["d_out"] += float(np.sum(diff * diff))
+        acc["r_out"] += float(np.sum(ro * ro))
+        if diff.size:
+            acc["max"] = max(acc["max"], float(np.max(np.abs(diff))))
+        if f_slice is not None:
+            f = f_slice.numpy().astype(np.float64)
+            assert np.all(np.isfinite(f)), f"{label}: non-finite final state"
+            acc["d_fin"] += float(np.sum((f - rf) ** 2))
+            acc["r_fin"] += float(np.sum(rf * rf))
+
+    def sub_inputs(**over):
+        e = dict(d)
+        e.update(over)
+        return e
+
+    if d["cu_seqlens"] is None:
+        for b in range(d["B"]):
+            sl = slice(b, b + 1)
+            sub = sub_inputs(B=1, N=1, q=d["q"][sl], k=d["k"][sl], v=d["v"][sl], g=d["g"][sl],
+                             beta=d["beta"][sl],
+                             initial_state=None if d["initial_state"] is None else d["initial_state"][sl])
+            compare(sub, go[sl], None if gf is None else gf[sl])
+    else:
+        cu = d["cu_seqlens"].tolist()
+        n = 0
+        N = len(cu) - 1
+        while n < N:
+            m = n + 1
+            while m < N and cu[m + 1] - cu[n] <= max_tokens:
+                m += 1
+            t0, t1 = cu[n], cu[m]
+            ts = slice(t0, t1)
+            sub = sub_inputs(T=t1 - t0, N=m - n, q=d["q"][:, ts], k=d["k"][:, ts], v=d["v"][:, ts],
+                             g=d["g"][:, ts], beta=d["beta"][:, ts],
+                             cu_seqlens=d["cu_seqlens"][n:m + 1] - t0,
+                             initial_state=None if d["initial_state"] is None else d["initial_state"][n:m])
+            compare(sub, go[:, ts], None if gf is None else gf[n:m])
+            n = m
+    rl = (acc["d_out"] ** 0.5) / (acc["r_out"] ** 0.5) if acc["r_out"] > 0 else acc["d_out"] ** 0.5
+    res = {"out_max_abs": acc["max"], "out_rel_l2": rl}
+    assert acc["max"] <= OUT_MAX_ABS, f"{label}: out max-abs {acc['max']:.3e} > {OUT_MAX_ABS}"
+    assert rl <= OUT_REL_L2, f"{label}: out rel-L2 {rl:.3e} > {OUT_REL_L2}"
+    if gf is not None:
+        srl = (acc["d_fin"] ** 0.5) / (acc["r_fin"] ** 0.5) if acc["r_fin"] > 0 else acc["d_fin"] ** 0.5
+        res["state_rel_l2"] = srl
+        tol = STATE_REL_L2[d["state_dtype"]]
+        assert srl <= tol, f"{label}: final_state rel-L2 {srl:.3e} > {tol}"
+    return res

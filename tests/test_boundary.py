@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(L):
 
 def test_version_and_status_strings(L):
     assert kda.lib().kda_version() >= 100
-    for code in range(0, 10):
+    for code in range(0, 11):
         s = kda.status_string(code)
         assert s.startswith("KDA_")
     assert "unknown" in kda.status_string(99)

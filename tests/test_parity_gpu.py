@@ -1,7 +1,7 @@
 """GPU parity: libkda (through the C ABI) against the fp64 oracle on the same
-seeded inputs.  Reduced sizes compare every element and still span several
-64-token chunks and ragged tails; the full workload sizes compare sampled
-(sequence, head) pairs, which the oracle computes one by one."""
+seeded inputs, element by element.  Reduced sizes span several 64-token chunks and
+ragged tails; the full workload sizes are compared in full too, the oracle running
+one batch row (or a group of varlen sequences) at a time."""
 import numpy as np
 import pytest
 import torch
@@ -38,29 +38,12 @@ def test_reduced_all_elements(name):
     print(name, res)
 
 
-def _sample_pairs(d, count, seed):
-    N, H = d["N"], d["H"]
-    r = np.random.default_rng(seed)
-    pairs = {(int(r.integers(N)), int(r.integers(H))) for _ in range(count)}
-    pairs.add((N - 1, H - 1))
-    if d["seqlens"] is not None:   # always include the longest sequence
-        pairs.add((int(np.argmax(d["seqlens"])), 0))
-    return sorted(pairs)
-
-
-@pytest.mark.parametrize("name,count", [("batch_state", 6), ("prefill_8k", 4),
-                                        ("varlen_uniform", 6), ("varlen_ragged", 5)])
-def test_full_size_sampled_pairs(name, count):
+@pytest.mark.parametrize("name", ["batch_state", "prefill_8k", "varlen_uniform", "varlen_ragged"])
+def test_full_size_all_elements(name):
     d = W.make_inputs(W.get(name))
     out, fin = pu.run_gpu(d)
-    pairs = _sample_pairs(d, count, seed=len(name))
-    ref_out, ref_fin = pu.run_oracle(d, pairs=pairs)
-    res = pu.check(d, out, fin, ref_out, ref_fin, pairs=pairs, label=name)
-    print(name, pairs, res)
-    # every output element was written (out was NaN-filled before the call)
-    assert torch.isfinite(out.float()).all()
-    if fin is not None:
-        assert torch.isfinite(fin.float()).all()
+    res = pu.check_full(d, out, fin, label=name)
+    print(name, res)
 
 
 def test_chained_calls_match_single_call():
@@ -235,14 +218,11 @@ def test_short_step_varlen_with_empty_sequences(seqlens):
         torch.testing.assert_close(fin[n], d["initial_state"][n].to(fin.dtype), rtol=0, atol=0)
 
 
-@pytest.mark.parametrize("name", ["decode", "decode_16"])
-def test_short_step_full_size_sampled(name):
+@pytest.mark.parametrize("name", ["decode", "decode_16", "step_64", "varlen_short"])
+def test_short_step_full_size_all_elements(name):
     d = W.make_inputs(W.get(name))
     out, fin = pu.run_gpu(d)
-    pairs = _sample_pairs(d, 8, seed=7)
-    ref_out, ref_fin = pu.run_oracle(d, pairs=pairs)
-    print(name, pu.check(d, out, fin, ref_out, ref_fin, pairs=pairs, label=name))
-    assert torch.isfinite(out.float()).all() and torch.isfinite(fin.float()).all()
+    print(name, pu.check_full(d, out, fin, label=name))
 
 
 def test_short_and_chunked_paths_agree_at_the_threshold():
@@ -436,14 +416,10 @@ def test_unbounded_gate_varlen_with_empty_sequences():
         torch.testing.assert_close(fin[n], d["initial_state"][n].to(fin.dtype), rtol=0, atol=0)
 
 
-def test_unbounded_gate_full_size_sampled():
+def test_unbounded_gate_full_size_all_elements():
     d = W.make_inputs(W.get("prefill_8k_unbounded"))
     out, fin = pu.run_gpu(d)
-    pairs = _sample_pairs(d, 4, seed=11)
-    ref_out, ref_fin = pu.run_oracle(d, pairs=pairs)
-    print("prefill_8k_unbounded", pu.check(d, out, fin, ref_out, ref_fin, pairs=pairs,
-                                           label="prefill_8k_unbounded"))
-    assert torch.isfinite(out.float()).all() and torch.isfinite(fin.float()).all()
+    print("prefill_8k_unbounded", pu.check_full(d, out, fin, label="prefill_8k_unbounded"))
 
 
 def test_unbounded_and_bounded_gates_differ():
@@ -466,3 +442,72 @@ def test_unbounded_gate_zero_length_passes_state_through(sd):
     assert dv["T"] == 0
     out, fin = pu.run_gpu(dv)
     torch.testing.assert_close(fin, dv["initial_state"].to(fin.dtype), rtol=0, atol=0)
+
+
+# ---- corners: long sequence-parallel splits, saturated gates, the fp16 operand range
+
+@pytest.mark.parametrize("name,over,segments", [("prefill_64k_h8", {}, 9),
+                                                ("prefill_8k", dict(T=65536, H=1, seed=77), 32)])
+def test_sequence_parallel_prefill_long_splits(name, over, segments):
+    # T = 65536 with 8 (sequence, head) units runs 9 segments per sequence, with one unit
+    # 32 (the most the path takes): the fp32 scan over 9 and 32 segment maps
+    d = W.make_inputs(W.get(name, **over))
+    out, fin = pu.run_gpu(d)
+    print(name, segments, pu.check_full(d, out, fin, label=f"{name} ({segments} segments)"))
+
+
+@pytest.mark.parametrize("g_value", [30.0, -30.0])
+@pytest.mark.parametrize("case", ["fixed", "varlen", "short"])
+def test_saturated_gate(case, g_value):
+    # g = +30: the gate sits at lower_bound = -5 on every token and channel (the 16-token
+    # blocks span e^-80, the largest range the factored operands meet); g = -30: no decay
+    wl = {"fixed": W.get("prefill_8k", T=1000, H=4, seed=81),
+          "varlen": W.get("varlen_ragged", H=3, seqlens=(65, 1, 130, 63, 200), seed=82),
+          "short": W.get("decode", B=3, T=40, H=2, seed=83)}[case]
+    d = W.make_inputs(wl)
+    d["g"] = torch.full_like(d["g"], g_value)
+    out, fin = pu.run_gpu(d)
+    ref_out, ref_fin = pu.run_oracle(d)
+    print(case, g_value, pu.check(d, out, fin, ref_out, ref_fin, label=f"saturated {case} g={g_value}"))
+
+
+def _call_status(d):
+    e = pu.to_device(d)
+    out = torch.empty((d["B"], d["T"], d["H"], 128), dtype=torch.bfloat16, device="cuda")
+    fin = torch.empty((d["N"], d["H"], 128, 128), dtype=pu.state_torch_dtype(d["state_dtype"]),
+                      device="cuda")
+    kda.kda_fwd(e["q"], e["k"], e["v"], e["g"], e["beta"], d["scale"], out, e["A_log"],
+                e["dt_bias"], d["lower_bound"], initial_state=e["initial_state"], final_state=fin,
+                cu_seqlens=e["cu_seqlens"])
+    return kda.get_device_status()
+
+
+@pytest.mark.parametrize("case", ["fixed", "varlen", "short"])
+@pytest.mark.parametrize("where", ["v", "state"])
+def test_fp16_operand_range_is_reported(case, where):
+    # a value beyond +-65504 where the tensor-core paths keep fp16 operands sets
+    # KDA_ERR_RANGE in the device status word, which the next status read clears
+    wl = {"fixed": W.get("prefill_8k", T=300, H=2, seed=84, state_dtype="fp32"),
+          "varlen": W.get("varlen_ragged", H=2, seqlens=(70, 130), seed=85),
+          "short": W.get("decode", B=2, T=8, H=2, seed=86)}[case]
+    d = W.make_inputs(wl)
+    assert _call_status(d) == kda.KDA_OK
+    if where == "v":
+        d["v"] = d["v"].clone()
+        d["v"][0, 3, 1, 5] = 1.0e5
+    else:
+        d["initial_state"] = d["initial_state"].clone()
+        d["initial_state"][-1, 1, 7, 9] = 1.0e5
+    assert _call_status(d) == kda.KDA_ERR_RANGE
+    assert kda.get_device_status() == kda.KDA_OK   # cleared by the read
+
+
+def test_one_token_step_has_no_fp16_limit():
+    # T = 1 runs the fp32 token recurrence: values far beyond the fp16 range are fine
+    d = W.make_inputs(W.get("decode", B=2, T=1, H=2, seed=87))
+    d["v"] = d["v"] * 1.0e5
+    d["initial_state"] = d["initial_state"] * 1.0e5
+    out, fin = pu.run_gpu(d)
+    ref_out, ref_fin = pu.run_oracle(d)
+    pu.check(d, out.float() / 1.0e5, fin / 1.0e5, ref_out / 1.0e5, ref_fin / 1.0e5,
+             label="decode large values")
