@@ -54,12 +54,13 @@ FLOPS_PER_TOKEN_HEAD = 2 * 64 * (3 * 128 + 2 * 128) + 2 * 3 * 128 * 128
 # Source files each kernel is built from (a stored ncu traffic figure is valid only
 # while these are unchanged).
 KERNEL_SOURCES = {
-    "cluster": ("kda_cluster.cu", "sm103.cuh", "kda_internal.h"),
+    "pool": ("kda_pool.cu", "kda_chunk.cuh", "sm103.cuh", "kda_internal.h"),
+    "cluster": ("kda_cluster.cu", "kda_chunk.cuh", "sm103.cuh", "kda_internal.h"),
     "decode": ("kda_decode.cu", "sm103.cuh", "kda_internal.h"),
     "short": ("kda_short.cu", "sm103.cuh", "kda_internal.h"),
     "recur": ("kda_recur.cu", "sm103.cuh", "kda_internal.h"),
 }
-KERNEL_NAMES = {"cluster": "kda_cluster_kernel", "decode": "kda_decode1_kernel", "short": "kda_short_kernel",
+KERNEL_NAMES = {"pool": "kda_pool_kernel", "cluster": "kda_cluster_kernel", "decode": "kda_decode1_kernel", "short": "kda_short_kernel",
                 "recur": "kda_recur_kernel"}
 CSRC = os.path.join("gated_delta_rule_52_gb300", "csrc")
 DECODE_MAX_T = 64   # calls with at most this many token rows run a kernel without workspace
@@ -109,6 +110,7 @@ def algorithmic_bytes(d) -> int:
 # k^T S, the rank-1 update and q^T S, each K x V multiply-adds, 2 flops each.
 RECUR_FLOPS_PER_TOKEN_HEAD = 4 * 128 * 128 * 2
 SM_MAX_MHZ = 2070   # GB300 maximum SM clock, used when nvidia-smi reports none
+SMS_DEFAULT = 152   # GB300 SM count, for host-side dispatch figures without a device
 
 
 def algorithmic_flops(d) -> int:
@@ -123,16 +125,27 @@ def workload_config(name: str, d) -> dict:
                      if d["lower_bound"] is None else "lower_bound sigmoid(exp(A_log) (g + dt_bias))")}
 
 
-def kernel_of(T: int, unbounded: bool = False) -> str:
+def kernel_of(T: int, unbounded: bool = False, varlen: bool = False) -> str:
     """The kernel libkda runs for a call of T packed token rows (the gate without a
-    lower bound always runs the token recurrence)."""
+    lower bound always runs the token recurrence; fixed-length calls of more than 64
+    rows run the persistent pool kernel, varlen calls the cluster kernel)."""
     if unbounded:
         return "recur"
-    return "decode" if T == 1 else ("short" if T <= DECODE_MAX_T else "cluster")
+    if T == 1:
+        return "decode"
+    if T <= DECODE_MAX_T:
+        return "short"
+    return "cluster" if varlen else "pool"
 
 
-def kernel_for(d) -> str:
-    return kernel_of(d["T"], d["lower_bound"] is None)
+def kernel_for(d, sms: int = SMS_DEFAULT) -> str:
+    """The dominant kernel of a kda_fwd call on these inputs (the sequence-parallel
+    path's state-only and output runs are cluster-kernel launches)."""
+    varlen = d["cu_seqlens"] is not None
+    if not varlen and d["lower_bound"] is not None and tsplit_segments(
+            d["N"], d["T"], d["H"], False, sms):
+        return "cluster"
+    return kernel_of(d["T"], d["lower_bound"] is None, varlen)
 
 
 # The dispatch rule of kda_fwd for the sequence-parallel path (kda_internal.h,
@@ -368,7 +381,9 @@ def run_ours(args):
     d_cpu = W.make_inputs(w)
     e = {key: (val.to(dev) if torch.is_tensor(val) else val) for key, val in d_cpu.items()}
     B, T, H, N = d_cpu["B"], d_cpu["T"], d_cpu["H"], d_cpu["N"]
-    lpc = launches_per_call(d_cpu, torch.cuda.get_device_properties(dev).multi_processor_count)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    lpc = launches_per_call(d_cpu, sms)
+    kern = kernel_for(d_cpu, sms)
     out = torch.empty((B, T, H, 128), dtype=torch.bfloat16, device=dev)
     fin = None
     if d_cpu["state_dtype"]:
@@ -495,39 +510,38 @@ def run_ours(args):
     abytes = algorithmic_bytes(d_cpu)
     achieved = abytes / (avg_launch_ms / 1e3) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-            "frac": achieved / hbm, "traffic": stored_traffic(w.name, kernel_for(d_cpu)),
+            "frac": achieved / hbm, "traffic": stored_traffic(w.name, kern),
             "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
             else f"{src} {hbm} GB/s",
             "kernel": ("kda_short_kernel + kda_cluster_kernel (kda_fwd: each on its own sequences, "
                        "2 launches per step, the time of the whole call)") if mixed_dispatch(d_cpu) else
-                      KERNEL_NAMES[kernel_for(d_cpu)] + (
+                      KERNEL_NAMES[kern] + (
                 " (kda_fwd: one launch per step)" if lpc == 1 else
                 f" (kda_fwd: sequence-parallel path, {lpc} launches per step, the time of the whole call)"),
             "algorithmic_bytes_per_launch": abytes,
             "algorithmic_flops_per_launch": algorithmic_flops(d_cpu),
             "tensor_frac": algorithmic_flops(d_cpu) / (avg_launch_ms / 1e3) / (tflops * 1e12)}
-    if kernel_for(d_cpu) == "recur":
-        # The token recurrence runs on the fp32 CUDA cores: 4 K V multiply-adds per
-        # token-head (decay, k^T S, the rank-1 update, q^T S), against 128 fp32 lanes per
-        # SM at the maximum SM clock.
-        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    if kern == "recur":
+        # `frac` stays the HBM roofline of the method (the same definition as every other
+        # workload).  The token recurrence itself runs on the fp32 CUDA cores: 4 K V
+        # multiply-adds per token-head (decay, k^T S, the rank-1 update, q^T S), against
+        # 128 fp32 lanes per SM at the maximum SM clock; that fraction is `alu_view`.
         mhz = (clk or {}).get("sm_max_mhz") or SM_MAX_MHZ
         peak_alu = sms * 128 * 2 * mhz * 1e6 / 1e12
         rflops = B * T * H * RECUR_FLOPS_PER_TOKEN_HEAD
         ach = rflops / (avg_launch_ms / 1e3) / 1e12
-        roof = dict(roof, bound="alu", achieved=ach, peak=peak_alu, unit="TFLOP/s", frac=ach / peak_alu,
-                    peak_source=f"derived: {sms} SMs x 128 fp32 lanes x 2 flops x {mhz:.0f} MHz",
-                    hbm_view={"achieved_gbs": achieved, "peak_gbs": hbm, "frac": achieved / hbm},
-                    algorithmic_flops_per_launch=rflops)
+        roof["alu_view"] = {"bound": "alu", "achieved": ach, "peak": peak_alu, "unit": "TFLOP/s",
+                            "frac": ach / peak_alu, "flops_per_launch": rflops,
+                            "peak_source": f"derived: {sms} SMs x 128 fp32 lanes x 2 flops x {mhz:.0f} MHz"}
     cpu = cpu_baseline(d_cpu) if ws == 1 else None
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": dict(workload_config(w.name, d_cpu),
-                       l2=f"algorithmic traffic {abytes / 1e6:.0f} MB per step "
-                          f"({'larger' if abytes > 129e6 else 'smaller'} than the 129 MB L2); "
-                          "a 256 MB flush write between timed steps",
-                       timing="CUDA events around each kda_fwd call"),
+            "config": workload_config(w.name, d_cpu),
+            "l2": f"algorithmic traffic {abytes / 1e6:.0f} MB per step "
+                  f"({'larger' if abytes > 129e6 else 'smaller'} than the 129 MB L2); "
+                  "a 256 MB flush write between timed steps",
+            "timing": "CUDA events around each kda_fwd call",
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
             "gpu_launches": args.steps * lpc,
             "wall_s_timed_region": wall}
@@ -537,9 +551,35 @@ def run_ours(args):
     return 0
 
 
+def free_port() -> int:
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def relaunch_cmd(args, argv) -> list:
+    """The torchrun command that runs this bench on `--gpus` ranks of this node."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+            f"--nproc-per-node={args.gpus}", "--master-addr", "127.0.0.1",
+            "--master-port", str(free_port()), os.path.abspath(__file__)] + list(argv)
+
+
+def check_world(args) -> str | None:
+    """--gpus must agree with the launcher's world size (None when it does)."""
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus < 1:
+        return f"--gpus {args.gpus}: at least one GPU"
+    if "WORLD_SIZE" in os.environ and ws != args.gpus:
+        return f"--gpus {args.gpus} but the launcher started {ws} ranks"
+    return None
+
+
 def main(argv=None):
+    argv = sys.argv[1:] if argv is None else argv
     ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--gpus", type=int, default=1,
+                    help="ranks (one per GPU); more than 1 without torchrun relaunches under it")
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
@@ -547,6 +587,12 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        return subprocess.call(relaunch_cmd(args, argv))
+    bad = check_world(args)
+    if bad:
+        print(bad, file=sys.stderr)
+        return 2
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -81,14 +81,19 @@ def test_max_over_ranks_without_group_is_identity():
 
 def test_kernel_of_follows_the_packed_token_count():
     # the kernel label and stored-traffic lookup follow the dispatch of kda_fwd:
-    # one row -> token recurrence, up to 64 -> 16-row blocks, more -> cluster kernel
+    # one row -> token recurrence, up to 64 -> 16-row blocks, more -> the pool kernel
+    # (fixed length) or the cluster kernel (varlen)
     import bench
     from gated_delta_rule_52_gb300 import workloads as W
     assert bench.kernel_of(1) == "decode"
     assert bench.kernel_of(2) == "short" and bench.kernel_of(64) == "short"
-    assert bench.kernel_of(65) == "cluster"
+    assert bench.kernel_of(65) == "pool" and bench.kernel_of(65, varlen=True) == "cluster"
     d = W.make_inputs(W.get("varlen_ragged", H=1, seqlens=(40, 30)))
-    assert bench.kernel_of(d["T"]) == "cluster"   # the ragged workload's T is the packed total
+    assert bench.kernel_for(d) == "cluster"   # the ragged workload's T is the packed total
+    assert bench.kernel_for(W.make_inputs(W.get("tiny"))) == "pool"
+    # few units on a long fixed-length call: the sequence-parallel path (cluster runs)
+    d8 = W.make_inputs(W.get("tiny", T=8192, H=1))
+    assert bench.kernel_for(d8) == "cluster" and bench.launches_per_call(d8, 152) > 1
     for k in bench.KERNEL_SOURCES:
         assert len(bench.kernel_source_hash(k)) == 16 and k in bench.KERNEL_NAMES
 
@@ -120,7 +125,7 @@ def test_gate_without_lower_bound_runs_the_recurrence():
     assert d["lower_bound"] is None
     assert bench.kernel_for(d) == "recur" and not bench.mixed_dispatch(d)
     assert bench.launches_per_call(d, 152) == 1
-    assert bench.kernel_of(8192, unbounded=True) == "recur" and bench.kernel_of(8192) == "cluster"
+    assert bench.kernel_of(8192, unbounded=True) == "recur" and bench.kernel_of(8192) == "pool"
     assert "recur" in bench.KERNEL_NAMES and len(bench.kernel_source_hash("recur")) == 16
 
 
@@ -132,3 +137,18 @@ def test_both_arms_report_the_same_workload_config():
     du = W.make_inputs(W.get("tiny", lower_bound=None))
     cu = bench.workload_config("tiny", du)
     assert cu["lower_bound"] is None and "softplus" in cu["gate"]
+
+
+def test_gpus_flag_is_checked_against_the_launcher(monkeypatch):
+    import argparse
+    args = argparse.Namespace(gpus=2, steps=3, warmup=3, impl="ours", workload="tiny")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    assert bench.check_world(args) is None
+    monkeypatch.setenv("WORLD_SIZE", "4")
+    assert "4 ranks" in bench.check_world(args)
+    monkeypatch.delenv("WORLD_SIZE")
+    cmd = bench.relaunch_cmd(args, ["--gpus", "2", "--steps", "3"])
+    assert "torch.distributed.run" in cmd and "--nproc-per-node=2" in cmd
+    assert cmd[cmd.index("--master-addr") + 1] == "127.0.0.1"
+    assert cmd[-3:] == ["--gpus", "2", "--steps", "3"][-3:]
+    assert bench.check_world(argparse.Namespace(gpus=0)) is not None
