@@ -26,8 +26,9 @@
 // Packet (c, j) goes through ring slot (c, j % D): the front waits until the chain
 // has loaded packet j - D out of it ("freed" flag), stores the packet, then sets
 // the slot's "ready" flag; the chain's loader warp waits for "ready", bulk-loads the
-// packet and sets "freed".  Flags hold the launch's epoch plus the packet index, so the
-// ring needs no clearing between calls.
+// packet and sets "freed".  Flags hold the packet index + 1; every call clears them (a
+// stream-ordered memset before the launch), so neither a reused workspace nor a replayed
+// CUDA graph can meet a flag that matches too early.
 //
 // Front CTA (per packet, pipelined as in the cluster kernel's front): warps 0-7 the
 // prologue (gate, block-local decay, the operands of G1 = [Kp; Qp] x Kn^T and the
@@ -111,11 +112,12 @@ constexpr uint32_t SMEM_BYTES = COMMON + 16 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // ---------------------------------------------------------------- ring and flags
-// Ring depth D (slots per chain).  A front publishes a packet only once it has issued
-// the stores of its next one, whose slot it waits out first: that slot's earlier packet
-// has index (i + nf) - D nc, which must lie below the held packet's index i, or the
-// pool could wait in a circle.  So D > nf / nc; a few more slots (at least kRingMin)
-// let the fronts run ahead of the chains without waiting on the ring.
+// Ring depth D (slots per chain).  Any D >= 1 is free of deadlock: the publication of a
+// packet waits only on work of its own front and on ring slots of packets of lower index
+// (a front publishes its previous packet before it waits for anything of the next one).
+// D is a matter of speed: with about nf / nc fronts per chain, D > nf / nc plus a few
+// slots (at least kRingMin) lets the fronts run ahead of the chains without waiting on
+// the ring.
 constexpr int kRingMin = 8;
 __host__ __device__ constexpr int64_t ring_depth(int64_t nc, int64_t nf) {
     return nf / nc + 6 > kRingMin ? nf / nc + 6 : kRingMin;
@@ -126,7 +128,6 @@ __host__ __device__ constexpr int64_t ring_depth(int64_t nc, int64_t nf) {
 struct PoolArgs {
     unsigned char *ring;
     unsigned long long *flags;
-    unsigned long long epoch;   // this launch's tag base (a per-process counter << 32)
     int nc, nf;                 // chain CTAs, front CTAs
     int depth;                  // ring slots per chain
     int nchunks;                // chunks per unit (fixed-length calls)
@@ -141,7 +142,7 @@ struct PoolArgs {
     __device__ unsigned long long *freed(int64_t c, int64_t j) const {
         return flags + (size_t)c * 2 * depth + depth + (size_t)(j % depth);
     }
-    __device__ unsigned long long tag(int64_t j) const { return epoch + (unsigned long long)j + 1ull; }
+    __device__ unsigned long long tag(int64_t j) const { return (unsigned long long)j + 1ull; }
 };
 
 __device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long *ptr) {
@@ -747,11 +748,19 @@ __device__ __forceinline__ void pool_front(const TmaMaps &maps, const Params &p,
             named_bar(2, NS);
             if (stid == kSolLead) {
                 mbar_arrive(&sm.s_done[m % 3]);
+                // The previous packet is published first: its T'/M stores were issued a
+                // task ago and the control warp's stores of it were complete before them,
+                // so this costs no wait, and a publication never waits on a ring slot.
+                if (pub_flag) {
+                    bulk_wait0();
+                    fence_proxy_async_global();
+                    st_release_gpu(pub_flag, pub_tag);
+                    pub_flag = nullptr;
+                }
                 // T' and M complete the packet, once the control warp has stored the rest
                 // (which also means the slot's earlier packet is out).  The packet is
-                // published one task later, when all its stores have completed for sure, so
-                // that the solver does not wait for them here (the ring depth makes that
-                // safe, see ring_depth).
+                // published one task later, so that the solver does not wait for the
+                // completion of its stores here.
                 bool ok = true;
                 if (ld_acquire_cta(&sm.ctl_count) <= (unsigned)m) {
                     const uint64_t t0 = globaltimer_ns();
@@ -763,11 +772,6 @@ __device__ __forceinline__ void pool_front(const TmaMaps &maps, const Params &p,
                     bulk_store(slot + RS_TP, smem + F_AMAT, 8192);
                     bulk_store(slot + RS_MM, smem + F_MST, 8192);
                     bulk_commit();
-                    if (pub_flag) {
-                        bulk_wait1();   // every group but this one is complete
-                        fence_proxy_async_global();
-                        st_release_gpu(pub_flag, pub_tag);
-                    }
                     pub_flag = a.ready(it.c, it.j);
                     pub_tag = a.tag(it.j);
                 } else {
@@ -1297,11 +1301,6 @@ cudaError_t launch_pool(const Params &p, int sms, cudaStream_t stream) {
     a.ring = p.ws;
     a.depth = (int)ring_depth(nc, nf);
     a.flags = reinterpret_cast<unsigned long long *>(p.ws + (size_t)nc * a.depth * kChunkBytes);
-    // A per-process counter in the high half: flags left by earlier calls never match
-    // this call's tags (packet indices stay below 2^32).
-    static std::atomic<unsigned long long> launches{0};
-    a.epoch = (launches.fetch_add(1) + 1) << 32;
-    if ((int64_t)a.waves * nchunks >= (int64_t(1) << 32)) return cudaErrorInvalidValue;
     TmaMaps maps;
     const int64_t rows = p.B * p.T;
     if (!encode_map(&maps.q, p.q, rows, p.H) || !encode_map(&maps.k, p.k, rows, p.H) ||
@@ -1322,6 +1321,9 @@ cudaError_t launch_pool(const Params &p, int sms, cudaStream_t stream) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    // the flags of this call start at zero (no packet index + 1 is zero)
+    e = cudaMemsetAsync(a.flags, 0, (size_t)nc * 2 * a.depth * sizeof(unsigned long long), stream);
+    if (e != cudaSuccess) return e;
     e = cudaLaunchKernelEx(&cfg, kda_pool_kernel, maps, p, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

@@ -89,20 +89,28 @@ typedef enum {
  *   stream         cudaStream_t to enqueue on (NULL = legacy default stream)
  *
  * Ownership: the caller owns every buffer and the call keeps no pointer after it
- * returns.  The only memory the call allocates is its workspace
- * (KDA_WORKSPACE_BYTES_PER_UNIT bytes per (sequence, head), holding the
- * per-chunk operands that move between the two CTAs of a cluster through L2),
- * taken stream-ordered on `stream` from a memory pool that libkda.so creates
- * once per device and keeps mapped, and released on `stream` after the kernel.
- * Calls of at most 64 token rows need no workspace.  A fixed-length call
+ * returns.  The only memory the call allocates is its workspace, taken
+ * stream-ordered on `stream` from a memory pool that libkda.so creates once per
+ * device and keeps mapped, and released on `stream` after the kernel:
+ *   - fixed-length calls of more than 64 rows run one persistent kernel, one CTA
+ *     per SM launched cooperatively (it starts once every CTA can be resident):
+ *     "front" CTAs form the chunk-parallel operands of every chunk and hand them
+ *     to "chain" CTAs, one per (sequence, head) in flight, through a ring of
+ *     packets in L2; the ring takes 8 or more slots of 66 KB per chain (33.8 MB
+ *     for 64 units on 152 SMs);
+ *   - varlen calls take KDA_WORKSPACE_BYTES_PER_UNIT bytes per (sequence, head),
+ *     the per-chunk operands that move between the two CTAs of a cluster;
+ *   - calls of at most 64 token rows need no workspace.
+ * A fixed-length call
  * (cu_seqlens == NULL) whose N * H (sequence, head) units would leave most of the
  * GPU idle, with T >= 8192, runs the sequence-parallel path: each sequence is cut
  * into P >= 4 segments of at least 2048 tokens, whose affine state maps are joined
  * by a scan (same results within the stated tolerances, three times the work on P
  * times the parallelism); its scratch, also from the pool, is about
  * N * H * P * (4 * 64 KB + KDA_WORKSPACE_BYTES_PER_UNIT) bytes.
- * kda_fwd_ws is the same call with a caller-provided workspace; it always takes
- * the plain path.  Both are asynchronous: they return once the work is enqueued,
+ * kda_fwd_ws is the same call with a caller-provided workspace; for more than 64
+ * rows it always runs the two-CTA cluster kernel, whose workspace kda_workspace_size
+ * gives (neither the ring nor the sequence-parallel scratch).  Both are asynchronous: they return once the work is enqueued,
  * without synchronising.
  * q/k/v/g/beta/out/A_log/dt_bias/states must be 16-byte aligned.  `out` must not
  * alias an input.

@@ -385,6 +385,22 @@ def test_cuda_graph_capture_replays_the_call(name, wl):
     torch.cuda.synchronize()
     assert kda.get_device_status() == kda.KDA_OK
     assert torch.equal(out, ref_out) and torch.equal(fin, ref_fin)
+    # A serving loop replays the graph on new inputs written into the same buffers: every
+    # replay must see only its own data (no state carried between replays of the call)
+    d2 = W.make_inputs(W.get("decode", state_dtype="fp32", seed=51, **wl))
+    for key in ("q", "k", "v", "g", "beta", "initial_state"):
+        e[key].copy_(d2[key].to(e[key].device))
+    call()
+    torch.cuda.synchronize()
+    ref_out2, ref_fin2 = out.clone(), fin.clone()
+    assert not torch.equal(ref_out2, ref_out)
+    for _ in range(2):
+        out.zero_()
+        fin.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert kda.get_device_status() == kda.KDA_OK
+        assert torch.equal(out, ref_out2) and torch.equal(fin, ref_fin2)
 
 
 # ---- the gate without a lower bound (kda_fwd_unbounded, the token recurrence)
