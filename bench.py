@@ -125,27 +125,33 @@ def workload_config(name: str, d) -> dict:
                      if d["lower_bound"] is None else "lower_bound sigmoid(exp(A_log) (g + dt_bias))")}
 
 
-def kernel_of(T: int, unbounded: bool = False, varlen: bool = False) -> str:
-    """The kernel libkda runs for a call of T packed token rows (the gate without a
-    lower bound always runs the token recurrence; fixed-length calls of more than 64
-    rows run the persistent pool kernel, varlen calls the cluster kernel)."""
+POOL_MAX_SEQS = 4096   # kda_internal.h kPoolMaxSeqs: larger varlen batches run the cluster kernel
+
+
+def kernel_of(T: int, unbounded: bool = False, varlen: bool = False, n_seqs: int = 1) -> str:
+    """The kernel libkda runs for a call of T packed token rows: calls of more than 64
+    rows run the persistent pool kernel, except varlen calls of more than POOL_MAX_SEQS
+    sequences (the cluster kernel; the token recurrence for the gate without a lower
+    bound); calls of at most 64 rows the one-token or 16-row-block kernels (the token
+    recurrence for the gate without a lower bound)."""
+    big_varlen = varlen and n_seqs > POOL_MAX_SEQS
     if unbounded:
-        return "recur"
+        return "recur" if T <= DECODE_MAX_T or big_varlen else "pool"
     if T == 1:
         return "decode"
     if T <= DECODE_MAX_T:
         return "short"
-    return "cluster" if varlen else "pool"
+    return "cluster" if big_varlen else "pool"
 
 
 def kernel_for(d, sms: int = SMS_DEFAULT) -> str:
     """The dominant kernel of a kda_fwd call on these inputs (the sequence-parallel
-    path's state-only and output runs are cluster-kernel launches)."""
+    path's state-only and output runs are pool-kernel launches)."""
     varlen = d["cu_seqlens"] is not None
     if not varlen and d["lower_bound"] is not None and tsplit_segments(
             d["N"], d["T"], d["H"], False, sms):
-        return "cluster"
-    return kernel_of(d["T"], d["lower_bound"] is None, varlen)
+        return "pool"
+    return kernel_of(d["T"], d["lower_bound"] is None, varlen, d["N"])
 
 
 # The dispatch rule of kda_fwd for the sequence-parallel path (kda_internal.h,
@@ -165,8 +171,8 @@ MIXED_MAX_AVG = 256   # kda_internal.h kMixedMaxAvg
 
 
 def mixed_dispatch(d) -> bool:
-    """A varlen call of more than 64 rows with at most 256 per sequence on average: the
-    short-step kernel and the cluster kernel each take their own sequences."""
+    """A varlen call of more than 64 rows with at most 256 per sequence on average (bounded
+    gate): the short-step kernel and the chunked kernel each take their own sequences."""
     return (d["lower_bound"] is not None and d["cu_seqlens"] is not None
             and DECODE_MAX_T < d["T"] <= MIXED_MAX_AVG * d["N"])
 
@@ -174,11 +180,14 @@ def mixed_dispatch(d) -> bool:
 def launches_per_call(d, sms: int) -> int:
     """libkda kernel launches of one kda_fwd call on these inputs."""
     if d["lower_bound"] is None:
-        return 1
+        return 2 if d["cu_seqlens"] is not None and kernel_for(d, sms) == "pool" else 1
     P = tsplit_segments(d["N"], d["T"], d["H"], d["cu_seqlens"] is not None, sms)
-    if P:   # segment bounds, segment states, 2 state-only runs, scan, output run (+ final copy)
-        return 6 + (d["state_dtype"] is not None)
-    return 2 if mixed_dispatch(d) else 1
+    if P:   # segment bounds, segment states, 3 runs of plan + pool, scan (+ final copy)
+        return 9 + (d["state_dtype"] is not None)
+    if d["T"] <= DECODE_MAX_T:
+        return 1
+    pool_varlen = d["cu_seqlens"] is not None and kernel_for(d, sms) == "pool"   # plan + pool
+    return (2 if pool_varlen else 1) + (1 if mixed_dispatch(d) else 0)
 
 
 def kernel_source_hash(kernel: str = "cluster") -> str:
@@ -513,11 +522,14 @@ def run_ours(args):
             "frac": achieved / hbm, "traffic": stored_traffic(w.name, kern),
             "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
             else f"{src} {hbm} GB/s",
-            "kernel": ("kda_short_kernel + kda_cluster_kernel (kda_fwd: each on its own sequences, "
-                       "2 launches per step, the time of the whole call)") if mixed_dispatch(d_cpu) else
+            "kernel": (f"kda_short_kernel + {KERNEL_NAMES[kern]} (kda_fwd: each on its own sequences, "
+                       f"{lpc} launches per step, the time of the whole call)") if mixed_dispatch(d_cpu) else
                       KERNEL_NAMES[kern] + (
                 " (kda_fwd: one launch per step)" if lpc == 1 else
-                f" (kda_fwd: sequence-parallel path, {lpc} launches per step, the time of the whole call)"),
+                f" (kda_fwd: sequence-parallel path, {lpc} launches per step, the time of the whole call)"
+                if tsplit_segments(d_cpu["N"], d_cpu["T"], d_cpu["H"], d_cpu["cu_seqlens"] is not None, sms)
+                and d_cpu["lower_bound"] is not None else
+                " (kda_fwd: a one-CTA plan and the pool, 2 launches per step, the time of the whole call)"),
             "algorithmic_bytes_per_launch": abytes,
             "algorithmic_flops_per_launch": algorithmic_flops(d_cpu),
             "tensor_frac": algorithmic_flops(d_cpu) / (avg_launch_ms / 1e3) / (tflops * 1e12)}

@@ -152,9 +152,16 @@ kda_status launch(kda::Params &p, void *stream, int64_t tsplit = 0, int pool_sms
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (tsplit > 0) {
-        e = kda::launch_tsplit(p, tsplit, p.ws, cs);
+        e = kda::launch_tsplit(p, tsplit, pool_sms, p.ws, cs);
     } else if (pool_sms > 0) {
-        e = kda::launch_pool(p, pool_sms, cs);
+        e = cudaSuccess;
+        if (p.cu_seqlens && p.T <= kda::kMixedMaxAvg * p.n_seqs && !p.unbounded) {
+            // mostly short sequences: those of at most kShortMaxT tokens on the short-step
+            // kernel, the rest on the pool, one launch after the other
+            p.mixed = 1;
+            e = kda::launch_short(p, cs);
+        }
+        if (e == cudaSuccess) e = kda::launch_pool(p, pool_sms, cs);
     } else if (p.T == 1) {
         e = kda::launch_decode(p, cs);
     } else if (p.T <= kda::kShortMaxT) {
@@ -212,10 +219,11 @@ kda_status kda_fwd(const void *q, const void *k, const void *v, const void *g, c
     int sms = 0;
     if (kda::sm_count(sms) != cudaSuccess) return KDA_ERR_CUDA;
     const int64_t tsplit = kda::tsplit_segments(p, sms);
-    // fixed-length calls otherwise run the persistent pool kernel
-    const int pool_sms = (tsplit == 0 && !p.cu_seqlens) ? sms : 0;
-    const size_t bytes = tsplit > 0     ? kda::tsplit_scratch_bytes(p.n_seqs, p.H, tsplit)
-                         : pool_sms > 0 ? kda::pool_scratch_bytes(p.n_seqs * p.H, pool_sms)
+    // other calls run the persistent pool kernel (varlen calls of up to kPoolMaxSeqs
+    // sequences), the rest the cluster kernel
+    const int pool_sms = (tsplit > 0 || kda::pool_takes(p, sms)) ? sms : 0;
+    const size_t bytes = tsplit > 0     ? kda::tsplit_scratch_bytes(p, tsplit, sms)
+                         : pool_sms > 0 ? kda::pool_scratch_bytes(p, pool_sms)
                                         : (size_t)(p.n_seqs * p.H) * kda::kWsBytesPerUnit;
     void *ws = nullptr;
     if (cudaMallocFromPoolAsync(&ws, bytes, pool, cs) != cudaSuccess) return KDA_ERR_CUDA;
@@ -256,8 +264,25 @@ kda_status kda_fwd_unbounded(const void *q, const void *k, const void *v, const 
                              final_state, state_dtype, cu_seqlens, num_seqs, B, T, H, K, V, p);
     if (st != KDA_OK) return st;
     if (p.n_seqs == 0 || p.H == 0) return KDA_OK;
-    return kda::launch_recur(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KDA_OK
-                                                                                : KDA_ERR_CUDA;
+    p.unbounded = 1;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    int sms = 0;
+    if (kda::sm_count(sms) != cudaSuccess) return KDA_ERR_CUDA;
+    // Calls of at most 64 rows, and varlen batches beyond the pool's plan, run the token
+    // recurrence; the rest the pool kernel's chunked form (every sequence on it).
+    if (p.T <= kda::kShortMaxT || !kda::pool_takes(p, sms))
+        return kda::launch_recur(p, cs) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return KDA_ERR_CUDA;
+    cudaMemPool_t pool = workspace_pool(device);
+    if (!pool) return KDA_ERR_CUDA;
+    void *ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, kda::pool_scratch_bytes(p, sms), pool, cs) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    p.ws = static_cast<unsigned char *>(ws);
+    st = launch(p, stream, 0, sms);
+    if (cudaFreeAsync(ws, cs) != cudaSuccess) st = KDA_ERR_CUDA;
+    return st;
 }
 
 kda_status kda_fwd_static(const void *q, const void *k, const void *v, const void *g,

@@ -38,8 +38,9 @@ struct Params {
     int64_t B, T, H;
     int *err;           // device error word (bounded waits that give up set it)
     unsigned char *ws;  // workspace: kWsBytesPerUnit bytes per (sequence, head), 16-byte aligned
+    int unbounded;      // the gate without a lower bound (lower_bound unused); pool kernel only
     int mixed;          // varlen call split by length: the short-step kernel takes the
-                        // sequences of at most kShortMaxT tokens, the cluster kernel the rest
+                        // sequences of at most kShortMaxT tokens, the chunked kernel the rest
 };
 
 // Token range of sequence n: packed batch row `b`, first token `t0`, `len` tokens.
@@ -86,11 +87,16 @@ cudaError_t launch_cluster(const Params &p, cudaStream_t stream);   // chunked, 
 cudaError_t launch_decode(const Params &p, cudaStream_t stream);    // token recurrence, T = 1 only
 cudaError_t launch_short(const Params &p, cudaStream_t stream);     // 16-row blocks, 2 <= T <= 64
 
-// Persistent pool kernel for fixed-length calls (cu_seqlens == nullptr, T > kShortMaxT):
-// chain CTAs run the state recurrence, front CTAs the chunk-parallel work, handing each
-// chunk over through a ring in p.ws (pool_scratch_bytes long).
+// Persistent pool kernel for calls of more than kShortMaxT rows: chain CTAs run the state
+// recurrence, front CTAs the chunk-parallel work, handing each chunk over through a ring
+// in p.ws (pool_scratch_bytes long).  Varlen calls (up to kPoolMaxSeqs sequences; with
+// p.mixed set, only the sequences of more than kShortMaxT tokens) first run a one-CTA plan
+// that orders the units longest first and spreads them over the chains.
+constexpr int64_t kPoolMaxSeqs = 4096;
 int64_t pool_chains(int64_t units, int sms);
-size_t pool_scratch_bytes(int64_t units, int sms);
+bool pool_takes(const Params &p, int sms);   // the pool path accepts this call
+size_t pool_scratch_bytes(const Params &p, int sms);
+size_t pool_scratch_bytes_varlen(int64_t N, int64_t H, int64_t T, int sms);   // N sequences, T packed rows
 cudaError_t launch_pool(const Params &p, int sms, cudaStream_t stream);
 
 // Sequence-parallel prefill (fixed-length calls with few (sequence, head) units): each
@@ -98,7 +104,7 @@ cudaError_t launch_pool(const Params &p, int sms, cudaStream_t stream);
 constexpr int64_t kTsplitMinSeg = 2048;
 constexpr int64_t kTsplitMaxSeg = 32;
 int64_t tsplit_segments(const Params &p, int sms);   // P, or 0: run the plain path
-size_t tsplit_scratch_bytes(int64_t N, int64_t H, int64_t P);
-cudaError_t launch_tsplit(const Params &p, int64_t P, unsigned char *scratch, cudaStream_t stream);
+size_t tsplit_scratch_bytes(const Params &p, int64_t P, int sms);
+cudaError_t launch_tsplit(const Params &p, int64_t P, int sms, unsigned char *scratch, cudaStream_t stream);
 
 }  // namespace kda

@@ -16,13 +16,20 @@
 //
 // Grid: one CTA per SM, launched cooperatively (all CTAs resident at once, which the
 // flag waits between CTAs need).  CTAs 0 .. nc-1 are chains, the rest fronts.
-//   Chain c owns units c, c + nc, ...; its packets (chunks) j = 0, 1, ... are chunk
-//   j % nchunks of unit c + (j / nchunks) nc.
-//   Front f takes the packets of global index i = f, f + nf, f + 2 nf, ... in the order
-//   i = j * nc + c (packet j of chain c), so fronts produce packets in the order the
-//   chains consume them.  The packet of lowest index not yet produced can always be
-//   produced (the slot it needs holds a packet of lower index, which its chain
-//   consumes), so the pool cannot deadlock.
+//   Fixed-length calls: chain c owns units c, c + nc, ...; its packets (chunks) j = 0,
+//   1, ... are chunk j % nchunks of unit c + (j / nchunks) nc.  Front f takes the
+//   packets of global index i = f, f + nf, f + 2 nf, ... in the order i = j * nc + c
+//   (packet j of chain c), so fronts produce packets in the order the chains consume
+//   them.
+//   Varlen calls: a one-CTA plan (pool_plan_kernel) sorts the sequences longest first
+//   and deals their (sequence, head) units to the chains in snake order (round w gives
+//   unit w nc + c to chain c in even rounds, w nc + nc - 1 - c in odd ones), so that
+//   every chain gets about the same number of packets.  Global index i then runs over
+//   steps j, and within a step over the chains that still have a packet j, longest
+//   chain first; the plan writes that list of packets for the fronts.
+//   Either way the packet of lowest index not yet produced can always be produced (the
+//   slot it needs holds a packet of lower index, which its chain consumes), so the pool
+//   cannot deadlock.
 // Packet (c, j) goes through ring slot (c, j % D): the front waits until the chain
 // has loaded packet j - D out of it ("freed" flag), stores the packet, then sets
 // the slot's "ready" flag; the chain's loader warp waits for "ready", bulk-loads the
@@ -41,6 +48,8 @@
 // Precision: G1 on bf16 operands of the raw q/k scaled by 16-token-block-local decay
 // factors, the other GEMMs on fp16 operands, fp32 accumulators, fp32 state.  Every wait
 // is bounded (2 s); a timeout sets the device error word and the CTA unwinds.
+#include <type_traits>
+
 #include "kda_chunk.cuh"
 
 namespace kda {
@@ -81,10 +90,26 @@ constexpr uint32_t PK_KB = 0, PK_QG = 16384, PK_KG = 32768, PK_TP = 49152, PK_MM
 constexpr uint32_t C_END = C_PK + 2 * C_PKSLOT;
 constexpr uint32_t F_END = F_TF + 64 * LDA * 4;
 
+// Rows of the decay-factor table of one chunk (per 16-token block b and channel c), with
+// Gs[b] the cumulative log2 decay before block b, G_C the chunk total and mu[b] half of
+// block b's total (the shift of the operand factors, see the prologue):
+//   pool_fac_base(b) + 0: 2^(Gs[b] + mu[b])       Q_hat Gamma, K_hat Gamma (with 2^(H - mu))
+//                    + 1: 2^(G_C - Gs[b] - mu[b]) Kbar (with 2^(mu - H))
+//                    + 2: 2^(mu[b])               b < 3: turns 2^(mu - H) into 2^(Gs[b+1] - G)
+//                    + 2 + (bt - b): 2^(Gs[bt] - Gs[b+1] + mu[bt])  key variant of row block bt > b
+// Every entry is at most 1.  Each variant is the product of two factors at most 1
+// (2^(Gs[b+1] - G) first, then the table entry), so where a factor underflows the term
+// it belongs to is below 2^-37 of the largest one.  With the lower bound, mu = 0 and the
+// variant of row block bt is 2^-H times the single entry 2^(Gs[bt] - Gs[b]) (row + 2 +
+// (bt - b); the row + 2 entry is unused): every block decays by at most 2^-115, so
+// neither factor leaves the fp32 range.
+constexpr int kPoolFacRows = 17;
+__device__ __forceinline__ int pool_fac_base(int b) { return b == 0 ? 0 : (b == 1 ? 6 : (b == 2 ? 11 : 15)); }
+
 struct FrontSmall {
     float rq[3][C], rk[3][C], beta[3][C];   // per norm slot (task % 3)
     float btot[4][DK];
-    float fac[kFacRows][DK];                 // decay factors, see fac_base
+    float fac[kPoolFacRows][DK];             // decay factors, see pool_fac_base
     float gamC_f[2][DK];                     // exp(G_C) per slot (store source)
     float gb[2][DK];                         // gate bias a2 * dt_bias[h] per slot (log2 units)
     float ga[2];                             // a2 = -exp(A_log[h]) log2(e) per slot
@@ -132,6 +157,11 @@ struct PoolArgs {
     int depth;                  // ring slots per chain
     int nchunks;                // chunks per unit (fixed-length calls)
     int waves;                  // ceil(units / nc)
+    // varlen calls: the plan of pool_plan_kernel (null for fixed-length calls)
+    const int4 *plist;          // packets in production order: {chain, packet, first row, h << 8 | rows}
+    const int *order;           // the sequences the pool takes, longest first
+    const int *chain_len;       // packets per chain
+    const int *counts;          // [0] packets in all, [1] units the pool takes
 
     __device__ unsigned char *slot(int64_t c, int64_t j) const {
         return ring + ((size_t)c * depth + (size_t)(j % depth)) * kChunkBytes;
@@ -229,9 +259,98 @@ struct TaskIt {
     __device__ bool valid() const { return i < end; }
 };
 
+// The packets of one front of a varlen call, from the plan's list (the entry one step
+// ahead is loaded a task early, so that its latency is hidden).
+struct TaskItV {
+    int64_t i, end;
+    int nf;
+    const int4 *pl;
+    int4 nxt;
+    int c, h, L;
+    int64_t j, row;
+    __device__ void take(const int4 e) {
+        c = e.x;
+        j = e.y;
+        row = e.z;
+        h = e.w >> 8;
+        L = e.w & 0xff;
+    }
+    __device__ void start(int f, const PoolArgs &a, int64_t, const Params &) {
+        pl = a.plist;
+        nf = a.nf;
+        end = a.counts[0];
+        i = f;
+        if (i < end) take(pl[i]);
+        if (i + nf < end) nxt = pl[i + nf];
+    }
+    __device__ void advance(const Params &) {
+        i += nf;
+        if (i < end) take(nxt);
+        if (i + nf < end) nxt = pl[i + nf];
+    }
+    __device__ bool valid() const { return i < end; }
+};
+
+// Varlen: unit of chain c in snake round w (see the plan), and the walk over a chain's
+// packets that skips units without tokens.
+struct UnitV {
+    int64_t row0;    // first token row of the sequence
+    int64_t sbase;   // element offset of the (sequence, head) state
+    int h, len, nch;
+    bool valid;
+};
+__device__ __forceinline__ UnitV unit_v(const Params &p, const PoolArgs &a, int c, int64_t w, int64_t U) {
+    UnitV u;
+    const int64_t k = w * a.nc + ((w & 1) ? (a.nc - 1 - c) : c);
+    u.valid = k < U;
+    u.row0 = u.sbase = 0;
+    u.h = u.len = u.nch = 0;
+    if (!u.valid) return u;
+    const int64_t sq = k / p.H;
+    u.h = (int)(k - sq * p.H);
+    const int n = a.order[sq];
+    u.row0 = p.cu_seqlens[n];
+    u.len = (int)(p.cu_seqlens[n + 1] - u.row0);
+    u.nch = (u.len + C - 1) / C;
+    u.sbase = ((int64_t)n * p.H + u.h) * DK * DK;
+    return u;
+}
+struct PkWalkV {
+    UnitV u;
+    int64_t w, U;
+    int m, c;
+    __device__ void skip(const Params &p, const PoolArgs &a) {
+        while (u.valid && m >= u.nch) {
+            ++w;
+            m = 0;
+            u = unit_v(p, a, c, w, U);
+        }
+    }
+    __device__ void start(const Params &p, const PoolArgs &a, int c_) {
+        c = c_;
+        U = a.counts[1];
+        w = 0;
+        m = 0;
+        u = unit_v(p, a, c, 0, U);
+        skip(p, a);
+    }
+    __device__ void next(const Params &p, const PoolArgs &a) {
+        ++m;
+        skip(p, a);
+    }
+    __device__ int64_t row() const { return u.row0 + (int64_t)m * C; }
+    __device__ int rows() const { return u.len - m * C < C ? u.len - m * C : C; }
+};
+
 // ============================================================== front CTA
+// UB: the gate without a lower bound, gk = -exp(A_log) softplus(g + dt_bias), each
+// token's log2 decay raised to at least kMinGate2 (see the gate step).
+constexpr float kMinGate2 = -14.f;
+
+template <bool VL, bool UB>
 __device__ __forceinline__ void pool_front(const TmaMaps &maps, const Params &p, const PoolArgs &a,
                                            unsigned char *smem, FrontSmall &sm, uint32_t tmem, int f) {
+    using TaskIt = typename std::conditional<VL, TaskItV, ::kda::TaskIt>::type;
     const int64_t units = p.n_seqs * p.H;
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -287,7 +406,7 @@ __device__ __forceinline__ void pool_front(const TmaMaps &maps, const Params &p,
             float2 H[4][4];
             {
                 const float2 a2v = make_float2(a2, a2), lb2v = make_float2(lb2, lb2);
-                const float2 one = make_float2(1.f, 1.f);
+                const float2 one = make_float2(1.f, 1.f), l2ev = make_float2(kLog2e, kLog2e);
                 float2 acc[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
@@ -299,9 +418,22 @@ __device__ __forceinline__ void pool_front(const TmaMaps &maps, const Params &p,
                         const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            const float2 z = fma2(bf16x2_to_f2(gw[i]), a2v, bias[i]);
-                            const float2 d = add2(make_float2(exp2f(z.x), exp2f(z.y)), one);
-                            acc[i] = fma2(lb2v, make_float2(__fdividef(1.f, d.x), __fdividef(1.f, d.y)), acc[i]);
+                            if constexpr (UB) {
+                                // y = (g + dt_bias) log2 e; softplus in log2 units is
+                                // max(y, 0) + log2(1 + 2^-|y|), the last term by its two-term
+                                // series where 2^-|y| < 1e-3 (lg2 of 1 + tiny loses it)
+                                const float2 y = fma2(bf16x2_to_f2(gw[i]), l2ev, bias[i]);
+                                const float tx = exp2f(-fabsf(y.x)), ty = exp2f(-fabsf(y.y));
+                                const float lx = tx < 1e-3f ? tx * kLog2e * (1.f - 0.5f * tx) : __log2f(1.f + tx);
+                                const float ly = ty < 1e-3f ? ty * kLog2e * (1.f - 0.5f * ty) : __log2f(1.f + ty);
+                                const float2 sp = make_float2(fmaxf(y.x, 0.f) + lx, fmaxf(y.y, 0.f) + ly);
+                                const float2 gk = mul2(a2v, sp);
+                                acc[i] = add2(acc[i], make_float2(fmaxf(gk.x, kMinGate2), fmaxf(gk.y, kMinGate2)));
+                            } else {
+                                const float2 z = fma2(bf16x2_to_f2(gw[i]), a2v, bias[i]);
+                                const float2 d = add2(make_float2(exp2f(z.x), exp2f(z.y)), one);
+                                acc[i] = fma2(lb2v, make_float2(__fdividef(1.f, d.x), __fdividef(1.f, d.y)), acc[i]);
+                            }
                         }
                     }
 #pragma unroll
@@ -326,27 +458,55 @@ __device__ __forceinline__ void pool_front(const TmaMaps &maps, const Params &p,
                     bt4[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
                     bt4[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
                 }
+                // UB: H relative to mu = half the block's total decay (lane 24 + cg holds
+                // the total), so that the row factors 2^(H - mu) and the diagonal key factors
+                // 2^(mu - H) both stay within 2^(+-total / 2).  With the lower bound a block
+                // decays by at most 2^-115 and mu = 0 (no shift) keeps every factor in range.
+                if constexpr (UB) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 mu = make_float2(-0.5f * __shfl_sync(0xffffffffu, acc[i].x, 24 + cg),
+                                                      -0.5f * __shfl_sync(0xffffffffu, acc[i].y, 24 + cg));
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) H[j][i] = add2(H[j][i], mu);
+                    }
+                }
             }
             named_bar(1, NP + NH);   // gate totals, and the helpers' norms and beta
 
             // decay factors per (block, channel): thread = channel, two blocks each
             {
                 const int c = tid & (DK - 1), bh = tid >> 7;
-                float Gs[4], tot = 0.f;
+                float Gs[4], mu[4], tot = 0.f;
 #pragma unroll
                 for (int bb = 0; bb < 4; ++bb) {
+                    const float bt = sm.btot[bb][c];
                     Gs[bb] = tot;
-                    tot += sm.btot[bb][c];
+                    mu[bb] = UB ? 0.5f * bt : 0.f;   // the prologue's shift of block bb (same value)
+                    tot += bt;
                 }
                 if (bh == 0) sm.gamC_f[s][c] = exp2f(tot);
+                // with mu[b] = half of block b's total (the shift of the operand factors):
+                // Q/K times 2^G = (2^(H - mu)) 2^(Gs + mu); Kbar = (2^(mu - H)) 2^(G_C - Gs - mu);
+                // key variant of row block bt = (2^(mu - H)) 2^(Gs[bt] - Gs[b] + mu[bt] - mu[b]);
+                // every table factor is at most 1
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
                     if ((b >> 1) != bh) continue;
-                    float *f = &sm.fac[fac_base(b)][c];
-                    f[0] = exp2f(Gs[b]);
-                    f[DK] = exp2f(tot - Gs[b]);
+                    float *f = &sm.fac[pool_fac_base(b)][c];
+                    f[0] = exp2f(Gs[b] + mu[b]);
+                    f[DK] = exp2f(tot - Gs[b] - mu[b]);
+                    if constexpr (UB) {
+                        if (b < 3) {
+                            f[2 * DK] = exp2f(mu[b]);
+                            const float gs_next = Gs[b] + 2.f * mu[b];   // Gs[b + 1]
 #pragma unroll
-                    for (int bt = b + 1; bt < 4; ++bt) f[(1 + bt - b) * DK] = exp2f(Gs[bt] - Gs[b]);
+                            for (int bt = b + 1; bt < 4; ++bt) f[(2 + bt - b) * DK] = exp2f(Gs[bt] - gs_next + mu[bt]);
+                        }
+                    } else {   // one step: 2^-H times 2^(Gs[bt] - Gs[b]) (at least 2^-115)
+#pragma unroll
+                        for (int bt = b + 1; bt < 4; ++bt) f[(2 + bt - b) * DK] = exp2f(Gs[bt] - Gs[b]);
+                    }
                 }
             }
             // [Kp; Qp] and Kn are free once G1 of the previous chunk completed
@@ -363,13 +523,13 @@ __device__ __forceinline__ void pool_front(const TmaMaps &maps, const Params &p,
                 break;
             }
 
-            // Operands.  G1 (bf16, raw q/k times block-local decay): Kp = k 2^H and
-            // Qp = q 2^H at rows 32 blk + r and 32 blk + 16 + r of [Kp; Qp]; key
-            // variants Kn(bt) = k 2^(Gs[bt] - Gs[blk] - H) at row variant_off(bt) + t for
-            // bt >= blk.  Chain (fp16, in place of the raw tiles): Q_hat*Gamma,
-            // K_hat*Gamma and Kbar = k_hat 2^(G_C - G).
+            // Operands (H here is the block-local decay minus mu).  G1 (bf16, raw q/k times
+            // block-local decay): Kp = k 2^H and Qp = q 2^H at rows 32 blk + r and
+            // 32 blk + 16 + r of [Kp; Qp]; key variants at row variant_off(bt) + t:
+            // k 2^-H for bt = blk, k 2^(Gs[bt] - G + mu[bt]) for bt > blk.  Chain (fp16, in
+            // place of the raw tiles): Q_hat*Gamma, K_hat*Gamma and Kbar = k_hat 2^(G_C - G).
             {
-                const int fb = fac_base(blk);
+                const int fb = pool_fac_base(blk);
                 const float4 *fs4 = reinterpret_cast<const float4 *>(&sm.fac[fb][c0]);
                 const float4 *fc4 = reinterpret_cast<const float4 *>(&sm.fac[fb + 1][c0]);
                 const float4 fsa = fs4[0], fsb = fs4[1], fca = fc4[0], fcb = fc4[1];
@@ -413,9 +573,17 @@ __device__ __forceinline__ void pool_front(const TmaMaps &maps, const Params &p,
                     sts128(sbase + rq_off + off, wq[0], wq[1], wq[2], wq[3]);
                     sts128(sbase + rk_off + off, wk[0], wk[1], wk[2], wk[3]);
                     sts128(sbase + rg_off + off, wb[0], wb[1], wb[2], wb[3]);
+                    if (UB && blk < 3) {   // 2^(mu - H) -> 2^(Gs[blk+1] - G), at most 1 (before the variants)
+                        const float4 *m4 = reinterpret_cast<const float4 *>(&sm.fac[fb + 2][c0]);
+                        const float4 ma = m4[0], mb = m4[1];
+                        kn[0] = mul2(kn[0], make_float2(ma.x, ma.y));
+                        kn[1] = mul2(kn[1], make_float2(ma.z, ma.w));
+                        kn[2] = mul2(kn[2], make_float2(mb.x, mb.y));
+                        kn[3] = mul2(kn[3], make_float2(mb.z, mb.w));
+                    }
 #pragma unroll 1
                     for (int bt = blk + 1; bt < 4; ++bt) {
-                        const float4 *d4 = reinterpret_cast<const float4 *>(&sm.fac[fb + 1 + bt - blk][c0]);
+                        const float4 *d4 = reinterpret_cast<const float4 *>(&sm.fac[fb + 2 + bt - blk][c0]);
                         const float4 da = d4[0], db = d4[1];
                         const float2 v0 = mul2(kn[0], make_float2(da.x, da.y)), v1 = mul2(kn[1], make_float2(da.z, da.w));
                         const float2 v2 = mul2(kn[2], make_float2(db.x, db.y)), v3 = mul2(kn[3], make_float2(db.z, db.w));
@@ -448,9 +616,15 @@ __device__ __forceinline__ void pool_front(const TmaMaps &maps, const Params &p,
         // the gate parameters of task t into slot ps (read by the prologue after the
         // first barrier of that task)
         auto stage_gate = [&](const TaskIt &t, int ps) {
-            const float a2 = -__expf(p.A_log[t.h]) * kLog2e;
-            for (int cch = htid; cch < DK; cch += NH) sm.gb[ps][cch] = a2 * p.dt_bias[t.h * DK + cch];
-            if (htid == 0) sm.ga[ps] = a2;
+            if constexpr (UB) {   // softplus argument bias (log2 units) and the rate -exp(A_log)
+                const float a = -__expf(p.A_log[t.h]);
+                for (int cch = htid; cch < DK; cch += NH) sm.gb[ps][cch] = kLog2e * p.dt_bias[t.h * DK + cch];
+                if (htid == 0) sm.ga[ps] = a;
+            } else {
+                const float a2 = -__expf(p.A_log[t.h]) * kLog2e;
+                for (int cch = htid; cch < DK; cch += NH) sm.gb[ps][cch] = a2 * p.dt_bias[t.h * DK + cch];
+                if (htid == 0) sm.ga[ps] = a2;
+            }
         };
         float nb = 0.f;   // logit of token htid, loaded one task ahead
         if (it.valid()) {
@@ -810,6 +984,7 @@ __device__ __forceinline__ void pool_front(const TmaMaps &maps, const Params &p,
 // its fp16 operand copy, decay by the next Gamma_C, initial and final state) and the
 // conversion of the next V to fp16, 8-11 the U and -W^T readouts, 12 the loader (ring
 // packets, V), 13 the MMA issuer, 14-15 the O readout (token rows, 16-byte stores).
+template <bool VL>
 __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p, const PoolArgs &a,
                                            unsigned char *smem, ChainSmall &cs, uint32_t tmem, int c) {
     const uint32_t sbase = smem_u32(smem);
@@ -818,8 +993,8 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
     const uint32_t D_S = tmem, D_W = tmem + 128, D_U0 = tmem + 192, D_O = tmem + 320;
     const int nchunks = a.nchunks;
     const int64_t units = p.n_seqs * p.H;
-    const int64_t nunits = (units - c + a.nc - 1) / a.nc;
-    const int64_t npk = nunits * nchunks;   // this chain's packets
+    const int64_t nunits = VL ? 0 : (units - c + a.nc - 1) / a.nc;
+    const int64_t npk = VL ? (int64_t)a.chain_len[c] : nunits * nchunks;   // this chain's packets
     auto pk_unit = [&](int64_t j) { return (int64_t)c + (j / nchunks) * a.nc; };
     auto pk_row = [&](int64_t j) {   // first token row of packet j in the [B*T] token rows
         return (pk_unit(j) / p.H) * p.T + (j % nchunks) * (int64_t)C;
@@ -1003,7 +1178,9 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
     if (warp >= 14) {
         // ------------------------------------------------ O readout: token rows (TMEM lanes 64-127)
         const int t = (quarter - 2) * 32 + lane;   // token of the chunk
-        for (int64_t j = 0; j < npk; ++j) {
+        PkWalkV ow;   // varlen: this packet's unit
+        if (VL) ow.start(p, a, c);
+        for (int64_t j = 0; j < npk; ++j, VL ? ow.next(p, a) : void()) {
             if (!wait(&cs.o_done[j & 1], par2(j))) return;
             tc_fence_after();
             uint32_t pk0[32];   // columns 0-63 as bf16 pairs
@@ -1021,10 +1198,24 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
             tmem_ld_wait();
             tc_fence_before();
             warp_arrive(&cs.o_free);
-            const int rem = (int)(p.T - (j % nchunks) * (int64_t)C);
-            if (p.out && t < (rem < C ? rem : C)) {
-                const int64_t u = pk_unit(j);
-                uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((pk_row(j) + t) * p.H + u % p.H) * DK);
+            int rows;
+            if constexpr (VL) {
+                rows = ow.rows();
+            } else {
+                const int rem = (int)(p.T - (j % nchunks) * (int64_t)C);
+                rows = rem < C ? rem : C;
+            }
+            if (p.out && t < rows) {
+                int64_t orow, oh;
+                if constexpr (VL) {
+                    orow = ow.row();
+                    oh = ow.u.h;
+                } else {
+                    const int64_t u = pk_unit(j);
+                    orow = pk_row(j);
+                    oh = u % p.H;
+                }
+                uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((orow + t) * p.H + oh) * DK);
 #pragma unroll
                 for (int q8 = 0; q8 < 8; ++q8)
                     dst[q8] = make_uint4(pk0[4 * q8], pk0[4 * q8 + 1], pk0[4 * q8 + 2], pk0[4 * q8 + 3]);
@@ -1068,10 +1259,20 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
         // V of packet jv into V buffer jv & 1 (warp 8, lane 0), free once G2u of packet
         // jv - 2 is done
         int64_t v_issued = 0;
+        PkWalkV vw;   // varlen: the unit of the next V to load (issued in packet order)
+        if (VL && warp == 8 && lane == 0) vw.start(p, a, c);
         auto issue_v = [&](int64_t jv) {
             const int sv = (int)(jv & 1);
+            int row, h;
+            if (VL) {
+                row = (int)vw.row();
+                h = vw.u.h;
+                vw.next(p, a);
+            } else {
+                row = (int)pk_row(jv);
+                h = (int)(pk_unit(jv) % p.H);
+            }
             if (p.v) {
-                const int row = (int)pk_row(jv), h = (int)(pk_unit(jv) % p.H);
                 unsigned char *vb = smem + C_V + sv * 16384;
                 mbar_arrive_expect_tx(&cs.vfull[sv], 16384);
                 tma_load_3d(vb, &maps.v, &cs.vfull[sv], 0, h, row);
@@ -1094,6 +1295,13 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
             return true;
         };
         const bool vlead = warp == 8 && lane == 0;
+        if (!p.v) {
+            // values of zero (a state-only run): both V buffers hold zeros for the whole
+            // run; each thread clears the pieces it converts later (same index pattern)
+            for (int sv = 0; sv < 2; ++sv)
+                for (int k16 = tid - 256; k16 < 1024; k16 += 128)
+                    *reinterpret_cast<uint4 *>(smem + C_V + sv * 16384 + k16 * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
         [&]() {
         if (vlead) {
             if (npk > 0) issue_v(0);
@@ -1138,11 +1346,35 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
     };
     bool rbad = false;   // a state value beyond the fp16 range of its operand copy
     int64_t j = 0;
-    for (int64_t w = 0; w < nunits; ++w) {
-        const int64_t unit = (int64_t)c + w * a.nc;
-        const int64_t h = unit % p.H, n = unit / p.H;
-        const size_t state_base = (size_t)(n * p.H + h) * DK * DK;
-        for (int m = 0; m < nchunks; ++m, ++j) {
+    const int64_t U = VL ? (int64_t)a.counts[1] : 0;
+    for (int64_t w = 0;; ++w) {
+        // the chain's unit of round w: its state offset and chunk count
+        size_t state_base;
+        int nch;
+        if constexpr (VL) {
+            const UnitV u = unit_v(p, a, c, w, U);
+            if (!u.valid) break;
+            if (u.nch == 0) {
+                // a sequence without tokens: its final state is its initial state
+                if (p.fin) {
+                    const int64_t n16 = (int64_t)DK * DK * (p.state_type == kStateBF16 ? 2 : 4) / 16;
+                    const int64_t b16 = u.sbase * (p.state_type == kStateBF16 ? 2 : 4) / 16;
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.fin) + b16;
+                    const uint4 *src = p.init ? reinterpret_cast<const uint4 *>(p.init) + b16 : nullptr;
+                    for (int64_t e = tid; e < n16; e += 256) dst[e] = src ? src[e] : make_uint4(0u, 0u, 0u, 0u);
+                }
+                continue;
+            }
+            state_base = (size_t)u.sbase;
+            nch = u.nch;
+        } else {
+            if (w >= nunits) break;
+            const int64_t unit = (int64_t)c + w * a.nc;
+            const int64_t h = unit % p.H, n = unit / p.H;
+            state_base = (size_t)(n * p.H + h) * DK * DK;
+            nch = nchunks;
+        }
+        for (int m = 0; m < nch; ++m, ++j) {
             const int sj = (int)(j & 1);
             float r[4][16];
             if (m == 0) {
@@ -1206,6 +1438,7 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
     flag_range(p, rbad);
 }
 
+template <bool VL, bool UB>
 __global__ void __launch_bounds__(NT, 1)
 kda_pool_kernel(const __grid_constant__ TmaMaps maps, Params p, PoolArgs a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -1261,13 +1494,115 @@ kda_pool_kernel(const __grid_constant__ TmaMaps maps, Params p, PoolArgs a) {
     const uint32_t tmem = *tmem_base;
 
     if (chain)
-        pool_chain(maps, p, a, smem, cs, tmem, cta);
+        pool_chain<VL>(maps, p, a, smem, cs, tmem, cta);
     else
-        pool_front(maps, p, a, smem, fs, tmem, cta - a.nc);
+        pool_front<VL, UB>(maps, p, a, smem, fs, tmem, cta - a.nc);
 
     tc_fence_before();
     __syncthreads();
     if (threadIdx.x < 32) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------- varlen plan
+// One CTA.  (1) The sequences the pool takes (all of them, or in a mixed-length call
+// those of more than kShortMaxT tokens), sorted by chunk count, longest first, ties by
+// index (bitonic sort of 64-bit keys in shared memory).  (2) Their (sequence, head)
+// units in that order, dealt to the chains in snake order; each chain's packet count.
+// (3) The chains ranked by packet count; off[j] = sum over chains of min(count, j), the
+// global index of the first packet of step j.  (4) The list of packets in global order:
+// packet j of the chain of rank r has index off[j] + r.
+constexpr int kPlanThreads = 1024;
+constexpr int kMaxChains = 512;
+
+__global__ void __launch_bounds__(kPlanThreads)
+pool_plan_kernel(Params p, PoolArgs a, int *order, int *chain_len, int *counts, int *off, int4 *plist,
+                 int npad) {
+    __shared__ unsigned long long key[kPoolMaxSeqs];
+    __shared__ int cl[kMaxChains], rk[kMaxChains];
+    __shared__ int s_n, s_lmax;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int N = (int)p.n_seqs, nc = a.nc;
+    const int64_t H = p.H;
+    if (tid == 0) {
+        s_n = 0;
+        s_lmax = 0;
+    }
+    for (int n = tid; n < npad; n += kPlanThreads) {
+        unsigned long long k = 0;   // zero: not the pool's (sorts last)
+        if (n < N) {
+            const int64_t len = p.cu_seqlens[n + 1] - p.cu_seqlens[n];
+            if (!(p.mixed && len <= kShortMaxT))
+                k = ((unsigned long long)((len + C - 1) / C) << 32) | (unsigned long long)(0xffffffffu - (unsigned)n);
+        }
+        key[n] = k;
+    }
+    __syncthreads();
+    for (int size = 2; size <= npad; size <<= 1)
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int t = tid; t < npad / 2; t += kPlanThreads) {
+                const int lo = 2 * t - (t & (stride - 1)), hi = lo + stride;
+                const unsigned long long x = key[lo], y = key[hi];
+                if ((x < y) == ((lo & size) == 0)) {   // descending where (lo & size) == 0
+                    key[lo] = y;
+                    key[hi] = x;
+                }
+            }
+            __syncthreads();
+        }
+    for (int sq = tid; sq < npad; sq += kPlanThreads)
+        if (key[sq] != 0 && (sq + 1 == npad || key[sq + 1] == 0)) s_n = sq + 1;
+    for (int sq = tid; sq < N; sq += kPlanThreads)
+        if (key[sq] != 0) order[sq] = (int)(0xffffffffu - (unsigned)(key[sq] & 0xffffffffu));
+    __syncthreads();
+    const int64_t U = (int64_t)s_n * H;
+    if (tid < nc) {
+        int64_t tot = 0;
+        for (int64_t w = 0;; ++w) {
+            const int64_t k = w * nc + ((w & 1) ? (nc - 1 - tid) : tid);
+            if (k >= U) break;
+            tot += (int64_t)(key[k / H] >> 32);
+        }
+        cl[tid] = (int)tot;
+        chain_len[tid] = (int)tot;
+        atomicMax(&s_lmax, (int)tot);
+    }
+    __syncthreads();
+    if (tid < nc) {
+        int r = 0;
+        for (int d = 0; d < nc; ++d) r += cl[d] > cl[tid] || (cl[d] == cl[tid] && d < tid);
+        rk[tid] = r;
+    }
+    const int lmax = s_lmax;
+    for (int j = tid; j <= lmax; j += kPlanThreads) {
+        int64_t o = 0;
+        for (int d = 0; d < nc; ++d) o += cl[d] < j ? cl[d] : j;
+        off[j] = (int)o;
+    }
+    if (tid == 0) {
+        int64_t tot = 0;
+        for (int d = 0; d < nc; ++d) tot += cl[d];
+        counts[0] = (int)tot;
+        counts[1] = (int)U;
+    }
+    __syncthreads();
+    for (int c = warp; c < nc; c += kPlanThreads / 32) {
+        int64_t j = 0;
+        for (int64_t w = 0;; ++w) {
+            const int64_t k = w * nc + ((w & 1) ? (nc - 1 - c) : c);
+            if (k >= U) break;
+            const int64_t sq = k / H;
+            const int h = (int)(k - sq * H);
+            const int n = (int)(0xffffffffu - (unsigned)(key[sq] & 0xffffffffu));
+            const int64_t t0 = p.cu_seqlens[n];
+            const int len = (int)(p.cu_seqlens[n + 1] - t0);
+            const int nch = (len + C - 1) / C;
+            for (int m = lane; m < nch; m += 32) {
+                const int rows = len - m * C < C ? len - m * C : C;
+                plist[off[j + m] + rk[c]] = make_int4(c, (int)(j + m), (int)(t0 + (int64_t)m * C), (h << 8) | rows);
+            }
+            j += nch;
+        }
+    }
 }
 
 }  // namespace
@@ -1281,9 +1616,48 @@ int64_t pool_chains(int64_t units, int sms) {
     return (units + waves - 1) / waves;
 }
 
-size_t pool_scratch_bytes(int64_t units, int sms) {
+// Workspace layout: the ring (nc x D packet slots), its flags (2 D words per chain), and
+// for varlen calls the plan: order [N], chain_len [nc], counts [4], off [P + 1] and the
+// packet list [P] (16-byte entries), P = H (ceil(T / 64) + N) bounding the packet count.
+namespace {
+struct PoolLayout {
+    size_t flags, order, chain_len, counts, off, plist, total;
+};
+size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
+PoolLayout pool_layout(int64_t N, int64_t H, int64_t T, bool varlen, int sms) {
+    const int64_t units = N * H;
     const int64_t nc = pool_chains(units, sms);
-    return (size_t)nc * ring_depth(nc, sms - nc) * (kChunkBytes + 2 * sizeof(unsigned long long));
+    const int64_t D = ring_depth(nc, sms - nc);
+    PoolLayout l;
+    l.flags = (size_t)nc * D * kChunkBytes;
+    size_t x = l.flags + (size_t)nc * 2 * D * sizeof(unsigned long long);
+    l.order = l.chain_len = l.counts = l.off = l.plist = 0;
+    if (varlen) {
+        const int64_t P = H * ((T + C - 1) / C + N);
+        l.order = up256(x);
+        l.chain_len = up256(l.order + 4 * (size_t)N);
+        l.counts = up256(l.chain_len + 4 * (size_t)nc);
+        l.off = up256(l.counts + 16);
+        l.plist = up256(l.off + 4 * (size_t)(P + 1));
+        x = l.plist + 16 * (size_t)P;
+    }
+    l.total = x;
+    return l;
+}
+}  // namespace
+
+size_t pool_scratch_bytes(const Params &p, int sms) {
+    return pool_layout(p.n_seqs, p.H, p.T, p.cu_seqlens != nullptr, sms).total;
+}
+size_t pool_scratch_bytes_varlen(int64_t N, int64_t H, int64_t T, int sms) {
+    return pool_layout(N, H, T, true, sms).total;
+}
+
+bool pool_takes(const Params &p, int sms) {
+    if (!p.cu_seqlens) return true;
+    const int64_t P = p.H * ((p.T + C - 1) / C + p.n_seqs);
+    return p.n_seqs <= kPoolMaxSeqs && pool_chains(p.n_seqs * p.H, sms) <= kMaxChains && P < (int64_t(1) << 30) &&
+           p.T < (int64_t(1) << 30) && p.H < (int64_t(1) << 22);
 }
 
 cudaError_t launch_pool(const Params &p, int sms, cudaStream_t stream) {
@@ -1291,16 +1665,25 @@ cudaError_t launch_pool(const Params &p, int sms, cudaStream_t stream) {
     if (units == 0) return cudaSuccess;
     const int64_t nc = pool_chains(units, sms);
     const int64_t nf = sms - nc;
-    const int64_t nchunks = (p.T + C - 1) / C;
-    if (nf < 1 || nchunks < 1) return cudaErrorInvalidValue;
-    PoolArgs a;
+    const bool vl = p.cu_seqlens != nullptr;
+    const int64_t nchunks = vl ? 0 : (p.T + C - 1) / C;
+    if (nf < 1 || (!vl && nchunks < 1)) return cudaErrorInvalidValue;
+    if (vl && !pool_takes(p, sms)) return cudaErrorInvalidValue;
+    const PoolLayout l = pool_layout(p.n_seqs, p.H, p.T, vl, sms);
+    PoolArgs a = {};
     a.nc = (int)nc;
     a.nf = (int)nf;
     a.nchunks = (int)nchunks;
-    a.waves = (int)((units + nc - 1) / nc);
+    a.waves = vl ? 0 : (int)((units + nc - 1) / nc);
     a.ring = p.ws;
     a.depth = (int)ring_depth(nc, nf);
-    a.flags = reinterpret_cast<unsigned long long *>(p.ws + (size_t)nc * a.depth * kChunkBytes);
+    a.flags = reinterpret_cast<unsigned long long *>(p.ws + l.flags);
+    if (vl) {
+        a.order = reinterpret_cast<const int *>(p.ws + l.order);
+        a.chain_len = reinterpret_cast<const int *>(p.ws + l.chain_len);
+        a.counts = reinterpret_cast<const int *>(p.ws + l.counts);
+        a.plist = reinterpret_cast<const int4 *>(p.ws + l.plist);
+    }
     TmaMaps maps;
     const int64_t rows = p.B * p.T;
     if (!encode_map(&maps.q, p.q, rows, p.H) || !encode_map(&maps.k, p.k, rows, p.H) ||
@@ -1308,9 +1691,27 @@ cudaError_t launch_pool(const Params &p, int sms, cudaStream_t stream) {
         return cudaErrorInvalidValue;
     static std::atomic<bool> attr_done[kMaxDevices];
     cudaError_t e = once_per_device(attr_done, [](int) {
-        return cudaFuncSetAttribute(kda_pool_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        const int sb = (int)SMEM_BYTES;
+        cudaError_t r = cudaFuncSetAttribute(kda_pool_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sb);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(kda_pool_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sb);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(kda_pool_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sb);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(kda_pool_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sb);
+        return r;
     });
     if (e != cudaSuccess) return e;
+    if (vl) {
+        int npad = 1;
+        while (npad < p.n_seqs) npad <<= 1;
+        pool_plan_kernel<<<1, kPlanThreads, 0, stream>>>(
+            p, a, reinterpret_cast<int *>(p.ws + l.order), reinterpret_cast<int *>(p.ws + l.chain_len),
+            reinterpret_cast<int *>(p.ws + l.counts), reinterpret_cast<int *>(p.ws + l.off),
+            reinterpret_cast<int4 *>(p.ws + l.plist), npad < 2 ? 2 : npad);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(nc + nf));
     cfg.blockDim = dim3(NT);
@@ -1324,7 +1725,12 @@ cudaError_t launch_pool(const Params &p, int sms, cudaStream_t stream) {
     // the flags of this call start at zero (no packet index + 1 is zero)
     e = cudaMemsetAsync(a.flags, 0, (size_t)nc * 2 * a.depth * sizeof(unsigned long long), stream);
     if (e != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, kda_pool_kernel, maps, p, a);
+    if (p.unbounded)
+        e = vl ? cudaLaunchKernelEx(&cfg, kda_pool_kernel<true, true>, maps, p, a)
+               : cudaLaunchKernelEx(&cfg, kda_pool_kernel<false, true>, maps, p, a);
+    else
+        e = vl ? cudaLaunchKernelEx(&cfg, kda_pool_kernel<true, false>, maps, p, a)
+               : cudaLaunchKernelEx(&cfg, kda_pool_kernel<false, false>, maps, p, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -11,10 +11,10 @@
 //   3. a scan over the segments: S_in(0) = S_0, S_in(s) = P_{s-1} S_in(s-1) + R_{s-1};
 //   4. every segment from S_in(s), writing the outputs (and, for the last segment,
 //      the final state).
-// Steps 1, 2 and 4 are the chunked cluster kernel over the segments as independent
-// packed sequences (segment boundaries as cu_seqlens); 1 and 2 write no outputs.
-// With P segments per sequence each of those launches has P times the parallelism
-// of the plain call, at three times its work.
+// Steps 1, 2 and 4 are the persistent pool kernel over the segments as independent
+// packed sequences (segment boundaries as cu_seqlens, so each run plans its units
+// first); 1 and 2 write no outputs.  With P segments per sequence each of those runs
+// has P times the parallelism of the plain call, at three times its work.
 #include <cuda_bf16.h>
 
 #include "kda_internal.h"
@@ -134,7 +134,7 @@ int64_t seg_len(int64_t T, int64_t P) {
 
 int64_t tsplit_segments(const Params &p, int sms) {
     if (p.cu_seqlens || p.B <= 0 || p.T < kTsplitMinSeg * 4) return 0;
-    const int64_t units = p.n_seqs * p.H, slots = sms / 2;   // clusters in flight
+    const int64_t units = p.n_seqs * p.H, slots = sms / 2;   // pool chains in flight
     if (units <= 0) return 0;
     int64_t P = slots / units;
     if (P > p.T / kTsplitMinSeg) P = p.T / kTsplitMinSeg;
@@ -142,12 +142,13 @@ int64_t tsplit_segments(const Params &p, int sms) {
     return P >= 4 ? P : 0;
 }
 
-size_t tsplit_scratch_bytes(int64_t N, int64_t H, int64_t P) {
+size_t tsplit_scratch_bytes(const Params &p, int64_t P, int sms) {
+    const int64_t N = p.n_seqs, H = p.H;
     const size_t cu = ((size_t)(N * P + 1) * 8 + 255) / 256 * 256;
-    return cu + 4 * (size_t)(N * P * H) * kStateBytes + (size_t)(N * P * H) * kWsBytesPerUnit;
+    return cu + 4 * (size_t)(N * P * H) * kStateBytes + pool_scratch_bytes_varlen(N * P, H, N * p.T, sms);
 }
 
-cudaError_t launch_tsplit(const Params &p, int64_t P, unsigned char *scratch, cudaStream_t stream) {
+cudaError_t launch_tsplit(const Params &p, int64_t P, int sms, unsigned char *scratch, cudaStream_t stream) {
     const int64_t N = p.n_seqs, H = p.H, T = p.T, Ls = seg_len(T, P), S = N * P;
     const size_t cu_bytes = ((size_t)(S + 1) * 8 + 255) / 256 * 256, sb = (size_t)(S * H) * kStateBytes;
     int64_t *cu = reinterpret_cast<int64_t *>(scratch);
@@ -168,17 +169,18 @@ cudaError_t launch_tsplit(const Params &p, int64_t P, unsigned char *scratch, cu
     q.B = 1;
     q.T = N * T;
     q.state_type = kStateFP32;
+    q.mixed = 0;   // every segment on the pool
     q.ws = ws;
     // 1. R_s from S = 0 (segment 0 from the call's initial state); no outputs
     q.init = sin;
     q.fin = R;
     q.out = nullptr;
-    if ((e = launch_cluster(q, stream)) != cudaSuccess) return e;
+    if ((e = launch_pool(q, sms, stream)) != cudaSuccess) return e;
     // 2. the transitions P_s: zero values from S = I; no outputs
     q.v = nullptr;
     q.init = fin3;
     q.fin = Pst;
-    if ((e = launch_cluster(q, stream)) != cudaSuccess) return e;
+    if ((e = launch_pool(q, sms, stream)) != cudaSuccess) return e;
     // 3. the scan
     const int scan_smem = (int)((kState + (int64_t)kScanRows * kZs) * 4);
     static std::atomic<bool> attr_done[kMaxDevices];
@@ -193,7 +195,7 @@ cudaError_t launch_tsplit(const Params &p, int64_t P, unsigned char *scratch, cu
     q.init = sin;
     q.fin = fin3;
     q.out = p.out;
-    if ((e = launch_cluster(q, stream)) != cudaSuccess) return e;
+    if ((e = launch_pool(q, sms, stream)) != cudaSuccess) return e;
     if (p.fin) {
         seg_final_kernel<<<dim3((unsigned)(N * H), 16), 256, 0, stream>>>(p.fin, p.state_type, fin3, P, H);
         e = cudaGetLastError();

@@ -82,18 +82,23 @@ def test_max_over_ranks_without_group_is_identity():
 def test_kernel_of_follows_the_packed_token_count():
     # the kernel label and stored-traffic lookup follow the dispatch of kda_fwd:
     # one row -> token recurrence, up to 64 -> 16-row blocks, more -> the pool kernel
-    # (fixed length) or the cluster kernel (varlen)
+    # (varlen batches of more than 4096 sequences: the cluster kernel)
     import bench
     from gated_delta_rule_52_gb300 import workloads as W
     assert bench.kernel_of(1) == "decode"
     assert bench.kernel_of(2) == "short" and bench.kernel_of(64) == "short"
-    assert bench.kernel_of(65) == "pool" and bench.kernel_of(65, varlen=True) == "cluster"
+    assert bench.kernel_of(65) == "pool" and bench.kernel_of(65, varlen=True) == "pool"
+    assert bench.kernel_of(10**5, varlen=True, n_seqs=5000) == "cluster"
     d = W.make_inputs(W.get("varlen_ragged", H=1, seqlens=(40, 30)))
-    assert bench.kernel_for(d) == "cluster"   # the ragged workload's T is the packed total
+    assert bench.kernel_for(d) == "pool"   # the ragged workload's T is the packed total
+    dl = W.make_inputs(W.get("varlen_ragged", H=1, seqlens=(600, 300)))
+    assert not bench.mixed_dispatch(dl) and bench.launches_per_call(dl, 152) == 2   # the plan and the pool
     assert bench.kernel_for(W.make_inputs(W.get("tiny"))) == "pool"
-    # few units on a long fixed-length call: the sequence-parallel path (cluster runs)
+    assert bench.launches_per_call(W.make_inputs(W.get("tiny")), 152) == 1
+    # few units on a long fixed-length call: the sequence-parallel path (three runs of
+    # plan + pool, the segment bounds and states, the scan, the final state)
     d8 = W.make_inputs(W.get("tiny", T=8192, H=1))
-    assert bench.kernel_for(d8) == "cluster" and bench.launches_per_call(d8, 152) > 1
+    assert bench.kernel_for(d8) == "pool" and bench.launches_per_call(d8, 152) == 10
     for k in bench.KERNEL_SOURCES:
         assert len(bench.kernel_source_hash(k)) == 16 and k in bench.KERNEL_NAMES
 
@@ -114,18 +119,24 @@ def test_mixed_dispatch_rule_mirror():
     # short-step kernel beside the cluster kernel (kda_api.cu), as bench.py mirrors it
     import bench
     from gated_delta_rule_52_gb300 import workloads as W
-    assert bench.mixed_dispatch(W.make_inputs(W.get("varlen_ragged", H=1, seqlens=(40, 30, 20))))
+    dm = W.make_inputs(W.get("varlen_ragged", H=1, seqlens=(40, 30, 20)))
+    assert bench.mixed_dispatch(dm) and bench.launches_per_call(dm, 152) == 3   # short, plan, pool
     assert not bench.mixed_dispatch(W.make_inputs(W.get("varlen_ragged", H=1, seqlens=(40, 20))))   # 60 rows
     assert not bench.mixed_dispatch(W.make_inputs(W.get("varlen_ragged", H=1, seqlens=(600, 20))))  # avg 310
     assert not bench.mixed_dispatch(W.make_inputs(W.get("tiny")))                                   # fixed length
 
 
-def test_gate_without_lower_bound_runs_the_recurrence():
+def test_gate_without_lower_bound_dispatch():
+    # the gate without a lower bound: the pool kernel above 64 rows (every sequence on it,
+    # no mixed split), the token recurrence for short calls and huge varlen batches
     d = W.make_inputs(W.get("varlen_ragged", H=1, seqlens=(40, 30, 20), lower_bound=None))
     assert d["lower_bound"] is None
-    assert bench.kernel_for(d) == "recur" and not bench.mixed_dispatch(d)
-    assert bench.launches_per_call(d, 152) == 1
-    assert bench.kernel_of(8192, unbounded=True) == "recur" and bench.kernel_of(8192) == "pool"
+    assert bench.kernel_for(d) == "pool" and not bench.mixed_dispatch(d)
+    assert bench.launches_per_call(d, 152) == 2
+    ds = W.make_inputs(W.get("varlen_ragged", H=1, seqlens=(40, 20), lower_bound=None))
+    assert bench.kernel_for(ds) == "recur" and bench.launches_per_call(ds, 152) == 1
+    assert bench.kernel_of(8192, unbounded=True) == "pool" and bench.kernel_of(8192) == "pool"
+    assert bench.kernel_of(10**6, unbounded=True, varlen=True, n_seqs=5000) == "recur"
     assert "recur" in bench.KERNEL_NAMES and len(bench.kernel_source_hash("recur")) == 16
 
 

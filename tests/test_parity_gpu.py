@@ -172,20 +172,40 @@ def test_many_short_sequences_longest_first_order():
     print("many-seqs", pu.check(d, out, fin, ref_out, ref_fin, label="many-seqs"))
 
 
+def test_more_sequences_than_the_pool_plans():
+    # Varlen calls of more than 4096 sequences skip the pool's one-CTA plan and run one
+    # two-CTA cluster per (sequence, head) instead; zero-length sequences in between
+    r = np.random.default_rng(11)
+    lens = [int(x) for x in r.integers(65, 90, 4100)]
+    lens[3], lens[4000] = 0, 0
+    d = W.make_inputs(W.get("varlen_ragged", H=1, seqlens=tuple(lens), seed=91))
+    assert d["N"] > 4096
+    out, fin = pu.run_gpu(d)
+    ref_out, ref_fin = pu.run_oracle(d)
+    print("4100 seqs", pu.check(d, out, fin, ref_out, ref_fin, label="4100 sequences"))
+
+
 def test_caller_workspace_entry_point():
-    # kda_fwd_ws with a caller buffer full of garbage gives kda_fwd's result bit for bit
+    # kda_fwd_ws (the cluster kernel on a caller buffer) matches the oracle, and a buffer
+    # full of garbage gives the result of a zeroed one bit for bit
     d = W.make_inputs(W.get("varlen_ragged", H=3, seqlens=(65, 1, 130, 63, 200)))
     e = pu.to_device(d)
     ref_out, ref_fin = pu.run_gpu(d)
-    out = torch.empty_like(ref_out, device="cuda")
-    fin = torch.empty_like(ref_fin, device="cuda")
-    ws = torch.full((kda.workspace_bytes(d["N"], d["H"]),), 0xFF, dtype=torch.uint8, device="cuda")
-    kda.kda_fwd(e["q"], e["k"], e["v"], e["g"], e["beta"], d["scale"], out, e["A_log"],
-                e["dt_bias"], d["lower_bound"], initial_state=e["initial_state"], final_state=fin,
-                cu_seqlens=e["cu_seqlens"], workspace=ws)
-    torch.cuda.synchronize()
-    assert kda.get_device_status() == kda.KDA_OK
-    assert torch.equal(out.cpu(), ref_out) and torch.equal(fin.cpu(), ref_fin)
+    outs = []
+    for fill in (0x00, 0xFF):
+        out = torch.empty_like(ref_out, device="cuda")
+        fin = torch.empty_like(ref_fin, device="cuda")
+        ws = torch.full((kda.workspace_bytes(d["N"], d["H"]),), fill, dtype=torch.uint8, device="cuda")
+        kda.kda_fwd(e["q"], e["k"], e["v"], e["g"], e["beta"], d["scale"], out, e["A_log"],
+                    e["dt_bias"], d["lower_bound"], initial_state=e["initial_state"], final_state=fin,
+                    cu_seqlens=e["cu_seqlens"], workspace=ws)
+        torch.cuda.synchronize()
+        assert kda.get_device_status() == kda.KDA_OK
+        outs.append((out.cpu(), fin.cpu()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    o_ref, f_ref = pu.run_oracle(d)
+    pu.check(d, outs[1][0], outs[1][1], o_ref, f_ref, label="kda_fwd_ws")
+    pu.check(d, ref_out, ref_fin, o_ref, f_ref, label="kda_fwd")
     with pytest.raises(kda.KDAError) as ei:
         kda.kda_fwd(e["q"], e["k"], e["v"], e["g"], e["beta"], d["scale"], out, e["A_log"],
                     e["dt_bias"], d["lower_bound"], initial_state=e["initial_state"],
@@ -403,7 +423,8 @@ def test_cuda_graph_capture_replays_the_call(name, wl):
         assert torch.equal(out, ref_out2) and torch.equal(fin, ref_fin2)
 
 
-# ---- the gate without a lower bound (kda_fwd_unbounded, the token recurrence)
+# ---- the gate without a lower bound (kda_fwd_unbounded: the pool kernel's chunked form above
+# 64 rows, the token recurrence for short calls)
 
 @pytest.mark.parametrize("B,T,H,sd,init,g_std", [(2, 300, 3, "fp32", "normal", 1.0),
                                                  (1, 1, 4, "bf16", "normal", 1.0),
@@ -420,6 +441,27 @@ def test_unbounded_gate_all_elements(B, T, H, sd, init, g_std):
     out, fin = pu.run_gpu(d, want_final=sd is not None)
     ref_out, ref_fin = pu.run_oracle(d, want_final=sd is not None)
     print("unbounded", B, T, H, sd, init, pu.check(d, out, fin, ref_out, ref_fin, label=f"unbounded T={T}"))
+
+
+@pytest.mark.parametrize("case", ["all", "half", "varlen"])
+def test_unbounded_gate_extreme_decays(case):
+    # softplus(g + dt_bias) near 30 gives per-token decays of e^-30 to e^-480 (past e^-60
+    # wherever exp(A_log) > 2); the chunked form raises each token's log2 decay to -14
+    # (a factor 2^-14 where the exact one is smaller), so the parity bars still hold
+    w = W.get("tiny", B=2, T=300, H=3, state_dtype="fp32", initial_state="normal", lower_bound=None, seed=93)
+    if case == "varlen":
+        w = W.get("varlen_ragged", H=3, seqlens=(300, 1, 129, 0, 70), lower_bound=None, seed=94)
+    d = W.make_inputs(w)
+    g = d["g"].float()
+    if case == "half":
+        mask = torch.rand(g.shape[:-1], generator=torch.Generator().manual_seed(5)) < 0.5
+        g[mask] = 30.0
+    else:
+        g[:] = 30.0
+    d["g"] = g.to(torch.bfloat16)
+    out, fin = pu.run_gpu(d)
+    ref_out, ref_fin = pu.run_oracle(d)
+    print("unbounded extreme", case, pu.check(d, out, fin, ref_out, ref_fin, label=f"unbounded extreme {case}"))
 
 
 def test_unbounded_gate_varlen_with_empty_sequences():
