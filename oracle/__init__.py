@@ -1,13 +1,15 @@
-"""fp64 CPU oracle for the KDA forward pass.
+"""fp64 CPU oracle for the KDA forward pass and its gradient.
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg may import this package.  The CUDA library never
 imports, links or runs anything here, and this package imports nothing from the
 CUDA path.
 
-``kda_oracle.c`` holds the arithmetic (a token-by-token recurrence in fp64); this
-module compiles it with gcc and marshals numpy arrays to it.  See that file's
-header for what is computed and which readings of the FlashKDA pages it takes.
+``kda_oracle.c`` holds the arithmetic (a token-by-token recurrence in fp64) and
+``kda_oracle_bwd.c`` its gradient (reverse-mode differentiation of the same loop,
+written out); this module compiles them with gcc and marshals numpy arrays to them.
+See the files' headers for what is computed and which readings of the FlashKDA pages
+they take.
 """
 from __future__ import annotations
 
@@ -20,6 +22,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kda_oracle.c")
+_SRCS = [_SRC, os.path.join(_HERE, "kda_oracle_bwd.c")]
 _LIB = os.path.join(_HERE, "libkda_oracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -29,10 +32,10 @@ def build(force: bool = False) -> str:
     """Compile the C oracle into ``oracle/libkda_oracle.so`` (gcc, -O2, OpenMP,
     no fast-math).  Returns the library path."""
     with _lock:
-        if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < max(map(os.path.getmtime, _SRCS)):
             tmp = _LIB + f".tmp{os.getpid()}"
             cmd = ["gcc", "-O2", "-fno-fast-math", "-fopenmp", "-fPIC", "-shared",
-                   "-o", tmp, _SRC, "-lm"]
+                   "-o", tmp] + _SRCS + ["-lm"]
             subprocess.run(cmd, check=True)
             os.replace(tmp, _LIB)
     return _LIB
@@ -54,6 +57,10 @@ def _load():
                                                ip, ip, ip, ip]
         lib.kda_oracle_activations.restype = ctypes.c_int
         lib.kda_oracle_max_threads.restype = ctypes.c_int
+        lib.kda_oracle_bwd.argtypes = [ip, ip, ip, ip, ip, d, ip, ip, d, ip, ip, ip, ip, i64,
+                                       i64, i64, i64, i64, i64, ip, ip, ip, ip, ip, ip, ip, ip,
+                                       ctypes.c_int]
+        lib.kda_oracle_bwd.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -148,3 +155,29 @@ def activations(q, k, g, beta, A_log, dt_bias, lower_bound):
     if rc:
         raise ValueError("oracle rejected the sizes")
     return qn, kn, gk, bo
+
+
+def kda_bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout, initial_state=None,
+            dfinal=None, cu_seqlens=None, want_dinit=True, nthreads=0):
+    """Gradients of L = sum(dout * out) + sum(dfinal * final_state) with respect to the
+    inputs of ``kda_fwd`` (same layouts), fp64.  Returns a dict with dq, dk, dv, dg,
+    dbeta (of the beta logits), dA_log, ddt_bias and dinit (the initial state's gradient,
+    None unless ``want_dinit``)."""
+    lib = _load()
+    q, k, v, g, beta = _f64(q), _f64(k), _f64(v), _f64(g), _f64(beta)
+    A_log, dt_bias, init = _f64(A_log), _f64(dt_bias), _f64(initial_state)
+    dout, dfin, cu = _f64(dout), _f64(dfinal), _i64(cu_seqlens)
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    N = (cu.shape[0] - 1) if cu is not None else B
+    r = {"dq": np.zeros((B, T, H, K)), "dk": np.zeros((B, T, H, K)), "dv": np.zeros((B, T, H, V)),
+         "dg": np.zeros((B, T, H, K)), "dbeta": np.zeros((B, T, H)), "dA_log": np.zeros(H),
+         "ddt_bias": np.zeros((H, K)), "dinit": np.zeros((N, H, V, K)) if want_dinit else None}
+    rc = lib.kda_oracle_bwd(_p(q), _p(k), _p(v), _p(g), _p(beta), float(scale), _p(A_log),
+                            _p(dt_bias), _lb(lower_bound), _p(init), _p(dout), _p(dfin), _p(cu),
+                            N if cu is not None else 0, B, T, H, K, V, _p(r["dq"]), _p(r["dk"]),
+                            _p(r["dv"]), _p(r["dg"]), _p(r["dbeta"]), _p(r["dA_log"]),
+                            _p(r["ddt_bias"]), _p(r["dinit"]), int(nthreads))
+    if rc:
+        raise ValueError(f"oracle rejected the sizes or cu_seqlens (code {rc})")
+    return r
