@@ -285,6 +285,47 @@ kda_status kda_fwd_unbounded(const void *q, const void *k, const void *v, const 
     return st;
 }
 
+kda_status kda_bwd(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                   float scale, const float *A_log, const float *dt_bias, float lower_bound,
+                   int unbounded, const void *initial_state, int state_dtype, const void *dout,
+                   const float *dfinal, const int64_t *cu_seqlens, int64_t num_seqs, int64_t B,
+                   int64_t T, int64_t H, int64_t K, int64_t V, float *dq, float *dk, float *dv,
+                   float *dg, float *dbeta, float *dA_log, float *ddt_bias,
+                   float *dinitial_state, void *stream) {
+    kda::Params p{};   // every field zero until validate() fills it
+    // dout stands where out stands in kda_fwd (same shape); no final state is an input
+    kda_status st = validate(q, k, v, g, beta, scale, const_cast<void *>(dout), A_log, dt_bias,
+                             unbounded ? 0.f : lower_bound, initial_state, nullptr,
+                             initial_state ? state_dtype : KDA_STATE_NONE, cu_seqlens, num_seqs, B,
+                             T, H, K, V, p);
+    if (st != KDA_OK) return st;
+    const bool has_tokens = B > 0 && T > 0 && H > 0;
+    if (has_tokens && (!dq || !dk || !dv || !dg || !dbeta)) return KDA_ERR_NULL;
+    if (H > 0 && (!dA_log || !ddt_bias)) return KDA_ERR_NULL;
+    const void *ptrs[] = {dfinal, dq, dk, dv, dg, dbeta, dA_log, ddt_bias, dinitial_state};
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return KDA_ERR_ALIGN;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    int sms = 0;
+    if (kda::sm_count(sms) != cudaSuccess) return KDA_ERR_CUDA;
+    kda::BwdGrads gr{static_cast<const __nv_bfloat16 *>(dout), dfinal, dq, dk, dv, dg, dbeta,
+                     dA_log, ddt_bias, dinitial_state};
+    void *ws = nullptr;
+    const size_t bytes = kda::bwd_scratch_bytes(p, sms);
+    if (p.n_seqs * p.H > 0) {
+        int device = 0;
+        if (cudaGetDevice(&device) != cudaSuccess) return KDA_ERR_CUDA;
+        cudaMemPool_t pool = workspace_pool(device);
+        if (!pool) return KDA_ERR_CUDA;
+        if (cudaMallocFromPoolAsync(&ws, bytes, pool, cs) != cudaSuccess) return KDA_ERR_CUDA;
+    }
+    st = kda::launch_bwd(p, gr, unbounded ? 1 : 0, static_cast<unsigned char *>(ws), sms, cs) == cudaSuccess
+             ? KDA_OK
+             : KDA_ERR_CUDA;
+    if (ws && cudaFreeAsync(ws, cs) != cudaSuccess) st = KDA_ERR_CUDA;
+    return st;
+}
+
 kda_status kda_fwd_static(const void *q, const void *k, const void *v, const void *g,
                           const void *beta, float scale, void *out, const float *A_log,
                           const float *dt_bias, float lower_bound, const void *initial_state,

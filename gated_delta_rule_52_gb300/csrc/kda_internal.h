@@ -107,4 +107,15 @@ int64_t tsplit_segments(const Params &p, int sms);   // P, or 0: run the plain p
 size_t tsplit_scratch_bytes(const Params &p, int64_t P, int sms);
 cudaError_t launch_tsplit(const Params &p, int64_t P, int sms, unsigned char *scratch, cudaStream_t stream);
 
+// Backward (kda_bwd): the gradients of L = sum(dout * out) + sum(dfinal * final) with
+// respect to the forward's inputs, fp32, on p's forward inputs.
+struct BwdGrads {
+    const __nv_bfloat16 *dout;   // [B,T,H,V]
+    const float *dfinal;         // [N,H,V,K] or null
+    float *dq, *dk, *dv, *dg, *dbeta, *dA_log, *ddt_bias, *dinit;   // dinit may be null
+};
+size_t bwd_scratch_bytes(const Params &p, int sms);
+cudaError_t launch_bwd(const Params &p, const BwdGrads &g, int unbounded, unsigned char *ws, int sms,
+                       cudaStream_t stream);
+
 }  // namespace kda

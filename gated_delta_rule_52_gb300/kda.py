@@ -40,7 +40,8 @@ KDA_STATE_FP32 = 2
 
 # Every symbol include/kda.h declares.
 EXPORTED = ("kda_fwd", "kda_fwd_ws", "kda_fwd_unbounded", "kda_workspace_size",
-            "kda_status_string", "kda_get_device_status", "kda_version", "kda_fwd_static")
+            "kda_status_string", "kda_get_device_status", "kda_version", "kda_fwd_static",
+            "kda_bwd")
 
 # Workspace bytes per (sequence, head) of kda_fwd_ws (KDA_WORKSPACE_BYTES_PER_UNIT).
 WORKSPACE_BYTES_PER_UNIT = 99328
@@ -79,6 +80,9 @@ def lib() -> ctypes.CDLL:
             L.kda_fwd_static.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp, f, vp, vp, ci, vp,
                                          i64, i64, i64, i64, i64, i64, vp]
             L.kda_fwd_static.restype = ci
+            L.kda_bwd.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, f, ci, vp, ci, vp, vp, vp, i64,
+                                  i64, i64, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+            L.kda_bwd.restype = ci
             L.kda_workspace_size.argtypes = [i64, i64]
             L.kda_workspace_size.restype = ctypes.c_size_t
             L.kda_status_string.argtypes = [ci]
@@ -144,7 +148,7 @@ def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_s
     With ``workspace`` (a CUDA uint8 tensor of at least ``workspace_bytes(N, H)``
     bytes) the call goes to kda_fwd_ws and allocates nothing.  ``lower_bound=None``
     selects the gate without a lower bound (kda_fwd_unbounded: -exp(A_log) softplus(g +
-    dt_bias), the token recurrence)."""
+    dt_bias); the chunked form above 64 rows, each token's decay floored at 2^-14)."""
     if q.dim() != 4:
         raise ValueError("q must be [B, T, H, K]")
     B, T, H, K = q.shape
@@ -225,6 +229,56 @@ def kda_fwd_static(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound,
                               num_seqs, B, T, H, K, V, _stream_handle(stream))
     if st != KDA_OK:
         raise KDAError(st, status_string(st))
+
+
+def kda_bwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound, dout, initial_state=None,
+            dfinal=None, cu_seqlens=None, want_dinit=True, stream=None) -> dict:
+    """Gradients of L = sum(dout * out) + sum(dfinal * final_state) through libkda.so's
+    kda_bwd, with respect to the inputs of ``kda_fwd`` (``lower_bound=None``: the gate
+    without a lower bound).  ``dout`` bf16 [B,T,H,V]; ``dfinal`` fp32 [N,H,V,K] or None.
+    Returns a dict of new fp32 CUDA tensors: dq, dk, dv, dg, dbeta (of the beta logits),
+    dA_log, ddt_bias and dinit (None unless ``want_dinit``); asynchronous on ``stream``."""
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, H, K]")
+    B, T, H, K = q.shape
+    V = v.shape[-1] if v.dim() == 4 else -1
+    for name, t, shape in (("q", q, None), ("k", k, (B, T, H, K)), ("g", g, (B, T, H, K)),
+                           ("v", v, (B, T, H, V)), ("beta", beta, (B, T, H)),
+                           ("dout", dout, (B, T, H, V))):
+        _check_tensor(name, t, torch.bfloat16, shape)
+    _check_tensor("A_log", A_log, torch.float32, (H,))
+    _check_tensor("dt_bias", dt_bias, torch.float32, (H, K))
+    num_seqs = 0
+    if cu_seqlens is not None:
+        _check_tensor("cu_seqlens", cu_seqlens, torch.int64)
+        if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+            raise ValueError("cu_seqlens must be 1-D with at least 2 entries")
+        num_seqs = cu_seqlens.numel() - 1
+    N = num_seqs if cu_seqlens is not None else B
+    code = state_dtype_code(initial_state, None)
+    if initial_state is not None:
+        _check_tensor("initial_state", initial_state, initial_state.dtype, (N, H, V, K))
+    if dfinal is not None:
+        _check_tensor("dfinal", dfinal, torch.float32, (N, H, V, K))
+    dev = q.device
+    r = {"dq": torch.empty((B, T, H, K), dtype=torch.float32, device=dev),
+         "dk": torch.empty((B, T, H, K), dtype=torch.float32, device=dev),
+         "dv": torch.empty((B, T, H, V), dtype=torch.float32, device=dev),
+         "dg": torch.empty((B, T, H, K), dtype=torch.float32, device=dev),
+         "dbeta": torch.empty((B, T, H), dtype=torch.float32, device=dev),
+         "dA_log": torch.empty((H,), dtype=torch.float32, device=dev),
+         "ddt_bias": torch.empty((H, K), dtype=torch.float32, device=dev),
+         "dinit": torch.empty((N, H, V, K), dtype=torch.float32, device=dev) if want_dinit else None}
+    unb = lower_bound is None
+    st = lib().kda_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(A_log),
+                       _ptr(dt_bias), 0.0 if unb else float(lower_bound), 1 if unb else 0,
+                       _ptr(initial_state), code, _ptr(dout), _ptr(dfinal), _ptr(cu_seqlens),
+                       num_seqs, B, T, H, K, V, _ptr(r["dq"]), _ptr(r["dk"]), _ptr(r["dv"]),
+                       _ptr(r["dg"]), _ptr(r["dbeta"]), _ptr(r["dA_log"]), _ptr(r["ddt_bias"]),
+                       _ptr(r["dinit"]), _stream_handle(stream))
+    if st != KDA_OK:
+        raise KDAError(st, status_string(st))
+    return r
 
 
 def get_device_status(stream=None) -> int:

@@ -173,18 +173,56 @@ kda_status kda_fwd_ws(const void *q, const void *k, const void *v, const void *g
  *
  * a per-token log decay in (-inf, 0) with no floor.  Everything else (norms, beta,
  * the recurrence, scale, states, cu_seqlens) is as for kda_fwd, whose argument list
- * this is without lower_bound.  Without the floor the decay over a few tokens can
- * leave the fp32 exponent range, so this call applies the recurrence token by token
- * (exact for any decay, down to zero) instead of the chunked tensor-core form; it is
- * the slower path.  It allocates nothing and needs no workspace; asynchronous like
- * kda_fwd.  Same argument errors as kda_fwd (no lower_bound check), KDA_ERR_CUDA if
- * the launch failed.
+ * this is without lower_bound.
+ * Calls of more than 64 token rows (up to 4096 sequences when varlen) run the chunked
+ * tensor-core form of kda_fwd's persistent kernel, with each token's decay factor
+ * floored at 2^-14 (about 6.1e-5) per key channel: where the exact factor is smaller,
+ * the state that crosses that token keeps at most 6.1e-5 of itself instead of less.
+ * They take a workspace from the same pool as kda_fwd.  Calls of at most 64 rows and
+ * larger varlen batches apply the recurrence token by token, exact for any decay,
+ * without workspace.  Asynchronous like kda_fwd.  Same argument errors as kda_fwd
+ * (no lower_bound check), KDA_ERR_CUDA if the workspace or a launch failed.
  */
 kda_status kda_fwd_unbounded(const void *q, const void *k, const void *v, const void *g,
                              const void *beta, float scale, void *out, const float *A_log,
                              const float *dt_bias, const void *initial_state, void *final_state,
                              int state_dtype, const int64_t *cu_seqlens, int64_t num_seqs,
                              int64_t B, int64_t T, int64_t H, int64_t K, int64_t V, void *stream);
+
+/*
+ * kda_bwd — gradients of the KDA forward.  The pages ship the forward only (the
+ * FlashKDA Q&A, its notes on training); this is the derivative of kda_fwd (or, with
+ * `unbounded` nonzero, of kda_fwd_unbounded's exact recurrence) for the scalar loss
+ *
+ *   L = sum(dout * out) + sum(dfinal * final_state),
+ *
+ * taken in reverse token order on the fp32 recurrence (states recomputed from
+ * per-64-token checkpoints), then through the norms, the beta sigmoid and the gate.
+ *
+ * Inputs: q, k, v, g, beta, scale, A_log, dt_bias, lower_bound (ignored when
+ * `unbounded`), initial_state, state_dtype, cu_seqlens, num_seqs, B, T, H, K, V as for
+ * kda_fwd (final_state is not an input here); dout bf16 [B,T,H,V], the gradient of
+ * out; dfinal fp32 [N,H,V,K] or NULL (zero), the gradient of the final state.
+ * Outputs (fp32, contiguous, caller-allocated, every element written):
+ *   dq, dk, dg [B,T,H,K]   gradients of q, k and g
+ *   dv [B,T,H,V]           gradient of v
+ *   dbeta [B,T,H]          gradient of the beta logits
+ *   dA_log [H], ddt_bias [H,K]   gradients of A_log and dt_bias (summed over tokens)
+ *   dinitial_state [N,H,V,K]     gradient of the initial state, or NULL (not written)
+ * Rows of cu_seqlens-packed calls all belong to some sequence, so dq..dbeta are fully
+ * written.  Takes a workspace from kda_fwd's pool: the state at the start of every
+ * 64-token chunk (64 KB each) plus 4 MB per SM in use.  Asynchronous.  Returns the
+ * argument errors of kda_fwd, KDA_ERR_NULL for a missing gradient buffer,
+ * KDA_ERR_ALIGN for one not 16-byte aligned, KDA_ERR_CUDA if the workspace or a launch
+ * failed.
+ */
+kda_status kda_bwd(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                   float scale, const float *A_log, const float *dt_bias, float lower_bound,
+                   int unbounded, const void *initial_state, int state_dtype, const void *dout,
+                   const float *dfinal, const int64_t *cu_seqlens, int64_t num_seqs, int64_t B,
+                   int64_t T, int64_t H, int64_t K, int64_t V, float *dq, float *dk, float *dv,
+                   float *dg, float *dbeta, float *dA_log, float *ddt_bias,
+                   float *dinitial_state, void *stream);
 
 /* Most (sequence, head) units, N * H, that one kda_fwd_static call may hold. */
 #define KDA_STATIC_MAX_UNITS 128
