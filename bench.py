@@ -587,6 +587,112 @@ def check_world(args) -> str | None:
     return None
 
 
+# The backward per (token, head): q, k, v, g, dout read (5 x 256 B) and beta (2 B);
+# dq, dk, dv, dg written in fp32 (4 x 512 B) and dbeta (4 B).  Its arithmetic on the fp32
+# lanes: the forward recurrence twice (the checkpoint sweep and the per-chunk
+# recomputation, 3 K V multiply-adds each) and the reverse step (about 9 K V).
+BWD_BYTES_PER_TOKEN_HEAD = 5 * 256 + 2 + 4 * 512 + 4
+BWD_ALU_FLOPS_PER_TOKEN_HEAD = 2 * (3 + 3 + 9) * 128 * 128
+
+
+def run_ours_bwd(args):
+    """Times kda_bwd (the gradients of every forward input) on a workload: inputs and the
+    upstream gradient resident, fp32 outputs allocated per call by the binding."""
+    import torch
+    from gated_delta_rule_52_gb300 import build as kbuild
+    from gated_delta_rule_52_gb300 import kda
+    from gated_delta_rule_52_gb300 import workloads as W
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    kbuild.build_library()
+    kda.lib()
+    w = W.get(args.workload)
+    d_cpu = W.make_inputs(w)
+    e = {key: (val.to(dev) if torch.is_tensor(val) else val) for key, val in d_cpu.items()}
+    B, T, H, N = d_cpu["B"], d_cpu["T"], d_cpu["H"], d_cpu["N"]
+    gen = torch.Generator().manual_seed(1)
+    dout = torch.randn(d_cpu["v"].shape, generator=gen).to(torch.bfloat16).to(dev)
+    dfin = torch.randn((N, H, 128, 128), generator=gen).to(dev) if d_cpu["state_dtype"] else None
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        return kda.kda_bwd(e["q"], e["k"], e["v"], e["g"], e["beta"], e["scale"], e["A_log"],
+                           e["dt_bias"], e["lower_bound"], dout, initial_state=e["initial_state"],
+                           dfinal=dfin, cu_seqlens=e["cu_seqlens"], stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if kda.get_device_status(stream) != kda.KDA_OK:
+        raise RuntimeError("device reported an error during warm-up")
+    clocks = ClockSampler(local)
+    clocks.start()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if kda.get_device_status(stream) != kda.KDA_OK:
+        raise RuntimeError("device reported an error during the timed region")
+    ms = sum(s.elapsed_time(t) for s, t in zip(starts, ends)) / args.steps
+    th = B * T * H
+    sb = {"fp32": 4, "bf16": 2, None: 0}[d_cpu["state_dtype"]]
+    abytes = th * BWD_BYTES_PER_TOKEN_HEAD + N * H * 128 * 128 * (sb + (8 if sb else 4))
+    hbm, _, src = measured_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = (clk or {}).get("sm_max_mhz") or SM_MAX_MHZ
+    peak_alu = sms * 128 * 2 * mhz * 1e6 / 1e12
+    ach = abytes / (ms / 1e3) / 1e9
+    alu = th * BWD_ALU_FLOPS_PER_TOKEN_HEAD / (ms / 1e3) / 1e12
+    line = {"metric": "KDA bwd tokens/s on 1 GB300 (gradients of every forward input)",
+            "value": B * T / (ms / 1e3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "pass": "bwd",
+            "config": workload_config(w.name, d_cpu),
+            "l2": "a 256 MB flush write between timed steps", "timing": "CUDA events around each kda_bwd call",
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                         "traffic": None, "peak_source": src,
+                         "kernel": "kda_bwd_state_kernel + kda_bwd_act_kernel (the time of the whole call)",
+                         "algorithmic_bytes_per_launch": abytes,
+                         "alu_view": {"bound": "alu", "achieved": alu, "peak": peak_alu, "unit": "TFLOP/s",
+                                      "frac": alu / peak_alu,
+                                      "flops_per_launch": th * BWD_ALU_FLOPS_PER_TOKEN_HEAD}},
+            "clocks": clk, "gpu_launches": args.steps * 2,
+            "cpu_baseline": bwd_cpu_baseline(d_cpu, dout.cpu(), None if dfin is None else dfin.cpu())}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bwd_cpu_baseline(d, dout, dfin, tokens=512):
+    """The backward oracle, as it stands, on the host cores: the first `tokens` tokens of
+    as many heads as cores (fixed-length workloads; None for varlen ones)."""
+    import oracle
+    if d["cu_seqlens"] is not None:
+        return None
+    cores = cpu_cores()
+    nthreads = min(cores, oracle.max_threads()) or cores
+    T, nh, B = min(tokens, d["T"]), min(nthreads, d["H"]), d["B"]
+    sl = lambda x: x[:, :T, :nh].contiguous()
+    init = None if d["initial_state"] is None else d["initial_state"][:, :nh].contiguous()
+    t0 = time.perf_counter()
+    oracle.kda_bwd(sl(d["q"]), sl(d["k"]), sl(d["v"]), sl(d["g"]), sl(d["beta"]), d["scale"],
+                   d["A_log"][:nh].contiguous(), d["dt_bias"][:nh].contiguous(), d["lower_bound"],
+                   sl(dout), initial_state=init, dfinal=None if dfin is None else dfin[:, :nh].contiguous(),
+                   nthreads=nthreads)
+    secs = time.perf_counter() - t0
+    return {"value": (B * T * nh / d["H"]) / secs, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+            "sample": f"{B} x {T} tokens x {nh} of {d['H']} heads, fp64 backward, {secs:.1f} s; "
+                      "tokens/s = token-heads / H / s"}
+
+
 def main(argv=None):
     argv = sys.argv[1:] if argv is None else argv
     ap = argparse.ArgumentParser()
@@ -596,6 +702,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="prefill_8k")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
+                    help="bwd times kda_bwd (the gradients) instead of the forward")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -607,6 +715,8 @@ def main(argv=None):
         return 2
     if args.impl == "reference":
         return run_reference(args)
+    if args.pass_ == "bwd":
+        return run_ours_bwd(args)
     return run_ours(args)
 
 

@@ -12,17 +12,22 @@
 //   dbeta_t = du . w_t;  dx = -beta_t du;  dS' = dS + k_t dx^T;
 //   dk_t = dS u_t + S'_t dx;  dalpha_t = rowsum(dS' * S_{t-1});  dS = Diag(alpha_t) dS'.
 //
-// Two kernels:
-//   kda_bwd_state_kernel: one CTA of 512 threads per (sequence, head) unit, persistent
-//     over the units.  A forward sweep stores the state at the start of every 64-token
-//     chunk (checkpoints); then, chunk by chunk in reverse, the chunk's states are
-//     recomputed from its checkpoint into a per-CTA scratch of 64 states, and the
-//     reverse step runs over the chunk's tokens.  The K x V state (fp32) lives in
-//     registers: thread = 4 key channels x 8 value columns.  It writes dv and, per
-//     token, dq_hat, dk_hat, dalpha and dbeta (of beta itself) into dq, dk, dg, dbeta.
-//   kda_bwd_act_kernel: the activations' derivatives per token row: the L2 norms, the
-//     beta sigmoid, alpha = exp(gk) and the gate (bounded or not), in place on dq, dk,
-//     dg, dbeta, and the sums over tokens of dA_log and ddt_bias.
+// Every value column v of the state evolves on its own (the per-token vectors alpha,
+// k, beta are shared, the columns never mix), and so does its gradient; only dq, dk,
+// dalpha and dbeta sum over the columns.  So:
+//   kda_bwd_state_kernel: a CTA of 16 warps takes 32 value columns of one (sequence,
+//     head) unit (four CTAs per unit, persistent over units x column slices), a warp
+//     two columns, lane = 4 key channels x 2 columns of the fp32 state in registers.
+//     The recurrence and its reverse run warp by warp with no CTA barrier per token:
+//     column sums are warp shuffles.  A forward sweep stores the slice's state at the
+//     start of every 32-token chunk; then chunk by chunk in reverse the chunk's states
+//     are recomputed into a per-CTA scratch and the reverse step runs over its tokens.
+//     The slice's shares of dq_hat, dk_hat, dalpha and dbeta go into shared per-token
+//     slots (shared-memory atomic adds over the warps) and, once per chunk, to a
+//     partial buffer per slice; dv and the initial state's gradient are the slice's own.
+//   kda_bwd_act_kernel: per token row, the four slices' shares summed, then the
+//     activations' derivatives: the L2 norms, the beta sigmoid, alpha = exp(gk) and the
+//     gate (bounded or not); dq, dk, dg, dbeta written, dA_log and ddt_bias summed.
 #include <cuda_bf16.h>
 
 #include "kda_internal.h"
@@ -32,24 +37,27 @@ namespace kda {
 namespace {
 
 constexpr int DKB = kHeadDim;   // K = V = 128
-constexpr int NTB = 512;        // threads of the state kernel
-constexpr int CB = 64;          // tokens per chunk
-constexpr int64_t kStateElems = (int64_t)DKB * DKB;
+constexpr int NTB = 512;        // threads of the state kernel: 16 warps
+constexpr int NSL = 4;          // value-column slices per unit (CTAs per unit)
+constexpr int CWB = DKB / NSL;  // 32 columns per CTA, 2 per warp
+constexpr int CB = 32;          // tokens per chunk
+constexpr int kSlice = DKB * CWB;   // floats of one slice of a state
 
 // shared memory of the state kernel (floats)
-constexpr int SB_Q = 0;                  // [64][128] q_hat
-constexpr int SB_K = SB_Q + CB * DKB;    // [64][128] k_hat
-constexpr int SB_A = SB_K + CB * DKB;    // [64][128] alpha = exp(gk)
-constexpr int SB_V = SB_A + CB * DKB;    // [64][128] v
-constexpr int SB_D = SB_V + CB * DKB;    // [64][128] dout
-constexpr int SB_W = SB_D + CB * DKB;    // [64][128] w = v - S'^T k_hat (reverse pass)
-constexpr int SB_RED = SB_W + CB * DKB;  // [16][128] column-sum partials, one row per warp
-constexpr int SB_VEC = SB_RED + 16 * DKB;   // [128] a column vector for every thread
-constexpr int SB_BETA = SB_VEC + DKB;       // [64] beta
-constexpr int SB_MISC = SB_BETA + CB;       // [4] dbeta partials of warps 0-3
-constexpr int SB_FLOATS = SB_MISC + 4;
+constexpr int SB_Q = 0;                    // [CB][128] q_hat
+constexpr int SB_K = SB_Q + CB * DKB;      // [CB][128] k_hat
+constexpr int SB_A = SB_K + CB * DKB;      // [CB][128] alpha = exp(gk)
+constexpr int SB_V = SB_A + CB * DKB;      // [CB][32] v of the slice
+constexpr int SB_D = SB_V + CB * CWB;      // [CB][32] dout of the slice
+constexpr int SB_W = SB_D + CB * CWB;      // [CB][32] w = v - S'^T k_hat of the slice
+constexpr int SB_GQ = SB_W + CB * CWB;     // [CB][128] the slice's share of dq_hat
+constexpr int SB_GK = SB_GQ + CB * DKB;    // [CB][128] ... of dk_hat
+constexpr int SB_GA = SB_GK + CB * DKB;    // [CB][128] ... of dalpha
+constexpr int SB_GB = SB_GA + CB * DKB;    // [CB] ... of dbeta
+constexpr int SB_BETA = SB_GB + CB;        // [CB] beta
+constexpr int SB_FLOATS = SB_BETA + CB;
 constexpr size_t kBwdSmem = (size_t)SB_FLOATS * 4;
-static_assert(kBwdSmem <= 232448, "shared memory budget");
+static_assert(2 * (kBwdSmem + 1024) <= 233472, "two CTAs per SM");
 
 struct BwdArgs {
     const __nv_bfloat16 *dout;   // [B,T,H,V]
@@ -57,8 +65,10 @@ struct BwdArgs {
     float *dq, *dk, *dv, *dg, *dbeta;   // token gradients
     float *dA_log, *ddt_bias;    // [H], [H,K]: summed over tokens (zeroed before)
     float *dinit;                // [N,H,V,K] or null
-    float *ckpt;                 // chunk-start states, kStateElems floats per slot
-    float *tok;                  // per CTA: CB states (the chunk's S_{t-1})
+    float *ckpt;                 // chunk-start slices, kSlice floats per slot
+    float *tok;                  // per CTA: CB slices (the chunk's S_{t-1})
+    float *pq, *pk, *pa, *pb;    // per slice: shares of dq_hat, dk_hat, dalpha [rows H 128], dbeta [rows H]
+    int64_t prow;                // rows H: the stride of one slice in pq, pk, pa (x 128) and pb
     int unbounded;
 };
 
@@ -73,10 +83,10 @@ __device__ __forceinline__ void bwd_span(const Params &p, int64_t n, int64_t &ro
     }
 }
 
-// Checkpoint slot of chunk ci of unit (n, h): sequence n owns chunk slots
-// [floor(row0 / 64) + n, floor(row0 / 64) + n + nchunks), which never overlap.
-__device__ __forceinline__ int64_t ckpt_slot(int64_t row0, int64_t n, int64_t ci, int64_t h, int64_t H) {
-    return ((row0 / CB + n + ci) * H + h);
+// Checkpoint slot of chunk ci of unit (n, h), slice sl: sequence n owns chunk slots
+// [floor(row0 / CB) + n, floor(row0 / CB) + n + nchunks), which never overlap.
+__device__ __forceinline__ int64_t ckpt_slot(int64_t row0, int64_t n, int64_t ci, int64_t h, int64_t H, int sl) {
+    return ((row0 / CB + n + ci) * H + h) * NSL + sl;
 }
 
 // The gate's log decay of one element (bounded: lb sigmoid(a x); else -a softplus(x)).
@@ -97,33 +107,27 @@ __device__ __forceinline__ float warp_sum(float x) {
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
     return x;
 }
-// Sum over the 16 lanes of a half-warp (the threads that share four key channels).
-__device__ __forceinline__ float half_sum(float x) {
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
-}
 
-// Loads the chunk of packed token rows [row, row + L) of head h into shared memory:
-// q_hat, k_hat, alpha, v, beta (and dout).  Rows t >= L hold q_hat = k_hat = v = dout = 0,
-// alpha = 1, beta = 0, a step that leaves the state as it is.  Warp w takes tokens
-// w, w + 16, ...; lane = four channels.
+// Loads the chunk of packed token rows [row, row + L) of head h: q_hat, k_hat, alpha
+// (all channels), beta, and v (and dout) of the slice's columns vb .. vb + 31; rows
+// t >= L hold q_hat = k_hat = v = dout = 0, alpha = 1, beta = 0.  Clears the gradient
+// slots.  Warp w takes tokens w, w + 16; lane = four channels.
 __device__ void bwd_prepare(const Params &p, const BwdArgs &b, float *sm, int64_t row, int L, int64_t h,
-                            bool with_dout) {
+                            int vb, bool with_dout) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const float a = expf(p.A_log[h]);
     const float4 dtb = reinterpret_cast<const float4 *>(p.dt_bias + h * DKB)[lane];
     for (int t = warp; t < CB; t += NTB / 32) {
-        float4 qn = make_float4(0.f, 0.f, 0.f, 0.f), kn = qn, vv = qn, dd = qn;
+        float4 qn = make_float4(0.f, 0.f, 0.f, 0.f), kn = qn;
         float4 al = make_float4(1.f, 1.f, 1.f, 1.f);
-        float be = 0.f;
+        float vv = 0.f, dd = 0.f, be = 0.f;
         if (t < L) {   // warp-uniform
             const int64_t tok = (row + t) * p.H + h;
             const float4 q = bf16x4_to_f4(reinterpret_cast<const uint2 *>(p.q + tok * DKB)[lane]);
             const float4 k = bf16x4_to_f4(reinterpret_cast<const uint2 *>(p.k + tok * DKB)[lane]);
             const float4 g = bf16x4_to_f4(reinterpret_cast<const uint2 *>(p.g + tok * DKB)[lane]);
-            vv = bf16x4_to_f4(reinterpret_cast<const uint2 *>(p.v + tok * DKB)[lane]);
-            if (with_dout) dd = bf16x4_to_f4(reinterpret_cast<const uint2 *>(b.dout + tok * DKB)[lane]);
+            vv = __bfloat162float(p.v[tok * DKB + vb + lane]);
+            if (with_dout) dd = __bfloat162float(b.dout[tok * DKB + vb + lane]);
             const float sq = warp_sum(q.x * q.x + q.y * q.y + q.z * q.z + q.w * q.w);
             const float sk = warp_sum(k.x * k.x + k.y * k.y + k.z * k.z + k.w * k.w);
             const float rq = 1.f / sqrtf(sq + 1e-6f), rk = 1.f / sqrtf(sk + 1e-6f);
@@ -138,254 +142,211 @@ __device__ void bwd_prepare(const Params &p, const BwdArgs &b, float *sm, int64_
         reinterpret_cast<float4 *>(sm + SB_Q + t * DKB)[lane] = qn;
         reinterpret_cast<float4 *>(sm + SB_K + t * DKB)[lane] = kn;
         reinterpret_cast<float4 *>(sm + SB_A + t * DKB)[lane] = al;
-        reinterpret_cast<float4 *>(sm + SB_V + t * DKB)[lane] = vv;
-        reinterpret_cast<float4 *>(sm + SB_D + t * DKB)[lane] = dd;
-        if (lane == 0) sm[SB_BETA + t] = be;
+        sm[SB_V + t * CWB + lane] = vv;
+        sm[SB_D + t * CWB + lane] = dd;
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        reinterpret_cast<float4 *>(sm + SB_GQ + t * DKB)[lane] = z;
+        reinterpret_cast<float4 *>(sm + SB_GK + t * DKB)[lane] = z;
+        reinterpret_cast<float4 *>(sm + SB_GA + t * DKB)[lane] = z;
+        if (lane == 0) {
+            sm[SB_BETA + t] = be;
+            sm[SB_GB + t] = 0.f;
+        }
     }
 }
 
-// Column sums over all 128 key channels: part[j] is this thread's sum over its four
-// channels for column 8 cg + j.  Leaves one partial per warp in SB_RED and syncs; the
-// caller's threads 0-127 then add the 16 partials of their column.
-__device__ __forceinline__ void col_partials(float *sm, const float (&part)[8]) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, cg = tid & 15;
-    float x[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) x[j] = part[j] + __shfl_xor_sync(0xffffffffu, part[j], 16);
-    if (lane < 16) {
-        float4 *r = reinterpret_cast<float4 *>(sm + SB_RED + warp * DKB + 8 * cg);
-        r[0] = make_float4(x[0], x[1], x[2], x[3]);
-        r[1] = make_float4(x[4], x[5], x[6], x[7]);
-    }
-    __syncthreads();
+// A lane's tile: key channels 4 lane + i (i < 4) of the warp's two value columns j.
+// Stored thread-major (two float4 per thread, coalesced) in checkpoints and scratch.
+__device__ __forceinline__ void tile_store(float *dst, const float (&s)[4][2]) {
+    float4 *d = reinterpret_cast<float4 *>(dst) + threadIdx.x * 2;
+    d[0] = make_float4(s[0][0], s[0][1], s[1][0], s[1][1]);
+    d[1] = make_float4(s[2][0], s[2][1], s[3][0], s[3][1]);
 }
-__device__ __forceinline__ float col_total(const float *sm, int col) {
-    float s = 0.f;
-#pragma unroll
-    for (int w = 0; w < 16; ++w) s += sm[SB_RED + w * DKB + col];
-    return s;
+__device__ __forceinline__ void tile_load(const float *src, float (&s)[4][2]) {
+    const float4 *d = reinterpret_cast<const float4 *>(src) + threadIdx.x * 2;
+    const float4 x = d[0], y = d[1];
+    s[0][0] = x.x; s[0][1] = x.y; s[1][0] = x.z; s[1][1] = x.w;
+    s[2][0] = y.x; s[2][1] = y.y; s[3][0] = y.z; s[3][1] = y.w;
 }
 
-// One forward step on the register tile s (rows r0.., columns c0..) of token t of the
-// chunk: S' = Diag(alpha) S; w = v - S'^T k_hat (into SB_W when store_w); S = S' + beta k_hat w^T.
-__device__ __forceinline__ void fwd_step(float *sm, float (&s)[4][8], int t, int r0, int c0, bool store_w) {
-    const int tid = threadIdx.x;
-    const float4 a4 = *reinterpret_cast<const float4 *>(sm + SB_A + t * DKB + r0);
-    const float4 k4 = *reinterpret_cast<const float4 *>(sm + SB_K + t * DKB + r0);
+// One forward step of token t on the warp's two columns: S' = Diag(alpha) S;
+// w = v - S'^T k_hat (into SB_W when store_w); S = S' + beta k_hat w^T.
+__device__ __forceinline__ void fwd_step(float *sm, float (&s)[4][2], int t, bool store_w) {
+    const int lane = threadIdx.x & 31, lc = 2 * (threadIdx.x >> 5);
+    const float4 a4 = *reinterpret_cast<const float4 *>(sm + SB_A + t * DKB + 4 * lane);
+    const float4 k4 = *reinterpret_cast<const float4 *>(sm + SB_K + t * DKB + 4 * lane);
     const float a[4] = {a4.x, a4.y, a4.z, a4.w}, kk[4] = {k4.x, k4.y, k4.z, k4.w};
-    float part[8];
+    float part[2] = {0.f, 0.f};
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        part[j] = 0.f;
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int j = 0; j < 2; ++j) {
             s[i][j] *= a[i];
             part[j] = fmaf(kk[i], s[i][j], part[j]);
         }
-    }
-    col_partials(sm, part);
-    if (tid < DKB) {
-        const float wv = sm[SB_V + t * DKB + tid] - col_total(sm, tid);
-        sm[SB_VEC + tid] = wv;
-        if (store_w) sm[SB_W + t * DKB + tid] = wv;
-    }
-    __syncthreads();
     const float be = sm[SB_BETA + t];
-    const float4 w0 = *reinterpret_cast<const float4 *>(sm + SB_VEC + c0);
-    const float4 w1 = *reinterpret_cast<const float4 *>(sm + SB_VEC + c0 + 4);
-    const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    float w[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) w[j] = sm[SB_V + t * CWB + lc + j] - warp_sum(part[j]);
+    if (store_w && lane == 0) {
+        sm[SB_W + t * CWB + lc] = w[0];
+        sm[SB_W + t * CWB + lc + 1] = w[1];
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const float bk = be * kk[i];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) s[i][j] = fmaf(bk, w[j], s[i][j]);
+        s[i][0] = fmaf(bk, w[0], s[i][0]);
+        s[i][1] = fmaf(bk, w[1], s[i][1]);
     }
 }
 
-// Register tile <-> a state stored thread-major (8 float4 per thread, coalesced).
-__device__ __forceinline__ void tile_store(float *dst, const float (&s)[4][8]) {
-    float4 *d = reinterpret_cast<float4 *>(dst) + threadIdx.x * 8;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        d[2 * i] = make_float4(s[i][0], s[i][1], s[i][2], s[i][3]);
-        d[2 * i + 1] = make_float4(s[i][4], s[i][5], s[i][6], s[i][7]);
-    }
-}
-__device__ __forceinline__ void tile_load(const float *src, float (&s)[4][8]) {
-    const float4 *d = reinterpret_cast<const float4 *>(src) + threadIdx.x * 8;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float4 x = d[2 * i], y = d[2 * i + 1];
-        s[i][0] = x.x; s[i][1] = x.y; s[i][2] = x.z; s[i][3] = x.w;
-        s[i][4] = y.x; s[i][5] = y.y; s[i][6] = y.z; s[i][7] = y.w;
-    }
-}
-
-// One reverse step of token t of the chunk (packed token row `row`): ds is dL/dS_t on
-// entry and dL/dS_{t-1} on exit; sp the state S_{t-1}.
-__device__ __forceinline__ void bwd_step(const Params &p, const BwdArgs &b, float *sm, float (&ds)[4][8],
-                                         const float (&sp)[4][8], int t, int64_t tok, int r0, int c0) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, cg = tid & 15;
-    const float4 a4 = *reinterpret_cast<const float4 *>(sm + SB_A + t * DKB + r0);
-    const float4 k4 = *reinterpret_cast<const float4 *>(sm + SB_K + t * DKB + r0);
-    const float4 q4 = *reinterpret_cast<const float4 *>(sm + SB_Q + t * DKB + r0);
+// One reverse step of token t on the warp's two columns: ds is dL/dS_t on entry and
+// dL/dS_{t-1} on exit; sp the state S_{t-1}.  The warp's shares of dq_hat, dk_hat,
+// dalpha and dbeta go to the token's slots by shared-memory atomic adds.
+__device__ __forceinline__ void bwd_step(const Params &p, const BwdArgs &b, float *sm, float (&ds)[4][2],
+                                         const float (&sp)[4][2], int t, int64_t tok, int vb) {
+    const int lane = threadIdx.x & 31, lc = 2 * (threadIdx.x >> 5);
+    const float4 a4 = *reinterpret_cast<const float4 *>(sm + SB_A + t * DKB + 4 * lane);
+    const float4 k4 = *reinterpret_cast<const float4 *>(sm + SB_K + t * DKB + 4 * lane);
+    const float4 q4 = *reinterpret_cast<const float4 *>(sm + SB_Q + t * DKB + 4 * lane);
     const float a[4] = {a4.x, a4.y, a4.z, a4.w}, kk[4] = {k4.x, k4.y, k4.z, k4.w};
     const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
-    float w[8], dd[8];
-    {
-        const float4 w0 = *reinterpret_cast<const float4 *>(sm + SB_W + t * DKB + c0);
-        const float4 w1 = *reinterpret_cast<const float4 *>(sm + SB_W + t * DKB + c0 + 4);
-        const float4 d0 = *reinterpret_cast<const float4 *>(sm + SB_D + t * DKB + c0);
-        const float4 d1 = *reinterpret_cast<const float4 *>(sm + SB_D + t * DKB + c0 + 4);
-        w[0] = w0.x; w[1] = w0.y; w[2] = w0.z; w[3] = w0.w; w[4] = w1.x; w[5] = w1.y; w[6] = w1.z; w[7] = w1.w;
-        dd[0] = d0.x; dd[1] = d0.y; dd[2] = d0.z; dd[3] = d0.w; dd[4] = d1.x; dd[5] = d1.y; dd[6] = d1.z; dd[7] = d1.w;
-    }
+    const float w[2] = {sm[SB_W + t * CWB + lc], sm[SB_W + t * CWB + lc + 1]};
+    const float dd[2] = {sm[SB_D + t * CWB + lc], sm[SB_D + t * CWB + lc + 1]};
     const float be = sm[SB_BETA + t], sc = p.scale;
-    // dq_hat = scale S_t do with S_t = Diag(alpha) S_{t-1} + beta k_hat w^T;  dS += scale q_hat do^T
-    float xq[4], part[8];
+    // dq_hat = scale S_t do, S_t = Diag(alpha) S_{t-1} + beta k_hat w^T;  dS += scale q_hat do^T
+    float xq[4], part[2] = {0.f, 0.f};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         float x = 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 2; ++j) {
             x = fmaf(fmaf(a[i], sp[i][j], be * kk[i] * w[j]), dd[j], x);
             ds[i][j] = fmaf(sc * qq[i], dd[j], ds[i][j]);
+            part[j] = fmaf(ds[i][j], kk[i], part[j]);
         }
-        xq[i] = x;
+        xq[i] = sc * x;
     }
-    // du = dS^T k_hat (column sums)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        part[j] = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) part[j] = fmaf(ds[i][j], kk[i], part[j]);
+    // du = dS^T k_hat (warp sums over the key channels)
+    const float du[2] = {warp_sum(part[0]), warp_sum(part[1])};
+    if (lane == 0) {
+        b.dv[tok * DKB + vb + lc] = be * du[0];
+        b.dv[tok * DKB + vb + lc + 1] = be * du[1];
+        atomicAdd(sm + SB_GB + t, du[0] * w[0] + du[1] * w[1]);
     }
-    col_partials(sm, part);
-    if (tid < DKB) {
-        const float du = col_total(sm, tid);
-        sm[SB_VEC + tid] = du;
-        b.dv[tok * DKB + tid] = be * du;
-        const float pb = warp_sum(du * sm[SB_W + t * DKB + tid]);   // warps 0-3, whole warps
-        if (lane == 0) sm[SB_MISC + warp] = pb;
-    }
-    __syncthreads();
-    float dx[8];
-    {
-        const float4 u0 = *reinterpret_cast<const float4 *>(sm + SB_VEC + c0);
-        const float4 u1 = *reinterpret_cast<const float4 *>(sm + SB_VEC + c0 + 4);
-        dx[0] = -be * u0.x; dx[1] = -be * u0.y; dx[2] = -be * u0.z; dx[3] = -be * u0.w;
-        dx[4] = -be * u1.x; dx[5] = -be * u1.y; dx[6] = -be * u1.z; dx[7] = -be * u1.w;
-    }
+    const float dx[2] = {-be * du[0], -be * du[1]};
     // dk_hat = dS (beta w) + S' dx;  dS' = dS + k_hat dx^T;  dalpha = rowsum(dS' * S_{t-1});
     // dS_{t-1} = Diag(alpha) dS'
-    float yk[4], za[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         float y = 0.f, z = 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 2; ++j) {
             y = fmaf(ds[i][j], be * w[j], y);
             y = fmaf(a[i] * sp[i][j], dx[j], y);
             const float dsp = fmaf(kk[i], dx[j], ds[i][j]);
             z = fmaf(dsp, sp[i][j], z);
             ds[i][j] = a[i] * dsp;
         }
-        yk[i] = y;
-        za[i] = z;
+        atomicAdd(sm + SB_GQ + t * DKB + 4 * lane + i, xq[i]);
+        atomicAdd(sm + SB_GK + t * DKB + 4 * lane + i, y);
+        atomicAdd(sm + SB_GA + t * DKB + 4 * lane + i, z);
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        xq[i] = half_sum(xq[i]);
-        yk[i] = half_sum(yk[i]);
-        za[i] = half_sum(za[i]);
-    }
-    if (cg == 0) {
-        *reinterpret_cast<float4 *>(b.dq + tok * DKB + r0) = make_float4(sc * xq[0], sc * xq[1], sc * xq[2], sc * xq[3]);
-        *reinterpret_cast<float4 *>(b.dk + tok * DKB + r0) = make_float4(yk[0], yk[1], yk[2], yk[3]);
-        *reinterpret_cast<float4 *>(b.dg + tok * DKB + r0) = make_float4(za[0], za[1], za[2], za[3]);
-    }
-    if (tid == 0) b.dbeta[tok] = sm[SB_MISC] + sm[SB_MISC + 1] + sm[SB_MISC + 2] + sm[SB_MISC + 3];
 }
 
-__global__ void __launch_bounds__(NTB, 1) kda_bwd_state_kernel(Params p, BwdArgs b) {
+__global__ void __launch_bounds__(NTB, 2) kda_bwd_state_kernel(Params p, BwdArgs b) {
     extern __shared__ __align__(16) float sm[];
-    const int tid = threadIdx.x, rg = tid >> 4, cg = tid & 15;
-    const int r0 = 4 * rg, c0 = 8 * cg;
-    const int64_t units = p.n_seqs * p.H;
-    float *tokst = b.tok + (size_t)blockIdx.x * CB * kStateElems;
-    for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
-        const int64_t n = u / p.H, h = u % p.H;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t work = p.n_seqs * p.H * NSL;
+    float *tokst = b.tok + (size_t)blockIdx.x * CB * kSlice;
+    for (int64_t wi = blockIdx.x; wi < work; wi += gridDim.x) {
+        const int64_t u = wi / NSL, n = u / p.H, h = u % p.H;
+        const int sl = (int)(wi % NSL), vb = sl * CWB, col = vb + 2 * warp;
         int64_t row0, len;
         bwd_span(p, n, row0, len);
         const int nch = (int)((len + CB - 1) / CB);
-        const size_t soff = (size_t)(n * p.H + h) * kStateElems;   // [V][K] state of the unit
-        float s[4][8];
+        const size_t soff = (size_t)(n * p.H + h) * DKB * DKB;   // [V][K] state of the unit
+        // the slice's share of the token gradients: slice 0 into the outputs, the others
+        // into the partial buffers
+        float *gq = sl == 0 ? b.dq : b.pq + (size_t)(sl - 1) * b.prow * DKB;
+        float *gk = sl == 0 ? b.dk : b.pk + (size_t)(sl - 1) * b.prow * DKB;
+        float *ga = sl == 0 ? b.dg : b.pa + (size_t)(sl - 1) * b.prow * DKB;
+        float *gb = sl == 0 ? b.dbeta : b.pb + (size_t)(sl - 1) * b.prow;
+        float s[4][2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) s[i][j] = 0.f;
-        if (p.init) {   // S[c][v] = init[v][c]
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const size_t off = soff + (size_t)(c0 + j) * DKB + r0;
-                const float4 x = p.state_type == kStateBF16
-                                     ? bf16x4_to_f4(*reinterpret_cast<const uint2 *>(
-                                           reinterpret_cast<const __nv_bfloat16 *>(p.init) + off))
-                                     : *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(p.init) + off);
-                s[0][j] = x.x; s[1][j] = x.y; s[2][j] = x.z; s[3][j] = x.w;
+        for (int j = 0; j < 2; ++j) {   // S[c][v] = init[v][c]
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (p.init) {
+                const size_t off = soff + (size_t)(col + j) * DKB + 4 * lane;
+                x = p.state_type == kStateBF16
+                        ? bf16x4_to_f4(*reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(p.init) + off))
+                        : *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(p.init) + off);
             }
+            s[0][j] = x.x; s[1][j] = x.y; s[2][j] = x.z; s[3][j] = x.w;
         }
-        // forward sweep: the state at the start of every chunk
+        // forward sweep: the slice's state at the start of every chunk
         for (int ci = 0; ci < nch; ++ci) {
             const int L = (int)(len - (int64_t)ci * CB < CB ? len - (int64_t)ci * CB : CB);
-            tile_store(b.ckpt + ckpt_slot(row0, n, ci, h, p.H) * kStateElems, s);
-            __syncthreads();   // every reader of the previous chunk's tiles is done
-            bwd_prepare(p, b, sm, row0 + (int64_t)ci * CB, L, h, false);
+            tile_store(b.ckpt + ckpt_slot(row0, n, ci, h, p.H, sl) * kSlice, s);
+            __syncthreads();   // every reader of the previous chunk's shared data is done
+            bwd_prepare(p, b, sm, row0 + (int64_t)ci * CB, L, h, vb, false);
             __syncthreads();
-            for (int t = 0; t < L; ++t) fwd_step(sm, s, t, r0, c0, false);
+            for (int t = 0; t < L; ++t) fwd_step(sm, s, t, false);
         }
         // reverse: dS from the final-state gradient, then chunk by chunk
-        float ds[4][8];
+        float ds[4][2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) ds[i][j] = 0.f;
-        if (b.dfinal) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float4 x = *reinterpret_cast<const float4 *>(b.dfinal + soff + (size_t)(c0 + j) * DKB + r0);
-                ds[0][j] = x.x; ds[1][j] = x.y; ds[2][j] = x.z; ds[3][j] = x.w;
-            }
+        for (int j = 0; j < 2; ++j) {
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (b.dfinal) x = *reinterpret_cast<const float4 *>(b.dfinal + soff + (size_t)(col + j) * DKB + 4 * lane);
+            ds[0][j] = x.x; ds[1][j] = x.y; ds[2][j] = x.z; ds[3][j] = x.w;
         }
         for (int ci = nch - 1; ci >= 0; --ci) {
             const int L = (int)(len - (int64_t)ci * CB < CB ? len - (int64_t)ci * CB : CB);
             const int64_t crow = row0 + (int64_t)ci * CB;
-            tile_load(b.ckpt + ckpt_slot(row0, n, ci, h, p.H) * kStateElems, s);
+            tile_load(b.ckpt + ckpt_slot(row0, n, ci, h, p.H, sl) * kSlice, s);
             __syncthreads();
-            bwd_prepare(p, b, sm, crow, L, h, true);
+            bwd_prepare(p, b, sm, crow, L, h, vb, true);
             __syncthreads();
             for (int t = 0; t < L; ++t) {   // S_{t-1} of every token, and w
-                tile_store(tokst + (size_t)t * kStateElems, s);
-                fwd_step(sm, s, t, r0, c0, true);
+                tile_store(tokst + (size_t)t * kSlice, s);
+                fwd_step(sm, s, t, true);
             }
+            __syncwarp();   // lane 0's w stores are visible to the warp
+            float sp[4][2], spn[4][2];
+            tile_load(tokst + (size_t)(L - 1) * kSlice, sp);
             for (int t = L - 1; t >= 0; --t) {   // this thread's own stores: no fence needed
-                float sp[4][8];
-                tile_load(tokst + (size_t)t * kStateElems, sp);
-                bwd_step(p, b, sm, ds, sp, t, (crow + t) * p.H + h, r0, c0);
-            }
-        }
-        if (b.dinit) {   // dinit[v][c] = dS_0[c][v]
+                if (t > 0) tile_load(tokst + (size_t)(t - 1) * kSlice, spn);
+                bwd_step(p, b, sm, ds, sp, t, (crow + t) * p.H + h, vb);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                *reinterpret_cast<float4 *>(b.dinit + soff + (size_t)(c0 + j) * DKB + r0) =
+                for (int i = 0; i < 4; ++i) {
+                    sp[i][0] = spn[i][0];
+                    sp[i][1] = spn[i][1];
+                }
+            }
+            __syncthreads();   // every warp's slot additions are in
+            for (int e = tid; e < L * DKB; e += NTB) {
+                const int t = e >> 7, r = e & (DKB - 1);
+                const int64_t o = ((crow + t) * p.H + h) * DKB + r;
+                gq[o] = sm[SB_GQ + t * DKB + r];
+                gk[o] = sm[SB_GK + t * DKB + r];
+                ga[o] = sm[SB_GA + t * DKB + r];
+            }
+            for (int t = tid; t < L; t += NTB) gb[(crow + t) * p.H + h] = sm[SB_GB + t];
+        }
+        if (b.dinit) {   // dinit[v][c] = dS_0[c][v] on the slice's columns
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                *reinterpret_cast<float4 *>(b.dinit + soff + (size_t)(col + j) * DKB + 4 * lane) =
                     make_float4(ds[0][j], ds[1][j], ds[2][j], ds[3][j]);
         }
     }
 }
 
-// Derivatives of the activations, one warp per token row of one head (lane = four
-// channels), 64 rows per block; in place on dq (dq_hat in), dk (dk_hat in), dg (dalpha
-// in) and dbeta (of beta in, of the logit out).  dA_log and ddt_bias receive one atomic
+// Per token row of one head (a warp per row, lane = four channels, 64 rows per block):
+// the four slices' shares of dq_hat, dk_hat, dalpha, dbeta summed (slice 0's sit in the
+// outputs already), then the derivatives of the L2 norms, the beta sigmoid, alpha =
+// exp(gk) and the gate; dq, dk, dg, dbeta written.  dA_log and ddt_bias take one atomic
 // add per block and channel.
 constexpr int kActRows = 64;
 __global__ void __launch_bounds__(256) kda_bwd_act_kernel(Params p, BwdArgs b, int64_t rows) {
@@ -396,7 +357,17 @@ __global__ void __launch_bounds__(256) kda_bwd_act_kernel(Params p, BwdArgs b, i
     const float a = expf(p.A_log[h]), lb = p.lower_bound;
     const float4 dtb4 = reinterpret_cast<const float4 *>(p.dt_bias + h * DKB)[lane];
     const float dtb[4] = {dtb4.x, dtb4.y, dtb4.z, dtb4.w};
+    const size_t sstride = (size_t)b.prow * DKB;
     float acct[4] = {0.f, 0.f, 0.f, 0.f}, acca = 0.f;
+    auto share4 = [&](float *out, const float *part, int64_t tok) {   // slice 0 + the others
+        float4 x = reinterpret_cast<const float4 *>(out + tok * DKB)[lane];
+#pragma unroll
+        for (int sl = 0; sl < NSL - 1; ++sl) {
+            const float4 y = reinterpret_cast<const float4 *>(part + sl * sstride + tok * DKB)[lane];
+            x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
+        }
+        return x;
+    };
     for (int r = warp; r < kActRows; r += 8) {
         const int64_t row = (int64_t)blockIdx.x * kActRows + r;
         if (row >= rows) break;   // warp-uniform
@@ -407,22 +378,24 @@ __global__ void __launch_bounds__(256) kda_bwd_act_kernel(Params p, BwdArgs b, i
             const __nv_bfloat16 *xp = which == 0 ? p.q : p.k;
             float *gp = which == 0 ? b.dq : b.dk;
             const float4 x = bf16x4_to_f4(reinterpret_cast<const uint2 *>(xp + tok * DKB)[lane]);
-            float4 *dp = reinterpret_cast<float4 *>(gp + tok * DKB) + lane;
-            const float4 dh = *dp;
+            const float4 dh = share4(gp, which == 0 ? b.pq : b.pk, tok);
             const float sq = warp_sum(x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w);
             const float xd = warp_sum(x.x * dh.x + x.y * dh.y + x.z * dh.z + x.w * dh.w);
-            const float nrm = sqrtf(sq + 1e-6f), inv = 1.f / nrm, c3 = xd * inv * inv * inv;
-            *dp = make_float4(dh.x * inv - x.x * c3, dh.y * inv - x.y * c3, dh.z * inv - x.z * c3,
-                              dh.w * inv - x.w * c3);
+            const float inv = 1.f / sqrtf(sq + 1e-6f), c3 = xd * inv * inv * inv;
+            reinterpret_cast<float4 *>(gp + tok * DKB)[lane] =
+                make_float4(dh.x * inv - x.x * c3, dh.y * inv - x.y * c3, dh.z * inv - x.z * c3,
+                            dh.w * inv - x.w * c3);
         }
         if (lane == 0) {
+            float dbe = b.dbeta[tok];
+#pragma unroll
+            for (int sl = 0; sl < NSL - 1; ++sl) dbe += b.pb[sl * b.prow + tok];
             const float be = 1.f / (1.f + expf(-__bfloat162float(p.beta[tok])));
-            b.dbeta[tok] = b.dbeta[tok] * be * (1.f - be);
+            b.dbeta[tok] = dbe * be * (1.f - be);
         }
         // the gate: alpha = exp(gk)
         const float4 g4 = bf16x4_to_f4(reinterpret_cast<const uint2 *>(p.g + tok * DKB)[lane]);
-        float4 *gp = reinterpret_cast<float4 *>(b.dg + tok * DKB) + lane;
-        const float4 da4 = *gp;
+        const float4 da4 = share4(b.dg, b.pa, tok);
         const float gg[4] = {g4.x, g4.y, g4.z, g4.w}, dal[4] = {da4.x, da4.y, da4.z, da4.w};
         float dgo[4];
 #pragma unroll
@@ -441,7 +414,7 @@ __global__ void __launch_bounds__(256) kda_bwd_act_kernel(Params p, BwdArgs b, i
             }
             acct[e] += dgo[e];
         }
-        *gp = make_float4(dgo[0], dgo[1], dgo[2], dgo[3]);
+        reinterpret_cast<float4 *>(b.dg + tok * DKB)[lane] = make_float4(dgo[0], dgo[1], dgo[2], dgo[3]);
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) red[warp][4 * lane + e] = acct[e];
@@ -462,22 +435,31 @@ __global__ void __launch_bounds__(256) kda_bwd_act_kernel(Params p, BwdArgs b, i
     }
 }
 
-size_t ckpt_bytes(const Params &p) {
-    const int64_t slots = ((p.B * p.T) / CB + p.n_seqs + 1) * p.H;
-    return (size_t)slots * kStateElems * 4;
+struct BwdLayout {
+    size_t ckpt, tok, part, total;
+    int64_t grid;
+};
+BwdLayout bwd_layout(const Params &p, int sms) {
+    BwdLayout l;
+    const int64_t work = p.n_seqs * p.H * NSL;
+    l.grid = work < 2 * (int64_t)sms ? work : 2 * (int64_t)sms;   // two CTAs per SM
+    const int64_t slots = ((p.B * p.T) / CB + p.n_seqs + 1) * p.H * NSL;
+    const int64_t prow = p.B * p.T * p.H;
+    l.ckpt = 0;
+    l.tok = (size_t)slots * kSlice * 4;
+    l.part = l.tok + (size_t)l.grid * CB * kSlice * 4;
+    l.total = l.part + (size_t)(NSL - 1) * (size_t)prow * (3 * DKB + 1) * 4;
+    return l;
 }
 
 }  // namespace
 
-size_t bwd_scratch_bytes(const Params &p, int sms) {
-    const int64_t units = p.n_seqs * p.H;
-    const int64_t grid = units < sms ? units : sms;
-    return ckpt_bytes(p) + (size_t)grid * CB * kStateElems * 4;
-}
+size_t bwd_scratch_bytes(const Params &p, int sms) { return bwd_layout(p, sms).total; }
 
 cudaError_t launch_bwd(const Params &p, const BwdGrads &g, int unbounded, unsigned char *ws, int sms,
                        cudaStream_t stream) {
-    const int64_t units = p.n_seqs * p.H;
+    const BwdLayout l = bwd_layout(p, sms);
+    const int64_t prow = p.B * p.T * p.H;
     BwdArgs b;
     b.dout = g.dout;
     b.dfinal = g.dfinal;
@@ -490,23 +472,28 @@ cudaError_t launch_bwd(const Params &p, const BwdGrads &g, int unbounded, unsign
     b.ddt_bias = g.ddt_bias;
     b.dinit = g.dinit;
     b.unbounded = unbounded;
-    b.ckpt = reinterpret_cast<float *>(ws);
-    b.tok = reinterpret_cast<float *>(ws + ckpt_bytes(p));
+    b.ckpt = reinterpret_cast<float *>(ws + l.ckpt);
+    b.tok = reinterpret_cast<float *>(ws + l.tok);
+    float *part = reinterpret_cast<float *>(ws + l.part);
+    b.pq = part;
+    b.pk = part + (size_t)(NSL - 1) * prow * DKB;
+    b.pa = part + (size_t)2 * (NSL - 1) * prow * DKB;
+    b.pb = part + (size_t)3 * (NSL - 1) * prow * DKB;
+    b.prow = prow;
     cudaError_t e = cudaSuccess;
     if (p.H > 0) {
         if ((e = cudaMemsetAsync(b.dA_log, 0, sizeof(float) * (size_t)p.H, stream)) != cudaSuccess) return e;
         if ((e = cudaMemsetAsync(b.ddt_bias, 0, sizeof(float) * (size_t)(p.H * DKB), stream)) != cudaSuccess)
             return e;
     }
-    if (units == 0) return cudaSuccess;
+    if (p.n_seqs * p.H == 0) return cudaSuccess;
     static std::atomic<bool> attr_done[kMaxDevices];
     e = once_per_device(attr_done, [](int) {
         return cudaFuncSetAttribute(kda_bwd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)kBwdSmem);
     });
     if (e != cudaSuccess) return e;
-    const int64_t grid = units < sms ? units : sms;
-    kda_bwd_state_kernel<<<(unsigned)grid, NTB, kBwdSmem, stream>>>(p, b);
+    kda_bwd_state_kernel<<<(unsigned)l.grid, NTB, kBwdSmem, stream>>>(p, b);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t rows = p.B * p.T;
     if (rows > 0) {
