@@ -37,9 +37,10 @@ namespace kda {
 namespace {
 
 constexpr int DKB = kHeadDim;   // K = V = 128
-constexpr int NTB = 512;        // threads of the state kernel: 16 warps
+constexpr int NTB = 256;        // threads of the state kernel: 8 warps
 constexpr int NSL = 4;          // value-column slices per unit (CTAs per unit)
-constexpr int CWB = DKB / NSL;  // 32 columns per CTA, 2 per warp
+constexpr int CWB = DKB / NSL;  // 32 columns per CTA, 4 per warp
+constexpr int CPW = 4;          // columns per warp
 constexpr int CB = 32;          // tokens per chunk
 constexpr int kSlice = DKB * CWB;   // floats of one slice of a state
 
@@ -155,93 +156,115 @@ __device__ void bwd_prepare(const Params &p, const BwdArgs &b, float *sm, int64_
     }
 }
 
-// A lane's tile: key channels 4 lane + i (i < 4) of the warp's two value columns j.
-// Stored thread-major (two float4 per thread, coalesced) in checkpoints and scratch.
-__device__ __forceinline__ void tile_store(float *dst, const float (&s)[4][2]) {
-    float4 *d = reinterpret_cast<float4 *>(dst) + threadIdx.x * 2;
-    d[0] = make_float4(s[0][0], s[0][1], s[1][0], s[1][1]);
-    d[1] = make_float4(s[2][0], s[2][1], s[3][0], s[3][1]);
+// A lane's tile: key channels 4 lane + i (i < 4) of the warp's four value columns j.
+// Stored thread-major (four float4 per thread, coalesced) in checkpoints and scratch.
+__device__ __forceinline__ void tile_store(float *dst, const float (&s)[4][CPW]) {
+    float4 *d = reinterpret_cast<float4 *>(dst) + threadIdx.x * 4;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[i] = make_float4(s[i][0], s[i][1], s[i][2], s[i][3]);
 }
-__device__ __forceinline__ void tile_load(const float *src, float (&s)[4][2]) {
-    const float4 *d = reinterpret_cast<const float4 *>(src) + threadIdx.x * 2;
-    const float4 x = d[0], y = d[1];
-    s[0][0] = x.x; s[0][1] = x.y; s[1][0] = x.z; s[1][1] = x.w;
-    s[2][0] = y.x; s[2][1] = y.y; s[3][0] = y.z; s[3][1] = y.w;
+__device__ __forceinline__ void tile_load(const float *src, float (&s)[4][CPW]) {
+    const float4 *d = reinterpret_cast<const float4 *>(src) + threadIdx.x * 4;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float4 x = d[i];
+        s[i][0] = x.x; s[i][1] = x.y; s[i][2] = x.z; s[i][3] = x.w;
+    }
 }
 
-// One forward step of token t on the warp's two columns: S' = Diag(alpha) S;
+// Sums of four columns over the warp's 32 lanes, every lane receiving all four: two
+// exchanges halve the columns a lane carries (lane bit 4, then bit 3), three more finish
+// the one left (lane 8 j then holds column j's sum), four broadcasts hand them round.
+__device__ __forceinline__ void col_sums4(const float (&x)[CPW], float (&out)[CPW]) {
+    const int lane = threadIdx.x & 31;
+    const bool b4 = lane & 16, b3 = lane & 8;
+    const float y0 = (b4 ? x[2] : x[0]) + __shfl_xor_sync(0xffffffffu, b4 ? x[0] : x[2], 16);
+    const float y1 = (b4 ? x[3] : x[1]) + __shfl_xor_sync(0xffffffffu, b4 ? x[1] : x[3], 16);
+    float z = (b3 ? y1 : y0) + __shfl_xor_sync(0xffffffffu, b3 ? y0 : y1, 8);
+    z += __shfl_xor_sync(0xffffffffu, z, 4);
+    z += __shfl_xor_sync(0xffffffffu, z, 2);
+    z += __shfl_xor_sync(0xffffffffu, z, 1);
+#pragma unroll
+    for (int j = 0; j < CPW; ++j) out[j] = __shfl_sync(0xffffffffu, z, 8 * j);
+}
+
+// One forward step of token t on the warp's four columns: S' = Diag(alpha) S;
 // w = v - S'^T k_hat (into SB_W when store_w); S = S' + beta k_hat w^T.
-__device__ __forceinline__ void fwd_step(float *sm, float (&s)[4][2], int t, bool store_w) {
-    const int lane = threadIdx.x & 31, lc = 2 * (threadIdx.x >> 5);
+__device__ __forceinline__ void fwd_step(float *sm, float (&s)[4][CPW], int t, bool store_w) {
+    const int lane = threadIdx.x & 31, lc = CPW * (threadIdx.x >> 5);
     const float4 a4 = *reinterpret_cast<const float4 *>(sm + SB_A + t * DKB + 4 * lane);
     const float4 k4 = *reinterpret_cast<const float4 *>(sm + SB_K + t * DKB + 4 * lane);
+    const float4 v4 = *reinterpret_cast<const float4 *>(sm + SB_V + t * CWB + lc);
     const float a[4] = {a4.x, a4.y, a4.z, a4.w}, kk[4] = {k4.x, k4.y, k4.z, k4.w};
-    float part[2] = {0.f, 0.f};
+    float part[CPW] = {0.f, 0.f, 0.f, 0.f}, ks[CPW];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < CPW; ++j) {
             s[i][j] *= a[i];
             part[j] = fmaf(kk[i], s[i][j], part[j]);
         }
+    col_sums4(part, ks);
+    const float w[CPW] = {v4.x - ks[0], v4.y - ks[1], v4.z - ks[2], v4.w - ks[3]};
+    if (store_w && lane == 0)
+        *reinterpret_cast<float4 *>(sm + SB_W + t * CWB + lc) = make_float4(w[0], w[1], w[2], w[3]);
     const float be = sm[SB_BETA + t];
-    float w[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) w[j] = sm[SB_V + t * CWB + lc + j] - warp_sum(part[j]);
-    if (store_w && lane == 0) {
-        sm[SB_W + t * CWB + lc] = w[0];
-        sm[SB_W + t * CWB + lc + 1] = w[1];
-    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const float bk = be * kk[i];
-        s[i][0] = fmaf(bk, w[0], s[i][0]);
-        s[i][1] = fmaf(bk, w[1], s[i][1]);
+#pragma unroll
+        for (int j = 0; j < CPW; ++j) s[i][j] = fmaf(bk, w[j], s[i][j]);
     }
 }
 
-// One reverse step of token t on the warp's two columns: ds is dL/dS_t on entry and
+// One reverse step of token t on the warp's four columns: ds is dL/dS_t on entry and
 // dL/dS_{t-1} on exit; sp the state S_{t-1}.  The warp's shares of dq_hat, dk_hat,
 // dalpha and dbeta go to the token's slots by shared-memory atomic adds.
-__device__ __forceinline__ void bwd_step(const Params &p, const BwdArgs &b, float *sm, float (&ds)[4][2],
-                                         const float (&sp)[4][2], int t, int64_t tok, int vb) {
-    const int lane = threadIdx.x & 31, lc = 2 * (threadIdx.x >> 5);
+__device__ __forceinline__ void bwd_step(const Params &p, const BwdArgs &b, float *sm, float (&ds)[4][CPW],
+                                         const float (&sp)[4][CPW], int t, int64_t tok, int vb) {
+    const int lane = threadIdx.x & 31, lc = CPW * (threadIdx.x >> 5);
     const float4 a4 = *reinterpret_cast<const float4 *>(sm + SB_A + t * DKB + 4 * lane);
     const float4 k4 = *reinterpret_cast<const float4 *>(sm + SB_K + t * DKB + 4 * lane);
     const float4 q4 = *reinterpret_cast<const float4 *>(sm + SB_Q + t * DKB + 4 * lane);
+    const float4 w4 = *reinterpret_cast<const float4 *>(sm + SB_W + t * CWB + lc);
+    const float4 d4 = *reinterpret_cast<const float4 *>(sm + SB_D + t * CWB + lc);
     const float a[4] = {a4.x, a4.y, a4.z, a4.w}, kk[4] = {k4.x, k4.y, k4.z, k4.w};
     const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
-    const float w[2] = {sm[SB_W + t * CWB + lc], sm[SB_W + t * CWB + lc + 1]};
-    const float dd[2] = {sm[SB_D + t * CWB + lc], sm[SB_D + t * CWB + lc + 1]};
+    const float w[CPW] = {w4.x, w4.y, w4.z, w4.w}, dd[CPW] = {d4.x, d4.y, d4.z, d4.w};
     const float be = sm[SB_BETA + t], sc = p.scale;
     // dq_hat = scale S_t do, S_t = Diag(alpha) S_{t-1} + beta k_hat w^T;  dS += scale q_hat do^T
-    float xq[4], part[2] = {0.f, 0.f};
+    float xq[4], part[CPW] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         float x = 0.f;
+        const float bk = be * kk[i], sq = sc * qq[i];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            x = fmaf(fmaf(a[i], sp[i][j], be * kk[i] * w[j]), dd[j], x);
-            ds[i][j] = fmaf(sc * qq[i], dd[j], ds[i][j]);
+        for (int j = 0; j < CPW; ++j) {
+            x = fmaf(fmaf(a[i], sp[i][j], bk * w[j]), dd[j], x);
+            ds[i][j] = fmaf(sq, dd[j], ds[i][j]);
             part[j] = fmaf(ds[i][j], kk[i], part[j]);
         }
         xq[i] = sc * x;
     }
-    // du = dS^T k_hat (warp sums over the key channels)
-    const float du[2] = {warp_sum(part[0]), warp_sum(part[1])};
-    if (lane == 0) {
-        b.dv[tok * DKB + vb + lc] = be * du[0];
-        b.dv[tok * DKB + vb + lc + 1] = be * du[1];
-        atomicAdd(sm + SB_GB + t, du[0] * w[0] + du[1] * w[1]);
+    // du = dS^T k_hat (sums over the key channels)
+    float du[CPW];
+    col_sums4(part, du);
+    if (lane < CPW) {
+        const float dl = lane == 0 ? du[0] : (lane == 1 ? du[1] : (lane == 2 ? du[2] : du[3]));
+        b.dv[tok * DKB + vb + lc + lane] = be * dl;
     }
-    const float dx[2] = {-be * du[0], -be * du[1]};
+    if (lane == 0)
+        atomicAdd(sm + SB_GB + t, du[0] * w[0] + du[1] * w[1] + du[2] * w[2] + du[3] * w[3]);
+    float dx[CPW];
+#pragma unroll
+    for (int j = 0; j < CPW; ++j) dx[j] = -be * du[j];
     // dk_hat = dS (beta w) + S' dx;  dS' = dS + k_hat dx^T;  dalpha = rowsum(dS' * S_{t-1});
     // dS_{t-1} = Diag(alpha) dS'
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         float y = 0.f, z = 0.f;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < CPW; ++j) {
             y = fmaf(ds[i][j], be * w[j], y);
             y = fmaf(a[i] * sp[i][j], dx[j], y);
             const float dsp = fmaf(kk[i], dx[j], ds[i][j]);
@@ -261,7 +284,7 @@ __global__ void __launch_bounds__(NTB, 2) kda_bwd_state_kernel(Params p, BwdArgs
     float *tokst = b.tok + (size_t)blockIdx.x * CB * kSlice;
     for (int64_t wi = blockIdx.x; wi < work; wi += gridDim.x) {
         const int64_t u = wi / NSL, n = u / p.H, h = u % p.H;
-        const int sl = (int)(wi % NSL), vb = sl * CWB, col = vb + 2 * warp;
+        const int sl = (int)(wi % NSL), vb = sl * CWB, col = vb + CPW * warp;
         int64_t row0, len;
         bwd_span(p, n, row0, len);
         const int nch = (int)((len + CB - 1) / CB);
@@ -272,9 +295,9 @@ __global__ void __launch_bounds__(NTB, 2) kda_bwd_state_kernel(Params p, BwdArgs
         float *gk = sl == 0 ? b.dk : b.pk + (size_t)(sl - 1) * b.prow * DKB;
         float *ga = sl == 0 ? b.dg : b.pa + (size_t)(sl - 1) * b.prow * DKB;
         float *gb = sl == 0 ? b.dbeta : b.pb + (size_t)(sl - 1) * b.prow;
-        float s[4][2];
+        float s[4][CPW];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {   // S[c][v] = init[v][c]
+        for (int j = 0; j < CPW; ++j) {   // S[c][v] = init[v][c]
             float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
             if (p.init) {
                 const size_t off = soff + (size_t)(col + j) * DKB + 4 * lane;
@@ -294,9 +317,9 @@ __global__ void __launch_bounds__(NTB, 2) kda_bwd_state_kernel(Params p, BwdArgs
             for (int t = 0; t < L; ++t) fwd_step(sm, s, t, false);
         }
         // reverse: dS from the final-state gradient, then chunk by chunk
-        float ds[4][2];
+        float ds[4][CPW];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < CPW; ++j) {
             float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
             if (b.dfinal) x = *reinterpret_cast<const float4 *>(b.dfinal + soff + (size_t)(col + j) * DKB + 4 * lane);
             ds[0][j] = x.x; ds[1][j] = x.y; ds[2][j] = x.z; ds[3][j] = x.w;
@@ -313,16 +336,15 @@ __global__ void __launch_bounds__(NTB, 2) kda_bwd_state_kernel(Params p, BwdArgs
                 fwd_step(sm, s, t, true);
             }
             __syncwarp();   // lane 0's w stores are visible to the warp
-            float sp[4][2], spn[4][2];
+            float sp[4][CPW], spn[4][CPW];
             tile_load(tokst + (size_t)(L - 1) * kSlice, sp);
             for (int t = L - 1; t >= 0; --t) {   // this thread's own stores: no fence needed
                 if (t > 0) tile_load(tokst + (size_t)(t - 1) * kSlice, spn);
                 bwd_step(p, b, sm, ds, sp, t, (crow + t) * p.H + h, vb);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    sp[i][0] = spn[i][0];
-                    sp[i][1] = spn[i][1];
-                }
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < CPW; ++j) sp[i][j] = spn[i][j];
             }
             __syncthreads();   // every warp's slot additions are in
             for (int e = tid; e < L * DKB; e += NTB) {
@@ -336,7 +358,7 @@ __global__ void __launch_bounds__(NTB, 2) kda_bwd_state_kernel(Params p, BwdArgs
         }
         if (b.dinit) {   // dinit[v][c] = dS_0[c][v] on the slice's columns
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
+            for (int j = 0; j < CPW; ++j)
                 *reinterpret_cast<float4 *>(b.dinit + soff + (size_t)(col + j) * DKB + 4 * lane) =
                     make_float4(ds[0][j], ds[1][j], ds[2][j], ds[3][j]);
         }
