@@ -15,12 +15,12 @@
 // Every value column v of the state evolves on its own (the per-token vectors alpha,
 // k, beta are shared, the columns never mix), and so does its gradient; only dq, dk,
 // dalpha and dbeta sum over the columns.  So:
-//   kda_bwd_state_kernel: a CTA of 16 warps takes 32 value columns of one (sequence,
+//   kda_bwd_state_kernel: a CTA of 8 warps takes 32 value columns of one (sequence,
 //     head) unit (four CTAs per unit, persistent over units x column slices), a warp
-//     two columns, lane = 4 key channels x 2 columns of the fp32 state in registers.
+//     four columns, lane = 4 key channels x 4 columns of the fp32 state in registers.
 //     The recurrence and its reverse run warp by warp with no CTA barrier per token:
 //     column sums are warp shuffles.  A forward sweep stores the slice's state at the
-//     start of every 32-token chunk; then chunk by chunk in reverse the chunk's states
+//     start of every 16-token chunk; then chunk by chunk in reverse the chunk's states
 //     are recomputed into a per-CTA scratch and the reverse step runs over its tokens.
 //     The slice's shares of dq_hat, dk_hat, dalpha and dbeta go into shared per-token
 //     slots (shared-memory atomic adds over the warps) and, once per chunk, to a
@@ -41,7 +41,7 @@ constexpr int NTB = 256;        // threads of the state kernel: 8 warps
 constexpr int NSL = 4;          // value-column slices per unit (CTAs per unit)
 constexpr int CWB = DKB / NSL;  // 32 columns per CTA, 4 per warp
 constexpr int CPW = 4;          // columns per warp
-constexpr int CB = 32;          // tokens per chunk
+constexpr int CB = 16;          // tokens per chunk (the scratch of all CTAs stays in L2)
 constexpr int kSlice = DKB * CWB;   // floats of one slice of a state
 
 // shared memory of the state kernel (floats)

@@ -185,6 +185,21 @@ def test_more_sequences_than_the_pool_plans():
     print("4100 seqs", pu.check(d, out, fin, ref_out, ref_fin, label="4100 sequences"))
 
 
+def test_the_most_sequences_the_pool_plans():
+    # 4096 sequences, the plan's limit (a full bitonic sort of 4096 keys), lengths from 0 to
+    # 600 with the average above 256 rows, so the pool takes every one of them (empty ones
+    # pass their state through)
+    r = np.random.default_rng(12)
+    lens = [int(x) for x in r.integers(0, 600, 4096)]
+    lens[0], lens[17], lens[4095] = 0, 1, 64
+    d = W.make_inputs(W.get("varlen_ragged", H=1, seqlens=tuple(lens), seed=92))
+    assert d["N"] == 4096 and d["T"] > 256 * d["N"]
+    out, fin = pu.run_gpu(d)
+    ref_out, ref_fin = pu.run_oracle(d)
+    print("4096 seqs", pu.check(d, out, fin, ref_out, ref_fin, label="4096 sequences"))
+    torch.testing.assert_close(fin[0], d["initial_state"][0].to(fin.dtype), rtol=0, atol=0)
+
+
 def test_caller_workspace_entry_point():
     # kda_fwd_ws (the cluster kernel on a caller buffer) matches the oracle, and a buffer
     # full of garbage gives the result of a zeroed one bit for bit
