@@ -386,8 +386,13 @@ def run_ours(args):
     kda.lib()
 
     w = W.get(args.workload)
-    w = W.get(args.workload, seed=shard_seed(w.seed, rank))
-    d_cpu = W.make_inputs(w)
+    if args.split == "heads":   # one problem, its heads split over the ranks (strong scaling)
+        from gated_delta_rule_52_gb300 import shard
+        d_cfg = W.make_inputs(w)
+        d_cpu = shard.shard(d_cfg, rank, ws)
+    else:                       # an independent problem per rank (weak scaling)
+        w = W.get(args.workload, seed=shard_seed(w.seed, rank))
+        d_cpu = d_cfg = W.make_inputs(w)
     e = {key: (val.to(dev) if torch.is_tensor(val) else val) for key, val in d_cpu.items()}
     B, T, H, N = d_cpu["B"], d_cpu["T"], d_cpu["H"], d_cpu["N"]
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -436,7 +441,9 @@ def run_ours(args):
     per_step = [s.elapsed_time(t) for s, t in zip(starts, ends)]
     kernel_ms = sum(per_step)
     times = [max_over_ranks(kernel_ms, dev)]
-    tokens_per_rank = B * T * args.steps
+    # with a head split every rank covers the whole call's tokens for its heads: the job
+    # processes B T tokens (of all H heads) per step
+    tokens_per_rank = B * T * args.steps / (ws if args.split == "heads" else 1)
     value, tmax = aggregate(tokens_per_rank, ws, times)
     ms_per_step = tmax / args.steps
     avg_launch_ms = kernel_ms / args.steps
@@ -548,8 +555,10 @@ def run_ours(args):
     cpu = cpu_baseline(d_cpu) if ws == 1 else None
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": workload_config(w.name, d_cpu),
+            "scaling": "strong" if args.split == "heads" else "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": dict(workload_config(w.name, d_cfg), **({"split": f"heads over {ws} ranks"}
+                                                             if args.split == "heads" else {})),
             "l2": f"algorithmic traffic {abytes / 1e6:.0f} MB per step "
                   f"({'larger' if abytes > 129e6 else 'smaller'} than the 129 MB L2); "
                   "a 256 MB flush write between timed steps",
@@ -702,6 +711,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="prefill_8k")
+    ap.add_argument("--split", choices=["problems", "heads"], default="problems",
+                    help="N > 1: an independent problem per rank (weak), or one problem's heads split")
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
                     help="bwd times kda_bwd (the gradients) instead of the forward")
     args = ap.parse_args(argv)

@@ -163,3 +163,59 @@ def test_gpus_flag_is_checked_against_the_launcher(monkeypatch):
     assert cmd[cmd.index("--master-addr") + 1] == "127.0.0.1"
     assert cmd[-3:] == ["--gpus", "2", "--steps", "3"][-3:]
     assert bench.check_world(argparse.Namespace(gpus=0)) is not None
+
+
+def test_head_ranges_cover_every_head_once():
+    from gated_delta_rule_52_gb300 import shard
+    for H in (1, 2, 5, 64, 67):
+        for world in (1, 2, 3, 8):
+            rs = [shard.head_range(r, world, H) for r in range(world)]
+            assert rs[0][0] == 0 and rs[-1][1] == H
+            assert all(a[1] == b[0] for a, b in zip(rs, rs[1:]))
+            sizes = [h1 - h0 for h0, h1 in rs]
+            assert max(sizes) - min(sizes) <= 1
+    with pytest.raises(ValueError):
+        shard.head_range(2, 2, 4)
+
+
+def _head_split_rank(rank, world, port, out):
+    # one problem, its heads split over the ranks: each rank runs its slice (the oracle
+    # stands in for a GPU here), the slices are gathered and joined
+    import oracle
+    from gated_delta_rule_52_gb300 import shard
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        d = W.make_inputs(W.get("varlen_ragged", H=5, seqlens=(40, 0, 70), seed=61))
+        s = shard.shard(d, rank, world)
+        o, f = oracle.kda_fwd(s["q"], s["k"], s["v"], s["g"], s["beta"], s["scale"], s["A_log"],
+                              s["dt_bias"], s["lower_bound"], initial_state=s["initial_state"],
+                              cu_seqlens=s["cu_seqlens"], nthreads=1)
+        o, f = torch.from_numpy(o), torch.from_numpy(f)
+        outs = [None] * world
+        fins = [None] * world
+        dist.all_gather_object(outs, o)
+        dist.all_gather_object(fins, f)
+        if rank == 0:
+            full_o, full_f = oracle.kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"],
+                                            d["A_log"], d["dt_bias"], d["lower_bound"],
+                                            initial_state=d["initial_state"],
+                                            cu_seqlens=d["cu_seqlens"], nthreads=1)
+            out["same"] = bool(torch.equal(shard.join(outs, "out"), torch.from_numpy(full_o)) and
+                               torch.equal(shard.join(fins, "final_state"), torch.from_numpy(full_f)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_head_split_of_one_problem_gloo_world2():
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_head_split_rank, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(180)
+        assert p.exitcode == 0
+    assert out["same"]   # every (sequence, head) is computed by exactly one rank, exactly
