@@ -319,6 +319,20 @@ def _random_case(i):
                       seqlens=tuple(lens), **common)
 
 
+@pytest.mark.parametrize("i", range(12))
+def test_random_configurations_without_a_lower_bound(i):
+    # the same random shapes with the gate without a lower bound (the pool kernel's
+    # chunked form above 64 rows, the token recurrence below)
+    w = _random_case(100 + i)
+    w = W.Workload(**{**w.__dict__, "lower_bound": None, "name": f"urand{i}"})
+    d = W.make_inputs(w)
+    assert d["lower_bound"] is None
+    want = w.state_dtype is not None
+    out, fin = pu.run_gpu(d, want_final=want)
+    ref_out, ref_fin = pu.run_oracle(d, want_final=want)
+    print(w.name, pu.check(d, out, fin, ref_out, ref_fin, label=w.name))
+
+
 @pytest.mark.parametrize("i", range(18))
 def test_random_configurations(i):
     w = _random_case(i)
