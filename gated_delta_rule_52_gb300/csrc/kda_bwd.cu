@@ -156,7 +156,8 @@ __device__ void bwd_prepare(const Params &p, const BwdArgs &b, float *sm, int64_
     }
 }
 
-// A lane's tile: key channels 4 lane + i (i < 4) of the warp's four value columns j.
+// A lane's tile: key channels lane + 32 i (i < 4) of the warp's four value columns j (a
+// stride of 32 channels, so that the lanes of a warp hit 32 different shared-memory banks).
 // Stored thread-major (four float4 per thread, coalesced) in checkpoints and scratch.
 __device__ __forceinline__ void tile_store(float *dst, const float (&s)[4][CPW]) {
     float4 *d = reinterpret_cast<float4 *>(dst) + threadIdx.x * 4;
@@ -192,10 +193,13 @@ __device__ __forceinline__ void col_sums4(const float (&x)[CPW], float (&out)[CP
 // w = v - S'^T k_hat (into SB_W when store_w); S = S' + beta k_hat w^T.
 __device__ __forceinline__ void fwd_step(float *sm, float (&s)[4][CPW], int t, bool store_w) {
     const int lane = threadIdx.x & 31, lc = CPW * (threadIdx.x >> 5);
-    const float4 a4 = *reinterpret_cast<const float4 *>(sm + SB_A + t * DKB + 4 * lane);
-    const float4 k4 = *reinterpret_cast<const float4 *>(sm + SB_K + t * DKB + 4 * lane);
     const float4 v4 = *reinterpret_cast<const float4 *>(sm + SB_V + t * CWB + lc);
-    const float a[4] = {a4.x, a4.y, a4.z, a4.w}, kk[4] = {k4.x, k4.y, k4.z, k4.w};
+    float a[4], kk[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        a[i] = sm[SB_A + t * DKB + lane + 32 * i];
+        kk[i] = sm[SB_K + t * DKB + lane + 32 * i];
+    }
     float part[CPW] = {0.f, 0.f, 0.f, 0.f}, ks[CPW];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -223,13 +227,15 @@ __device__ __forceinline__ void fwd_step(float *sm, float (&s)[4][CPW], int t, b
 __device__ __forceinline__ void bwd_step(const Params &p, const BwdArgs &b, float *sm, float (&ds)[4][CPW],
                                          const float (&sp)[4][CPW], int t, int64_t tok, int vb) {
     const int lane = threadIdx.x & 31, lc = CPW * (threadIdx.x >> 5);
-    const float4 a4 = *reinterpret_cast<const float4 *>(sm + SB_A + t * DKB + 4 * lane);
-    const float4 k4 = *reinterpret_cast<const float4 *>(sm + SB_K + t * DKB + 4 * lane);
-    const float4 q4 = *reinterpret_cast<const float4 *>(sm + SB_Q + t * DKB + 4 * lane);
     const float4 w4 = *reinterpret_cast<const float4 *>(sm + SB_W + t * CWB + lc);
     const float4 d4 = *reinterpret_cast<const float4 *>(sm + SB_D + t * CWB + lc);
-    const float a[4] = {a4.x, a4.y, a4.z, a4.w}, kk[4] = {k4.x, k4.y, k4.z, k4.w};
-    const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
+    float a[4], kk[4], qq[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        a[i] = sm[SB_A + t * DKB + lane + 32 * i];
+        kk[i] = sm[SB_K + t * DKB + lane + 32 * i];
+        qq[i] = sm[SB_Q + t * DKB + lane + 32 * i];
+    }
     const float w[CPW] = {w4.x, w4.y, w4.z, w4.w}, dd[CPW] = {d4.x, d4.y, d4.z, d4.w};
     const float be = sm[SB_BETA + t], sc = p.scale;
     // dq_hat = scale S_t do, S_t = Diag(alpha) S_{t-1} + beta k_hat w^T;  dS += scale q_hat do^T
@@ -271,9 +277,9 @@ __device__ __forceinline__ void bwd_step(const Params &p, const BwdArgs &b, floa
             z = fmaf(dsp, sp[i][j], z);
             ds[i][j] = a[i] * dsp;
         }
-        atomicAdd(sm + SB_GQ + t * DKB + 4 * lane + i, xq[i]);
-        atomicAdd(sm + SB_GK + t * DKB + 4 * lane + i, y);
-        atomicAdd(sm + SB_GA + t * DKB + 4 * lane + i, z);
+        atomicAdd(sm + SB_GQ + t * DKB + lane + 32 * i, xq[i]);
+        atomicAdd(sm + SB_GK + t * DKB + lane + 32 * i, y);
+        atomicAdd(sm + SB_GA + t * DKB + lane + 32 * i, z);
     }
 }
 
@@ -297,16 +303,15 @@ __global__ void __launch_bounds__(NTB, 2) kda_bwd_state_kernel(Params p, BwdArgs
         float *gb = sl == 0 ? b.dbeta : b.pb + (size_t)(sl - 1) * b.prow;
         float s[4][CPW];
 #pragma unroll
-        for (int j = 0; j < CPW; ++j) {   // S[c][v] = init[v][c]
-            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (p.init) {
-                const size_t off = soff + (size_t)(col + j) * DKB + 4 * lane;
-                x = p.state_type == kStateBF16
-                        ? bf16x4_to_f4(*reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(p.init) + off))
-                        : *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(p.init) + off);
+        for (int j = 0; j < CPW; ++j)   // S[c][v] = init[v][c]
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const size_t off = soff + (size_t)(col + j) * DKB + lane + 32 * i;
+                s[i][j] = !p.init ? 0.f
+                          : p.state_type == kStateBF16
+                              ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p.init)[off])
+                              : reinterpret_cast<const float *>(p.init)[off];
             }
-            s[0][j] = x.x; s[1][j] = x.y; s[2][j] = x.z; s[3][j] = x.w;
-        }
         // forward sweep: the slice's state at the start of every chunk
         for (int ci = 0; ci < nch; ++ci) {
             const int L = (int)(len - (int64_t)ci * CB < CB ? len - (int64_t)ci * CB : CB);
@@ -319,11 +324,10 @@ __global__ void __launch_bounds__(NTB, 2) kda_bwd_state_kernel(Params p, BwdArgs
         // reverse: dS from the final-state gradient, then chunk by chunk
         float ds[4][CPW];
 #pragma unroll
-        for (int j = 0; j < CPW; ++j) {
-            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (b.dfinal) x = *reinterpret_cast<const float4 *>(b.dfinal + soff + (size_t)(col + j) * DKB + 4 * lane);
-            ds[0][j] = x.x; ds[1][j] = x.y; ds[2][j] = x.z; ds[3][j] = x.w;
-        }
+        for (int j = 0; j < CPW; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                ds[i][j] = b.dfinal ? b.dfinal[soff + (size_t)(col + j) * DKB + lane + 32 * i] : 0.f;
         for (int ci = nch - 1; ci >= 0; --ci) {
             const int L = (int)(len - (int64_t)ci * CB < CB ? len - (int64_t)ci * CB : CB);
             const int64_t crow = row0 + (int64_t)ci * CB;
@@ -359,8 +363,8 @@ __global__ void __launch_bounds__(NTB, 2) kda_bwd_state_kernel(Params p, BwdArgs
         if (b.dinit) {   // dinit[v][c] = dS_0[c][v] on the slice's columns
 #pragma unroll
             for (int j = 0; j < CPW; ++j)
-                *reinterpret_cast<float4 *>(b.dinit + soff + (size_t)(col + j) * DKB + 4 * lane) =
-                    make_float4(ds[0][j], ds[1][j], ds[2][j], ds[3][j]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) b.dinit[soff + (size_t)(col + j) * DKB + lane + 32 * i] = ds[i][j];
         }
     }
 }
