@@ -41,6 +41,11 @@ struct Params {
     int unbounded;      // the gate without a lower bound (lower_bound unused); pool kernel only
     int mixed;          // varlen call split by length: the short-step kernel takes the
                         // sequences of at most kShortMaxT tokens, the chunked kernel the rest
+    // Pool kernel, varlen state-only runs (out == nullptr, bounded gate): a second state
+    // carried beside the first over the same packets, with values of zero (U = -W S),
+    // from init2 to fin2 (fp32, [N][H][V][K]); fin2 == nullptr: no second state
+    const float *init2;
+    float *fin2;
 };
 
 // Token range of sequence n: packed batch row `b`, first token `t0`, `len` tokens.

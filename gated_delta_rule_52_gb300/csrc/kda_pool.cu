@@ -88,6 +88,14 @@ constexpr uint32_t C_PK = 98304;       // 2 packet slots
 constexpr uint32_t C_PKSLOT = 65536;
 constexpr uint32_t PK_KB = 0, PK_QG = 16384, PK_KG = 32768, PK_TP = 49152, PK_MM = 57344;
 constexpr uint32_t C_END = C_PK + 2 * C_PKSLOT;
+// chain with a second state (state-only runs): no O, so no Q_hat*Gamma or M in a packet;
+// the second state's S^T and U^T copies take their place
+constexpr uint32_t C2_SHP = 98304;      // second S^T fp16: 2 x [128 c][64 v]
+constexpr uint32_t C2_UHP = 131072;     // second U^T fp16: [128 v][64 t]
+constexpr uint32_t C2_PK = 147456;      // 2 packet slots: Kbar, K_hat*Gamma, T'
+constexpr uint32_t C2_PKSLOT = 40960;
+constexpr uint32_t P2_KB = 0, P2_KG = 16384, P2_TP = 32768;
+static_assert(C2_PK + 2 * C2_PKSLOT <= C_END, "second-state chain layout");
 constexpr uint32_t F_END = F_TF + 64 * LDA * 4;
 
 // Rows of the decay-factor table of one chunk (per 16-token block b and channel c), with
@@ -125,6 +133,7 @@ struct ChainSmall {
     // waiter could otherwise fall two phases behind
     uint64_t full_e[2], full_l[2], vfull[2], vconv[2], u_done[2], o_done[2];
     uint64_t w_done, s_done, o_free, sh_ready, s_scaled, uh_ready, wt_ready, fin;
+    uint64_t up_done;    // G3u of the second state (runs with a second state only)
     int abort;
 };
 constexpr uint32_t F_SMALL = F_END;
@@ -984,13 +993,22 @@ __device__ __forceinline__ void pool_front(const TmaMaps &maps, const Params &p,
 // its fp16 operand copy, decay by the next Gamma_C, initial and final state) and the
 // conversion of the next V to fp16, 8-11 the U and -W^T readouts, 12 the loader (ring
 // packets, V), 13 the MMA issuer, 14-15 the O readout (token rows, 16-byte stores).
-template <bool VL>
+// With a second state (DUAL; state-only runs of the sequence-parallel path) there is no
+// O: G3o, G5 and the O readout drop out, and a second state S_2 with values of zero runs
+// beside S on the same packets (G3u: U_2^T = S_2^T (-W^T); G4: S_2 += Kbar^T U_2), its
+// accumulators in the O columns and its operand copies in the shared memory that the
+// packets' Q_hat*Gamma and M parts leave free.
+template <bool VL, bool DUAL>
 __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p, const PoolArgs &a,
                                            unsigned char *smem, ChainSmall &cs, uint32_t tmem, int c) {
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3;
+    // TMEM columns: S, W^T, two U^T buffers, then O, or (second state) S_2 and U_2^T
     const uint32_t D_S = tmem, D_W = tmem + 128, D_U0 = tmem + 192, D_O = tmem + 320;
+    const uint32_t D_S2 = tmem + 320, D_U2 = tmem + 448;
+    constexpr uint32_t O_PK = DUAL ? C2_PK : C_PK, O_SLOT = DUAL ? C2_PKSLOT : C_PKSLOT;
+    constexpr uint32_t O_KB = DUAL ? P2_KB : PK_KB, O_KG = DUAL ? P2_KG : PK_KG, O_TP = DUAL ? P2_TP : PK_TP;
     const int nchunks = a.nchunks;
     const int64_t units = p.n_seqs * p.H;
     const int64_t nunits = VL ? 0 : (units - c + a.nc - 1) / a.nc;
@@ -999,7 +1017,7 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
     auto pk_row = [&](int64_t j) {   // first token row of packet j in the [B*T] token rows
         return (pk_unit(j) / p.H) * p.T + (j % nchunks) * (int64_t)C;
     };
-    auto pk_slot = [&](int64_t j) { return sbase + C_PK + (uint32_t)(j & 1) * C_PKSLOT; };
+    auto pk_slot = [&](int64_t j) { return sbase + O_PK + (uint32_t)(j & 1) * O_SLOT; };
     auto par2 = [](int64_t j) { return (uint32_t)((j >> 1) & 1); };   // phase of a [j & 1] barrier
     auto par1 = [](int64_t j) { return (uint32_t)(j & 1); };          // phase of a per-packet barrier
     // bounded wait that also gives up once another role has aborted
@@ -1043,8 +1061,8 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
                         const unsigned char *slot = a.slot(c, je);
                         const uint32_t dst = pk_slot(je), fb = smem_u32(&cs.full_e[je & 1]);
                         mbar_arrive_expect_tx(&cs.full_e[je & 1], 16384 + 8192);
-                        bulk_load(dst + PK_KG, slot + RS_KG, 16384, fb);
-                        bulk_load(dst + PK_TP, slot + RS_TP, 8192, fb);
+                        bulk_load(dst + O_KG, slot + RS_KG, 16384, fb);
+                        bulk_load(dst + O_TP, slot + RS_TP, 8192, fb);
                         ++je;
                         ready_je = false;
                         progress = true;
@@ -1053,10 +1071,15 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
                 if (jl < je && (jl < 2 || mbar_try_wait(&cs.o_done[jl & 1], par2(jl - 2)))) {
                     const unsigned char *slot = a.slot(c, jl);
                     const uint32_t dst = pk_slot(jl), fb = smem_u32(&cs.full_l[jl & 1]);
-                    mbar_arrive_expect_tx(&cs.full_l[jl & 1], 16384 * 2 + 8192 + 512);
-                    bulk_load(dst + PK_KB, slot + RS_KB, 16384, fb);
-                    bulk_load(dst + PK_QG, slot + RS_QG, 16384, fb);
-                    bulk_load(dst + PK_MM, slot + RS_MM, 8192, fb);
+                    if constexpr (DUAL) {   // no O: Kbar and exp(G_C) only
+                        mbar_arrive_expect_tx(&cs.full_l[jl & 1], 16384 + 512);
+                        bulk_load(dst + O_KB, slot + RS_KB, 16384, fb);
+                    } else {
+                        mbar_arrive_expect_tx(&cs.full_l[jl & 1], 16384 * 2 + 8192 + 512);
+                        bulk_load(dst + PK_KB, slot + RS_KB, 16384, fb);
+                        bulk_load(dst + PK_QG, slot + RS_QG, 16384, fb);
+                        bulk_load(dst + PK_MM, slot + RS_MM, 8192, fb);
+                    }
                     bulk_load(smem_u32(&cs.gamC[jl & 1][0]), slot + RS_GC, 512, fb);
                     ++jl;
                     progress = true;
@@ -1096,17 +1119,19 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
             const uint64_t dSH = sdesc_sw128(sbase + C_SH, 16384, 1024);    // S^T, A MN-major
             const uint64_t dWT = sdesc_sw128(sbase + C_WT, 16384, 1024);    // -W^T, B MN-major
             const uint64_t dUH = sdesc_sw128(sbase + C_UH, 16, 1024);       // U^T as A / U as B, K-major
+            const uint64_t dSH2 = sdesc_sw128(sbase + C2_SHP, 16384, 1024);  // second state's S^T
+            const uint64_t dUH2 = sdesc_sw128(sbase + C2_UHP, 16, 1024);     // second state's U
             auto issue_g2w = [&](int64_t jn) {   // G2w of packet jn
                 const uint32_t pk = pk_slot(jn);
-                const uint64_t dKG = sdesc_sw128(pk + PK_KG, 8192, 1024);
-                const uint64_t dTP = sdesc_sw128(pk + PK_TP, 16, 1024);
+                const uint64_t dKG = sdesc_sw128(pk + O_KG, 8192, 1024);
+                const uint64_t dTP = sdesc_sw128(pk + O_TP, 16, 1024);
                 tc_fence_after();
                 for (int ks = 0; ks < C / 16; ++ks)
                     mma_bf16(D_W, dKG + (uint64_t)(ks * 128), dTP + (uint64_t)(ks * 2), id_n64_mk, ks > 0);
                 mma_commit(&cs.w_done);
             };
             auto issue_g2u = [&](int64_t jn) {   // G2u of packet jn, once its V is fp16
-                const uint64_t dTP = sdesc_sw128(pk_slot(jn) + PK_TP, 16, 1024);
+                const uint64_t dTP = sdesc_sw128(pk_slot(jn) + O_TP, 16, 1024);
                 const uint64_t dV = sdesc_sw128(sbase + C_V + (uint32_t)(jn & 1) * 16384, 8192, 1024);
                 if (!wait(&cs.vconv[jn & 1], par2(jn))) return false;
                 tc_fence_after();
@@ -1130,6 +1155,30 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
                 for (int ks = 0; ks < DK / 16; ++ks)
                     mma_bf16(du, dSH + (uint64_t)(ks * 128), dWT + (uint64_t)(ks * 128), id_n64_mm, true);
                 mma_commit(&cs.u_done[sj]);
+                if constexpr (DUAL) {
+                    // the second state, values of zero: U_2^T = S_2^T (-W^T)
+                    for (int ks = 0; ks < DK / 16; ++ks)
+                        mma_bf16(D_U2, dSH2 + (uint64_t)(ks * 128), dWT + (uint64_t)(ks * 128), id_n64_mm, ks > 0);
+                    mma_commit(&cs.up_done);
+                    // G4 on both states: S += Kbar^T U
+                    if (!wait(&cs.full_l[sj], par2(j)) || !wait(&cs.uh_ready, par1(j)) ||
+                        !wait(&cs.s_scaled, par1(j)))
+                        return;
+                    tc_fence_after();
+                    const uint64_t dKB = sdesc_sw128(pk + O_KB, 8192, 1024);
+                    for (int ks = 0; ks < C / 16; ++ks)
+                        mma_bf16(D_S, dKB + (uint64_t)(ks * 128), dUH + (uint64_t)(ks * 2), id_n128_mk, true);
+                    for (int ks = 0; ks < C / 16; ++ks)
+                        mma_bf16(D_S2, dKB + (uint64_t)(ks * 128), dUH2 + (uint64_t)(ks * 2), id_n128_mk, true);
+                    mma_commit(&cs.s_done);
+                    mma_commit(&cs.o_done[sj]);   // the packet's late part is consumed
+                    if (j + 1 < npk) {
+                        if (!wait(&cs.full_e[sj ^ 1], par2(j + 1))) return;
+                        issue_g2w(j + 1);
+                        if (!issue_g2u(j + 1)) return;
+                    }
+                    continue;
+                }
                 // G3o: O = (Q_hat Gamma) S into lanes 64-127 (the A operand starts 64 rows
                 // before Q_hat Gamma; rows 0-63 of O are unused), right behind G3u, so that
                 // the S copy is free again when G4 completes
@@ -1177,6 +1226,7 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
 
     if (warp >= 14) {
         // ------------------------------------------------ O readout: token rows (TMEM lanes 64-127)
+        if constexpr (DUAL) return;   // state-only: no O
         const int t = (quarter - 2) * 32 + lane;   // token of the chunk
         PkWalkV ow;   // varlen: this packet's unit
         if (VL) ow.start(p, a, c);
@@ -1321,6 +1371,13 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
                 read64(D_U0 + (uint32_t)sj * 64, r);
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) st_pack16<true>(sbase + C_UH, lv, 16 * jj, r[jj], rbad);
+                if constexpr (DUAL) {   // and the second state's
+                    if (!wait(&cs.up_done, par1(j))) return;
+                    tc_fence_after();
+                    read64(D_U2, r);
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) st_pack16<true>(sbase + C2_UHP, lv, 16 * jj, r[jj], rbad);
+                }
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -1339,9 +1396,9 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
     // ------------------------------------------------ state warps 0-7 (lane quarter, column half)
     const int half = warp >> 2;
     const int cc = quarter * 32 + lane;   // key channel (TMEM lane of D_S)
-    auto ld_s = [&](float (&r)[4][16]) {
+    auto ld_s = [&](float (&r)[4][16], uint32_t col) {   // this warp's part of S (col D_S) or S_2
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) tmem_ld16(tmem_addr(D_S, quarter * 32, 64 * half + 16 * jj), r[jj]);
+        for (int jj = 0; jj < 4; ++jj) tmem_ld16(tmem_addr(col, quarter * 32, 64 * half + 16 * jj), r[jj]);
         tmem_ld_wait();
     };
     bool rbad = false;   // a state value beyond the fp16 range of its operand copy
@@ -1363,6 +1420,12 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
                     const uint4 *src = p.init ? reinterpret_cast<const uint4 *>(p.init) + b16 : nullptr;
                     for (int64_t e = tid; e < n16; e += 256) dst[e] = src ? src[e] : make_uint4(0u, 0u, 0u, 0u);
                 }
+                if (DUAL && p.fin2) {   // the second state (fp32) likewise
+                    const int64_t n16 = (int64_t)DK * DK * 4 / 16, b16 = u.sbase * 4 / 16;
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.fin2) + b16;
+                    const uint4 *src = p.init2 ? reinterpret_cast<const uint4 *>(p.init2) + b16 : nullptr;
+                    for (int64_t e = tid; e < n16; e += 256) dst[e] = src ? src[e] : make_uint4(0u, 0u, 0u, 0u);
+                }
                 continue;
             }
             state_base = (size_t)u.sbase;
@@ -1374,38 +1437,59 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
             state_base = (size_t)(n * p.H + h) * DK * DK;
             nch = nchunks;
         }
+        // the unit's initial states (the previous unit's final states are out of TMEM)
+        auto ld_init = [&](float (&r)[4][16], bool second) {
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const size_t off = state_base + (size_t)(64 * half + 16 * jj + e) * DK + cc;
+                    float x = 0.f;
+                    if (second) {
+                        if (p.init2) x = p.init2[off];
+                    } else if (p.init) {
+                        x = p.state_type == kStateBF16
+                                ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p.init)[off])
+                                : reinterpret_cast<const float *>(p.init)[off];
+                    }
+                    r[jj][e] = x;
+                }
+        };
         for (int m = 0; m < nch; ++m, ++j) {
             const int sj = (int)(j & 1);
             float r[4][16];
             if (m == 0) {
-                // the unit's initial state (the previous unit's final state is out of D_S)
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        float x = 0.f;
-                        if (p.init) {
-                            const size_t off = state_base + (size_t)(64 * half + 16 * jj + e) * DK + cc;
-                            x = p.state_type == kStateBF16
-                                    ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p.init)[off])
-                                    : reinterpret_cast<const float *>(p.init)[off];
-                        }
-                        r[jj][e] = x;
-                    }
+                ld_init(r, false);
             } else {
                 if (!wait(&cs.s_done, par1(j - 1))) return;
                 tc_fence_after();
-                ld_s(r);
+                ld_s(r, D_S);
             }
             // the S^T operand of this chunk (G3o of the previous one, which read the last
             // copy, completed before G4 did)
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) st_pack16<true>(sbase + C_SH + half * 16384, cc, 16 * jj, r[jj], rbad);
+            if constexpr (DUAL) {   // and the second state's (r then holds S_2)
+                if (m == 0) ld_init(r, true);
+                else ld_s(r, D_S2);
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) st_pack16<true>(sbase + C2_SHP + half * 16384, cc, 16 * jj, r[jj], rbad);
+            }
             fence_proxy_async_smem();
             warp_arrive(&cs.sh_ready);
             // D_S = Diag(Gamma_C) S, the decayed state G4 accumulates onto
             if (!wait(&cs.full_l[sj], par2(j))) return;
             const float g = cs.gamC[sj][cc];
+            if constexpr (DUAL) {
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) r[jj][e] *= g;
+                    tmem_st16(tmem_addr(D_S2, quarter * 32, 64 * half + 16 * jj), r[jj]);
+                }
+                if (m == 0) ld_init(r, false);   // the first state again
+                else ld_s(r, D_S);
+            }
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
 #pragma unroll
@@ -1421,7 +1505,7 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
         tc_fence_after();
         if (p.fin) {
             float r[4][16];
-            ld_s(r);
+            ld_s(r, D_S);
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
@@ -1433,12 +1517,21 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
                         reinterpret_cast<float *>(p.fin)[off] = r[jj][e];
                 }
         }
+        if (DUAL && p.fin2) {
+            float r[4][16];
+            ld_s(r, D_S2);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    p.fin2[state_base + (size_t)(64 * half + 16 * jj + e) * DK + cc] = r[jj][e];
+        }
         tc_fence_before();
     }
     flag_range(p, rbad);
 }
 
-template <bool VL, bool UB>
+template <bool VL, bool UB, bool DUAL>
 __global__ void __launch_bounds__(NT, 1)
 kda_pool_kernel(const __grid_constant__ TmaMaps maps, Params p, PoolArgs a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -1469,6 +1562,7 @@ kda_pool_kernel(const __grid_constant__ TmaMaps maps, Params p, PoolArgs a) {
             mbar_init(&cs.uh_ready, 4);
             mbar_init(&cs.wt_ready, 4);
             mbar_init(&cs.fin, 1);
+            mbar_init(&cs.up_done, 1);
             cs.abort = 0;
         } else {
             for (int i = 0; i < 2; ++i) {
@@ -1494,7 +1588,7 @@ kda_pool_kernel(const __grid_constant__ TmaMaps maps, Params p, PoolArgs a) {
     const uint32_t tmem = *tmem_base;
 
     if (chain)
-        pool_chain<VL>(maps, p, a, smem, cs, tmem, cta);
+        pool_chain<VL, DUAL>(maps, p, a, smem, cs, tmem, cta);
     else
         pool_front<VL, UB>(maps, p, a, smem, fs, tmem, cta - a.nc);
 
@@ -1669,6 +1763,8 @@ cudaError_t launch_pool(const Params &p, int sms, cudaStream_t stream) {
     const int64_t nchunks = vl ? 0 : (p.T + C - 1) / C;
     if (nf < 1 || (!vl && nchunks < 1)) return cudaErrorInvalidValue;
     if (vl && !pool_takes(p, sms)) return cudaErrorInvalidValue;
+    // a second state: varlen, bounded gate, state-only
+    if (p.fin2 && (!vl || p.unbounded || p.out)) return cudaErrorInvalidValue;
     const PoolLayout l = pool_layout(p.n_seqs, p.H, p.T, vl, sms);
     PoolArgs a = {};
     a.nc = (int)nc;
@@ -1692,13 +1788,15 @@ cudaError_t launch_pool(const Params &p, int sms, cudaStream_t stream) {
     static std::atomic<bool> attr_done[kMaxDevices];
     cudaError_t e = once_per_device(attr_done, [](int) {
         const int sb = (int)SMEM_BYTES;
-        cudaError_t r = cudaFuncSetAttribute(kda_pool_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sb);
+        cudaError_t r = cudaFuncSetAttribute(kda_pool_kernel<false, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sb);
         if (r == cudaSuccess)
-            r = cudaFuncSetAttribute(kda_pool_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sb);
+            r = cudaFuncSetAttribute(kda_pool_kernel<true, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sb);
         if (r == cudaSuccess)
-            r = cudaFuncSetAttribute(kda_pool_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sb);
+            r = cudaFuncSetAttribute(kda_pool_kernel<false, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sb);
         if (r == cudaSuccess)
-            r = cudaFuncSetAttribute(kda_pool_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sb);
+            r = cudaFuncSetAttribute(kda_pool_kernel<true, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sb);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(kda_pool_kernel<true, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sb);
         return r;
     });
     if (e != cudaSuccess) return e;
@@ -1725,12 +1823,14 @@ cudaError_t launch_pool(const Params &p, int sms, cudaStream_t stream) {
     // the flags of this call start at zero (no packet index + 1 is zero)
     e = cudaMemsetAsync(a.flags, 0, (size_t)nc * 2 * a.depth * sizeof(unsigned long long), stream);
     if (e != cudaSuccess) return e;
-    if (p.unbounded)
-        e = vl ? cudaLaunchKernelEx(&cfg, kda_pool_kernel<true, true>, maps, p, a)
-               : cudaLaunchKernelEx(&cfg, kda_pool_kernel<false, true>, maps, p, a);
+    if (p.fin2)
+        e = cudaLaunchKernelEx(&cfg, kda_pool_kernel<true, false, true>, maps, p, a);
+    else if (p.unbounded)
+        e = vl ? cudaLaunchKernelEx(&cfg, kda_pool_kernel<true, true, false>, maps, p, a)
+               : cudaLaunchKernelEx(&cfg, kda_pool_kernel<false, true, false>, maps, p, a);
     else
-        e = vl ? cudaLaunchKernelEx(&cfg, kda_pool_kernel<true, false>, maps, p, a)
-               : cudaLaunchKernelEx(&cfg, kda_pool_kernel<false, false>, maps, p, a);
+        e = vl ? cudaLaunchKernelEx(&cfg, kda_pool_kernel<true, false, false>, maps, p, a)
+               : cudaLaunchKernelEx(&cfg, kda_pool_kernel<false, false, false>, maps, p, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

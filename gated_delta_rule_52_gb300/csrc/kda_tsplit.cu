@@ -5,16 +5,16 @@
 // with R the state reached from S_in = 0 (the chunk equations of the tensor-core
 // path: U = T'V - W S_in, S_out = Diag(Gamma_C) S_in + Kbar^T U).  So a sequence
 // cut into segments runs as:
-//   1. every segment from S = 0 (segment 0 from the call's initial state): R_s;
-//   2. every segment with v = 0 from S = I: the transition P_s (the same kernel, the
-//      identity as the initial state and zero values);
+//   1. every segment from S = 0 (segment 0 from the call's initial state): R_s; and
+//   2. beside it, over the same chunk packets, every segment with v = 0 from S = I:
+//      the transition P_s (the pool kernel's second state, one run for both);
 //   3. a scan over the segments: S_in(0) = S_0, S_in(s) = P_{s-1} S_in(s-1) + R_{s-1};
 //   4. every segment from S_in(s), writing the outputs (and, for the last segment,
 //      the final state).
-// Steps 1, 2 and 4 are the persistent pool kernel over the segments as independent
+// Steps 1-2 and 4 are the persistent pool kernel over the segments as independent
 // packed sequences (segment boundaries as cu_seqlens, so each run plans its units
-// first); 1 and 2 write no outputs.  With P segments per sequence each of those runs
-// has P times the parallelism of the plain call, at three times its work.
+// first); 1-2 writes no outputs.  With P segments per sequence each of those runs has
+// P times the parallelism of the plain call; the chunk work (the fronts) is done twice.
 #include <cuda_bf16.h>
 
 #include "kda_internal.h"
@@ -171,16 +171,17 @@ cudaError_t launch_tsplit(const Params &p, int64_t P, int sms, unsigned char *sc
     q.state_type = kStateFP32;
     q.mixed = 0;   // every segment on the pool
     q.ws = ws;
-    // 1. R_s from S = 0 (segment 0 from the call's initial state); no outputs
+    // 1 and 2 in one state-only run over the same packets: R_s from S = 0 (segment 0
+    // from the call's initial state), and beside it the transition P_s from S = I with
+    // values of zero
     q.init = sin;
     q.fin = R;
     q.out = nullptr;
+    q.init2 = fin3;
+    q.fin2 = Pst;
     if ((e = launch_pool(q, sms, stream)) != cudaSuccess) return e;
-    // 2. the transitions P_s: zero values from S = I; no outputs
-    q.v = nullptr;
-    q.init = fin3;
-    q.fin = Pst;
-    if ((e = launch_pool(q, sms, stream)) != cudaSuccess) return e;
+    q.init2 = nullptr;
+    q.fin2 = nullptr;
     // 3. the scan
     const int scan_smem = (int)((kState + (int64_t)kScanRows * kZs) * 4);
     static std::atomic<bool> attr_done[kMaxDevices];
@@ -191,7 +192,6 @@ cudaError_t launch_tsplit(const Params &p, int64_t P, int sms, unsigned char *sc
     seg_scan_kernel<<<dim3((unsigned)(N * H), DK / kScanRows), 256, scan_smem, stream>>>(sin, R, Pst, P, H);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // 4. every segment from its entering state, with outputs
-    q.v = p.v;
     q.init = sin;
     q.fin = fin3;
     q.out = p.out;
