@@ -105,7 +105,7 @@ typedef enum {
  * (cu_seqlens == NULL) whose N * H (sequence, head) units would leave most of the
  * GPU idle, with T >= 8192, runs the sequence-parallel path: each sequence is cut
  * into P >= 4 segments of at least 2048 tokens, whose affine state maps are joined
- * by a scan (same results within the stated tolerances, three times the work on P
+ * by a scan (same results within the stated tolerances, twice the chunk work on P
  * times the parallelism); its scratch, also from the pool, is about
  * N * H * P * (4 * 64 KB + KDA_WORKSPACE_BYTES_PER_UNIT) bytes.
  * kda_fwd_ws is the same call with a caller-provided workspace; for more than 64
