@@ -62,13 +62,13 @@ __global__ void seg_init_kernel(float *r0, float *id, const void *init, int stat
 
 // The scan of step 3: sin[s] = sin[s-1] x Pst[s-1] + R[s-1] in the stored (transposed)
 // layout, sin[0] given; fp32 on paired FMAs.  The rows of the product are independent,
-// so grid (sequence states, 8): block y carries rows 16 y .. 16 y + 15 through every
-// step, reading each transition (L2-resident) whole.  256 threads, thread (tr, tc) =
-// row 16 y + tr, columns 2 tc + 32 c + (0, 1), c = 0..3.  The block's rows sit in
-// shared memory padded to 129 floats (reads are broadcasts), the transition unpadded
-// (reads are 16 consecutive float pairs of a half-warp).
+// so grid (sequence states, 32): block y carries rows 4 y .. 4 y + 3 through every step,
+// reading each transition (L2-resident) whole into shared memory.  256 threads, thread
+// (tr, tc) = row 4 y + tr, columns 2 tc and 2 tc + 1.  The block's rows sit in shared
+// memory padded to 129 floats (a warp shares its row: reads are broadcasts), the
+// transition unpadded (a warp reads 32 consecutive float pairs).
 constexpr int kZs = DK + 1;
-constexpr int kScanRows = 16;
+constexpr int kScanRows = 4;
 __global__ void __launch_bounds__(256) seg_scan_kernel(float *sin, const float *R, const float *Pst,
                                                        int64_t P, int64_t H) {
     extern __shared__ __align__(16) float scan_sm[];
@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(256) seg_scan_kernel(float *sin, const float *
     float *zs = scan_sm + kState;        // [tr][j]: this block's rows of the entering state
     const int64_t b = blockIdx.x / H, h = blockIdx.x % H;
     const int rb = (int)blockIdx.y * kScanRows;
-    const int tid = threadIdx.x, tr = tid >> 4, tc = tid & 15;
+    const int tid = threadIdx.x, tr = tid >> 6, tc = tid & 63;
     auto slot = [&](int64_t s) { return ((b * P + s) * H + h) * kState; };
     const float *z0 = sin + slot(0) + (int64_t)rb * DK;
     for (int i = tid; i < kScanRows * DK; i += 256) zs[(i / DK) * kZs + i % DK] = z0[i];
@@ -85,29 +85,18 @@ __global__ void __launch_bounds__(256) seg_scan_kernel(float *sin, const float *
         for (int i = tid * 4; i < kState; i += 1024)
             *reinterpret_cast<float4 *>(pm + i) = *reinterpret_cast<const float4 *>(ps + i);
         __syncthreads();
-        float2 acc[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[c] = make_float2(0.f, 0.f);
-#pragma unroll 8
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll 16
         for (int j = 0; j < DK; ++j) {
             const float z = zs[tr * kZs + j];
-            const float2 z2 = make_float2(z, z);
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                acc[c] = sm103::fma2(z2, *reinterpret_cast<const float2 *>(pm + j * DK + 2 * tc + 32 * c), acc[c]);
+            acc = sm103::fma2(make_float2(z, z), *reinterpret_cast<const float2 *>(pm + j * DK + 2 * tc), acc);
         }
         __syncthreads();   // every thread is done with zs and pm
-        const int v = rb + tr;
-        const float *rs = R + slot(s - 1) + (int64_t)v * DK;
-        float *out = sin + slot(s) + (int64_t)v * DK;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int k = 2 * tc + 32 * c;
-            const float2 x = sm103::add2(acc[c], *reinterpret_cast<const float2 *>(rs + k));
-            *reinterpret_cast<float2 *>(out + k) = x;
-            zs[tr * kZs + k] = x.x;
-            zs[tr * kZs + k + 1] = x.y;
-        }
+        const int v = rb + tr, k = 2 * tc;
+        const float2 x = sm103::add2(acc, *reinterpret_cast<const float2 *>(R + slot(s - 1) + (int64_t)v * DK + k));
+        *reinterpret_cast<float2 *>(sin + slot(s) + (int64_t)v * DK + k) = x;
+        zs[tr * kZs + k] = x.x;
+        zs[tr * kZs + k + 1] = x.y;
     }
 }
 
