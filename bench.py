@@ -163,7 +163,10 @@ TSPLIT_MIN_SEG, TSPLIT_MAX_SEG = 2048, 32
 def tsplit_segments(N: int, T: int, H: int, varlen: bool, sms: int) -> int:
     if varlen or N <= 0 or T < 4 * TSPLIT_MIN_SEG or N * H <= 0:
         return 0
-    P = min((sms // 2) // (N * H), T // TSPLIT_MIN_SEG, TSPLIT_MAX_SEG)
+    P = (sms * 7 // 16) // (N * H)
+    if P < 4 and (sms // 2) // (N * H) >= 4:
+        P = 4
+    P = min(P, T // TSPLIT_MIN_SEG, TSPLIT_MAX_SEG)
     return P if P >= 4 else 0
 
 

@@ -106,7 +106,10 @@ def test_kernel_of_follows_the_packed_token_count():
 def test_tsplit_rule_mirror():
     # the few-units rule of kda_fwd's sequence-parallel path, as bench.py mirrors it
     import bench
-    assert bench.tsplit_segments(1, 65536, 8, False, 152) == 9      # 76 clusters / 8 units
+    assert bench.tsplit_segments(1, 65536, 8, False, 152) == 8      # 66 chains (7/16 of 152) / 8 units
+    assert bench.tsplit_segments(1, 65536, 16, False, 152) == 4
+    assert bench.tsplit_segments(1, 65536, 19, False, 152) == 4     # 4 segments up to 152 / 8 units
+    assert bench.tsplit_segments(1, 65536, 20, False, 152) == 0
     assert bench.tsplit_segments(1, 8192, 64, False, 152) == 0      # the headline: units fill the GPU
     assert bench.tsplit_segments(1, 8192, 2, False, 152) == 4       # capped by 2048-token segments
     assert bench.tsplit_segments(1, 65536, 1, False, 152) == 32     # capped at 32 segments
