@@ -1702,12 +1702,25 @@ pool_plan_kernel(Params p, PoolArgs a, int *order, int *chain_len, int *counts, 
 }  // namespace
 
 int64_t pool_chains(int64_t units, int sms) {
-    // At most half the SMs run chains; the units are spread evenly over the fewest
-    // waves that this allows.
+    // A chain runs its units one after another, about 7K cycles per chunk; the fronts
+    // take every chunk of every unit, about 9.5K cycles each, on the SMs the chains
+    // leave.  In units of one unit's chunk count the run takes about
+    //   max(ceil(units / nc) * 7, units * 9.5 / (sms - nc)),
+    // and nc (at most half the SMs) minimises it; on a tie, the fewer chains.
     int64_t cap = sms / 2;
-    if (cap < 1) cap = 1;
-    const int64_t waves = (units + cap - 1) / cap;
-    return (units + waves - 1) / waves;
+    if (cap > units) cap = units;
+    if (cap < 1) return 1;
+    int64_t best = 1;
+    double best_t = 0.0;
+    for (int64_t nc = 1; nc <= cap; ++nc) {
+        const double tc = (double)((units + nc - 1) / nc) * 14.0, tf = (double)units * 19.0 / (double)(sms - nc);
+        const double t = tc > tf ? tc : tf;
+        if (nc == 1 || t < best_t) {
+            best = nc;
+            best_t = t;
+        }
+    }
+    return best;
 }
 
 // Workspace layout: the ring (nc x D packet slots), its flags (2 D words per chain), and
