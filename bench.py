@@ -155,8 +155,8 @@ def kernel_for(d, sms: int = SMS_DEFAULT) -> str:
 
 
 # The dispatch rule of kda_fwd for the sequence-parallel path (kda_internal.h,
-# tsplit_segments): fixed-length calls whose (sequence, head) units leave clusters
-# idle run each sequence as P >= 4 segments of at least 2048 tokens.
+# tsplit_segments): fixed-length calls of at most sms / 8 (sequence, head) units run
+# each sequence as P >= 4 segments of at least 2048 tokens, P units near 7/16 of the SMs.
 TSPLIT_MIN_SEG, TSPLIT_MAX_SEG = 2048, 32
 
 
