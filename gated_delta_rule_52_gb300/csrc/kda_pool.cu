@@ -121,7 +121,10 @@ struct FrontSmall {
     float gamC_f[2][DK];                     // exp(G_C) per slot (store source)
     float gb[2][DK];                         // gate bias a2 * dt_bias[h] per slot (log2 units)
     float ga[2];                             // a2 = -exp(A_log[h]) log2(e) per slot
-    uint64_t raw_full[2], g1_done[2], am_free[2], pdone[2];
+    uint64_t raw_full[2], g1_done[2], am_free[2];
+    // the prologue's "task m ready", per task % 3: the prologue runs at most three tasks
+    // ahead of the solver (s_done), so no waiter falls a whole phase behind
+    uint64_t pdone[3];
     uint64_t s_done[3];   // the solver is done with norm slot task % 3
     unsigned int ctl_count;   // tasks whose chain tiles the control warp has stored (complete)
     int abort_p, abort_s;
@@ -608,7 +611,7 @@ __device__ __forceinline__ void pool_front(const TmaMaps &maps, const Params &p,
             fence_proxy_async_smem();
             named_bar(3, NP);
 
-            if (tid == kProLead) mbar_arrive(&sm.pdone[s]);   // operands and rq/rk/beta of chunk m ready
+            if (tid == kProLead) mbar_arrive(&sm.pdone[m % 3]);   // operands and rq/rk/beta of chunk m ready
         }
     } else if (tid >= kHelp0 && tid < kHelp0 + NH) {
         // ------------------------------------------------ helper group
@@ -692,7 +695,7 @@ __device__ __forceinline__ void pool_front(const TmaMaps &maps, const Params &p,
             int m = 0;
             for (; it.valid(); ++m, it.advance(p), ahead.advance(p), nx.advance(p)) {
                 const int s = m & 1;
-                bool ok = mbar_wait(&sm.pdone[s], (m >> 1) & 1, kWait);
+                bool ok = mbar_wait(&sm.pdone[m % 3], (m / 3) & 1, kWait);
                 if (ok && m >= 2) ok = mbar_wait(&sm.am_free[s], ((m - 2) >> 1) & 1, kWait);
                 if (ok) {
                     tc_fence_after();
@@ -762,7 +765,7 @@ __device__ __forceinline__ void pool_front(const TmaMaps &maps, const Params &p,
             const int s = m & 1;
             if (stid == kSolLead) {
                 bulk_wait_read0();   // the previous T'/M staging is shipped
-                if (!mbar_wait(&sm.pdone[s], (m >> 1) & 1, kWait) ||
+                if (!mbar_wait(&sm.pdone[m % 3], (m / 3) & 1, kWait) ||
                     !mbar_wait(&sm.g1_done[s], (m >> 1) & 1, kWait)) {
                     set_err(p);
                     sm.abort_s = 1;
@@ -1569,10 +1572,12 @@ kda_pool_kernel(const __grid_constant__ TmaMaps maps, Params p, PoolArgs a) {
                 mbar_init(&fs.raw_full[i], 1);
                 mbar_init(&fs.g1_done[i], 1);
                 mbar_init(&fs.am_free[i], 1);
-                mbar_init(&fs.pdone[i], 1);
             }
             fs.ctl_count = 0;
-            for (int i = 0; i < 3; ++i) mbar_init(&fs.s_done[i], 1);
+            for (int i = 0; i < 3; ++i) {
+                mbar_init(&fs.s_done[i], 1);
+                mbar_init(&fs.pdone[i], 1);
+            }
             fs.abort_p = fs.abort_s = 0;
             fs.dec_p = fs.dec_s = 0;
         }
