@@ -1182,6 +1182,14 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
                     }
                     continue;
                 }
+                // G2w of the next packet right behind G3u when its operands are in (D_W
+                // was read out before G3u), so that its readout overlaps this chunk's
+                const bool more = j + 1 < npk;
+                bool g2w_early = false;
+                if (more && mbar_try_wait(&cs.full_e[sj ^ 1], par2(j + 1))) {
+                    issue_g2w(j + 1);
+                    g2w_early = true;
+                }
                 // G3o: O = (Q_hat Gamma) S into lanes 64-127 (the A operand starts 64 rows
                 // before Q_hat Gamma; rows 0-63 of O are unused), right behind G3u, so that
                 // the S copy is free again when G4 completes
@@ -1203,10 +1211,9 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
                         mma_bf16(D_S, dKB + (uint64_t)(ks * 128), dUH + (uint64_t)(ks * 2), id_n128_mk, true);
                     mma_commit(&cs.s_done);
                 }
-                // G2w of the next packet (the -W^T readout of this one is done), so that its
-                // readout runs beside the S readout
-                const bool more = j + 1 < npk;
-                if (more) {
+                // otherwise G2w of the next packet here, so that its readout runs beside the
+                // S readout
+                if (more && !g2w_early) {
                     if (!wait(&cs.full_e[sj ^ 1], par2(j + 1))) return;
                     issue_g2w(j + 1);
                 }
@@ -1335,32 +1342,12 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
             }
             v_issued = jv + 1;
         };
-        // V of packet jv to fp16, in place (the 128 threads of warps 8-11)
-        auto convert_v = [&](int64_t jv) -> bool {
-            const int sv = (int)(jv & 1);
-            if (!wait(&cs.vfull[sv], par2(jv))) return false;
-            for (int k16 = tid - 256; k16 < 1024; k16 += 128) {
-                uint4 *ptr = reinterpret_cast<uint4 *>(smem + C_V + sv * 16384 + k16 * 16);
-                *ptr = bf16_to_f16x8(*ptr, rbad);
-            }
-            fence_proxy_async_smem();
-            warp_arrive(&cs.vconv[sv]);
-            return true;
-        };
         const bool vlead = warp == 8 && lane == 0;
-        if (!p.v) {
-            // values of zero (a state-only run): both V buffers hold zeros for the whole
-            // run; each thread clears the pieces it converts later (same index pattern)
-            for (int sv = 0; sv < 2; ++sv)
-                for (int k16 = tid - 256; k16 < 1024; k16 += 128)
-                    *reinterpret_cast<uint4 *>(smem + C_V + sv * 16384 + k16 * 16) = make_uint4(0u, 0u, 0u, 0u);
-        }
         [&]() {
         if (vlead) {
             if (npk > 0) issue_v(0);
             if (npk > 1) issue_v(1);
         }
-        if (npk > 0 && !convert_v(0)) return;
         if (npk > 0 && !w_readout(0)) return;
         for (int64_t j = 0; j < npk; ++j) {
             const int sj = (int)(j & 1);
@@ -1385,7 +1372,7 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
             fence_proxy_async_smem();
             tc_fence_before();
             warp_arrive(&cs.uh_ready);
-            if (j + 1 < npk && (!w_readout(j + 1) || !convert_v(j + 1))) return;
+            if (j + 1 < npk && !w_readout(j + 1)) return;
         }
         }();
         flag_range(p, rbad);
@@ -1404,7 +1391,28 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
         for (int jj = 0; jj < 4; ++jj) tmem_ld16(tmem_addr(col, quarter * 32, 64 * half + 16 * jj), r[jj]);
         tmem_ld_wait();
     };
-    bool rbad = false;   // a state value beyond the fp16 range of its operand copy
+    bool rbad = false;   // a state (or V) value beyond the fp16 range of its operand copy
+    // V of packet jv to fp16, in place (the 256 threads of warps 0-7, while their state
+    // waits for G4)
+    auto convert_v = [&](int64_t jv) -> bool {
+        const int sv = (int)(jv & 1);
+        if (!wait(&cs.vfull[sv], par2(jv))) return false;
+        for (int k16 = tid; k16 < 1024; k16 += 256) {
+            uint4 *ptr = reinterpret_cast<uint4 *>(smem + C_V + sv * 16384 + k16 * 16);
+            *ptr = bf16_to_f16x8(*ptr, rbad);
+        }
+        fence_proxy_async_smem();
+        warp_arrive(&cs.vconv[sv]);
+        return true;
+    };
+    if (!p.v) {
+        // values of zero (a state-only run): both V buffers hold zeros for the whole run;
+        // each thread clears the pieces it converts later (same index pattern)
+        for (int sv = 0; sv < 2; ++sv)
+            for (int k16 = tid; k16 < 1024; k16 += 256)
+                *reinterpret_cast<uint4 *>(smem + C_V + sv * 16384 + k16 * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (npk > 0 && !convert_v(0)) return;
     int64_t j = 0;
     const int64_t U = VL ? (int64_t)a.counts[1] : 0;
     for (int64_t w = 0;; ++w) {
@@ -1502,6 +1510,7 @@ __device__ __forceinline__ void pool_chain(const TmaMaps &maps, const Params &p,
             tmem_st_wait();
             tc_fence_before();
             warp_arrive(&cs.s_scaled);
+            if (j + 1 < npk && !convert_v(j + 1)) return;
         }
         // final state from the fp32 master
         if (!wait(&cs.s_done, par1(j - 1))) return;
@@ -1553,7 +1562,7 @@ kda_pool_kernel(const __grid_constant__ TmaMaps maps, Params p, PoolArgs a) {
                 mbar_init(&cs.full_e[i], 1);
                 mbar_init(&cs.full_l[i], 1);
                 mbar_init(&cs.vfull[i], 1);
-                mbar_init(&cs.vconv[i], 4);     // the four U / W readout warps
+                mbar_init(&cs.vconv[i], 8);     // the eight state warps
                 mbar_init(&cs.u_done[i], 1);
                 mbar_init(&cs.o_done[i], 1);
             }
