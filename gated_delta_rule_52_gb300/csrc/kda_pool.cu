@@ -42,8 +42,9 @@
 // chain tiles K_hat*Gamma, Q_hat*Gamma, Kbar), warps 13-15 row norms and beta, warp 12
 // G1 and the ring stores of the chain tiles, warps 8-11 the A/M readout, the blocked
 // inverse and T', stored with M.
-// Chain CTA: the state steps on tcgen05 with the fp32 state in TMEM (as the cluster
-// kernel's chain; -W is read out by warps 8 and 9 only), warp 12 the ring loader.
+// Chain CTA: the state steps on tcgen05 with the fp32 state in TMEM (roles at
+// pool_chain); in the state-only runs of the sequence-parallel path it carries a second
+// state with values of zero beside the first (DUAL).
 //
 // Precision: G1 on bf16 operands of the raw q/k scaled by 16-token-block-local decay
 // factors, the other GEMMs on fp16 operands, fp32 accumulators, fp32 state.  Every wait
