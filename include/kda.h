@@ -98,8 +98,11 @@ typedef enum {
  *     to "chain" CTAs, one per (sequence, head) in flight, through a ring of
  *     packets in L2; the ring takes 8 or more slots of 66 KB per chain (33.8 MB
  *     for 64 units on 152 SMs);
- *   - varlen calls take KDA_WORKSPACE_BYTES_PER_UNIT bytes per (sequence, head),
- *     the per-chunk operands that move between the two CTAs of a cluster;
+ *   - varlen calls of up to 4096 sequences run the same kernel after a one-CTA
+ *     plan (longest sequences first), with the ring and the plan's packet list in
+ *     the workspace; varlen calls of more sequences take
+ *     KDA_WORKSPACE_BYTES_PER_UNIT bytes per (sequence, head), the per-chunk
+ *     operands that move between the two CTAs of a cluster;
  *   - calls of at most 64 token rows need no workspace.
  * A fixed-length call
  * (cu_seqlens == NULL) whose N * H (sequence, head) units would leave most of the
@@ -122,7 +125,8 @@ typedef enum {
  * a NaN) sets KDA_ERR_RANGE in the device status word that kda_get_device_status
  * returns, and its outputs are then undefined; the call itself still returns KDA_OK
  * (the check runs on the device).  Calls of one token row (the fp32 token recurrence)
- * and kda_fwd_unbounded have no such limit.
+ * have no such limit, nor have kda_fwd_unbounded calls that run its token recurrence
+ * (below); its chunked form has the same limit.
  *
  * Returns KDA_OK, or an argument error (nothing enqueued), or KDA_ERR_CUDA if
  * the workspace allocation or the launch failed.
@@ -180,7 +184,9 @@ kda_status kda_fwd_ws(const void *q, const void *k, const void *v, const void *g
  * the state that crosses that token keeps at most 6.1e-5 of itself instead of less.
  * They take a workspace from the same pool as kda_fwd.  Calls of at most 64 rows and
  * larger varlen batches apply the recurrence token by token, exact for any decay,
- * without workspace.  Asynchronous like kda_fwd.  Same argument errors as kda_fwd
+ * without workspace.  The chunked form holds the same values as fp16 MMA operands as
+ * kda_fwd's and reports values beyond +-65504 the same way (KDA_ERR_RANGE in the
+ * device status word).  Asynchronous like kda_fwd.  Same argument errors as kda_fwd
  * (no lower_bound check), KDA_ERR_CUDA if the workspace or a launch failed.
  */
 kda_status kda_fwd_unbounded(const void *q, const void *k, const void *v, const void *g,
@@ -197,7 +203,7 @@ kda_status kda_fwd_unbounded(const void *q, const void *k, const void *v, const 
  *   L = sum(dout * out) + sum(dfinal * final_state),
  *
  * taken in reverse token order on the fp32 recurrence (states recomputed from
- * per-64-token checkpoints), then through the norms, the beta sigmoid and the gate.
+ * checkpoints every 16 tokens), then through the norms, the beta sigmoid and the gate.
  *
  * Inputs: q, k, v, g, beta, scale, A_log, dt_bias, lower_bound (ignored when
  * `unbounded`), initial_state, state_dtype, cu_seqlens, num_seqs, B, T, H, K, V as for
