@@ -404,11 +404,13 @@ def test_mixed_length_batches(seqlens, sd):
 
 
 @pytest.mark.parametrize("name,wl", [("decode", dict(B=2, T=1, H=2)), ("short", dict(B=2, T=8, H=2)),
-                                     ("prefill", dict(B=1, T=300, H=2))])
+                                     ("prefill", dict(B=1, T=300, H=2)),
+                                     ("sequence_parallel", dict(B=1, T=8192, H=2))])
 def test_cuda_graph_capture_replays_the_call(name, wl):
     # A serving loop captures kda_fwd in a CUDA graph: the workspace is stream-ordered
     # pool memory and every launch goes to the capturing stream, so a replay must give
-    # the direct call's results exactly.
+    # the direct call's results exactly.  T=8192 with 2 units takes the sequence-parallel
+    # path (segment kernels, two plan + pool runs with their flag clears, the scan).
     d = W.make_inputs(W.get("decode", state_dtype="fp32", seed=50, **wl))
     e = pu.to_device(d)
     out = torch.empty((d["B"], d["T"], d["H"], 128), dtype=torch.bfloat16, device="cuda")
