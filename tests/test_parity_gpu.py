@@ -571,14 +571,18 @@ def _call_status(d):
     return kda.get_device_status()
 
 
-@pytest.mark.parametrize("case", ["fixed", "varlen", "short"])
+@pytest.mark.parametrize("case", ["fixed", "varlen", "short", "unbounded", "sequence_parallel"])
 @pytest.mark.parametrize("where", ["v", "state"])
 def test_fp16_operand_range_is_reported(case, where):
     # a value beyond +-65504 where the tensor-core paths keep fp16 operands sets
-    # KDA_ERR_RANGE in the device status word, which the next status read clears
+    # KDA_ERR_RANGE in the device status word, which the next status read clears (the
+    # gate without a lower bound in its chunked form, and the sequence-parallel runs,
+    # included)
     wl = {"fixed": W.get("prefill_8k", T=300, H=2, seed=84, state_dtype="fp32"),
           "varlen": W.get("varlen_ragged", H=2, seqlens=(70, 130), seed=85),
-          "short": W.get("decode", B=2, T=8, H=2, seed=86)}[case]
+          "short": W.get("decode", B=2, T=8, H=2, seed=86),
+          "unbounded": W.get("prefill_8k", T=300, H=2, seed=88, state_dtype="fp32", lower_bound=None),
+          "sequence_parallel": W.get("prefill_8k", T=8192, H=2, seed=89, state_dtype="fp32")}[case]
     d = W.make_inputs(wl)
     assert _call_status(d) == kda.KDA_OK
     if where == "v":
