@@ -148,8 +148,7 @@ def kernel_for(d, sms: int = SMS_DEFAULT) -> str:
     """The dominant kernel of a kda_fwd call on these inputs (the sequence-parallel
     path's state-only and output runs are pool-kernel launches)."""
     varlen = d["cu_seqlens"] is not None
-    if not varlen and d["lower_bound"] is not None and tsplit_segments(
-            d["N"], d["T"], d["H"], False, sms):
+    if not varlen and tsplit_segments(d["N"], d["T"], d["H"], False, sms):
         return "pool"
     return kernel_of(d["T"], d["lower_bound"] is None, varlen, d["N"])
 
@@ -182,11 +181,11 @@ def mixed_dispatch(d) -> bool:
 
 def launches_per_call(d, sms: int) -> int:
     """libkda kernel launches of one kda_fwd call on these inputs."""
-    if d["lower_bound"] is None:
-        return 2 if d["cu_seqlens"] is not None and kernel_for(d, sms) == "pool" else 1
     P = tsplit_segments(d["N"], d["T"], d["H"], d["cu_seqlens"] is not None, sms)
     if P:   # segment bounds, segment states, 2 runs of plan + pool, scan (+ final copy)
         return 7 + (d["state_dtype"] is not None)
+    if d["lower_bound"] is None:
+        return 2 if d["cu_seqlens"] is not None and kernel_for(d, sms) == "pool" else 1
     if d["T"] <= DECODE_MAX_T:
         return 1
     pool_varlen = d["cu_seqlens"] is not None and kernel_for(d, sms) == "pool"   # plan + pool
@@ -538,7 +537,7 @@ def run_ours(args):
                 " (kda_fwd: one launch per step)" if lpc == 1 else
                 f" (kda_fwd: sequence-parallel path, {lpc} launches per step, the time of the whole call)"
                 if tsplit_segments(d_cpu["N"], d_cpu["T"], d_cpu["H"], d_cpu["cu_seqlens"] is not None, sms)
-                and d_cpu["lower_bound"] is not None else
+                else
                 " (kda_fwd: a one-CTA plan and the pool, 2 launches per step, the time of the whole call)"),
             "algorithmic_bytes_per_launch": abytes,
             "algorithmic_flops_per_launch": algorithmic_flops(d_cpu),

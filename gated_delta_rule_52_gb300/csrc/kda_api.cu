@@ -269,18 +269,20 @@ kda_status kda_fwd_unbounded(const void *q, const void *k, const void *v, const 
     int sms = 0;
     if (kda::sm_count(sms) != cudaSuccess) return KDA_ERR_CUDA;
     // Calls of at most 64 rows, and varlen batches beyond the pool's plan, run the token
-    // recurrence; the rest the pool kernel's chunked form (every sequence on it).
-    if (p.T <= kda::kShortMaxT || !kda::pool_takes(p, sms))
+    // recurrence; the rest the pool kernel's chunked form (every sequence on it), long
+    // fixed-length calls with few units sequence-parallel as in kda_fwd.
+    const int64_t tsplit = p.T > kda::kShortMaxT ? kda::tsplit_segments(p, sms) : 0;
+    if (tsplit == 0 && (p.T <= kda::kShortMaxT || !kda::pool_takes(p, sms)))
         return kda::launch_recur(p, cs) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess) return KDA_ERR_CUDA;
     cudaMemPool_t pool = workspace_pool(device);
     if (!pool) return KDA_ERR_CUDA;
+    const size_t bytes = tsplit > 0 ? kda::tsplit_scratch_bytes(p, tsplit, sms) : kda::pool_scratch_bytes(p, sms);
     void *ws = nullptr;
-    if (cudaMallocFromPoolAsync(&ws, kda::pool_scratch_bytes(p, sms), pool, cs) != cudaSuccess)
-        return KDA_ERR_CUDA;
+    if (cudaMallocFromPoolAsync(&ws, bytes, pool, cs) != cudaSuccess) return KDA_ERR_CUDA;
     p.ws = static_cast<unsigned char *>(ws);
-    st = launch(p, stream, 0, sms);
+    st = launch(p, stream, tsplit, sms);
     if (cudaFreeAsync(ws, cs) != cudaSuccess) st = KDA_ERR_CUDA;
     return st;
 }

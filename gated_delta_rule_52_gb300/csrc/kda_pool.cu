@@ -1792,8 +1792,8 @@ cudaError_t launch_pool(const Params &p, int sms, cudaStream_t stream) {
     const int64_t nchunks = vl ? 0 : (p.T + C - 1) / C;
     if (nf < 1 || (!vl && nchunks < 1)) return cudaErrorInvalidValue;
     if (vl && !pool_takes(p, sms)) return cudaErrorInvalidValue;
-    // a second state: varlen, bounded gate, state-only
-    if (p.fin2 && (!vl || p.unbounded || p.out)) return cudaErrorInvalidValue;
+    // a second state: varlen, state-only
+    if (p.fin2 && (!vl || p.out)) return cudaErrorInvalidValue;
     const PoolLayout l = pool_layout(p.n_seqs, p.H, p.T, vl, sms);
     PoolArgs a = {};
     a.nc = (int)nc;
@@ -1826,6 +1826,8 @@ cudaError_t launch_pool(const Params &p, int sms, cudaStream_t stream) {
             r = cudaFuncSetAttribute(kda_pool_kernel<true, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sb);
         if (r == cudaSuccess)
             r = cudaFuncSetAttribute(kda_pool_kernel<true, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sb);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(kda_pool_kernel<true, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sb);
         return r;
     });
     if (e != cudaSuccess) return e;
@@ -1853,7 +1855,8 @@ cudaError_t launch_pool(const Params &p, int sms, cudaStream_t stream) {
     e = cudaMemsetAsync(a.flags, 0, (size_t)nc * 2 * a.depth * sizeof(unsigned long long), stream);
     if (e != cudaSuccess) return e;
     if (p.fin2)
-        e = cudaLaunchKernelEx(&cfg, kda_pool_kernel<true, false, true>, maps, p, a);
+        e = p.unbounded ? cudaLaunchKernelEx(&cfg, kda_pool_kernel<true, true, true>, maps, p, a)
+                        : cudaLaunchKernelEx(&cfg, kda_pool_kernel<true, false, true>, maps, p, a);
     else if (p.unbounded)
         e = vl ? cudaLaunchKernelEx(&cfg, kda_pool_kernel<true, true, false>, maps, p, a)
                : cudaLaunchKernelEx(&cfg, kda_pool_kernel<false, true, false>, maps, p, a);

@@ -182,7 +182,8 @@ kda_status kda_fwd_ws(const void *q, const void *k, const void *v, const void *g
  * tensor-core form of kda_fwd's persistent kernel, with each token's decay factor
  * floored at 2^-14 (about 6.1e-5) per key channel: where the exact factor is smaller,
  * the state that crosses that token keeps at most 6.1e-5 of itself instead of less.
- * They take a workspace from the same pool as kda_fwd.  Calls of at most 64 rows and
+ * Long fixed-length calls with few (sequence, head) units run sequence-parallel as in
+ * kda_fwd.  They take a workspace from the same pool as kda_fwd.  Calls of at most 64 rows and
  * larger varlen batches apply the recurrence token by token, exact for any decay,
  * without workspace.  The chunked form holds the same values as fp16 MMA operands as
  * kda_fwd's and reports values beyond +-65504 the same way (KDA_ERR_RANGE in the

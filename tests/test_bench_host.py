@@ -141,6 +141,9 @@ def test_gate_without_lower_bound_dispatch():
     assert bench.kernel_of(8192, unbounded=True) == "pool" and bench.kernel_of(8192) == "pool"
     assert bench.kernel_of(10**6, unbounded=True, varlen=True, n_seqs=5000) == "recur"
     assert "recur" in bench.KERNEL_NAMES and len(bench.kernel_source_hash("recur")) == 16
+    # long fixed-length calls with few units: the sequence-parallel path, both gates
+    du = W.make_inputs(W.get("tiny", T=8192, H=1, lower_bound=None))
+    assert bench.kernel_for(du) == "pool" and bench.launches_per_call(du, 152) == 8
 
 
 def test_both_arms_report_the_same_workload_config():

@@ -557,6 +557,16 @@ def test_sequence_parallel_prefill_long_splits(name, over, segments):
     print(name, segments, pu.check_full(d, out, fin, label=f"{name} ({segments} segments)"))
 
 
+@pytest.mark.parametrize("T,H", [(8192, 2), (65536, 8)])
+def test_sequence_parallel_unbounded_gate(T, H):
+    # the gate without a lower bound takes the sequence-parallel path too (4 and 8
+    # segments): the floored per-token decays make the same affine segment maps
+    d = W.make_inputs(W.get("prefill_8k", B=1, T=T, H=H, seed=95 + H, state_dtype="fp32",
+                            lower_bound=None, g_std=1.5))
+    out, fin = pu.run_gpu(d)
+    print(T, H, pu.check_full(d, out, fin, label=f"unbounded sequence-parallel T={T} H={H}"))
+
+
 @pytest.mark.parametrize("g_value", [30.0, -30.0])
 @pytest.mark.parametrize("case", ["fixed", "varlen", "short"])
 def test_saturated_gate(case, g_value):
