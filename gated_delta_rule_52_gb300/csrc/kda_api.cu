@@ -250,6 +250,13 @@ kda_status kda_fwd_ws(const void *q, const void *k, const void *v, const void *g
     if ((uint64_t)workspace_bytes < (uint64_t)units * kda::kWsBytesPerUnit) return KDA_ERR_VALUE;
     if (units == 0) return KDA_OK;
     p.ws = static_cast<unsigned char *>(workspace);
+    // a fixed-length call of more than 64 rows with room for the pool kernel's ring
+    // (kda_workspace_size_pool) runs the pool kernel; otherwise the cluster kernel
+    if (!p.cu_seqlens && p.T > kda::kShortMaxT) {
+        int sms = 0;
+        if (kda::sm_count(sms) != cudaSuccess) return KDA_ERR_CUDA;
+        if (workspace_bytes >= kda::pool_scratch_bytes(p, sms)) return launch(p, stream, 0, sms);
+    }
     return launch(p, stream);
 }
 
@@ -346,6 +353,19 @@ kda_status kda_fwd_static(const void *q, const void *k, const void *v, const voi
     if (static_workspace(ws) != cudaSuccess) return KDA_ERR_CUDA;
     p.ws = ws;
     return launch(p, stream);
+}
+
+size_t kda_workspace_size_pool(int64_t num_seqs, int64_t H) {
+    if (num_seqs <= 0 || H <= 0 || num_seqs > (int64_t(1) << 30) || H > (int64_t(1) << 22)) return 0;
+    int sms = 0;
+    if (kda::sm_count(sms) != cudaSuccess) return 0;
+    kda::Params p{};
+    p.n_seqs = num_seqs;
+    p.H = H;
+    p.B = num_seqs;
+    const size_t pool = kda::pool_scratch_bytes(p, sms);
+    const size_t cluster = kda_workspace_size(num_seqs, H);
+    return pool > cluster ? pool : cluster;
 }
 
 size_t kda_workspace_size(int64_t num_seqs, int64_t H) {

@@ -39,7 +39,7 @@ KDA_STATE_BF16 = 1
 KDA_STATE_FP32 = 2
 
 # Every symbol include/kda.h declares.
-EXPORTED = ("kda_fwd", "kda_fwd_ws", "kda_fwd_unbounded", "kda_workspace_size",
+EXPORTED = ("kda_fwd", "kda_fwd_ws", "kda_fwd_unbounded", "kda_workspace_size", "kda_workspace_size_pool",
             "kda_status_string", "kda_get_device_status", "kda_version", "kda_fwd_static",
             "kda_bwd")
 
@@ -85,6 +85,8 @@ def lib() -> ctypes.CDLL:
             L.kda_bwd.restype = ci
             L.kda_workspace_size.argtypes = [i64, i64]
             L.kda_workspace_size.restype = ctypes.c_size_t
+            L.kda_workspace_size_pool.argtypes = [i64, i64]
+            L.kda_workspace_size_pool.restype = ctypes.c_size_t
             L.kda_status_string.argtypes = [ci]
             L.kda_status_string.restype = ctypes.c_char_p
             L.kda_get_device_status.argtypes = [vp]
@@ -139,6 +141,12 @@ def state_dtype_code(initial_state, final_state) -> int:
 def workspace_bytes(num_seqs: int, H: int) -> int:
     """Size of the workspace kda_fwd_ws needs for N sequences of H heads."""
     return int(num_seqs) * int(H) * WORKSPACE_BYTES_PER_UNIT
+
+
+def workspace_bytes_pool(num_seqs: int, H: int) -> int:
+    """Size of a kda_fwd_ws workspace with which fixed-length calls of more than 64 rows
+    run the persistent pool kernel (kda_workspace_size_pool; on the current device)."""
+    return int(lib().kda_workspace_size_pool(int(num_seqs), int(H)))
 
 
 def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=None,

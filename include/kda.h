@@ -112,8 +112,9 @@ typedef enum {
  * times the parallelism); its scratch, also from the pool, is about
  * N * H * P * (4 * 64 KB + KDA_WORKSPACE_BYTES_PER_UNIT) bytes.
  * kda_fwd_ws is the same call with a caller-provided workspace; for more than 64
- * rows it always runs the two-CTA cluster kernel, whose workspace kda_workspace_size
- * gives (neither the ring nor the sequence-parallel scratch).  Both are asynchronous: they return once the work is enqueued,
+ * rows it runs the two-CTA cluster kernel, whose workspace kda_workspace_size gives,
+ * or, for fixed-length calls whose workspace holds kda_workspace_size_pool bytes, the
+ * persistent pool kernel (never the sequence-parallel path).  Both are asynchronous: they return once the work is enqueued,
  * without synchronising.
  * q/k/v/g/beta/out/A_log/dt_bias/states must be 16-byte aligned.  `out` must not
  * alias an input.
@@ -145,6 +146,14 @@ kda_status kda_fwd(const void *q, const void *k, const void *v, const void *g, c
  * cu_seqlens, else B): N * H * KDA_WORKSPACE_BYTES_PER_UNIT.  Returns 0 for negative
  * sizes or a product that does not fit in size_t.  Pure host arithmetic. */
 size_t kda_workspace_size(int64_t num_seqs, int64_t H);
+
+/* Bytes of a kda_fwd_ws workspace with which fixed-length calls of more than 64 rows
+ * run the persistent pool kernel (its ring of chain packets and their flags) instead
+ * of the cluster kernel, on the current device: at least kda_workspace_size, and
+ * independent of T.  Varlen calls through kda_fwd_ws keep the cluster kernel.  Queries
+ * the current device's SM count; returns 0 for sizes out of range or if that query
+ * fails.  A workspace sized on one device is valid on devices with as many SMs. */
+size_t kda_workspace_size_pool(int64_t num_seqs, int64_t H);
 
 /*
  * kda_fwd_ws — kda_fwd without any allocation: the caller passes the workspace.

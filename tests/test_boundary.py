@@ -197,6 +197,12 @@ def test_workspace_size_query(L):
     assert L.kda_workspace_size(0, 5) == 0 and L.kda_workspace_size(3, 0) == 0
     assert L.kda_workspace_size(-1, 5) == 0 and L.kda_workspace_size(3, -2) == 0
     assert L.kda_workspace_size(1 << 40, 1 << 30) == 0   # does not fit in size_t
+    # the pool-sized workspace: 0 for sizes out of range, and (it queries the device's SM
+    # count) without a device; with one, at least the cluster kernel's size
+    assert L.kda_workspace_size_pool(0, 5) == 0 and L.kda_workspace_size_pool(-1, 5) == 0
+    assert L.kda_workspace_size_pool(3, 1 << 40) == 0
+    n = L.kda_workspace_size_pool(3, 5)
+    assert n == 0 or n >= L.kda_workspace_size(3, 5)
 
 
 def test_static_entry_point_rejects_calls_above_its_limit(L):

@@ -240,6 +240,33 @@ def test_caller_workspace_entry_point():
     assert ei.value.status == kda.KDA_ERR_VALUE
 
 
+def test_caller_workspace_pool_path():
+    # a fixed-length kda_fwd_ws call whose workspace holds kda_workspace_size_pool bytes
+    # runs the pool kernel (one with the cluster kernel's size runs the cluster kernel):
+    # both match the oracle, and garbage in the workspace gives the result of zeros
+    d = W.make_inputs(W.get("prefill_8k", B=2, T=300, H=3, seed=96, state_dtype="fp32"))
+    e = pu.to_device(d)
+    n_pool, n_cluster = kda.workspace_bytes_pool(d["N"], d["H"]), kda.workspace_bytes(d["N"], d["H"])
+    assert n_pool >= n_cluster > 0
+    ref_out, ref_fin = pu.run_oracle(d)
+    res = []
+    for size, fill in ((n_pool, 0x00), (n_pool, 0xFF), (n_cluster, 0xFF)):
+        out = torch.empty((d["B"], d["T"], d["H"], 128), dtype=torch.bfloat16, device="cuda")
+        fin = torch.empty((d["N"], d["H"], 128, 128), dtype=torch.float32, device="cuda")
+        ws = torch.full((size,), fill, dtype=torch.uint8, device="cuda")
+        kda.kda_fwd(e["q"], e["k"], e["v"], e["g"], e["beta"], d["scale"], out, e["A_log"],
+                    e["dt_bias"], d["lower_bound"], initial_state=e["initial_state"], final_state=fin,
+                    workspace=ws)
+        torch.cuda.synchronize()
+        assert kda.get_device_status() == kda.KDA_OK
+        pu.check(d, out.cpu(), fin.cpu(), ref_out, ref_fin, label=f"kda_fwd_ws {size} bytes")
+        res.append((out.cpu(), fin.cpu()))
+    assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
+    # the pool path gives kda_fwd's results bit for bit (same kernel, same inputs)
+    out2, fin2 = pu.run_gpu(d)
+    assert torch.equal(out2, res[0][0]) and torch.equal(fin2.float(), res[0][1].float())
+
+
 # ---- short steps (T <= 64 token rows): the token recurrence (T = 1) and the 16-row-block kernel
 
 @pytest.mark.parametrize("T,sd,init", [(1, "fp32", "normal"), (1, "bf16", "none"), (1, None, "normal"),
