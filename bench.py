@@ -155,14 +155,14 @@ def kernel_for(d, sms: int = SMS_DEFAULT) -> str:
 
 # The dispatch rule of kda_fwd for the sequence-parallel path (kda_internal.h,
 # tsplit_segments): fixed-length calls of at most sms / 8 (sequence, head) units run
-# each sequence as P >= 4 segments of at least 2048 tokens, P units near 7/16 of the SMs.
+# each sequence as P >= 4 segments of at least 2048 tokens, P units near 3/8 of the SMs.
 TSPLIT_MIN_SEG, TSPLIT_MAX_SEG = 2048, 32
 
 
 def tsplit_segments(N: int, T: int, H: int, varlen: bool, sms: int) -> int:
     if varlen or N <= 0 or T < 4 * TSPLIT_MIN_SEG or N * H <= 0:
         return 0
-    P = (sms * 7 // 16) // (N * H)
+    P = (sms * 3 // 8) // (N * H)
     if P < 4 and (sms // 2) // (N * H) >= 4:
         P = 4
     P = min(P, T // TSPLIT_MIN_SEG, TSPLIT_MAX_SEG)

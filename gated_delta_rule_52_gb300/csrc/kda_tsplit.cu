@@ -125,11 +125,11 @@ int64_t tsplit_segments(const Params &p, int sms) {
     if (p.cu_seqlens || p.B <= 0 || p.T < kTsplitMinSeg * 4) return 0;
     const int64_t units = p.n_seqs * p.H;
     if (units <= 0) return 0;
-    // Each run is bound by the slower of its chains (T / P chunks in a row, about 7K
+    // Each run is bound by the slower of its chains (T / P chunks in a row, about 6K
     // cycles each) and its fronts (every chunk of every unit, about 9.5K cycles each, over
-    // the SMs the chains leave): they balance with the chains on about 7/16 of the SMs.
+    // the SMs the chains leave): they balance with the chains on about 3/8 of the SMs.
     // Up to sms / 8 units, 4 segments still beat the plain path.
-    int64_t P = (sms * 7 / 16) / units;
+    int64_t P = (sms * 3 / 8) / units;
     if (P < 4 && (sms / 2) / units >= 4) P = 4;
     if (P > p.T / kTsplitMinSeg) P = p.T / kTsplitMinSeg;
     if (P > kTsplitMaxSeg) P = kTsplitMaxSeg;

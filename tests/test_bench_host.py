@@ -106,7 +106,7 @@ def test_kernel_of_follows_the_packed_token_count():
 def test_tsplit_rule_mirror():
     # the few-units rule of kda_fwd's sequence-parallel path, as bench.py mirrors it
     import bench
-    assert bench.tsplit_segments(1, 65536, 8, False, 152) == 8      # 66 chains (7/16 of 152) / 8 units
+    assert bench.tsplit_segments(1, 65536, 8, False, 152) == 7      # 57 chains (3/8 of 152) / 8 units
     assert bench.tsplit_segments(1, 65536, 16, False, 152) == 4
     assert bench.tsplit_segments(1, 65536, 19, False, 152) == 4     # 4 segments up to 152 / 8 units
     assert bench.tsplit_segments(1, 65536, 20, False, 152) == 0

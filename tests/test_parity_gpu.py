@@ -574,11 +574,11 @@ def test_unbounded_gate_zero_length_passes_state_through(sd):
 
 # ---- corners: long sequence-parallel splits, saturated gates, the fp16 operand range
 
-@pytest.mark.parametrize("name,over,segments", [("prefill_64k_h8", {}, 8),
+@pytest.mark.parametrize("name,over,segments", [("prefill_64k_h8", {}, 7),
                                                 ("prefill_8k", dict(T=65536, H=1, seed=77), 32)])
 def test_sequence_parallel_prefill_long_splits(name, over, segments):
-    # T = 65536 with 8 (sequence, head) units runs 8 segments per sequence, with one unit
-    # 32 (the most the path takes): the fp32 scan over 8 and 32 segment maps
+    # T = 65536 with 8 (sequence, head) units runs 7 segments per sequence, with one unit
+    # 32 (the most the path takes): the fp32 scan over 7 and 32 segment maps
     d = W.make_inputs(W.get(name, **over))
     out, fin = pu.run_gpu(d)
     print(name, segments, pu.check_full(d, out, fin, label=f"{name} ({segments} segments)"))
