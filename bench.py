@@ -182,8 +182,8 @@ def mixed_dispatch(d) -> bool:
 def launches_per_call(d, sms: int) -> int:
     """libkda kernel launches of one kda_fwd call on these inputs."""
     P = tsplit_segments(d["N"], d["T"], d["H"], d["cu_seqlens"] is not None, sms)
-    if P:   # segment bounds, segment states, 2 runs of plan + pool, scan (+ final copy)
-        return 7 + (d["state_dtype"] is not None)
+    if P:   # segment bounds, segment states, one plan, 2 pool runs, scan (+ final copy)
+        return 6 + (d["state_dtype"] is not None)
     if d["lower_bound"] is None:
         return 2 if d["cu_seqlens"] is not None and kernel_for(d, sms) == "pool" else 1
     if d["T"] <= DECODE_MAX_T:

@@ -102,7 +102,9 @@ int64_t pool_chains(int64_t units, int sms);
 bool pool_takes(const Params &p, int sms);   // the pool path accepts this call
 size_t pool_scratch_bytes(const Params &p, int sms);
 size_t pool_scratch_bytes_varlen(int64_t N, int64_t H, int64_t T, int sms);   // N sequences, T packed rows
-cudaError_t launch_pool(const Params &p, int sms, cudaStream_t stream);
+// plan_ready: a varlen call whose plan an earlier launch on the same stream wrote into the
+// same workspace for the same cu_seqlens, H and sms (the plan kernel is skipped)
+cudaError_t launch_pool(const Params &p, int sms, cudaStream_t stream, bool plan_ready = false);
 
 // Sequence-parallel prefill (fixed-length calls with few (sequence, head) units): each
 // sequence cut into P segments of at least kTsplitMinSeg tokens, P in [4, kTsplitMaxSeg].

@@ -1783,7 +1783,7 @@ bool pool_takes(const Params &p, int sms) {
            p.T < (int64_t(1) << 30) && p.H < (int64_t(1) << 22);
 }
 
-cudaError_t launch_pool(const Params &p, int sms, cudaStream_t stream) {
+cudaError_t launch_pool(const Params &p, int sms, cudaStream_t stream, bool plan_ready) {
     const int64_t units = p.n_seqs * p.H;
     if (units == 0) return cudaSuccess;
     const int64_t nc = pool_chains(units, sms);
@@ -1831,7 +1831,7 @@ cudaError_t launch_pool(const Params &p, int sms, cudaStream_t stream) {
         return r;
     });
     if (e != cudaSuccess) return e;
-    if (vl) {
+    if (vl && !plan_ready) {
         int npad = 1;
         while (npad < p.n_seqs) npad <<= 1;
         pool_plan_kernel<<<1, kPlanThreads, 0, stream>>>(

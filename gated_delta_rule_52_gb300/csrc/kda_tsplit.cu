@@ -185,11 +185,12 @@ cudaError_t launch_tsplit(const Params &p, int64_t P, int sms, unsigned char *sc
         return e;
     seg_scan_kernel<<<dim3((unsigned)(N * H), DK / kScanRows), 256, scan_smem, stream>>>(sin, R, Pst, P, H);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    // 4. every segment from its entering state, with outputs
+    // 4. every segment from its entering state, with outputs (the same segments, heads
+    // and workspace as the first run: its plan stands)
     q.init = sin;
     q.fin = fin3;
     q.out = p.out;
-    if ((e = launch_pool(q, sms, stream)) != cudaSuccess) return e;
+    if ((e = launch_pool(q, sms, stream, true)) != cudaSuccess) return e;
     if (p.fin) {
         seg_final_kernel<<<dim3((unsigned)(N * H), 16), 256, 0, stream>>>(p.fin, p.state_type, fin3, P, H);
         e = cudaGetLastError();

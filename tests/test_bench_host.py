@@ -95,10 +95,10 @@ def test_kernel_of_follows_the_packed_token_count():
     assert not bench.mixed_dispatch(dl) and bench.launches_per_call(dl, 152) == 2   # the plan and the pool
     assert bench.kernel_for(W.make_inputs(W.get("tiny"))) == "pool"
     assert bench.launches_per_call(W.make_inputs(W.get("tiny")), 152) == 1
-    # few units on a long fixed-length call: the sequence-parallel path (two runs of
-    # plan + pool, the segment bounds and states, the scan, the final state)
+    # few units on a long fixed-length call: the sequence-parallel path (one plan, two
+    # pool runs, the segment bounds and states, the scan, the final state)
     d8 = W.make_inputs(W.get("tiny", T=8192, H=1))
-    assert bench.kernel_for(d8) == "pool" and bench.launches_per_call(d8, 152) == 8
+    assert bench.kernel_for(d8) == "pool" and bench.launches_per_call(d8, 152) == 7
     for k in bench.KERNEL_SOURCES:
         assert len(bench.kernel_source_hash(k)) == 16 and k in bench.KERNEL_NAMES
 
@@ -143,7 +143,7 @@ def test_gate_without_lower_bound_dispatch():
     assert "recur" in bench.KERNEL_NAMES and len(bench.kernel_source_hash("recur")) == 16
     # long fixed-length calls with few units: the sequence-parallel path, both gates
     du = W.make_inputs(W.get("tiny", T=8192, H=1, lower_bound=None))
-    assert bench.kernel_for(du) == "pool" and bench.launches_per_call(du, 152) == 8
+    assert bench.kernel_for(du) == "pool" and bench.launches_per_call(du, 152) == 7
 
 
 def test_both_arms_report_the_same_workload_config():
