@@ -123,11 +123,13 @@ def test_out_guard_region_untouched():
     pu.check(d, out.cpu(), fin.cpu(), ref_out, ref_fin, label="guard")
 
 
-@pytest.mark.parametrize("B,T,H,lb", [(3, 200, 64, -5.0), (2, 130, 65, -2.0), (3, 200, 64, None)])
+@pytest.mark.parametrize("B,T,H,lb", [(3, 200, 64, -5.0), (2, 130, 65, -2.0), (3, 200, 64, None),
+                                      (1, 300, 3, -5.0), (1, 200, 1, None), (1, 1000, 5, None)])
 def test_fixed_length_more_units_than_chains(B, T, H, lb):
     # more (sequence, head) units than the pool runs chains (192 units on 64 chains, 130 on
     # 65): each chain takes its units one after another, its state leaving TMEM between
-    # them; ragged last chunks; both gates
+    # them; and small odd unit counts (3, 1 and 5 units, one chain each); ragged last
+    # chunks; both gates
     d = W.make_inputs(W.get("prefill_8k", B=B, T=T, H=H, seed=90 + H, state_dtype="fp32",
                             lower_bound=lb))
     out, fin = pu.run_gpu(d)
